@@ -1,0 +1,462 @@
+"""Pins for the CPU oracle: each test checks it against something other than
+itself -- the page's printed figures, closed forms, invariants, an
+independent brute force, exhaustive enumeration, or a library routine.
+
+All CPU; no GPU needed.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import bruteforce as bf
+from oracle.expected_topk import expected_topk_exact, get_expected_topk, variance_topk_exact
+from combine_moe_get_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _random_small_case(seed: int):
+    g = torch.Generator().manual_seed(seed)
+    R = [1, 2, 3, 4, 8][seed % 5]
+    m = [1, 2, 4][(seed // 5) % 3]
+    E = R * m
+    k = int(torch.randint(1, min(E, 8) + 1, (1,), generator=g))
+    T = int(torch.randint(0, 65, (1,), generator=g))
+    topk = wl.make_topk_uniform(g, T, E, k)
+    if seed % 2:
+        topk = wl.mask_random_lanes(g, topk, 0.25)
+    w = wl.make_weights(g, T, k)
+    H = 128 * int(torch.randint(1, 3, (1,), generator=g))
+    x = wl.make_x(g, T, H)
+    return topk, w, x, E, R
+
+
+# ---------------------------------------------------------------- page figures / closed form
+
+def _golden_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "expected_topk_pages.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                G, E, k, val, factor, note = line.split()
+                rows.append((int(G), int(E), int(k), float(val), factor, note))
+    return rows
+
+
+def test_expected_topk_pages_worked_figures():
+    rows = _golden_rows()
+    assert len(rows) == 2
+    for G, E, k, printed, factor, note in rows:
+        exact = expected_topk_exact(E, G, k)
+        if note == "approx":
+            # one expert per rank: k distinct experts always land on k distinct ranks
+            assert exact == k
+            assert abs(float(exact) - printed) < 0.5
+        else:
+            # reproduce the page's own arithmetic (multiplier `factor`), and show the
+            # formula gives a different value
+            miss = Fraction(math.comb(E - E // G, k), math.comb(E, k))
+            assert abs(int(factor) * float(1 - miss) - printed) < 0.01
+            assert abs(float(exact) - 7.904810) < 1e-6
+
+
+def _enumerate_distinct(E, G, k):
+    m = E // G
+    ds = [len({e // m for e in s}) for s in itertools.combinations(range(E), k)]
+    n = len(ds)
+    mean = Fraction(sum(ds), n)
+    var = Fraction(sum(d * d for d in ds), n) - mean * mean
+    return mean, var
+
+
+@pytest.mark.parametrize("E,G,k", [(8, 4, 3), (12, 3, 4), (10, 5, 2), (16, 8, 5), (9, 9, 3), (6, 1, 2)])
+def test_expected_topk_closed_form_vs_enumeration(E, G, k):
+    mean, var = _enumerate_distinct(E, G, k)
+    assert expected_topk_exact(E, G, k) == mean
+    assert variance_topk_exact(E, G, k) == var
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("dsv3", None), ("decode", None),
+                                    ("layout_2048", None), ("layout_2048", 1 << 16)])
+def test_oracle_mean_distinct_ranks_vs_closed_form(name, T):
+    w = wl.CONFIGS[name]
+    inp = wl.make_inputs(w, with_partial=False, num_tokens=T)
+    if not w.layout_only:
+        inp.x = None
+    lay = oracle.layout(inp.topk_idx.numpy(), w.num_experts, w.num_ranks)
+    D = lay["is_token_in_rank"].sum(axis=1).astype(np.float64)
+    mu = float(expected_topk_exact(w.num_experts, w.num_ranks, w.num_topk))
+    var = float(variance_topk_exact(w.num_experts, w.num_ranks, w.num_topk))
+    n = D.size
+    if var == 0.0:
+        assert np.all(D == mu)
+    else:
+        se = math.sqrt(var / n)
+        assert abs(D.mean() - mu) < 5 * se, (D.mean(), mu, se)
+        # sample variance within a loose band of the exact variance
+        assert 0.5 * var < D.var() < 1.5 * var
+
+
+# ---------------------------------------------------------------- layout
+
+def _check_layout_invariants(lay, topk, E, R):
+    topk = np.asarray(topk)
+    T, k = topk.shape
+    m = E // R
+    valid = (topk >= 0) & (topk < E)
+    N = int(lay["is_token_in_rank"].sum())
+    assert lay["num_recv"] == N
+    assert lay["num_tokens_per_rank"].sum() == N
+    assert lay["num_tokens_per_expert"].sum() == valid.sum()
+    assert lay["rank_prefix"][-1] == N and lay["rank_prefix"][0] == 0
+    assert np.all(np.diff(lay["rank_prefix"]) == lay["num_tokens_per_rank"])
+    assert np.all(np.diff(lay["expert_prefix"]) == lay["num_tokens_per_expert"])
+    np.testing.assert_array_equal(lay["num_tokens_per_rank"], lay["is_token_in_rank"].sum(axis=0))
+    np.testing.assert_array_equal(lay["num_tokens_per_expert"],
+                                  np.bincount(topk[valid], minlength=E))
+    dst = lay["token_dst_row"]
+    rows = dst[dst >= 0]
+    assert rows.size == N
+    np.testing.assert_array_equal(np.sort(rows), np.arange(N))
+    # each (token, rank) pair has exactly one row, held by its lowest choice index
+    for t in range(T):
+        seen = {}
+        for j in range(k):
+            if valid[t, j]:
+                r = int(topk[t, j]) // m
+                if r not in seen:
+                    seen[r] = j
+                    row = int(dst[t, j])
+                    assert lay["rank_prefix"][r] <= row < lay["rank_prefix"][r + 1]
+                    continue
+            assert dst[t, j] == -1
+        assert set(seen) == set(np.nonzero(lay["is_token_in_rank"][t])[0].tolist())
+    # rows of one rank are ordered by source token
+    src = np.full(N, -1)
+    for t in range(T):
+        for j in range(k):
+            if dst[t, j] >= 0:
+                src[dst[t, j]] = t
+    for r in range(R):
+        seg = src[lay["rank_prefix"][r]:lay["rank_prefix"][r + 1]]
+        assert np.all(np.diff(seg) > 0)
+
+
+def _cmp_layout(a, b):
+    for key in ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank",
+                "rank_prefix", "expert_prefix", "token_dst_row"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_oracle_layout_vs_bruteforce_random_small(seed):
+    topk, _, _, E, R = _random_small_case(seed)
+    a = oracle.layout(topk.numpy(), E, R)
+    b = bf.layout(topk.numpy(), E, R)
+    _cmp_layout(a, b)
+    assert a["flags"] == 0 and not b["bad_topk"]
+    if topk.shape[0]:
+        _check_layout_invariants(a, topk.numpy(), E, R)
+
+
+def test_oracle_layout_tiny_vs_bruteforce_and_invariants():
+    w = wl.CONFIGS["tiny"]
+    inp = wl.make_inputs(w)
+    a = oracle.layout(inp.topk_idx.numpy(), w.num_experts, w.num_ranks)
+    _cmp_layout(a, bf.layout(inp.topk_idx.numpy(), w.num_experts, w.num_ranks))
+    _check_layout_invariants(a, inp.topk_idx.numpy(), w.num_experts, w.num_ranks)
+
+
+def test_oracle_layout_duplicates_and_bad_entries():
+    # duplicate experts in a row count once per choice for experts, once per rank for ranks;
+    # entries outside [-1, E) are flagged and treated as masked
+    topk = np.array([[3, 3, 2, -1], [7, 0, 17, -5], [-1, -1, -1, -1], [4, 5, 6, 7]], np.int64)
+    E, R = 8, 2
+    a = oracle.layout(topk, E, R)
+    b = bf.layout(topk, E, R)
+    _cmp_layout(a, b)
+    assert a["flags"] & oracle.ORACLE_BAD_TOPK and b["bad_topk"]
+    assert a["num_tokens_per_expert"][3] == 2
+    np.testing.assert_array_equal(a["token_dst_row"][2], [-1, -1, -1, -1])
+    # token 3 goes to rank 1 only, via its first choice
+    assert a["token_dst_row"][3, 0] >= 0 and np.all(a["token_dst_row"][3, 1:] == -1)
+
+
+def test_oracle_layout_empty():
+    topk = np.zeros((0, 4), np.int64)
+    a = oracle.layout(topk, 16, 4)
+    assert a["num_recv"] == 0 and a["flags"] == 0
+    assert np.all(a["rank_prefix"] == 0) and np.all(a["expert_prefix"] == 0)
+
+
+@pytest.mark.parametrize("name", ["dsv3", "skewed", "decode"])
+def test_oracle_layout_invariants_full_configs(name):
+    w = wl.CONFIGS[name]
+    g = torch.Generator().manual_seed(w.seed)
+    if w.routing == "zipf":
+        topk = wl.make_topk_zipf(g, w.num_tokens, w.num_experts, w.num_topk, w.zipf_s)
+    else:
+        topk = wl.make_topk_uniform(g, w.num_tokens, w.num_experts, w.num_topk)
+    a = oracle.layout(topk.numpy(), w.num_experts, w.num_ranks)
+    assert a["flags"] == 0
+    # whole-config invariants (vectorised)
+    N = a["num_recv"]
+    assert a["num_tokens_per_expert"].sum() == w.num_tokens * w.num_topk
+    dst = a["token_dst_row"]
+    np.testing.assert_array_equal(np.sort(dst[dst >= 0]), np.arange(N))
+    assert N == a["is_token_in_rank"].sum()
+
+
+# ---------------------------------------------------------------- number formats
+
+def _all_finite_bf16_as_f32():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = bf.bf16_bits_to_f32(bits)
+    return f[np.isfinite(f)]
+
+
+def _e4m3_midpoints():
+    vals = bf._E4M3
+    mids = (vals[:-1] + vals[1:]) / 2
+    out = []
+    for mval in mids:
+        m32 = np.float32(mval)
+        assert float(m32) == mval          # midpoints are exact in fp32
+        out += [m32, np.nextafter(m32, np.float32(np.inf)), np.nextafter(m32, np.float32(0))]
+    out += [np.float32(448), np.float32(464), np.float32(480), np.float32(1e30), np.float32(2.0 ** -10),
+            np.float32(2.0 ** -10 * 3), np.float32(0.0)]
+    a = np.array(out, np.float32)
+    return np.concatenate([a, -a])
+
+
+def test_e4m3_encoder_vs_table_search():
+    g = np.random.default_rng(0)
+    xs = np.concatenate([
+        _all_finite_bf16_as_f32(),
+        _e4m3_midpoints(),
+        g.uniform(-480, 480, 1_000_000).astype(np.float32),
+        g.uniform(-0.05, 0.05, 200_000).astype(np.float32),
+        (g.standard_normal(200_000) * 2.0 ** -8).astype(np.float32),
+    ])
+    np.testing.assert_array_equal(oracle.e4m3_from_float_array(xs), bf.e4m3_encode(xs))
+
+
+def test_e4m3_encoder_vs_torch_cast_in_range():
+    # torch's float8_e4m3fn cast rounds to nearest even; it does not saturate, so
+    # compare only within the finite range
+    g = np.random.default_rng(1)
+    xs = np.concatenate([g.uniform(-448, 448, 1_000_000).astype(np.float32), _e4m3_midpoints()])
+    xs = xs[np.abs(xs) <= 448]
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_from_float_array(xs), ref)
+
+
+def test_e4m3_decode_roundtrip_all_codes():
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            assert math.isnan(oracle.e4m3_to_float(c))
+            continue
+        v = oracle.e4m3_to_float(c)
+        assert oracle.e4m3_from_float(v) == (c if v != 0 or c & 0x80 == 0 else c)
+        assert v == bf.e4m3_decode(np.array([c], np.uint8))[0]
+    assert oracle.e4m3_to_float(0x7E) == 448.0 and oracle.e4m3_to_float(0x01) == 2.0 ** -9
+
+
+def test_bf16_rounding_vs_torch_cast():
+    g = np.random.default_rng(2)
+    bits = g.integers(0, 1 << 32, 2_000_000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    # exact ties: low half 0x8000 with odd and even kept halves
+    ties = ((g.integers(0, 1 << 16, 4096, dtype=np.uint32) << 16) | 0x8000).view(np.float32)
+    ties = ties[np.isfinite(ties)]
+    xs = np.concatenate([f, ties, np.array([3.3895314e38, -3.3895314e38, 0.0, -0.0], np.float32)])
+    ref = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.bf16_from_float_array(xs), ref)
+
+
+# ---------------------------------------------------------------- dispatch
+
+def _dispatch_both(topk, w, x, E, R, fp8):
+    lay = oracle.layout(topk.numpy(), E, R)
+    N = lay["num_recv"]
+    a = oracle.dispatch(_bits(x), topk.numpy(), w.numpy(), E, R, lay["token_dst_row"], N, fp8=fp8)
+    b = bf.dispatch(_bits(x), topk.numpy(), w.numpy(), E, R, fp8=fp8)
+    return lay, a, b
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("seed", range(12))
+def test_oracle_dispatch_vs_bruteforce_random_small(seed, fp8):
+    topk, w, x, E, R = _random_small_case(seed)
+    lay, a, b = _dispatch_both(topk, w, x, E, R, fp8)
+    assert a["flags"] == 0
+    for key in ("recv_x", "recv_src_idx", "recv_topk_idx"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    np.testing.assert_array_equal(a["recv_topk_weights"].view(np.uint32), b["recv_topk_weights"].view(np.uint32))
+    if fp8:
+        np.testing.assert_array_equal(a["recv_x_scales"].view(np.uint32), b["recv_x_scales"].view(np.uint32))
+        np.testing.assert_array_equal(a["x_scales"].view(np.uint32), b["x_scales"].view(np.uint32))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_oracle_dispatch_tiny_vs_bruteforce(fp8):
+    wk = wl.CONFIGS["tiny"]
+    inp = wl.make_inputs(wk)
+    lay, a, b = _dispatch_both(inp.topk_idx, inp.topk_weights, inp.x, wk.num_experts, wk.num_ranks, fp8)
+    np.testing.assert_array_equal(a["recv_x"], b["recv_x"])
+    np.testing.assert_array_equal(a["recv_topk_idx"], b["recv_topk_idx"])
+    np.testing.assert_array_equal(a["recv_topk_weights"], b["recv_topk_weights"])
+
+
+def _dispatch_invariants(inp, E, R, fp8):
+    topk = inp.topk_idx.numpy()
+    T, k = topk.shape
+    m = E // R
+    lay = oracle.layout(topk, E, R)
+    N = lay["num_recv"]
+    xb = _bits(inp.x)
+    d = oracle.dispatch(xb, topk, inp.topk_weights.numpy(), E, R, lay["token_dst_row"], N, fp8=fp8)
+    src = d["recv_src_idx"]
+    ridx = d["recv_topk_idx"]
+    rank_of_row = np.searchsorted(lay["rank_prefix"], np.arange(N), side="right") - 1
+    # localised indices map back to the source choices
+    glob = np.where(ridx >= 0, ridx + (rank_of_row * m)[:, None], -1)
+    src_topk = topk[src]
+    np.testing.assert_array_equal(glob[ridx >= 0], src_topk[ridx >= 0])
+    assert np.all((src_topk[ridx < 0] // m != rank_of_row[np.nonzero(ridx < 0)[0]]) | (src_topk[ridx < 0] < 0))
+    assert (ridx >= 0).sum() == (topk >= 0).sum()
+    # weights: the local weights of a token's rows add up to all its weights
+    wsum = np.zeros(T, np.float64)
+    np.add.at(wsum, src, d["recv_topk_weights"].astype(np.float64).sum(axis=1))
+    np.testing.assert_allclose(wsum, inp.topk_weights.numpy().astype(np.float64).sum(axis=1), rtol=1e-6)
+    if not fp8:
+        np.testing.assert_array_equal(d["recv_x"], xb[src])
+        return
+    # FP8: codes and scales are those of the source row, written once per (token, rank)
+    q = d["recv_x"]
+    s = d["recv_x_scales"]
+    np.testing.assert_array_equal(s, d["x_scales"][src])
+    xf = bf.bf16_bits_to_f32(xb[src]).reshape(N, -1, 128)
+    amax = np.abs(xf).max(axis=2)
+    # the block's largest magnitude encodes to +-448
+    arg = np.abs(xf).argmax(axis=2)
+    qb = q.reshape(N, -1, 128)
+    top = np.take_along_axis(qb, arg[..., None], axis=2)[..., 0]
+    assert np.all((top & 0x7F) == 0x7E)
+    # reconstruction error within half an E4M3 step (relative 2^-4 in the normal range)
+    dec = bf.e4m3_decode(qb.reshape(-1)).reshape(qb.shape) * s[..., None].astype(np.float64)
+    err = np.abs(dec - xf)
+    bound = np.maximum(np.abs(xf) * 2.0 ** -4, 2.0 ** -10 * s[..., None]) * 1.0001
+    assert np.all(err <= bound)
+    np.testing.assert_array_equal(s, (amax / np.float32(448)).astype(np.float32))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_oracle_dispatch_invariants_dsv3_slice(fp8):
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=512)
+    _dispatch_invariants(inp, wk.num_experts, wk.num_ranks, fp8)
+
+
+def test_oracle_fp8_zero_block_and_capacity():
+    x = torch.zeros(2, 256, dtype=torch.bfloat16)
+    x[1, 128:] = torch.linspace(-3, 3, 128).to(torch.bfloat16)
+    topk = np.array([[0, 5], [1, 6]], np.int64)
+    lay = oracle.layout(topk, 8, 2)
+    d = oracle.dispatch(_bits(x), topk, None, 8, 2, lay["token_dst_row"], lay["num_recv"], fp8=True)
+    assert d["flags"] == 0
+    assert np.all(d["x_scales"][0] == 0) and d["x_scales"][1, 0] == 0
+    assert d["x_scales"][1, 1] == np.float32(3.0) / np.float32(448.0)
+    rows0 = lay["token_dst_row"][0][lay["token_dst_row"][0] >= 0]
+    assert np.all(d["recv_x"][rows0] == 0)
+    # capacity one short of N: the last row is flagged and not written
+    d2 = oracle.dispatch(_bits(x), topk, None, 8, 2, lay["token_dst_row"], lay["num_recv"] - 1,
+                         fp8=False, fill_x=0xFFFF)
+    assert d2["flags"] & oracle.ORACLE_CAPACITY
+
+
+# ---------------------------------------------------------------- combine
+
+@pytest.mark.parametrize("seed", range(20))
+def test_oracle_combine_vs_bruteforce_random_small(seed):
+    topk, _, _, E, R = _random_small_case(seed)
+    g = torch.Generator().manual_seed(1000 + seed)
+    lay = oracle.layout(topk.numpy(), E, R)
+    H = 64
+    partial = _bits(wl.make_partial(g, max(lay["num_recv"], 1), H))
+    a, flags = oracle.combine(partial, lay["token_dst_row"])
+    assert flags == 0
+    np.testing.assert_array_equal(a, bf.combine(partial, lay["token_dst_row"]))
+
+
+def test_oracle_combine_sums_in_ascending_rank_order():
+    # one token on all four ranks (rows 0..3 = ranks 0..3) whose choices list the ranks
+    # as 2, 3, 1, 0. Row values 1, 2^-8, 2^-24, 2^-24: in ascending row order both 2^-24
+    # terms are absorbed (fp32 ties to even) and 1 + 2^-8 is a bf16 tie that rounds to 1;
+    # in choice order they add up to 2^-23 first and the result rounds up to 1 + 2^-7.
+    topk = np.array([[2, 3, 1, 0]], np.int64)
+    lay = oracle.layout(topk, 4, 4)
+    np.testing.assert_array_equal(lay["token_dst_row"], [[2, 3, 1, 0]])
+    vals = np.array([[1.0], [2.0 ** -8], [2.0 ** -24], [2.0 ** -24]], np.float32)
+    partial = bf.f32_to_bf16_bits(vals)
+    out, _ = oracle.combine(partial, lay["token_dst_row"])
+    assert bf.bf16_bits_to_f32(out)[0, 0] == np.float32(1.0)
+    # the other order really does differ (so the check above can see a wrong order)
+    acc = np.float32(0)
+    for row in (2, 3, 1, 0):
+        acc = np.float32(acc + vals[row, 0])
+    assert bf.bf16_bits_to_f32(bf.f32_to_bf16_bits(np.array([acc])))[0] == np.float32(1.0 + 2.0 ** -7)
+
+
+def test_oracle_dispatch_then_combine_is_d_times_x():
+    # partial = recv_x: each token comes back as bf16(D_t * x_t); sums of <= 8 copies of a
+    # bf16 value are exact in fp32, so only the final rounding remains (torch's cast)
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=256)
+    topk = inp.topk_idx.numpy()
+    lay = oracle.layout(topk, wk.num_experts, wk.num_ranks)
+    d = oracle.dispatch(_bits(inp.x), topk, None, wk.num_experts, wk.num_ranks,
+                        lay["token_dst_row"], lay["num_recv"])
+    out, _ = oracle.combine(d["recv_x"], lay["token_dst_row"])
+    D = torch.from_numpy(lay["is_token_in_rank"].sum(axis=1).astype(np.float32))
+    ref = (inp.x.float() * D[:, None]).to(torch.bfloat16)
+    np.testing.assert_array_equal(out, _bits(ref))
+
+
+def test_oracle_identity_expert_returns_x():
+    # expert = identity scaled by the row's local weights; weights sum to 1 per token,
+    # so combine returns x up to two bf16 roundings (unit roundoff 2^-8 each -> 2^-7)
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=256)
+    topk = inp.topk_idx.numpy()
+    lay = oracle.layout(topk, wk.num_experts, wk.num_ranks)
+    d = oracle.dispatch(_bits(inp.x), topk, inp.topk_weights.numpy(), wk.num_experts, wk.num_ranks,
+                        lay["token_dst_row"], lay["num_recv"])
+    wrow = d["recv_topk_weights"].sum(axis=1)
+    partial = bf.f32_to_bf16_bits(bf.bf16_bits_to_f32(d["recv_x"]) * wrow[:, None])
+    out, _ = oracle.combine(partial, lay["token_dst_row"])
+    got = bf.bf16_bits_to_f32(out).astype(np.float64)
+    x = inp.x.float().numpy().astype(np.float64)
+    assert np.all(np.abs(got - x) <= 2.0 ** -7 * np.abs(x) * 1.01 + 1e-30)
+
+
+def test_oracle_combine_token_without_rows_is_zero():
+    topk = np.array([[-1, -1], [0, 1]], np.int64)
+    lay = oracle.layout(topk, 2, 2)
+    partial = bf.f32_to_bf16_bits(np.ones((2, 16), np.float32))
+    out, _ = oracle.combine(partial, lay["token_dst_row"])
+    assert np.all(out[0] == 0) and np.all(bf.bf16_bits_to_f32(out[1]) == 2.0)
