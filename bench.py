@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark: one step = layout -> dispatch (bf16) -> combine over one batch of
+the DeepSeek-V3-shaped workload (4096 tokens, hidden 7168 bf16, 256 experts
+over 8 logical ranks, top-8), synthetic inputs resident in HBM.
+
+Prints ONE JSON line (rank 0). Default: 1 GPU, a few hundred ms of timed GPU
+work, plus the CPU oracle timed on the host as a reported baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+path shards by tokens and has no exchange step): weak scaling, max-over-ranks
+time, whole-job tokens/s. ``--impl reference`` times the CPU oracle (the only
+reference implementation available for this path) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from combine_moe_get_gb300 import workloads as wl  # noqa: E402
+
+WORKLOAD = "dsv3"
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of peak), DSv3 shape"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ measured peaks, clocks, profiles
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        target = str(device_index)
+        try:
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+            if bus:
+                target = bus
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", "-i", target, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                    "-lms", "200"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        smax = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def profiled_traffic(kernel: str, source: str):
+    """DRAM bytes per launch recorded in profiles/<kernel>_<workload>.md, if the
+    kernel source has not changed since (its sha256 is recorded beside it)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.md")
+    src = os.path.join(ROOT, "combine_moe_get_gb300", "csrc", source)
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except Exception:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def time_oracle(inp, w, budget_s: float, min_steps: int = 1):
+    """Full oracle steps (layout + dispatch + combine) until `budget_s` elapses."""
+    import oracle
+    topk = inp.topk_idx.numpy()
+    xb = inp.x.view(torch.int16).numpy().view(np.uint16)
+    wts = inp.topk_weights.numpy()
+    pb = inp.partial.view(torch.int16).numpy().view(np.uint16)
+    cap = wl.recv_capacity(w.num_tokens, w.num_topk, w.num_ranks)
+    steps, t0 = 0, time.perf_counter()
+    while steps < min_steps or time.perf_counter() - t0 < budget_s:
+        lay = oracle.layout(topk, w.num_experts, w.num_ranks)
+        oracle.dispatch(xb, topk, wts, w.num_experts, w.num_ranks, lay["token_dst_row"], cap)
+        oracle.combine(pb[: lay["num_recv"]], lay["token_dst_row"])
+        steps += 1
+    dt = time.perf_counter() - t0
+    return steps, dt
+
+
+# ------------------------------------------------------------------ the GPU step
+
+class Step:
+    def __init__(self, moe, w, inp, device):
+        self.moe, self.w = moe, w
+        T, k, E, R, H = w.num_tokens, w.num_topk, w.num_experts, w.num_ranks, w.hidden
+        self.cap = wl.recv_capacity(T, k, R)
+        self.x = inp.x.to(device)
+        self.topk = inp.topk_idx.to(device)
+        self.wts = inp.topk_weights.to(device)
+        self.partial = inp.partial.to(device)
+        self.status = moe.new_status(device)
+        self.lay = moe.Layout.empty(T, k, E, R, device)
+        self.ws = torch.empty(moe.moe_get_layout_workspace_size(T, E, R), dtype=torch.uint8, device=device)
+        self.disp = moe.Dispatched(
+            recv_x=torch.empty(self.cap, H, dtype=torch.bfloat16, device=device), recv_x_scales=None,
+            recv_topk_idx=torch.empty(self.cap, k, dtype=torch.int64, device=device),
+            recv_topk_weights=torch.empty(self.cap, k, dtype=torch.float32, device=device),
+            recv_src_idx=torch.empty(self.cap, dtype=torch.int32, device=device), x_scales=None)
+        self.disp8 = moe.Dispatched(
+            recv_x=torch.empty(self.cap, H, dtype=torch.uint8, device=device),
+            recv_x_scales=torch.empty(self.cap, H // 128, dtype=torch.float32, device=device),
+            recv_topk_idx=self.disp.recv_topk_idx, recv_topk_weights=self.disp.recv_topk_weights,
+            recv_src_idx=self.disp.recv_src_idx, x_scales=torch.empty(T, H // 128, dtype=torch.float32, device=device))
+        self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+
+    def layout(self):
+        self.moe.moe_get_layout(self.topk, self.w.num_experts, self.w.num_ranks, out=self.lay, workspace=self.ws,
+                                status=self.status)
+
+    def dispatch(self, fp8=False):
+        self.moe.moe_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks,
+                              self.lay.token_dst_row, self.cap, quantize_fp8=fp8,
+                              out=self.disp8 if fp8 else self.disp, status=self.status)
+
+    def combine(self):
+        self.moe.moe_combine(self.partial, self.lay.token_dst_row, out=self.out, status=self.status)
+
+
+def run_ours(args, world, rank, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    from combine_moe_get_gb300 import binding as moe
+
+    w = wl.CONFIGS[WORKLOAD]
+    inp = wl.make_inputs(dataclass_replace_seed(w, w.seed + rank))
+    st = Step(moe, w, inp, device)
+    T, H = w.num_tokens, w.hidden
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def one(events=None):
+        if events:
+            events[0].record(stream)
+        st.layout()
+        if events:
+            events[1].record(stream)
+        st.dispatch()
+        if events:
+            events[2].record(stream)
+        st.combine()
+        if events:
+            events[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    moe.check_status(st.status, "warm-up")
+    N = int(st.lay.rank_prefix[-1].item())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(device.index) as clk:
+        for i in range(args.steps):
+            flush.zero_()                       # L2 flush between steps, outside the events
+            one(evs[i])
+        torch.cuda.synchronize()
+    barrier(world)
+    moe.check_status(st.status, "timed steps")
+    clocks = clk.summary()
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dis_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    com_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    mean = statistics.fmean
+    ms_per_step = max_over_ranks(mean(step_ms), world, device)
+    tokens_per_s = world * T / (ms_per_step / 1e3)
+
+    # FP8 dispatch (fused quantisation), timed alone with the same flush discipline
+    fp8_ms = []
+    for i in range(max(3, args.steps // 2) + 2):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        st.dispatch(fp8=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            fp8_ms.append(a.elapsed_time(b))
+    moe.check_status(st.status, "fp8 dispatch")
+
+    peak, peak_kind = hbm_peak()
+    row = H * 2
+    bytes_bf16 = T * row + N * row                      # x read once + one row per (token, rank)
+    bytes_fp8 = T * row + N * H + N * (H // 128) * 4    # x read + e4m3 rows + scales
+    kern = {
+        "layout_us": mean(lay_ms) * 1e3,
+        "dispatch_us": mean(dis_ms) * 1e3,
+        "combine_us": mean(com_ms) * 1e3,
+        "dispatch_fp8_us": mean(fp8_ms) * 1e3,
+    }
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
+    kern["dispatch_gbs"] = gbs(bytes_bf16, mean(dis_ms))
+    kern["combine_gbs"] = gbs(bytes_bf16, mean(com_ms))
+    kern["dispatch_fp8_gbs"] = gbs(bytes_fp8, mean(fp8_ms))
+    for key in ("dispatch", "combine", "dispatch_fp8"):
+        kern[f"{key}_frac"] = kern[f"{key}_gbs"] / peak
+    dominant = "dispatch" if mean(dis_ms) >= mean(com_ms) else "combine"
+    dom_ms = mean(dis_ms) if dominant == "dispatch" else mean(com_ms)
+    achieved = gbs(bytes_bf16, dom_ms)
+    traffic = profiled_traffic(f"{dominant}_kernel", f"{dominant}.cu")
+
+    e2e = run_e2e(moe, st, inp, w, device, args)
+
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 rows, uniform top-8 routing)",
+        "config": {"workload": "DeepSeek-V3 prefill shape: T=4096, H=7168 bf16, E=256 over R=8 logical ranks, "
+                               "top-8 uniform, softmax weights", "tokens": T, "hidden": H,
+                   "experts": w.num_experts, "ranks": w.num_ranks, "topk": w.num_topk, "recv_rows": N,
+                   "step": "layout + dispatch(bf16) + combine", "l2": f"flushed between steps ({flush.numel() >> 20} MiB memset, untimed)",
+                   "parallelism": f"replicas x{world} (independent token shards, no collective)"},
+        "roofline": {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": bytes_bf16},
+        "kernels": kern,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        steps, dt = time_oracle(inp, w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": steps * T / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{steps} full oracle steps (layout+dispatch+combine) of the same "
+                                          f"workload, {dt:.1f} s single-threaded"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(moe, st, inp, w, device, args):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's inputs, a 4-byte read of the receive count, H2D of the partial rows,
+    D2H of the combined output -- all inside the timed region."""
+    T, H = w.num_tokens, w.hidden
+    hx = inp.x.pin_memory()
+    htopk = inp.topk_idx.pin_memory()
+    hw = inp.topk_weights.pin_memory()
+    hpart = inp.partial.pin_memory()
+    hout = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    hcount = torch.empty(1, dtype=torch.int32).pin_memory()
+    times, h2d, d2h = [], 0, 0
+    for i in range(args.warmup + max(3, args.steps // 2)):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        st.x.copy_(hx, non_blocking=True)
+        st.topk.copy_(htopk, non_blocking=True)
+        st.wts.copy_(hw, non_blocking=True)
+        st.layout()
+        hcount.copy_(st.lay.rank_prefix[-1:], non_blocking=True)
+        torch.cuda.synchronize()
+        n = int(hcount.item())
+        st.dispatch()
+        st.partial[:n].copy_(hpart[:n], non_blocking=True)
+        st.combine()
+        hout.copy_(st.out, non_blocking=True)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            h2d = hx.numel() * 2 + htopk.numel() * 8 + hw.numel() * 4 + n * H * 2
+            d2h = 4 + hout.numel() * 2
+    moe.check_status(st.status, "e2e")
+    sec = statistics.fmean(times)
+    return {"value": T / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": sec * 1e3}
+
+
+def dataclass_replace_seed(w, seed):
+    import dataclasses
+    return dataclasses.replace(w, seed=seed)
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = wl.CONFIGS[WORKLOAD]
+    inp = wl.make_inputs(w)
+    time_oracle(inp, w, 0.0, min_steps=args.warmup)
+    steps, dt = time_oracle(inp, w, 0.0, min_steps=args.steps)
+    T = w.num_tokens
+    value = steps * T / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "DeepSeek-V3 prefill shape: T=4096, H=7168 bf16, E=256 over R=8 logical ranks, "
+                               "top-8 uniform, softmax weights", "step": "layout + dispatch(bf16) + combine"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} full oracle steps of the workload, single-threaded"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+"""Thin Python binding of ``libmoe_get.so`` (the C ABI in ``include/moe_get.h``).
+
+Argument marshalling only: every function takes CUDA tensors, allocates the
+outputs it is not given with torch (device memory is torch's job here), and
+passes raw pointers, sizes and the current CUDA stream to the C entry point
+of the same name. All computation runs in the library's CUDA kernels; there
+is no CPU path. If the library cannot be built or loaded, import fails.
+
+Errors the host detects come back as ``MoeError``. Errors that depend on the
+data land in the int32 ``status`` tensor (first error wins; never cleared by
+the library): call ``check_status`` after synchronising.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_MISALIGNED = 2
+MOE_ERR_CAPACITY = 3
+MOE_ERR_BAD_TOPK = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_CUDA = 6
+MOE_ERR_WORKSPACE = 7
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+class MoeLayoutC(ctypes.Structure):
+    _fields_ = [("num_tokens_per_rank", _P), ("num_tokens_per_expert", _P), ("is_token_in_rank", _P),
+                ("rank_prefix", _P), ("expert_prefix", _P), ("token_dst_row", _P)]
+
+
+class MoeLayoutOptionsC(ctypes.Structure):
+    _fields_ = [("wait_timeout_ns", ctypes.c_int64), ("test_unpublished_tile", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _load():
+    if not os.path.exists(_build.LIB) or not _build.up_to_date():
+        _build.build()
+    lib = ctypes.CDLL(_build.LIB)
+    lib.moe_get_version.restype = _I
+    lib.moe_status_string.argtypes = [_I]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_get_layout_workspace_size.argtypes = [_I, _I, _I]
+    lib.moe_get_layout_workspace_size.restype = ctypes.c_size_t
+    lib.moe_get_layout.argtypes = [_P, _I, _I, _I, _I, MoeLayoutC, _P, ctypes.c_size_t, _P, _P]
+    lib.moe_get_layout.restype = _I
+    lib.moe_get_layout_ex.argtypes = [_P, _I, _I, _I, _I, MoeLayoutC, _P, ctypes.c_size_t, _P, _P,
+                                      ctypes.POINTER(MoeLayoutOptionsC)]
+    lib.moe_get_layout_ex.restype = _I
+    lib.moe_dispatch.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.moe_dispatch.restype = _I
+    lib.moe_combine.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
+    lib.moe_combine.restype = _I
+    return lib
+
+
+LIB = _load()
+
+
+def status_string(code: int) -> str:
+    return LIB.moe_status_string(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmoe_get takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libmoe_get takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(code: int, where: str) -> None:
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_status(status: torch.Tensor, where: str = "kernel") -> None:
+    code = int(status.item())
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+@dataclasses.dataclass
+class Layout:
+    num_tokens_per_rank: torch.Tensor     # [R] int32
+    num_tokens_per_expert: torch.Tensor   # [E] int32
+    is_token_in_rank: torch.Tensor        # [T, R] uint8
+    rank_prefix: torch.Tensor             # [R+1] int32
+    expert_prefix: torch.Tensor           # [E+1] int32
+    token_dst_row: torch.Tensor           # [T, k] int32
+
+    @staticmethod
+    def empty(num_tokens: int, num_topk: int, num_experts: int, num_ranks: int, device) -> "Layout":
+        i32 = dict(dtype=torch.int32, device=device)
+        return Layout(torch.empty(num_ranks, **i32), torch.empty(num_experts, **i32),
+                      torch.empty(num_tokens, num_ranks, dtype=torch.uint8, device=device),
+                      torch.empty(num_ranks + 1, **i32), torch.empty(num_experts + 1, **i32),
+                      torch.empty(num_tokens, num_topk, **i32))
+
+    def c(self) -> MoeLayoutC:
+        return MoeLayoutC(*(_ptr(getattr(self, f.name)) for f in dataclasses.fields(self)))
+
+
+def moe_get_layout_workspace_size(num_tokens: int, num_experts: int, num_ranks: int) -> int:
+    return int(LIB.moe_get_layout_workspace_size(num_tokens, num_experts, num_ranks))
+
+
+def moe_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
+                   out: Optional[Layout] = None, workspace: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None, stream=None,
+                   wait_timeout_ns: int = 0, test_unpublished_tile: int = -1) -> Layout:
+    """Counts, membership, prefixes and receive rows of ``topk_idx`` [T, k] int64."""
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    out = out or Layout.empty(T, k, num_experts, num_ranks, dev)
+    ws_bytes = moe_get_layout_workspace_size(T, num_experts, num_ranks)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    status = new_status(dev) if status is None else status
+    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile))
+    code = LIB.moe_get_layout_ex(_ptr(topk_idx), T, k, num_experts, num_ranks, out.c(), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream),
+                                 ctypes.byref(opts))
+    _check(code, "moe_get_layout")
+    return out
+
+
+@dataclasses.dataclass
+class Dispatched:
+    recv_x: torch.Tensor                      # [capacity, H] bf16 or uint8 (E4M3 codes)
+    recv_x_scales: Optional[torch.Tensor]     # [capacity, H/128] fp32 (FP8)
+    recv_topk_idx: Optional[torch.Tensor]     # [capacity, k] int64
+    recv_topk_weights: Optional[torch.Tensor] # [capacity, k] fp32
+    recv_src_idx: Optional[torch.Tensor]      # [capacity] int32
+    x_scales: Optional[torch.Tensor]          # [T, H/128] fp32 (FP8)
+
+
+def moe_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
+                 num_experts: int, num_ranks: int, token_dst_row: torch.Tensor, recv_capacity: int, *,
+                 quantize_fp8: bool = False, out: Optional[Dispatched] = None, with_metadata: bool = True,
+                 status: Optional[torch.Tensor] = None, stream=None) -> Dispatched:
+    """Row copies (bf16, or fused E4M3 quantisation) and per-row metadata."""
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    dev = x.device
+    if out is None:
+        nb = H // 128
+        out = Dispatched(
+            recv_x=torch.empty(recv_capacity, H, dtype=torch.uint8 if quantize_fp8 else torch.bfloat16, device=dev),
+            recv_x_scales=torch.empty(recv_capacity, nb, dtype=torch.float32, device=dev) if quantize_fp8 else None,
+            recv_topk_idx=torch.empty(recv_capacity, k, dtype=torch.int64, device=dev) if with_metadata else None,
+            recv_topk_weights=(torch.empty(recv_capacity, k, dtype=torch.float32, device=dev)
+                               if with_metadata else None),
+            recv_src_idx=torch.empty(recv_capacity, dtype=torch.int32, device=dev) if with_metadata else None,
+            x_scales=torch.empty(T, nb, dtype=torch.float32, device=dev) if quantize_fp8 else None)
+    status = new_status(dev) if status is None else status
+    code = LIB.moe_dispatch(_ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), k, num_experts, num_ranks,
+                            _ptr(token_dst_row), recv_capacity, int(bool(quantize_fp8)), _ptr(out.recv_x),
+                            _ptr(out.recv_x_scales), _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights),
+                            _ptr(out.recv_src_idx), _ptr(out.x_scales), _ptr(status), _stream(stream))
+    _check(code, "moe_dispatch")
+    return out
+
+
+def moe_combine(partial: torch.Tensor, token_dst_row: torch.Tensor, *, out: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[t] = bf16(fp32 sum of partial rows of token t in ascending rank order)."""
+    rows, H = partial.shape
+    T, k = token_dst_row.shape
+    dev = partial.device
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev) if out is None else out
+    status = new_status(dev) if status is None else status
+    code = LIB.moe_combine(_ptr(partial), rows, T, H, k, _ptr(token_dst_row), _ptr(out), _ptr(status),
+                           _stream(stream))
+    _check(code, "moe_combine")
+    return out

@@ -1,0 +1,279 @@
+// moe_api.cu -- the extern "C" entry points of libmoe_get.so.
+//
+// Every entry point validates its arguments on the host before it touches
+// CUDA, so argument errors come back as return codes without a launch (and
+// can be checked on a machine without a GPU). Then it hands a plain launch
+// description to the kernel launcher of its step.
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+#include <utility>
+
+#include <cuda_runtime.h>
+
+#include "../../include/moe_get.h"
+#include "moe_internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ device facts
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<long long> g_smem_sm[kMaxDevices];
+std::atomic<long long> g_smem_optin[kMaxDevices];
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return 0;
+    return d;
+}
+
+int query_attr(cudaDeviceAttr attr, int dev) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess) return 0;
+    return v;
+}
+}  // namespace
+
+int device_sm_count() {
+    const int d = current_device();
+    int v = g_sm_count[d].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = query_attr(cudaDevAttrMultiProcessorCount, d);
+        if (v <= 0) v = 1;
+        g_sm_count[d].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+size_t device_smem_per_sm() {
+    const int d = current_device();
+    long long v = g_smem_sm[d].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = query_attr(cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
+        if (v <= 0) v = 48 * 1024;
+        g_smem_sm[d].store(v, std::memory_order_relaxed);
+    }
+    return (size_t)v;
+}
+
+size_t device_smem_optin() {
+    const int d = current_device();
+    long long v = g_smem_optin[d].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = query_attr(cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+        if (v <= 0) v = 48 * 1024;
+        g_smem_optin[d].store(v, std::memory_order_relaxed);
+    }
+    return (size_t)v;
+}
+
+int ensure_dynamic_smem(const void *kernel, size_t bytes) {
+    static std::mutex mu;
+    static std::unordered_map<const void *, size_t> done[kMaxDevices];
+    const int d = current_device();
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &cur = done[d][kernel];
+    if (bytes <= cur) return MOE_OK;
+    if (bytes > 48 * 1024) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    cur = bytes;
+    return MOE_OK;
+}
+
+namespace {
+int env_int(const char *name, int dflt) {
+    const char *v = std::getenv(name);
+    if (v == nullptr || *v == '\0') return dflt;
+    char *end = nullptr;
+    long x = std::strtol(v, &end, 0);
+    return (end && *end == '\0' && x > 0 && x < (1L << 30)) ? (int)x : dflt;
+}
+}  // namespace
+
+const Tuning &tuning() {
+    static const Tuning t = [] {
+        Tuning x;
+        x.dispatch_warps = env_int("MOE_TUNE_DISPATCH_WARPS", 8);
+        x.dispatch_stages = env_int("MOE_TUNE_DISPATCH_STAGES", 3);
+        x.dispatch_chunk = env_int("MOE_TUNE_DISPATCH_CHUNK", 8192);
+        x.combine_warps = env_int("MOE_TUNE_COMBINE_WARPS", 4);
+        x.combine_stages = env_int("MOE_TUNE_COMBINE_STAGES", 3);
+        x.combine_stage_bytes = env_int("MOE_TUNE_COMBINE_STAGE_BYTES", 16384);
+        x.ctas_per_sm = env_int("MOE_TUNE_CTAS_PER_SM", 0);
+        x.l2_hints = env_int("MOE_TUNE_L2_HINTS", 1) & 3;
+        return x;
+    }();
+    return t;
+}
+
+}  // namespace moe
+
+// ------------------------------------------------------------------ validation helpers
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool shape_ok(int T, int k, int E, int R) {
+    if (T < 0 || k < 1 || k > MOE_MAX_TOPK) return false;
+    if (R < 1 || R > MOE_MAX_RANKS || E < 1 || E > MOE_MAX_EXPERTS || E % R != 0) return false;
+    if ((int64_t)T * k >= (int64_t)1 << 31) return false;
+    return true;
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ C ABI
+
+extern "C" {
+
+MOE_API int moe_get_version(void) { return 100; }
+
+MOE_API const char *moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED";
+        case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
+        case MOE_ERR_BAD_TOPK: return "MOE_ERR_BAD_TOPK";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, int num_ranks) {
+    if (!shape_ok(num_tokens, 1, num_experts, num_ranks)) return 0;
+    return moe::layout_workspace_bytes(num_tokens, num_experts, num_ranks);
+}
+
+static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
+                         size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
+                         int unpublished_tile) {
+    if (!shape_ok(T, k, E, R)) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * R >= (int64_t)1 << 40) return MOE_ERR_INVALID_ARG;
+    if (!status || !o.num_tokens_per_rank || !o.num_tokens_per_expert || !o.rank_prefix || !o.expert_prefix)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !o.is_token_in_rank || !o.token_dst_row || !workspace)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(status, 4) || !aligned(o.num_tokens_per_rank, 4) || !aligned(o.num_tokens_per_expert, 4) ||
+        !aligned(o.rank_prefix, 4) || !aligned(o.expert_prefix, 4))
+        return MOE_ERR_MISALIGNED;
+    if (T > 0) {
+        if (!aligned(topk_idx, 8) || !aligned(o.token_dst_row, 4) || !aligned(o.is_token_in_rank, 4) ||
+            !aligned(workspace, 16))
+            return MOE_ERR_MISALIGNED;
+        if (workspace_bytes < moe::layout_workspace_bytes(T, E, R)) return MOE_ERR_WORKSPACE;
+    }
+    moe::LayoutLaunch L;
+    L.topk_idx = topk_idx;
+    L.num_tokens = T;
+    L.num_topk = k;
+    L.num_experts = E;
+    L.num_ranks = R;
+    L.out = o;
+    L.workspace = workspace;
+    L.status = status;
+    L.stream = stream;
+    L.timeout_ns = timeout_ns;
+    L.unpublished_tile = unpublished_tile;
+    return moe::launch_layout(L);
+}
+
+MOE_API int moe_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts, int num_ranks,
+                           moe_layout_t layout, void *workspace, size_t workspace_bytes, int32_t *status,
+                           void *stream) {
+    return layout_common(topk_idx, num_tokens, num_topk, num_experts, num_ranks, layout, workspace,
+                         workspace_bytes, status, stream, 0, -1);
+}
+
+MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                              int num_ranks, moe_layout_t layout, void *workspace, size_t workspace_bytes,
+                              int32_t *status, void *stream, const moe_layout_options_t *options) {
+    int64_t timeout = 0;
+    int unpublished = -1;
+    if (options) {
+        timeout = options->wait_timeout_ns;
+        unpublished = options->test_unpublished_tile;
+    }
+    return layout_common(topk_idx, num_tokens, num_topk, num_experts, num_ranks, layout, workspace,
+                         workspace_bytes, status, stream, timeout, unpublished);
+}
+
+MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                         const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                         const int32_t *token_dst_row, int recv_capacity, int quantize_fp8, void *recv_x,
+                         float *recv_x_scales, int64_t *recv_topk_idx, float *recv_topk_weights,
+                         int32_t *recv_src_idx, float *x_scales, int32_t *status, void *stream) {
+    const int T = num_tokens, H = hidden;
+    if (!shape_ok(T, num_topk, num_experts, num_ranks)) return MOE_ERR_INVALID_ARG;
+    if (recv_capacity < 0 || H < 8 || H % 8 != 0 || (quantize_fp8 && H % 128 != 0)) return MOE_ERR_INVALID_ARG;
+    if (H > (1 << 24)) return MOE_ERR_INVALID_ARG;
+    if (!status) return MOE_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!x || !topk_idx || !token_dst_row || (recv_capacity > 0 && !recv_x)) return MOE_ERR_INVALID_ARG;
+        if (quantize_fp8 && recv_capacity > 0 && !recv_x_scales) return MOE_ERR_INVALID_ARG;
+        if (!aligned(x, 16) || (recv_x && !aligned(recv_x, 16)) || !aligned(topk_idx, 8) ||
+            !aligned(token_dst_row, 4) || !aligned(status, 4) || (topk_weights && !aligned(topk_weights, 4)) ||
+            (recv_x_scales && !aligned(recv_x_scales, 4)) || (recv_topk_idx && !aligned(recv_topk_idx, 8)) ||
+            (recv_topk_weights && !aligned(recv_topk_weights, 4)) || (recv_src_idx && !aligned(recv_src_idx, 4)) ||
+            (x_scales && !aligned(x_scales, 4)))
+            return MOE_ERR_MISALIGNED;
+    }
+    moe::DispatchLaunch L;
+    L.x = x;
+    L.num_tokens = T;
+    L.hidden = H;
+    L.topk_idx = topk_idx;
+    L.topk_weights = topk_weights;
+    L.num_topk = num_topk;
+    L.num_experts = num_experts;
+    L.num_ranks = num_ranks;
+    L.token_dst_row = token_dst_row;
+    L.recv_capacity = recv_capacity;
+    L.quantize_fp8 = quantize_fp8;
+    L.recv_x = recv_x;
+    L.recv_x_scales = quantize_fp8 ? recv_x_scales : nullptr;
+    L.recv_topk_idx = recv_topk_idx;
+    L.recv_topk_weights = recv_topk_weights;
+    L.recv_src_idx = recv_src_idx;
+    L.x_scales = quantize_fp8 ? x_scales : nullptr;
+    L.status = status;
+    L.stream = stream;
+    return moe::launch_dispatch(L);
+}
+
+MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
+                        const int32_t *token_dst_row, void *out, int32_t *status, void *stream) {
+    const int T = num_tokens, H = hidden;
+    if (T < 0 || num_topk < 1 || num_topk > MOE_MAX_TOPK || num_partial_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0 || H > (1 << 24) || (int64_t)T * num_topk >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
+    if (!status) return MOE_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!token_dst_row || !out || (num_partial_rows > 0 && !partial)) return MOE_ERR_INVALID_ARG;
+        if ((partial && !aligned(partial, 16)) || !aligned(out, 16) || !aligned(token_dst_row, 4) ||
+            !aligned(status, 4))
+            return MOE_ERR_MISALIGNED;
+    }
+    moe::CombineLaunch L;
+    L.partial = partial;
+    L.num_partial_rows = num_partial_rows;
+    L.num_tokens = T;
+    L.hidden = H;
+    L.num_topk = num_topk;
+    L.token_dst_row = token_dst_row;
+    L.out = out;
+    L.status = status;
+    L.stream = stream;
+    return moe::launch_combine(L);
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// moe_internal.h -- host-side interfaces between the C ABI entry points
+// (moe_api.cu) and the kernel launchers (layout.cu, dispatch.cu, combine.cu).
+// Arguments reaching a launcher have already been validated.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe_get.h"
+
+namespace moe {
+
+// Per-device facts, queried once per device (thread-safe).
+int device_sm_count();             // SMs of the current device
+size_t device_smem_per_sm();       // shared memory per SM (bytes)
+size_t device_smem_optin();        // max dynamic shared memory per block (bytes)
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` (cached).
+int ensure_dynamic_smem(const void *kernel, size_t bytes);
+
+// Tuning knobs, read once from MOE_TUNE_* environment variables (0 = default).
+struct Tuning {
+    int dispatch_warps, dispatch_stages, dispatch_chunk;
+    int combine_warps, combine_stages, combine_stage_bytes;
+    int ctas_per_sm;
+    int l2_hints;  // bit 0: evict-first on single-use loads; bit 1: evict-first on stores
+};
+const Tuning &tuning();
+
+struct LayoutLaunch {
+    const int64_t *topk_idx;
+    int num_tokens, num_topk, num_experts, num_ranks;
+    moe_layout_t out;
+    void *workspace;
+    int32_t *status;
+    void *stream;
+    int64_t timeout_ns;     // <= 0: default
+    int unpublished_tile;   // test hook, -1 = off
+};
+
+size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
+int launch_layout(const LayoutLaunch &L);
+
+struct DispatchLaunch {
+    const void *x;
+    int num_tokens, hidden;
+    const int64_t *topk_idx;
+    const float *topk_weights;
+    int num_topk, num_experts, num_ranks;
+    const int32_t *token_dst_row;
+    int recv_capacity;
+    int quantize_fp8;
+    void *recv_x;
+    float *recv_x_scales;
+    int64_t *recv_topk_idx;
+    float *recv_topk_weights;
+    int32_t *recv_src_idx;
+    float *x_scales;
+    int32_t *status;
+    void *stream;
+};
+
+int launch_dispatch(const DispatchLaunch &L);
+
+struct CombineLaunch {
+    const void *partial;
+    int num_partial_rows, num_tokens, hidden, num_topk;
+    const int32_t *token_dst_row;
+    void *out;
+    int32_t *status;
+    void *stream;
+};
+
+int launch_combine(const CombineLaunch &L);
+
+}  // namespace moe

@@ -1,0 +1,209 @@
+/*
+ * moe_get.h -- C ABI of the single-GPU MoE layout / dispatch / combine library
+ * (libmoe_get.so, CUDA kernels for sm_103a).
+ *
+ * Expert parallelism on one GPU: the R "ranks" are logical destination
+ * partitions laid out one after another in one receive buffer in HBM.
+ * Nothing crosses GPUs.
+ *
+ * Notation (DeepEP V2 deep-dive page, "DeepEP V2 深度深潜", sections 2.2-3.5):
+ *   T = num_tokens, H = hidden, E = num_experts, R = num_ranks,
+ *   m = E / R experts per rank (E % R == 0), k = num_topk (1..32),
+ *   rank(e) = e / m for an expert e >= 0; a top-k entry of -1 is masked.
+ *   D_t = number of distinct ranks of token t; N = sum_t D_t received rows.
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers, row-major and contiguous,
+ *     allocated and owned by the caller. The library never allocates, frees or
+ *     synchronises; every call is asynchronous on `stream` (a cudaStream_t
+ *     passed as void*; NULL = the legacy default stream).
+ *   - The return value reports errors the host can see before launching:
+ *     MOE_ERR_INVALID_ARG (null pointer, size out of range), MOE_ERR_MISALIGNED
+ *     (a row pointer or row pitch not 16-byte aligned) or MOE_ERR_CUDA (a launch
+ *     failed). Nothing is launched when the return value is not MOE_OK.
+ *   - Errors that depend on the data are written by the kernels to the device
+ *     word `*status` (int32): the first error wins (compare-and-swap from 0),
+ *     later ones are dropped. The library never clears `*status`: zero it before
+ *     the first call whose errors you want to see, and read it after the stream
+ *     has synchronised. Data errors are MOE_ERR_BAD_TOPK (a top-k entry outside
+ *     [-1, E); that entry is treated as masked), MOE_ERR_CAPACITY (a receive row
+ *     at or beyond the receive capacity; that row is not written / not read) and
+ *     MOE_ERR_TIMEOUT (a bounded wait inside a kernel ran out; the outputs of
+ *     that call are unspecified).
+ *   - T == 0 is a valid no-op that still writes zero counts and prefixes.
+ */
+#ifndef MOE_GET_H
+#define MOE_GET_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_MISALIGNED = 2,
+    MOE_ERR_CAPACITY = 3,
+    MOE_ERR_BAD_TOPK = 4,
+    MOE_ERR_TIMEOUT = 5,
+    MOE_ERR_CUDA = 6,
+    MOE_ERR_WORKSPACE = 7
+} moe_status_t;
+
+/* Limits checked on the host (MOE_ERR_INVALID_ARG beyond them). */
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_RANKS 1024
+#define MOE_MAX_EXPERTS 8192
+
+/* Outputs of moe_get_layout: all DEVICE pointers, caller-owned. */
+typedef struct {
+    int32_t *num_tokens_per_rank;   /* [R]    tokens received by each rank (each token once per rank) */
+    int32_t *num_tokens_per_expert; /* [E]    valid top-k entries naming each expert (one per entry)  */
+    uint8_t *is_token_in_rank;      /* [T, R] 1 if token t has at least one expert on rank r, else 0  */
+    int32_t *rank_prefix;           /* [R+1]  exclusive prefix of num_tokens_per_rank; [R] = N          */
+    int32_t *expert_prefix;         /* [E+1]  exclusive prefix of num_tokens_per_expert                 */
+    int32_t *token_dst_row;         /* [T, k] global receive row of (t, rank(topk_idx[t,j])) held by the
+                                               lowest entry j naming that rank, -1 for every other entry */
+} moe_layout_t;
+
+/* Bytes of device workspace moe_get_layout needs for these sizes (16-byte
+ * aligned pointer required). Host-only; never fails (0 for invalid sizes). */
+MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, int num_ranks);
+
+/*
+ * moe_get_layout -- routing counts, membership and receive positions.
+ *
+ * Page: notify warps of the dispatch kernel (section 3.3 stage 1): per valid
+ * top-k entry one count for its expert, and one count per rank after the
+ * entries of a token are de-duplicated by rank; then prefix sums giving the
+ * receive offsets (section 3.5, "prefix sum -> psum_num_recv_tokens"). The
+ * rank of an expert is expert / experts_per_rank (section 2.2).
+ *
+ * Receive order (the page assigns slots by atomicAdd, i.e. arrival order; this
+ * library fixes a deterministic order instead): rank r's rows occupy
+ * [rank_prefix[r], rank_prefix[r+1]) in ascending source-token order, so
+ *   token_dst_row[t, j] = rank_prefix[r] + #{t' < t : is_token_in_rank[t', r]}.
+ * The in-rank position is a column-wise exclusive scan over tokens, computed by
+ * a single-pass decoupled-lookback scan over tiles of tokens (the only
+ * inter-CTA wait of the library; bounded, MOE_ERR_TIMEOUT on expiry).
+ *
+ *   topk_idx   [T, k] int64, device. -1 = masked; other values outside [0, E)
+ *              raise MOE_ERR_BAD_TOPK and are treated as masked.
+ *   layout     output arrays (all must be non-null when T > 0; rank_prefix and
+ *              expert_prefix, num_tokens_per_* are always written).
+ *   workspace  device scratch of at least moe_get_layout_workspace_size()
+ *              bytes; contents need not be initialised (the call clears it with
+ *              cudaMemsetAsync on `stream`). Must not be shared by calls that
+ *              overlap on the GPU.
+ *   status     device int32, see conventions.
+ * Limits: 1 <= k <= 32, k <= E, 1 <= R <= 1024, E <= 8192, E % R == 0,
+ * T * k < 2^31, T * R < 2^40.
+ */
+MOE_API int moe_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                           int num_ranks, moe_layout_t layout, void *workspace, size_t workspace_bytes,
+                           int32_t *status, void *stream);
+
+/* Options of moe_get_layout_ex. */
+typedef struct {
+    /* Bound on each wait of the lookback scan, in nanoseconds of the GPU's
+     * global timer; <= 0 selects the default (1 s). On expiry the kernel writes
+     * MOE_ERR_TIMEOUT to *status and finishes without waiting further. */
+    int64_t wait_timeout_ns;
+    /* Failure-injection hook for tests: the tile of 128 tokens with this index
+     * never publishes its scan status, so that the tiles after it (and the
+     * final count step) run out of their bounded waits and report
+     * MOE_ERR_TIMEOUT. -1 = off (the only value for production use). */
+    int32_t test_unpublished_tile;
+} moe_layout_options_t;
+
+/*
+ * moe_get_layout_ex -- moe_get_layout with options (NULL = defaults).
+ * Same arguments, outputs and errors as moe_get_layout.
+ */
+MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                              int num_ranks, moe_layout_t layout, void *workspace, size_t workspace_bytes,
+                              int32_t *status, void *stream, const moe_layout_options_t *options);
+
+/*
+ * moe_dispatch -- copy each token once per distinct destination rank.
+ *
+ * Page: dispatch warps (section 3.3 stage 2) load a token's hidden row once
+ * and store it once per de-duplicated destination rank; the HBM model of
+ * section 1.3 (factor 2) counts one read per token and one write per rank.
+ * Receive rows hold, per row (section 3.4 TokenLayout, section 3.5 outputs):
+ *   recv_x[row]            = x[t]                      (bf16 mode), or
+ *   recv_x[row]            = e4m3(x[t] / scale) and
+ *   recv_x_scales[row, b]  = scale[t, b]               (FP8 mode, see below)
+ *   recv_src_idx[row]      = t
+ *   recv_topk_idx[row, j]  = topk_idx[t, j] - r*m if rank(topk_idx[t, j]) == r, else -1
+ *   recv_topk_weights[row, j] = topk_weights[t, j] if that entry is local, else 0
+ * where row = token_dst_row[t, j] >= 0 for the owning entry j and r its rank.
+ *
+ * FP8 mode (quantize_fp8 != 0; H % 128 == 0): per token and per block of 128
+ * channels, amax = max |x|, scale = amax / 448 (fp32, round to nearest),
+ * code = E4M3(x / scale) (IEEE fp32 division, round to nearest even,
+ * saturating to +-448); a block with amax == 0 has scale 0 and codes 0.
+ *
+ *   x                  [T, H] bf16, device, 16-byte aligned, H % 8 == 0.
+ *   topk_idx           [T, k] int64 (the same array given to moe_get_layout).
+ *   topk_weights       [T, k] fp32 or NULL (then recv_topk_weights may be NULL).
+ *   token_dst_row      [T, k] int32 from moe_get_layout.
+ *   recv_capacity      rows available in the receive arrays; rows >= capacity
+ *                      raise MOE_ERR_CAPACITY and are skipped. N <= T*min(k, R).
+ *   recv_x             [capacity, H] bf16, or [capacity, H] uint8 E4M3 in FP8 mode.
+ *   recv_x_scales      [capacity, H/128] fp32 (FP8 mode only, else ignored).
+ *   recv_topk_idx      [capacity, k] int64, may be NULL (not written).
+ *   recv_topk_weights  [capacity, k] fp32, may be NULL.
+ *   recv_src_idx       [capacity] int32, may be NULL.
+ *   x_scales           [T, H/128] fp32 source-side scales (FP8 mode), may be NULL.
+ */
+MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                         const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                         const int32_t *token_dst_row, int recv_capacity, int quantize_fp8,
+                         void *recv_x, float *recv_x_scales, int64_t *recv_topk_idx,
+                         float *recv_topk_weights, int32_t *recv_src_idx, float *x_scales,
+                         int32_t *status, void *stream);
+
+/*
+ * moe_combine -- gather the per-rank partial rows of each token back into
+ * token order and reduce them.
+ *
+ * Page: the expert side writes one partial row per (token, rank) into the
+ * owner's combine buffer and an epilogue reduces them (Mega-MoE combine push
+ * on the DeepEP/DeepGEMM comparison page; "consume ready partial rows in the
+ * reduce epilogue" on the Ascend send-ordering page). Reduction order:
+ *   out[t] = bf16_rn( sum over the rows of t in ascending rank order of
+ *                     float(partial[row]) ), accumulated in fp32 from +0.0f,
+ * ascending rank being ascending row because rank regions are in rank order.
+ * A token with no rows gets +0. No weights are applied (the expert stage
+ * applies them).
+ *
+ *   partial          [num_partial_rows, H] bf16, device, 16-byte aligned, H % 8 == 0.
+ *   token_dst_row    [T, k] int32 from moe_get_layout; rows >= num_partial_rows
+ *                    raise MOE_ERR_CAPACITY and are skipped.
+ *   out              [T, H] bf16, device, 16-byte aligned.
+ */
+MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_tokens, int hidden,
+                        int num_topk, const int32_t *token_dst_row, void *out, int32_t *status,
+                        void *stream);
+
+/* Human-readable name of a moe_status_t value (static string). */
+MOE_API const char *moe_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+MOE_API int moe_get_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GET_H */

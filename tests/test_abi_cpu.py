@@ -1,0 +1,124 @@
+"""The C-ABI library builds, loads, exports every symbol its header declares,
+and rejects bad arguments on the host before touching CUDA (so these run on a
+machine without a GPU; every call below fails validation by design)."""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from combine_moe_get_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = cuda_build.build()
+    from combine_moe_get_gb300 import binding
+    assert binding.library_path() == path
+    return binding
+
+
+def _declared_symbols():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = "\n".join(line for line in text.splitlines() if not line.lstrip().startswith("#"))
+        names += re.findall(r"MOE_API\s+[^;{]*?\b(\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_entry_points():
+    names = _declared_symbols()
+    for required in ("moe_get_layout", "moe_dispatch", "moe_combine", "moe_get_layout_workspace_size"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib.library_path())
+    for name in _declared_symbols():
+        assert hasattr(raw, name), f"{name} declared in include/ but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.LIB.moe_get_version() >= 100
+    for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (2, "MOE_ERR_MISALIGNED"),
+                       (3, "MOE_ERR_CAPACITY"), (4, "MOE_ERR_BAD_TOPK"), (5, "MOE_ERR_TIMEOUT"),
+                       (6, "MOE_ERR_CUDA"), (7, "MOE_ERR_WORKSPACE")]:
+        assert lib.status_string(code) == name
+    assert lib.status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    ws = lib.moe_get_layout_workspace_size
+    assert ws(4096, 256, 8) > 0
+    assert ws(0, 256, 8) > 0
+    assert ws(1 << 20, 2048, 256) >= (1 << 20) // 128 * 256 * 8
+    assert ws(4096, 255, 8) == 0          # E % R != 0
+    assert ws(4096, 256, 2048) == 0       # too many ranks
+    assert ws(-1, 256, 8) == 0
+
+
+# Fake device addresses: validation rejects the call before any is dereferenced.
+A = 0x7F0000000000          # 256-byte aligned
+MIS = A + 2                 # misaligned for anything wider than 2 bytes
+
+
+def _layout_struct(lib, base=A):
+    return lib.MoeLayoutC(base, base + 0x1000, base + 0x2000, base + 0x3000, base + 0x4000, base + 0x5000)
+
+
+def _layout(lib, T=128, k=2, E=16, R=4, topk=A, ws=A + 0x100000, ws_bytes=1 << 30, status=A + 0x200000, lay=None):
+    return lib.LIB.moe_get_layout(topk, T, k, E, R, lay or _layout_struct(lib), ws, ws_bytes, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=0), 1), (dict(k=33), 1), (dict(E=15), 1), (dict(R=0), 1), (dict(R=2048, E=2048), 1),
+    (dict(E=16384, R=4), 1), (dict(T=-1), 1), (dict(status=None), 1), (dict(topk=None), 1),
+    (dict(ws=None), 1), (dict(topk=MIS), 2), (dict(ws=MIS), 2), (dict(status=MIS), 2),
+    (dict(ws_bytes=16), 7),
+])
+def test_layout_rejects_bad_arguments(lib, kw, code):
+    assert _layout(lib, **kw) == code
+
+
+def test_layout_rejects_null_or_misaligned_outputs(lib):
+    s = _layout_struct(lib)
+    s.token_dst_row = None
+    assert _layout(lib, lay=s) == 1
+    s = _layout_struct(lib)
+    s.rank_prefix = MIS
+    assert _layout(lib, lay=s) == 2
+
+
+def _dispatch(lib, x=A, T=128, H=256, topk=A + 0x10000, w=None, k=2, E=16, R=4, dst=A + 0x20000, cap=256,
+              fp8=0, recv=A + 0x100000, scales=None, status=A + 0x300000):
+    return lib.LIB.moe_dispatch(x, T, H, topk, w, k, E, R, dst, cap, fp8, recv, scales, None, None, None, None,
+                                status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=12), 1), (dict(H=0), 1), (dict(fp8=1, H=264, scales=A + 0x400000), 1), (dict(fp8=1), 1),
+    (dict(k=40), 1), (dict(E=17), 1), (dict(cap=-1), 1), (dict(x=None), 1), (dict(recv=None), 1),
+    (dict(status=None), 1), (dict(x=A + 8), 2), (dict(recv=A + 8), 2), (dict(dst=MIS), 2),
+])
+def test_dispatch_rejects_bad_arguments(lib, kw, code):
+    assert _dispatch(lib, **kw) == code
+
+
+def _combine(lib, partial=A, rows=256, T=128, H=256, k=2, dst=A + 0x10000, out=A + 0x100000, status=A + 0x200000):
+    return lib.LIB.moe_combine(partial, rows, T, H, k, dst, out, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=4), 1), (dict(k=0), 1), (dict(rows=-1), 1), (dict(T=-5), 1), (dict(out=None), 1),
+    (dict(partial=None), 1), (dict(dst=None), 1), (dict(status=None), 1), (dict(partial=A + 4), 2),
+    (dict(out=A + 8), 2),
+])
+def test_combine_rejects_bad_arguments(lib, kw, code):
+    assert _combine(lib, **kw) == code

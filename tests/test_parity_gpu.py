@@ -1,0 +1,324 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact for layout outputs, receive rows (bf16 bits, E4M3 codes, fp32
+scales) and metadata; combine within 1e-2 relative / 1e-3 absolute, and
+additionally bit-exact, since both sides add the same fp32 values in the same
+(ascending-rank) order and round once. Full configuration sizes, ragged token
+counts across tile and chunk boundaries, masked / invalid routing, capacity
+overflow, maximum sizes, determinism and the bounded-wait failure path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_get_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+POISON_BF16 = 0x7FBF          # a NaN pattern no kernel writes on purpose
+LAYOUT_KEYS = ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "rank_prefix",
+               "expert_prefix", "token_dst_row")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from combine_moe_get_gb300 import binding
+    return binding
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def gpu_layout(moe, topk_cpu, E, R, **kw):
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk_cpu.to(DEV), E, R, status=status, **kw)
+    torch.cuda.synchronize()
+    out = {k: getattr(lay, k).cpu().numpy() for k in LAYOUT_KEYS}
+    return lay, out, int(status.item())
+
+
+def assert_layout_equal(got, ref):
+    for key in LAYOUT_KEYS:
+        np.testing.assert_array_equal(got[key], ref[key], err_msg=key)
+
+
+def topk_for(w: wl.Workload, T=None):
+    return wl.make_inputs(w, with_partial=False, num_tokens=T).topk_idx
+
+
+# ------------------------------------------------------------------ layout
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode", "layout_2048", "layout_2048_1m"])
+def test_layout_parity_configs(moe, name):
+    w = wl.CONFIGS[name]
+    topk = topk_for(w)
+    _, got, st = gpu_layout(moe, topk, w.num_experts, w.num_ranks)
+    ref = oracle.layout(topk.numpy(), w.num_experts, w.num_ranks)
+    assert st == 0 and ref["flags"] == 0
+    assert_layout_equal(got, ref)
+
+
+SHAPES = [  # (T, k, E, R)
+    (1, 2, 16, 4), (31, 2, 16, 4), (32, 8, 256, 8), (33, 8, 256, 8), (127, 8, 256, 256), (128, 8, 256, 64),
+    (129, 8, 256, 8), (1000, 6, 48, 3), (257, 1, 8, 1), (300, 32, 64, 8), (513, 5, 20, 5), (4097, 8, 256, 8),
+    (200, 32, 8192, 1024), (130, 3, 7, 7),
+]
+
+
+@pytest.mark.parametrize("T,k,E,R", SHAPES)
+@pytest.mark.parametrize("mask", [0.0, 0.3])
+def test_layout_parity_shapes(moe, T, k, E, R, mask):
+    g = torch.Generator().manual_seed(T * 131 + k * 7 + R)
+    topk = wl.make_topk_uniform(g, T, E, min(k, E)) if k <= E else None
+    if mask:
+        topk = wl.mask_random_lanes(g, topk, mask)
+    _, got, st = gpu_layout(moe, topk, E, R)
+    ref = oracle.layout(topk.numpy(), E, R)
+    assert st == 0
+    assert_layout_equal(got, ref)
+
+
+def test_layout_duplicates_all_masked_and_bad_entries(moe):
+    g = torch.Generator().manual_seed(5)
+    T, k, E, R = 700, 8, 64, 8
+    topk = torch.randint(0, E, (T, k), generator=g)          # with duplicates inside rows
+    topk[::7] = -1                                            # all-masked tokens
+    topk[3, 2] = E + 5                                        # invalid entries
+    topk[400, 0] = -9
+    _, got, st = gpu_layout(moe, topk, E, R)
+    ref = oracle.layout(topk.numpy(), E, R)
+    assert ref["flags"] & oracle.ORACLE_BAD_TOPK
+    assert st == moe.MOE_ERR_BAD_TOPK
+    assert_layout_equal(got, ref)
+
+
+def test_layout_empty(moe):
+    topk = torch.zeros(0, 8, dtype=torch.int64)
+    lay, got, st = gpu_layout(moe, topk, 256, 8)
+    assert st == 0
+    for key in ("num_tokens_per_rank", "num_tokens_per_expert", "rank_prefix", "expert_prefix"):
+        assert np.all(got[key] == 0), key
+
+
+def test_layout_deterministic_and_reuses_workspace(moe):
+    w = wl.CONFIGS["skewed"]
+    topk = topk_for(w).to(DEV)
+    ws = torch.empty(moe.moe_get_layout_workspace_size(w.num_tokens, w.num_experts, w.num_ranks),
+                     dtype=torch.uint8, device=DEV)
+    outs = []
+    for _ in range(3):
+        ws.fill_(0xAB)   # the call must clear its own workspace
+        status = moe.new_status(DEV)
+        lay = moe.moe_get_layout(topk, w.num_experts, w.num_ranks, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append({k: getattr(lay, k).cpu().numpy() for k in LAYOUT_KEYS})
+    for o in outs[1:]:
+        assert_layout_equal(o, outs[0])
+
+
+def test_layout_bounded_wait_reports_timeout(moe):
+    # one tile never publishes its scan status: the tiles after it give up after
+    # the bounded wait and report MOE_ERR_TIMEOUT; the context stays usable
+    T, k, E, R = 1024, 8, 256, 8
+    topk = wl.make_topk_uniform(torch.Generator().manual_seed(1), T, E, k)
+    _, _, st = gpu_layout(moe, topk, E, R, wait_timeout_ns=20_000_000, test_unpublished_tile=2)
+    assert st == moe.MOE_ERR_TIMEOUT
+    # last tile unpublished: nobody waits on it, the count step must still notice
+    _, _, st = gpu_layout(moe, topk, E, R, wait_timeout_ns=20_000_000, test_unpublished_tile=7)
+    assert st == moe.MOE_ERR_TIMEOUT
+    _, got, st = gpu_layout(moe, topk, E, R)
+    assert st == 0
+    assert_layout_equal(got, oracle.layout(topk.numpy(), E, R))
+
+
+# ------------------------------------------------------------------ dispatch
+
+def run_dispatch(moe, inp, E, R, fp8, cap=None, guard=0, weights=True):
+    T, H = inp.x.shape
+    k = inp.topk_idx.shape[1]
+    cap = wl.recv_capacity(T, k, R) if cap is None else cap
+    topk = inp.topk_idx.to(DEV)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk, E, R, status=status)
+    rows = cap + guard
+    out = moe.Dispatched(
+        recv_x=(torch.full((rows, H), 0xEE, dtype=torch.uint8, device=DEV) if fp8 else
+                torch.full((rows, H), POISON_BF16, dtype=torch.int16, device=DEV).view(torch.bfloat16)),
+        recv_x_scales=torch.full((rows, H // 128), -1.0, device=DEV) if fp8 else None,
+        recv_topk_idx=torch.full((rows, k), -7, dtype=torch.int64, device=DEV),
+        recv_topk_weights=torch.full((rows, k), -7.0, device=DEV),
+        recv_src_idx=torch.full((rows,), -7, dtype=torch.int32, device=DEV),
+        x_scales=torch.full((T, H // 128), -1.0, device=DEV) if fp8 else None)
+    w = inp.topk_weights.to(DEV) if weights else None
+    moe.moe_dispatch(inp.x.to(DEV), topk, w, E, R, lay.token_dst_row, cap, quantize_fp8=fp8, out=out, status=status)
+    torch.cuda.synchronize()
+    return lay, out, int(status.item())
+
+
+def check_dispatch(moe, inp, E, R, fp8, weights=True):
+    lay, out, st = run_dispatch(moe, inp, E, R, fp8, weights=weights)
+    assert st == 0
+    topk = inp.topk_idx.numpy()
+    ref_lay = oracle.layout(topk, E, R)
+    N = ref_lay["num_recv"]
+    cap = out.recv_x.shape[0]
+    ref = oracle.dispatch(bits16(inp.x), topk, inp.topk_weights.numpy() if weights else None, E, R,
+                          ref_lay["token_dst_row"], N, fp8=fp8)
+    assert int(lay.rank_prefix[-1].item()) == N
+    if fp8:
+        np.testing.assert_array_equal(out.recv_x[:N].cpu().numpy(), ref["recv_x"])
+        np.testing.assert_array_equal(out.recv_x_scales[:N].cpu().numpy().view(np.uint32),
+                                      ref["recv_x_scales"].view(np.uint32))
+        np.testing.assert_array_equal(out.x_scales.cpu().numpy().view(np.uint32), ref["x_scales"].view(np.uint32))
+        assert np.all(out.recv_x[N:].cpu().numpy() == 0xEE)
+    else:
+        np.testing.assert_array_equal(bits16(out.recv_x[:N]), ref["recv_x"])
+        assert np.all(bits16(out.recv_x[N:]) == POISON_BF16)
+    np.testing.assert_array_equal(out.recv_src_idx[:N].cpu().numpy(), ref["recv_src_idx"])
+    np.testing.assert_array_equal(out.recv_topk_idx[:N].cpu().numpy(), ref["recv_topk_idx"])
+    np.testing.assert_array_equal(out.recv_topk_weights[:N].cpu().numpy().view(np.uint32),
+                                  ref["recv_topk_weights"].view(np.uint32))
+    assert np.all(out.recv_src_idx[N:cap].cpu().numpy() == -7)
+
+
+@pytest.mark.parametrize("name,fp8", [("tiny", False), ("tiny", True), ("dsv3", False), ("dsv3_fp8", True),
+                                      ("skewed", False), ("skewed", True), ("decode", False), ("decode", True)])
+def test_dispatch_parity_configs(moe, name, fp8):
+    w = wl.CONFIGS[name]
+    inp = wl.make_inputs(w, with_partial=False)
+    check_dispatch(moe, inp, w.num_experts, w.num_ranks, fp8)
+
+
+DISPATCH_SHAPES = [  # (T, H, k, E, R)
+    (1, 128, 2, 16, 4), (33, 7168, 8, 256, 8), (129, 384, 8, 256, 256), (1000, 1024, 6, 48, 3),
+    (77, 8, 2, 16, 4), (300, 4096, 32, 64, 8), (513, 7040, 5, 20, 5), (64, 16384, 8, 256, 8),
+    (250, 7160, 8, 256, 64),
+]
+
+
+@pytest.mark.parametrize("T,H,k,E,R", DISPATCH_SHAPES)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_dispatch_parity_shapes(moe, T, H, k, E, R, fp8):
+    if fp8 and H % 128:
+        pytest.skip("FP8 needs H % 128 == 0")
+    g = torch.Generator().manual_seed(T + H + k)
+    x = wl.make_x(g, T, H)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
+    inp = wl.Inputs(None, x, topk, wl.make_weights(g, T, k), None)
+    check_dispatch(moe, inp, E, R, fp8, weights=(T % 2 == 0))
+
+
+def test_dispatch_fp8_special_blocks(moe):
+    # zero blocks (scale 0, codes 0), tiny values (E4M3 subnormals), exact ties, large magnitudes
+    T, H, E, R, k = 8, 1024, 16, 4, 2
+    x = torch.zeros(T, H)
+    x[1] = torch.linspace(-3e-3, 3e-3, H)
+    x[2, :128] = 1.0
+    x[2, 128:256] = torch.tensor([448.0 * (i + 1) / 128 for i in range(128)])
+    x[3] = torch.randn(H, generator=torch.Generator().manual_seed(0)) * 1e4
+    x[4, ::2] = -2.0 ** -20
+    x[5] = torch.arange(H) % 17 - 8.0
+    inp = wl.Inputs(None, x.to(torch.bfloat16), torch.tensor([[0, 5], [1, 2], [3, 15], [8, 9], [0, 12],
+                                                                [4, 7], [-1, -1], [11, 10]]),
+                    torch.full((T, k), 0.5), None)
+    check_dispatch(moe, inp, E, R, True)
+
+
+def test_dispatch_capacity_overflow_writes_nothing_beyond(moe):
+    w = wl.CONFIGS["tiny"]
+    inp = wl.make_inputs(w, with_partial=False)
+    ref = oracle.layout(inp.topk_idx.numpy(), w.num_experts, w.num_ranks)
+    N = ref["num_recv"]
+    cap, guard = N - 9, 16
+    lay, out, st = run_dispatch(moe, inp, w.num_experts, w.num_ranks, False, cap=cap, guard=guard)
+    assert st == moe.MOE_ERR_CAPACITY
+    assert np.all(bits16(out.recv_x[cap:]) == POISON_BF16)
+    assert np.all(out.recv_src_idx[cap:].cpu().numpy() == -7)
+    d = oracle.dispatch(bits16(inp.x), inp.topk_idx.numpy(), inp.topk_weights.numpy(), w.num_experts, w.num_ranks,
+                        ref["token_dst_row"], cap)
+    np.testing.assert_array_equal(bits16(out.recv_x[:cap]), d["recv_x"])
+
+
+def test_dispatch_deterministic(moe):
+    w = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(w, with_partial=False, num_tokens=1024)
+    a = run_dispatch(moe, inp, w.num_experts, w.num_ranks, True)[1]
+    b = run_dispatch(moe, inp, w.num_experts, w.num_ranks, True)[1]
+    assert torch.equal(a.recv_x, b.recv_x) and torch.equal(a.recv_x_scales, b.recv_x_scales)
+
+
+# ------------------------------------------------------------------ combine
+
+def check_combine(moe, topk, partial, E, R):
+    topk_d = topk.to(DEV)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk_d, E, R, status=status)
+    out = moe.moe_combine(partial.to(DEV), lay.token_dst_row, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_lay = oracle.layout(topk.numpy(), E, R)
+    ref, flags = oracle.combine(bits16(partial), ref_lay["token_dst_row"])
+    assert flags == 0
+    got = bits16(out)
+    # the stated gate: 1e-2 relative / 1e-3 absolute in bf16
+    g32 = (got.astype(np.uint32) << 16).view(np.float32)
+    r32 = (ref.astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_allclose(g32, r32, rtol=1e-2, atol=1e-3)
+    # and the stronger one: same fp32 additions in the same order, one rounding
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode"])
+def test_combine_parity_configs(moe, name):
+    w = wl.CONFIGS[name]
+    inp = wl.make_inputs(w)
+    check_combine(moe, inp.topk_idx, inp.partial, w.num_experts, w.num_ranks)
+
+
+@pytest.mark.parametrize("T,H,k,E,R", DISPATCH_SHAPES)
+def test_combine_parity_shapes(moe, T, H, k, E, R):
+    g = torch.Generator().manual_seed(7 * T + H)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
+    partial = wl.make_partial(g, wl.recv_capacity(T, k, R), H)
+    check_combine(moe, topk, partial, E, R)
+
+
+def test_combine_partial_rows_short_reports_capacity(moe):
+    w = wl.CONFIGS["tiny"]
+    inp = wl.make_inputs(w)
+    topk = inp.topk_idx.to(DEV)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk, w.num_experts, w.num_ranks, status=status)
+    N = int(lay.rank_prefix[-1].item())
+    moe.moe_combine(inp.partial[: N - 3].to(DEV), lay.token_dst_row, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == moe.MOE_ERR_CAPACITY
+
+
+# ------------------------------------------------------------------ composite
+
+def test_dispatch_then_combine_identity_expert(moe):
+    # expert = identity times the row's local weights; weights sum to 1, so combine
+    # gives x back within two bf16 roundings; and with partial = recv_x, D_t * x_t exactly
+    w = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(w, with_partial=False, num_tokens=2048)
+    lay, out, st = run_dispatch(moe, inp, w.num_experts, w.num_ranks, False)
+    assert st == 0
+    N = int(lay.rank_prefix[-1].item())
+    rx = out.recv_x[:N]
+    partial = (rx.float() * out.recv_topk_weights[:N].sum(dim=1, keepdim=True)).to(torch.bfloat16)
+    status = moe.new_status(DEV)
+    y = moe.moe_combine(partial, lay.token_dst_row, status=status).float().cpu()
+    x = inp.x.float()
+    assert torch.all((y - x).abs() <= 2.0 ** -7 * x.abs() * 1.01)
+    y2 = moe.moe_combine(rx, lay.token_dst_row, status=status).cpu()
+    D = lay.is_token_in_rank.sum(dim=1).float().cpu()
+    assert torch.equal(y2.view(torch.int16), (x * D[:, None]).to(torch.bfloat16).view(torch.int16))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
