@@ -28,6 +28,7 @@
 // Kernel 2 adds rank_prefix[r] to each owned in-rank position.
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "moe_common.cuh"
@@ -345,3 +346,85 @@ int launch_layout(const LayoutLaunch &L) {
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------------ layout without caller workspace
+//
+// moe_get_layout_noalloc serves callers that cannot allocate device memory
+// themselves -- for example a plugin inside a host framework that owns every
+// device allocation and hands out no workspace, or a latency-critical loop in
+// which a cudaMalloc (which may synchronise the device) is not acceptable.
+// Its lookback scratch is this file-scope device array, which every GPU that
+// loads the library holds until the process exits. Host code cannot use the
+// array's name as a device address (on the host it names a stand-in object),
+// so the device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, on the first call made on
+// that device; that first call should therefore come before any stream
+// capture. All calls share the array and it keeps the previous call's
+// contents: each call clears the part it uses (cudaMemsetAsync on its
+// stream), and calls whose executions overlap on the GPU race on it.
+namespace moe {
+namespace {
+
+static __device__ __align__(256) uint8_t g_layout_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+void *noalloc_scratch_address(int *err) {
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = MOE_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_layout_scratch) != cudaSuccess || p == nullptr) {
+            *err = MOE_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+extern "C" MOE_API int moe_get_layout_noalloc(const int64_t *topk_idx, int num_tokens, int num_topk,
+                                              int num_experts, int num_ranks, moe_layout_t layout,
+                                              int32_t *status, void *stream) {
+    const int T = num_tokens, k = num_topk, E = num_experts, R = num_ranks;
+    if (T < 0 || k < 1 || k > MOE_MAX_TOPK || R < 1 || R > MOE_MAX_RANKS || E < 1 || E > MOE_MAX_EXPERTS ||
+        E % R != 0 || (int64_t)T * k >= ((int64_t)1 << 31) || (int64_t)T * R >= ((int64_t)1 << 40))
+        return MOE_ERR_INVALID_ARG;
+    if (!status || !layout.num_tokens_per_rank || !layout.num_tokens_per_expert || !layout.rank_prefix ||
+        !layout.expert_prefix)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !layout.is_token_in_rank || !layout.token_dst_row)) return MOE_ERR_INVALID_ARG;
+    if (!moe::is_aligned(status, 4) || !moe::is_aligned(layout.num_tokens_per_rank, 4) ||
+        !moe::is_aligned(layout.num_tokens_per_expert, 4) || !moe::is_aligned(layout.rank_prefix, 4) ||
+        !moe::is_aligned(layout.expert_prefix, 4))
+        return MOE_ERR_MISALIGNED;
+    if (T > 0 && (!moe::is_aligned(topk_idx, 8) || !moe::is_aligned(layout.token_dst_row, 4) ||
+                  !moe::is_aligned(layout.is_token_in_rank, 4)))
+        return MOE_ERR_MISALIGNED;
+    if (moe::layout_workspace_bytes(T, E, R) > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
+    int err = MOE_OK;
+    void *scratch = moe::noalloc_scratch_address(&err);
+    if (scratch == nullptr) return err;
+    moe::LayoutLaunch L;
+    L.topk_idx = topk_idx;
+    L.num_tokens = T;
+    L.num_topk = k;
+    L.num_experts = E;
+    L.num_ranks = R;
+    L.out = layout;
+    L.workspace = scratch;
+    L.status = status;
+    L.stream = stream;
+    L.timeout_ns = 0;
+    L.unpublished_tile = -1;
+    return moe::launch_layout(L);
+}

@@ -105,7 +105,7 @@ MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, in
  *              cudaMemsetAsync on `stream`). Must not be shared by calls that
  *              overlap on the GPU.
  *   status     device int32, see conventions.
- * Limits: 1 <= k <= 32, k <= E, 1 <= R <= 1024, E <= 8192, E % R == 0,
+ * Limits: 1 <= k <= 32, 1 <= R <= 1024, E <= 8192, E % R == 0,
  * T * k < 2^31, T * R < 2^40.
  */
 MOE_API int moe_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
@@ -195,6 +195,35 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
 MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_tokens, int hidden,
                         int num_topk, const int32_t *token_dst_row, void *out, int32_t *status,
                         void *stream);
+
+/* Size of the library's own layout scratch (bytes), used by moe_get_layout_noalloc. */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * moe_get_layout_noalloc -- moe_get_layout for callers that cannot allocate
+ * device memory (the pages have no counterpart; this is a library addition).
+ *
+ * Some callers cannot call cudaMalloc: a plugin running inside a host
+ * framework that owns every device allocation and hands out no workspace, or
+ * a latency-critical loop where an allocation (which may synchronise the
+ * device) is not acceptable. This entry point takes the same inputs and
+ * outputs as moe_get_layout but no workspace: it uses a scratch array of
+ * MOE_NOALLOC_SCRATCH_BYTES that the library keeps in device memory (held by
+ * every GPU that loads the library until the process exits). It allocates
+ * nothing and calls no allocating routine.
+ *
+ *   - The first call on a device looks up the scratch's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Sizes whose workspace (moe_get_layout_workspace_size) exceeds
+ *     MOE_NOALLOC_SCRATCH_BYTES return MOE_ERR_WORKSPACE and launch nothing.
+ *   - Every call shares the one scratch array, which keeps the previous
+ *     call's contents; each call clears what it uses on its own stream.
+ *     Calls whose executions overlap on the GPU (e.g. on two streams without
+ *     ordering between them) race on the scratch and give wrong results.
+ * Outputs, status word and errors are as for moe_get_layout.
+ */
+MOE_API int moe_get_layout_noalloc(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                                   int num_ranks, moe_layout_t layout, int32_t *status, void *stream);
 
 /* Human-readable name of a moe_status_t value (static string). */
 MOE_API const char *moe_status_string(int status);
