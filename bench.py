@@ -230,16 +230,16 @@ def run_ours(args, world, rank, local):
 
     def one(events=None):
         if events:
-            events[0].record(stream)
+            events[0].record()
         st.layout()
         if events:
-            events[1].record(stream)
+            events[1].record()
         st.dispatch()
         if events:
-            events[2].record(stream)
+            events[2].record()
         st.combine()
         if events:
-            events[3].record(stream)
+            events[3].record()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -248,34 +248,71 @@ def run_ours(args, world, rank, local):
     moe.check_status(st.status, "warm-up")
     N = int(st.lay.rank_prefix[-1].item())
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # The step is captured once in a CUDA graph (after warm-up: no allocation or
+    # attribute setting happens during capture) and replayed, so host-side
+    # submission cost never leaves the GPU idle inside the timed events.
+    timing = "cuda-graph replay"
+    try:
+        evs_g = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one(evs_g)
+        graph.replay()
+        torch.cuda.synchronize()
+    except Exception as exc:  # eager fallback (e.g. no external events in this torch)
+        graph, timing = None, f"eager ({type(exc).__name__})"
+
+    times = []
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(device.index) as clk:
         for i in range(args.steps):
             flush.zero_()                       # L2 flush between steps, outside the events
-            one(evs[i])
+            if graph is not None:
+                graph.replay()
+                torch.cuda.synchronize()
+                times.append([evs_g[0].elapsed_time(evs_g[j]) for j in (1, 2, 3)] +
+                             [evs_g[j].elapsed_time(evs_g[j + 1]) for j in (0, 1, 2)])
+            else:
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                one(ev)
+                torch.cuda.synchronize()
+                times.append([ev[0].elapsed_time(ev[j]) for j in (1, 2, 3)] +
+                             [ev[j].elapsed_time(ev[j + 1]) for j in (0, 1, 2)])
         torch.cuda.synchronize()
     barrier(world)
     moe.check_status(st.status, "timed steps")
     clocks = clk.summary()
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    lay_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dis_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    com_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [t[2] for t in times]
+    lay_ms = [t[3] for t in times]
+    dis_ms = [t[4] for t in times]
+    com_ms = [t[5] for t in times]
     mean = statistics.fmean
     ms_per_step = max_over_ranks(mean(step_ms), world, device)
     tokens_per_s = world * T / (ms_per_step / 1e3)
 
     # FP8 dispatch (fused quantisation), timed alone with the same flush discipline
     fp8_ms = []
+    a = torch.cuda.Event(enable_timing=True, external=graph is not None)
+    b = torch.cuda.Event(enable_timing=True, external=graph is not None)
+    st.dispatch(fp8=True)                       # first call outside any capture
+    torch.cuda.synchronize()
+    g8 = None
+    if graph is not None:
+        g8 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g8):
+            a.record()
+            st.dispatch(fp8=True)
+            b.record()
     for i in range(max(3, args.steps // 2) + 2):
         flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        st.dispatch(fp8=True)
-        b.record(stream)
+        if g8 is not None:
+            g8.replay()
+        else:
+            a.record(stream)
+            st.dispatch(fp8=True)
+            b.record(stream)
         torch.cuda.synchronize()
         if i >= 2:
             fp8_ms.append(a.elapsed_time(b))
@@ -311,7 +348,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": "DeepSeek-V3 prefill shape: T=4096, H=7168 bf16, E=256 over R=8 logical ranks, "
                                "top-8 uniform, softmax weights", "tokens": T, "hidden": H,
                    "experts": w.num_experts, "ranks": w.num_ranks, "topk": w.num_topk, "recv_rows": N,
-                   "step": "layout + dispatch(bf16) + combine", "l2": f"flushed between steps ({flush.numel() >> 20} MiB memset, untimed)",
+                   "step": "layout + dispatch(bf16) + combine", "timing": timing, "l2": f"flushed between steps ({flush.numel() >> 20} MiB memset, untimed)",
                    "parallelism": f"replicas x{world} (independent token shards, no collective)"},
         "roofline": {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
@@ -402,7 +439,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -9,13 +9,27 @@
 // (ascending row, since rank regions are laid out in rank order), then one
 // round-to-nearest-even cast to bf16.
 //
-// GB300 design: persistent grid, one independent pipeline per warp. A unit is
-// one chunk of one token's output row. For a unit, the lanes holding the
-// token's receive rows sort them (rank among valid rows), lane 0 arms the
-// stage's mbarrier with D * chunk bytes, and each of those lanes issues one
-// cp.async.bulk of its row's chunk into slot `rank` of the stage. S-1 units
-// stay in flight while the warp sums the landed stage slot by slot (16-byte
-// shared loads, conflict-free) and writes 16-byte bf16 vectors to `out`.
+// GB300 design. Combine moves ~85% of its bytes as loads that must sit in
+// shared memory until they are summed. Each SM's bulk-copy (TMA) engine keeps
+// a bounded number of copies in flight, so the bytes in flight -- and the
+// bandwidth -- grow with the size of each copy: whole rows (14 KB at H=7168)
+// are copied at once. One CTA per SM owns a ring of chunk-sized slots
+// (~220 KB) and a contiguous range of tokens; a unit is one chunk (by default
+// a whole row) of one token.
+//   producer warp  reads a token's receive rows, ranks them (ascending), takes
+//                  D free slots from the ring (D = the token's row count, not
+//                  k, so no slot is reserved for an absent row), arms the
+//                  unit's mbarrier with D * chunk bytes and issues one
+//                  cp.async.bulk per row into the slots. Slots come back in
+//                  unit order through per-unit "empty" mbarriers.
+//   consumer warps take (unit, slice) items round-robin, a slice being a
+//                  <= 4 KB column range of the chunk, wait on the unit's
+//                  "full" mbarrier, and sum slot by slot with all of the
+//                  lane's vectors in flight at once (up to 8 x 16 B per lane,
+//                  packed add.rn.f32x2: 32 independent fp32-pair chains per
+//                  lane), store 16-byte bf16 vectors and arrive on the unit's
+//                  "empty" mbarrier (one arrival per slice).
+// Every wait is bounded (MOE_ERR_TIMEOUT on expiry).
 #include <algorithm>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -28,129 +42,202 @@ namespace moe {
 
 namespace {
 
-constexpr int kMaxStages = 8;
-constexpr int kHeadBytes = 128;   // mbarriers [kMaxStages] + row counts [kMaxStages]
+constexpr int kUnits = 16;       // unit ring entries
+constexpr int kVMax = 8;         // 16-byte vectors per lane per slice -> slice <= 32 * 8 * 16 = 4096 B
+constexpr int kHeadBytes = 512;  // full[kUnits] + empty[kUnits] mbarriers, unit entries
 constexpr unsigned kFull = 0xffffffffu;
 
 struct CombineArgs {
     const uint8_t *partial;
     int64_t row_bytes;   // H * 2
     int num_rows;
-    int k;
+    int T, k;
     const int32_t *dst_row;
     uint8_t *out;
     int32_t *status;
     int chunk_bytes, num_chunks;
-    int64_t num_units;
-    int stages, slots, warp_smem, l2_hints;
+    int slice_bytes, num_slices;   // consumer column slices of a chunk
+    int num_slots;       // ring slots of chunk_bytes
+    int l2_hints;
     uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
-    acc[0] += __uint_as_float(v.x << 16); acc[1] += __uint_as_float(v.x & 0xffff0000u);
-    acc[2] += __uint_as_float(v.y << 16); acc[3] += __uint_as_float(v.y & 0xffff0000u);
-    acc[4] += __uint_as_float(v.z << 16); acc[5] += __uint_as_float(v.z & 0xffff0000u);
-    acc[6] += __uint_as_float(v.w << 16); acc[7] += __uint_as_float(v.w & 0xffff0000u);
+struct UnitEntry {
+    int D;       // rows of the unit
+    int start;   // first ring slot (the unit's rows occupy start, start+1, ... mod num_slots)
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
 }
 
-__global__ void __launch_bounds__(512) combine_kernel(const CombineArgs a) {
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// bf16 pair (lo in bits 0..15, hi in bits 16..31) -> two fp32 {lo, hi}; exact
+__device__ __forceinline__ uint64_t widen_bf16x2(uint32_t w) { return pack2(w << 16, w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t narrow_bf16x2(uint64_t p) {
+    const float lo = __uint_as_float((uint32_t)p), hi = __uint_as_float((uint32_t)(p >> 32));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+__global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kUnits;
+    UnitEntry *entry = reinterpret_cast<UnitEntry *>(empty + kUnits);
+    uint8_t *ring = smem + kHeadBytes;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int warps = blockDim.x >> 5;
-    const int S = a.stages;
-    const int chunk = a.chunk_bytes;
-    uint8_t *wbase = smem + (size_t)warp * a.warp_smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(wbase);
-    int *dcount = reinterpret_cast<int *>(wbase + kMaxStages * 8);
-    uint8_t *stages = wbase + kHeadBytes;
-    const size_t stage_bytes = (size_t)a.slots * chunk;
+    const int consumers = (blockDim.x >> 5) - 1;
+    const int NS = a.num_slots, CH = a.chunk_bytes, nch = a.num_chunks;
 
-    const int64_t gw = (int64_t)blockIdx.x * warps + warp;
-    const int64_t GW = (int64_t)gridDim.x * warps;
-    if (gw >= a.num_units) return;
-    const int64_t n_w = (a.num_units - 1 - gw) / GW + 1;
-    const uint64_t pol_load = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
+    // contiguous token range of this CTA
+    const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
+    const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
+    const int64_t n_units = (int64_t)(t_end - t_begin) * nch;
 
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) {
+        for (int e = 0; e < kUnits; ++e) {
+            mbar_init(&full[e], 1);
+            mbar_init(&empty[e], (uint32_t)a.num_slices);
+        }
         fence_barrier_init();
     }
-    __syncwarp();
+    __syncthreads();
+    if (n_units == 0) return;
 
-    auto fetch_row = [&](int64_t i) -> int {
-        const int64_t u = gw + i * GW;
-        const int64_t t = u / a.num_chunks;
-        return lane < a.k ? a.dst_row[t * a.k + lane] : -1;
-    };
-    // arm stage (i % S) for unit i and issue its row loads; `row` is this lane's receive row
-    auto issue = [&](int64_t i, int row) {
-        const int64_t u = gw + i * GW;
-        const int64_t t = u / a.num_chunks;
-        const int64_t off = (u - t * a.num_chunks) * (int64_t)chunk;
-        const uint32_t nbytes = (uint32_t)min((int64_t)chunk, a.row_bytes - off);
-        const int s = (int)(i % S);
-        if (row >= a.num_rows) {
-            if (off == 0) report(a.status, MOE_ERR_CAPACITY);
-            row = -1;
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
+        int64_t head = 0, tail = 0, oldest = 0;
+        int row = -1, pos = 0, D = 0;
+        int row_next = (lane < a.k) ? a.dst_row[(int64_t)t_begin * a.k + lane] : -1;
+        for (int64_t j = 0; j < n_units; ++j) {
+            const int tl = (int)(j / nch), c = (int)(j - (int64_t)tl * nch);
+            const int t = t_begin + tl;
+            const int64_t off = (int64_t)c * CH;
+            const uint32_t nbytes = (uint32_t)min((int64_t)CH, a.row_bytes - off);
+            if (c == 0) {
+                row = row_next;
+                if (t + 1 < t_end && lane < a.k) row_next = a.dst_row[(int64_t)(t + 1) * a.k + lane];
+                if (row >= a.num_rows) {
+                    report(a.status, MOE_ERR_CAPACITY);
+                    row = -1;
+                }
+                const unsigned vmask = __ballot_sync(kFull, row >= 0);
+                D = __popc(vmask);
+                pos = 0;
+                for (int jj = 0; jj < a.k; ++jj) {
+                    const int o = __shfl_sync(kFull, row, jj);
+                    pos += (row >= 0 && ((vmask >> jj) & 1u) && o < row) ? 1 : 0;
+                }
+            }
+            // wait until the unit entry and D slots are free (units are released in order)
+            bool ok = true;
+            while (ok && (j - oldest >= kUnits || head + D - tail > NS)) {
+                const int eo = (int)(oldest % kUnits);
+                ok = mbar_wait_bounded(&empty[eo], (uint32_t)((oldest / kUnits) & 1), a.timeout_ns);
+                if (ok) {
+                    tail += entry[eo].D;
+                    ++oldest;
+                }
+            }
+            if (!__all_sync(kFull, ok)) {
+                if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
+                break;
+            }
+            const int e = (int)(j % kUnits);
+            __syncwarp();   // every lane has read entry[eo] before lane 0 rewrites an entry
+            if (lane == 0) {
+                entry[e].D = D;
+                entry[e].start = (int)(head % NS);
+                mbar_arrive_expect_tx(&full[e], (uint32_t)D * nbytes);
+            }
+            __syncwarp();
+            if (row >= 0) {
+                const int slot = (int)((head + pos) % NS);
+                bulk_load(ring + (size_t)slot * CH, a.partial + (int64_t)row * a.row_bytes + off, nbytes, &full[e],
+                          pol);
+            }
+            head += D;
         }
-        const bool valid = row >= 0;
-        const unsigned vmask = __ballot_sync(kFull, valid);
-        int pos = 0;
-        for (int jj = 0; jj < a.k; ++jj) {
-            const int o = __shfl_sync(kFull, row, jj);
-            pos += (valid && ((vmask >> jj) & 1u) && o < row) ? 1 : 0;
-        }
-        if (lane == 0) {
-            dcount[s] = __popc(vmask);
-            mbar_arrive_expect_tx(&bars[s], (uint32_t)__popc(vmask) * nbytes);
-        }
-        __syncwarp();
-        if (valid)
-            bulk_load(stages + s * stage_bytes + (size_t)pos * chunk, a.partial + (int64_t)row * a.row_bytes + off,
-                      nbytes, &bars[s], pol_load);
-    };
+        return;
+    }
 
-    const int64_t pro = min((int64_t)S, n_w);
-    for (int64_t i = 0; i < pro; ++i) issue(i, fetch_row(i));
-
-    for (int64_t i = 0; i < n_w; ++i) {
-        const int s = (int)(i % S);
-        const uint32_t parity = (uint32_t)((i / S) & 1);
-        const int row_next = (i + S < n_w) ? fetch_row(i + S) : -1;
-        const int64_t u = gw + i * GW;
-        const int64_t t = u / a.num_chunks;
-        const int64_t off = (u - t * a.num_chunks) * (int64_t)chunk;
-        const int nbytes = (int)min((int64_t)chunk, a.row_bytes - off);
-
-        const bool ok = mbar_wait_bounded(&bars[s], parity, a.timeout_ns);
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    const int nsl = a.num_slices, SL = a.slice_bytes;
+    const int64_t n_items = n_units * nsl;
+    for (int64_t q = cw; q < n_items; q += consumers) {
+        const int64_t j = q / nsl;
+        const int sl = (int)(q - j * nsl);
+        const int tl = (int)(j / nch), c = (int)(j - (int64_t)tl * nch);
+        const int t = t_begin + tl;
+        const int64_t off = (int64_t)c * CH;                       // chunk offset in the row
+        const int cbytes = (int)min((int64_t)CH, a.row_bytes - off);
+        const int soff = sl * SL;                                  // slice offset in the chunk
+        const int nvec = max(0, min(SL, cbytes - soff)) / 16;
+        const int e = (int)(j % kUnits);
+        const bool ok = mbar_wait_bounded(&full[e], (uint32_t)((j / kUnits) & 1), a.timeout_ns);
         if (!__all_sync(kFull, ok)) {
             if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
             break;
         }
-        const int D = dcount[s];
-        const uint8_t *st = stages + s * stage_bytes;
-        uint8_t *dst = a.out + t * a.row_bytes + off;
-        for (int v = lane; v < nbytes / 16; v += 32) {
-            float acc[8];
+        const int D = entry[e].D;
+        int slot = entry[e].start;
+        uint64_t acc[kVMax][4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-            for (int d = 0; d < D; ++d) add_bf16x8(acc, *reinterpret_cast<const uint4 *>(st + (size_t)d * chunk + v * 16));
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4 *>(dst + v * 16) = o;
+        for (int v = 0; v < kVMax; ++v)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[v][p] = 0ull;   // +0.0f pairs
+        for (int d = 0; d < D; ++d) {
+            const uint8_t *base = ring + (size_t)slot * CH + soff + lane * 16;
+#pragma unroll
+            for (int v = 0; v < kVMax; ++v) {
+                if (lane + 32 * v < nvec) {
+                    const uint4 qv = lds128(base + v * 512);
+                    acc[v][0] = add_f32x2(acc[v][0], widen_bf16x2(qv.x));
+                    acc[v][1] = add_f32x2(acc[v][1], widen_bf16x2(qv.y));
+                    acc[v][2] = add_f32x2(acc[v][2], widen_bf16x2(qv.z));
+                    acc[v][3] = add_f32x2(acc[v][3], widen_bf16x2(qv.w));
+                }
+            }
+            if (++slot == NS) slot = 0;
+        }
+        uint8_t *dst = a.out + (int64_t)t * a.row_bytes + off + soff + lane * 16;
+#pragma unroll
+        for (int v = 0; v < kVMax; ++v) {
+            if (lane + 32 * v < nvec) {
+                uint4 o;
+                o.x = narrow_bf16x2(acc[v][0]);
+                o.y = narrow_bf16x2(acc[v][1]);
+                o.z = narrow_bf16x2(acc[v][2]);
+                o.w = narrow_bf16x2(acc[v][3]);
+                *reinterpret_cast<uint4 *>(dst + v * 512) = o;
+            }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (i + S < n_w) issue(i + S, row_next);
+        if (lane == 0) mbar_arrive(&empty[e]);
     }
 }
 
@@ -167,33 +254,35 @@ int launch_combine(const CombineLaunch &L) {
     a.partial = static_cast<const uint8_t *>(L.partial);
     a.row_bytes = (int64_t)L.hidden * 2;
     a.num_rows = L.num_partial_rows;
+    a.T = L.num_tokens;
     a.k = L.num_topk;
     a.dst_row = L.token_dst_row;
     a.out = static_cast<uint8_t *>(L.out);
     a.status = L.status;
     a.l2_hints = tu.l2_hints;
     a.timeout_ns = kDefaultWaitNs;
-    a.slots = L.num_topk;
-    a.stages = std::min(kMaxStages, std::max(2, tu.combine_stages));
 
-    const int64_t max_chunk = std::max<int64_t>(16, std::min<int64_t>(65536, tu.combine_stage_bytes) / a.slots / 16 * 16);
-    const int64_t nch = (a.row_bytes + max_chunk - 1) / max_chunk;
-    a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, 16);
+    // equal chunks no larger than the tuned maximum, small enough that the
+    // ring holds a unit of k rows with room to spare (k + 4 slots)
+    const size_t budget = std::min<size_t>(device_smem_optin(), (size_t)std::max(64 << 10, tu.combine_ring_bytes));
+    int64_t nch = (a.row_bytes + tu.combine_chunk - 1) / std::max(16, tu.combine_chunk);
+    while (true) {
+        a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, 16);
+        if ((int64_t)(budget - kHeadBytes) / a.chunk_bytes >= (int64_t)a.k + 4 || a.chunk_bytes <= 16) break;
+        ++nch;
+    }
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
-    a.num_units = (int64_t)L.num_tokens * a.num_chunks;
-
-    const int64_t per_warp = round_up(kHeadBytes + (int64_t)a.stages * a.slots * a.chunk_bytes, 128);
-    a.warp_smem = (int)per_warp;
-    const int fit = (int)std::min<int64_t>(16, (int64_t)device_smem_optin() / per_warp);
-    if (fit < 1) return MOE_ERR_INVALID_ARG;
-    const int warps = std::max(1, std::min(fit, tu.combine_warps));
-    const size_t smem = (size_t)per_warp * warps;
+    a.num_slots = (int)((budget - kHeadBytes) / (size_t)a.chunk_bytes);
+    if (a.num_slots < a.k) return MOE_ERR_INVALID_ARG;   // a unit of k rows must fit in the ring
+    // consumer slices: equal pieces of at most 32 lanes x kVMax x 16 B
+    a.num_slices = (int)((a.chunk_bytes + 32 * kVMax * 16 - 1) / (32 * kVMax * 16));
+    a.slice_bytes = (int)round_up((a.chunk_bytes + a.num_slices - 1) / a.num_slices, 16);
+    const size_t smem = kHeadBytes + (size_t)a.num_slots * a.chunk_bytes;
     if (ensure_dynamic_smem((const void *)combine_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
-    int ctas_per_sm = (int)std::max<size_t>(1, device_smem_per_sm() / (smem + 1024));
-    if (tu.ctas_per_sm > 0) ctas_per_sm = std::min(ctas_per_sm, tu.ctas_per_sm);
-    const int64_t want = (a.num_units + warps - 1) / warps;
-    const int grid = (int)std::min<int64_t>(want, (int64_t)device_sm_count() * ctas_per_sm);
-    combine_kernel<<<grid, warps * 32, smem, st>>>(a);
+
+    const int consumers = std::max(1, std::min(8, tu.combine_warps));
+    const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
+    combine_kernel<<<grid, (consumers + 1) * 32, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

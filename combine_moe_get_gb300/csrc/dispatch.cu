@@ -63,6 +63,20 @@ struct DispatchArgs {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// x / scale as the IEEE fp32 quotient, as far as its E4M3 code can tell.
+// q0 = RN(x * RN(1/scale)) is within 3 fp32 ulps of RN(x / scale) (two
+// roundings of relative size <= 2^-24 each against one). E4M3 rounding (3
+// mantissa bits, RNE) is a step function of its fp32 argument whose steps sit
+// at midpoints, whose fp32 mantissa has low 20 bits == 0x80000 in the normal
+// range. So when q0 is more than 4 ulps from a midpoint and |q0| >= 2^-6 (below
+// that the E4M3 quantum is fixed), q0 and RN(x / scale) get the same code;
+// otherwise the quotient must be taken with the IEEE division.
+__device__ __forceinline__ bool e4m3_needs_exact(float q0) {
+    const uint32_t b = __float_as_uint(q0) & 0x7fffffffu;
+    const uint32_t m = b & 0xfffffu;
+    return ((m + 4u - 0x80000u) <= 8u) || (b < 0x3c800000u);   // |m - 0x80000| <= 4, or |q0| < 2^-6
+}
+
 // Quantise one 128-channel block held by a half-warp (16 lanes x 8 values).
 // Returns the block's scale; writes the 8 codes of this lane to `q8`.
 __device__ __forceinline__ float quantize_lane8(const uint4 v, uint2 &q8) {
@@ -77,12 +91,30 @@ __device__ __forceinline__ float quantize_lane8(const uint4 v, uint2 &q8) {
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     const float scale = amax / 448.0f;   // IEEE division (no fast-math)
-    uint32_t c[8];
+    uint32_t c[4];
+    if (scale == 0.0f) {
+        c[0] = c[1] = c[2] = c[3] = 0u;
+    } else {
+        const float rcp = __frcp_rn(scale);
+        float q[8];
+        unsigned exact = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        c[i] = (scale == 0.0f) ? 0u : (uint32_t)__nv_cvt_float_to_fp8(f[i] / scale, __NV_SATFINITE, __NV_E4M3);
-    q8.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-    q8.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+        for (int i = 0; i < 8; ++i) {
+            q[i] = f[i] * rcp;
+            exact |= e4m3_needs_exact(q[i]) ? (1u << i) : 0u;
+        }
+        if (exact) {                         // rare: near a rounding midpoint or tiny
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if ((exact >> i) & 1u) q[i] = f[i] / scale;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(q[2 * i], q[2 * i + 1]), __NV_SATFINITE,
+                                                      __NV_E4M3);   // .x -> low byte
+    }
+    q8.x = c[0] | (c[1] << 16);
+    q8.y = c[2] | (c[3] << 16);
     return scale;
 }
 
@@ -234,6 +266,220 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
     if (lane == 0) bulk_wait_all();
 }
 
+// ------------------------------------------------------------------ FP8 dispatch, row pipeline
+//
+// FP8 dispatch does real arithmetic per element, so it runs as a CTA-level
+// pipeline over whole rows. One CTA per SM owns a contiguous token range:
+//   producer warp    one cp.async.bulk per token row (bf16, 14 KB at H=7168)
+//                    into an input ring;
+//   quantiser warps  (row, slice) items round-robin, a slice being up to 8
+//                    blocks of 128 channels; each half-warp quantises one block
+//                    (amax, scale = amax/448, E4M3 codes) into an output ring
+//                    slot holding the row's codes followed by its scales;
+//   store warp       one cp.async.bulk of the code row (and of the scale row
+//                    when its pitch is a multiple of 16 bytes) per destination
+//                    rank, plus the per-row metadata.
+// Ring slots are handed back through mbarriers; every wait is bounded.
+
+constexpr int kFp8MaxSlots = 16;
+
+struct Fp8Args {
+    const uint8_t *x;
+    int64_t row_bytes;           // H * 2
+    int H, nb;                   // nb = H / 128
+    int T, k, m, E;
+    const int64_t *topk;
+    const float *topk_w;
+    const int32_t *dst_row;
+    int capacity;
+    uint8_t *recv_x;
+    float *recv_scales;
+    int64_t *recv_topk_idx;
+    float *recv_topk_w;
+    int32_t *recv_src;
+    float *x_scales;
+    int32_t *status;
+    int n_in, n_out;             // ring slots
+    int slice_blocks, num_slices;
+    int out_slot_bytes;          // H + scale bytes, rounded to 16
+    int scales_bulk;             // scale rows can be bulk-stored (nb * 4 % 16 == 0)
+    int l2_hints;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__global__ void __launch_bounds__(32 * 18, 1) dispatch_fp8_rows_kernel(const Fp8Args a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *in_full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *in_empty = in_full + kFp8MaxSlots;
+    uint64_t *out_full = in_empty + kFp8MaxSlots;
+    uint64_t *out_empty = out_full + kFp8MaxSlots;
+    uint8_t *in_ring = smem + 4 * kFp8MaxSlots * 8;
+    uint8_t *out_ring = in_ring + (size_t)a.n_in * a.row_bytes;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int quantizers = (blockDim.x >> 5) - 2;
+    const int NI = a.n_in, NO = a.n_out, nsl = a.num_slices;
+
+    const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
+    const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
+    const int n = t_end - t_begin;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NI; ++i) {
+            mbar_init(&in_full[i], 1);
+            mbar_init(&in_empty[i], (uint32_t)nsl);
+        }
+        for (int i = 0; i < NO; ++i) {
+            mbar_init(&out_full[i], (uint32_t)nsl);
+            mbar_init(&out_empty[i], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (n <= 0) return;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
+            for (int j = 0; j < n; ++j) {
+                const int s = j % NI;
+                if (j >= NI && !mbar_wait_bounded(&in_empty[s], (uint32_t)(((j / NI) - 1) & 1), a.timeout_ns)) {
+                    report(a.status, MOE_ERR_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&in_full[s], (uint32_t)a.row_bytes);
+                bulk_load(in_ring + (size_t)s * a.row_bytes, a.x + (int64_t)(t_begin + j) * a.row_bytes,
+                          (uint32_t)a.row_bytes, &in_full[s], pol);
+            }
+        }
+        return;
+    }
+
+    if (warp == 1) {
+        // ------------------------------------------------------------ store warp
+        const uint64_t pol = (a.l2_hints & 2) ? policy_evict_first() : policy_evict_normal();
+        const int scale_bytes = a.nb * 4;
+        int row_n = -1;
+        int64_t e_n = -1;
+        float w_n = 0.0f;
+        if (lane < a.k) {
+            const int64_t base = (int64_t)t_begin * a.k + lane;
+            row_n = a.dst_row[base];
+            e_n = a.topk[base];
+            if (a.topk_w) w_n = a.topk_w[base];
+        }
+        bool failed = false;
+        for (int j = 0; j < n; ++j) {
+            const int t = t_begin + j;
+            const int o = j % NO;
+            int row = row_n;
+            const int64_t e = e_n;
+            const float wgt = w_n;
+            if (j + 1 < n && lane < a.k) {
+                const int64_t base = (int64_t)(t + 1) * a.k + lane;
+                row_n = a.dst_row[base];
+                e_n = a.topk[base];
+                if (a.topk_w) w_n = a.topk_w[base];
+            }
+            if (row >= a.capacity) {
+                report(a.status, MOE_ERR_CAPACITY);
+                row = -1;
+            }
+            const unsigned dmask = __ballot_sync(kFull, row >= 0);
+            const bool ok = mbar_wait_bounded(&out_full[o], (uint32_t)((j / NO) & 1), a.timeout_ns);
+            if (!__all_sync(kFull, ok)) {
+                if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
+                failed = true;
+                break;
+            }
+            const uint8_t *codes = out_ring + (size_t)o * a.out_slot_bytes;
+            const float *sc = reinterpret_cast<const float *>(codes + a.H);
+            unsigned mm = dmask;
+            while (mm) {
+                const int jd = __ffs(mm) - 1;
+                mm &= mm - 1;
+                const int rowd = __shfl_sync(kFull, row, jd);
+                if (lane == 0) {
+                    bulk_store(a.recv_x + (int64_t)rowd * a.H, codes, (uint32_t)a.H, pol);
+                    if (a.scales_bulk)
+                        bulk_store(a.recv_scales + (int64_t)rowd * a.nb, sc, (uint32_t)scale_bytes, pol);
+                }
+                if (!a.scales_bulk)
+                    for (int b = lane; b < a.nb; b += 32) a.recv_scales[(int64_t)rowd * a.nb + b] = sc[b];
+                const int64_t ed = __shfl_sync(kFull, e, jd);
+                const int rd = (int)(ed / a.m);
+                if (lane < a.k) {
+                    const bool local = e >= 0 && e < a.E && (int)(e / a.m) == rd;
+                    if (a.recv_topk_idx) a.recv_topk_idx[(int64_t)rowd * a.k + lane] = local ? e - (int64_t)rd * a.m : -1;
+                    if (a.recv_topk_w) a.recv_topk_w[(int64_t)rowd * a.k + lane] = local ? wgt : 0.0f;
+                }
+                if (lane == 0 && a.recv_src) a.recv_src[rowd] = (int32_t)t;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                bulk_commit();
+                if (j >= 1) {                    // the previous row's stores have read their slot
+                    bulk_wait_read<1>();
+                    mbar_arrive_plain(&out_empty[(j - 1) % NO]);
+                }
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            bulk_wait_all();
+            if (!failed) mbar_arrive_plain(&out_empty[(n - 1) % NO]);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- quantiser warps
+    const int qw = warp - 2;
+    const int half = lane >> 4, hl = lane & 15;
+    const int64_t n_items = (int64_t)n * nsl;
+    for (int64_t q = qw; q < n_items; q += quantizers) {
+        const int j = (int)(q / nsl);
+        const int sl = (int)(q - (int64_t)j * nsl);
+        const int t = t_begin + j;
+        const int si = j % NI, so = j % NO;
+        bool ok = mbar_wait_bounded(&in_full[si], (uint32_t)((j / NI) & 1), a.timeout_ns);
+        if (ok && j >= NO) ok = mbar_wait_bounded(&out_empty[so], (uint32_t)(((j / NO) - 1) & 1), a.timeout_ns);
+        if (!__all_sync(kFull, ok)) {
+            if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
+            break;
+        }
+        const uint8_t *src = in_ring + (size_t)si * a.row_bytes;
+        uint8_t *codes = out_ring + (size_t)so * a.out_slot_bytes;
+        float *sc = reinterpret_cast<float *>(codes + a.H);
+        const int b_begin = sl * a.slice_blocks;
+        const int b_end = min(a.nb, b_begin + a.slice_blocks);
+        for (int b0 = b_begin; b0 < b_end; b0 += 2) {
+            const int b = b0 + half;
+            const bool act = b < b_end;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (act) v = *reinterpret_cast<const uint4 *>(src + (size_t)b * 256 + hl * 16);
+            uint2 q8;
+            const float scale = quantize_lane8(v, q8);
+            if (act) {
+                *reinterpret_cast<uint2 *>(codes + (size_t)b * 128 + hl * 8) = q8;
+                if (hl == 0) {
+                    sc[b] = scale;
+                    if (a.x_scales) a.x_scales[(int64_t)t * a.nb + b] = scale;
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_plain(&in_empty[si]);
+            mbar_arrive_plain(&out_full[so]);
+        }
+    }
+}
+
 inline int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
@@ -265,6 +511,42 @@ int launch_dispatch(const DispatchLaunch &L) {
     a.status = L.status;
     a.l2_hints = tu.l2_hints;
     a.timeout_ns = kDefaultWaitNs;
+
+    if (fp8 && tu.fp8_rows) {
+        Fp8Args f;
+        f.x = a.x;
+        f.row_bytes = a.row_bytes;
+        f.H = L.hidden;
+        f.nb = L.hidden / 128;
+        f.T = L.num_tokens;
+        f.k = a.k; f.m = a.m; f.E = a.E;
+        f.topk = a.topk; f.topk_w = a.topk_w; f.dst_row = a.dst_row; f.capacity = a.capacity;
+        f.recv_x = a.recv_x; f.recv_scales = a.recv_scales; f.recv_topk_idx = a.recv_topk_idx;
+        f.recv_topk_w = a.recv_topk_w; f.recv_src = a.recv_src; f.x_scales = a.x_scales;
+        f.status = a.status;
+        f.slice_blocks = 8;
+        f.num_slices = (f.nb + f.slice_blocks - 1) / f.slice_blocks;
+        f.out_slot_bytes = (int)round_up((int64_t)f.H + (int64_t)f.nb * 4, 16);
+        f.scales_bulk = ((f.nb * 4) % 16 == 0) ? 1 : 0;
+        f.l2_hints = a.l2_hints;
+        f.timeout_ns = a.timeout_ns;
+        const size_t head = 4 * kFp8MaxSlots * 8;
+        const size_t optin = device_smem_optin();
+        f.n_out = std::max(2, std::min(kFp8MaxSlots, tu.fp8_out_slots));
+        f.n_in = std::max(2, std::min(kFp8MaxSlots, tu.fp8_in_slots));
+        // shrink the rings until they fit (the input ring first, keeping at least two slots each)
+        while (head + (size_t)f.n_in * f.row_bytes + (size_t)f.n_out * f.out_slot_bytes > optin && f.n_in > 2) --f.n_in;
+        while (head + (size_t)f.n_in * f.row_bytes + (size_t)f.n_out * f.out_slot_bytes > optin && f.n_out > 2) --f.n_out;
+        const size_t smem = head + (size_t)f.n_in * f.row_bytes + (size_t)f.n_out * f.out_slot_bytes;
+        if (smem <= optin) {
+            if (ensure_dynamic_smem((const void *)dispatch_fp8_rows_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
+            const int qwarps = std::max(1, std::min(16, tu.fp8_quant_warps));
+            const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
+            dispatch_fp8_rows_kernel<<<grid, (qwarps + 2) * 32, smem, st>>>(f);
+            return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+        }
+        // rows too large for the rings: fall through to the chunked kernel
+    }
 
     // chunking: equal chunks no larger than the tuned maximum
     const int64_t align = fp8 ? 256 : 16;

@@ -9,23 +9,29 @@
 // in-rank position of (t, r) is a column-wise exclusive scan of
 // is_token_in_rank over tokens.
 //
-// Kernel 1 (one CTA per tile of kTile tokens, tiles claimed by an atomic
-// ticket so that every predecessor of a tile is already resident):
+// One CTA per tile of kTile tokens:
 //   pass 1  lanes hold one top-k entry each; __match_any_sync de-duplicates the
 //           (token, rank) pairs, the lowest lane owning each; a shared bitmap
-//           [rank][token-word] records membership; a shared histogram counts
-//           experts.
-//   scan    per rank, popcounts give the tile aggregate; a decoupled lookback
-//           (Merrill & Garland, "Single-pass Parallel Prefix Scan with
-//           Decoupled Look-back", 2016) over R-wide vectors gives the tile's
-//           exclusive prefix. Each (tile, rank) status is one 64-bit word
-//           {flag:32 | value:32}, written in one store, so no fence is needed
-//           between value and flag. Waits are bounded (MOE_ERR_TIMEOUT).
-//   pass 2  the owning lane writes its in-rank position; is_token_in_rank rows
-//           are expanded from the bitmap.
+//           [rank][token-word] records membership, a shared histogram counts
+//           experts, and each entry's owned rank (or -1) is kept in shared
+//           memory for pass 2.
+//   scan    per rank, popcounts give the tile aggregate, published for all
+//           ranks first; then a decoupled lookback (Merrill & Garland,
+//           "Single-pass Parallel Prefix Scan with Decoupled Look-back", 2016)
+//           over R-wide vectors gives the tile's exclusive prefix. A group of
+//           G lanes serves one rank and reads G predecessor tiles per step.
+//           Each (tile, rank) status is one 64-bit word {flag:32 | value:32},
+//           written in one store, so value and flag change together. Waits
+//           are bounded (MOE_ERR_TIMEOUT).
 //   last    the last CTA to finish (done counter) writes per-rank and
 //           per-expert counts and their exclusive prefixes.
-// Kernel 2 adds rank_prefix[r] to each owned in-rank position.
+//   pass 2  the owning entries get their receive rows.
+// When every tile fits on the GPU at once, the kernel is launched
+// cooperatively (all CTAs co-resident, tile = blockIdx): after the last CTA
+// publishes the prefixes, every tile waits (bounded) for them and writes final
+// global rows -- one launch. Otherwise tiles are claimed by an atomic ticket
+// (so every predecessor of a tile is already resident), pass 2 writes in-rank
+// positions, and a second small kernel adds rank_prefix[r].
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -48,7 +54,8 @@ constexpr uint64_t kFlagInclusive = 2ull << 32;
 struct WsHeader {
     uint32_t ticket;
     uint32_t done;
-    uint32_t pad[30];
+    uint32_t ready;      // cooperative mode: prefixes published
+    uint32_t pad[29];
 };
 static_assert(sizeof(WsHeader) == 128, "header is one 128-byte line");
 
@@ -67,25 +74,31 @@ inline WsLayout ws_layout(int T, int E, int R) {
     return w;
 }
 
-inline size_t smem_bytes(int E, int R) {
-    // bitmap u32 [R][kWords] | word prefix u16 [R][kWords] | exclusive prefix i32 [R] | expert hist i32 [E]
-    return align_up((size_t)R * kWords * 4, 16) + align_up((size_t)R * kWords * 2, 16) +
-           align_up((size_t)R * 4, 16) + align_up((size_t)E * 4, 16);
+// Shared memory: bitmap u32 [R][kWords] | word prefix u16 [R][kWords] |
+// exclusive prefix i32 [R] | expert histogram i32 [E] | owned rank i16 [kTile * k]
+struct SmemLayout {
+    size_t wprefix, excl, hist, own, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int E, int R, int k) {
+    SmemLayout s;
+    s.wprefix = align_up((size_t)R * kWords * 4, 16);
+    s.excl = s.wprefix + align_up((size_t)R * kWords * 2, 16);
+    s.hist = s.excl + align_up((size_t)R * 4, 16);
+    s.own = s.hist + align_up((size_t)E * 4, 16);
+    s.total = s.own + align_up((size_t)kTile * k * 2, 16);
+    return s;
 }
 
 // Exclusive scan of n int32 counts (read from `in`, copied to `copy_out` when
 // non-null) into prefix[0..n]; one CTA of kThreads threads.
-__device__ void block_exclusive_scan(const int32_t *in, int n, int32_t *copy_out, int32_t *prefix, bool in_volatile) {
+__device__ void block_exclusive_scan(const int32_t *in, int n, int32_t *copy_out, int32_t *prefix) {
     __shared__ int32_t warp_sums[kWarps];
     __shared__ int32_t carry_total;
     const int per = (n + kThreads - 1) / kThreads;
     const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
     int32_t local = 0;
-    for (int i = lo; i < hi; ++i) {
-        int32_t v = in_volatile ? *reinterpret_cast<const volatile int32_t *>(in + i) : in[i];
-        local += v;
-    }
-    // inclusive warp scan of the per-thread sums
+    for (int i = lo; i < hi; ++i) local += __ldcg(in + i);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int32_t incl = local;
 #pragma unroll
@@ -107,7 +120,7 @@ __device__ void block_exclusive_scan(const int32_t *in, int n, int32_t *copy_out
     __syncthreads();
     int32_t run = warp_sums[warp] + incl - local;
     for (int i = lo; i < hi; ++i) {
-        int32_t v = in_volatile ? *reinterpret_cast<const volatile int32_t *>(in + i) : in[i];
+        const int32_t v = __ldcg(in + i);
         if (copy_out) copy_out[i] = v;
         prefix[i] = run;
         run += v;
@@ -119,6 +132,7 @@ __device__ void block_exclusive_scan(const int32_t *in, int n, int32_t *copy_out
 struct TileArgs {
     const int64_t *topk;
     int T, k, E, R, m, num_tiles;
+    int group;             // lanes per rank in the lookback (power of two, <= 32)
     uint8_t *is_token_in_rank;
     int32_t *token_dst_row;
     int32_t *num_tokens_per_rank, *num_tokens_per_expert, *rank_prefix, *expert_prefix;
@@ -129,31 +143,25 @@ struct TileArgs {
     int unpublished_tile;  // test hook: this tile never publishes its status (-1 = none)
 };
 
-// Route of one lane: expert e (or -1) and its rank (or -1); flags bad entries.
-__device__ __forceinline__ int lane_route(const TileArgs &a, int64_t e, int32_t *status, bool report_bad) {
-    if (e == -1) return -1;
-    if (e < 0 || e >= a.E) {
-        if (report_bad) report(status, MOE_ERR_BAD_TOPK);
-        return -1;
-    }
-    return (int)(e / a.m);
-}
-
+template <bool kCooperative>
 __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int R = a.R, E = a.E, k = a.k;
+    const SmemLayout sl = smem_layout(E, R, k);
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem);
-    uint16_t *wprefix = reinterpret_cast<uint16_t *>(smem + align_up((size_t)R * kWords * 4, 16));
-    int32_t *excl = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(wprefix) + align_up((size_t)R * kWords * 2, 16));
-    int32_t *hist = reinterpret_cast<int32_t *>(reinterpret_cast<uint8_t *>(excl) + align_up((size_t)R * 4, 16));
+    uint16_t *wprefix = reinterpret_cast<uint16_t *>(smem + sl.wprefix);
+    int32_t *excl = reinterpret_cast<int32_t *>(smem + sl.excl);
+    int32_t *hist = reinterpret_cast<int32_t *>(smem + sl.hist);
+    int16_t *own = reinterpret_cast<int16_t *>(smem + sl.own);
     __shared__ int s_tile;
     __shared__ int s_last;
+    __shared__ int s_ok;
 
     WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
     int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
     uint64_t *tile_status = reinterpret_cast<uint64_t *>(a.ws + a.status_off);
 
-    if (threadIdx.x == 0) s_tile = (int)atomicAdd(&hdr->ticket, 1u);
+    if (threadIdx.x == 0) s_tile = kCooperative ? (int)blockIdx.x : (int)atomicAdd(&hdr->ticket, 1u);
     for (int i = threadIdx.x; i < R * kWords; i += kThreads) bitmap[i] = 0u;
     for (int i = threadIdx.x; i < E; i += kThreads) hist[i] = 0;
     __syncthreads();
@@ -166,19 +174,25 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
     const int sub = lane / k, j = lane - sub * k;
     const bool lane_used = sub < tpp;
 
-    // ---- pass 1: membership bitmap and expert histogram
+    // ---- pass 1: membership bitmap, expert histogram, owned ranks
     for (int base = warp * tpp; base < tcount; base += kWarps * tpp) {
         const int tl = base + sub;
         const bool act = lane_used && tl < tcount;
         int r = -1;
         if (act) {
-            int64_t e = ld_nc_i64(a.topk + (int64_t)(t0 + tl) * k + j);
-            r = lane_route(a, e, a.status, true);
-            if (r >= 0) atomicAdd(&hist[(int)e], 1);
+            const int64_t e = ld_nc_i64(a.topk + (int64_t)(t0 + tl) * k + j);
+            if (e >= 0 && e < E) {
+                r = (int)(e / a.m);
+                atomicAdd(&hist[(int)e], 1);
+            } else if (e != -1) {
+                report(a.status, MOE_ERR_BAD_TOPK);
+            }
         }
         const int key = (r >= 0) ? (sub * R + r) : -(lane + 1);
         const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (r >= 0 && (__ffs(peers) - 1) == lane) atomicOr(&bitmap[r * kWords + (tl >> 5)], 1u << (tl & 31));
+        const bool owner = r >= 0 && (__ffs(peers) - 1) == lane;
+        if (owner) atomicOr(&bitmap[r * kWords + (tl >> 5)], 1u << (tl & 31));
+        if (act) own[tl * k + j] = (int16_t)(owner ? r : -1);
     }
     __syncthreads();
 
@@ -195,33 +209,50 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
         excl[r] = (int32_t)run;   // holds the aggregate until the lookback below
         if (publish) st_relaxed_gpu_u64(my_status + r, (tile == 0 ? kFlagInclusive : kFlagAggregate) | run);
     }
-    // ---- decoupled lookback: exclusive prefix of this tile, then its inclusive prefix
-    for (int r = threadIdx.x; r < R; r += kThreads) {
-        const uint32_t agg = (uint32_t)excl[r];
-        uint32_t ex = 0;
-        if (tile > 0) {
-            int p = tile - 1;
-            uint64_t deadline = 0;
-            while (p >= 0) {
-                const uint64_t w = ld_relaxed_gpu_u64(tile_status + (size_t)p * R + r);
-                const uint64_t flag = w & 0xffffffff00000000ull;
-                if (flag == 0) {
-                    const uint64_t now = globaltimer_ns();
-                    if (deadline == 0) {
-                        deadline = now + a.timeout_ns;
-                    } else if (now > deadline) {
-                        report(a.status, MOE_ERR_TIMEOUT);
-                        break;
+    __syncthreads();
+
+    // ---- decoupled lookback, G lanes per rank, G predecessors per step
+    {
+        const int G = a.group;
+        const int ngroups = kThreads / G;
+        const int gi = threadIdx.x / G, gl = threadIdx.x % G;
+        const int gbase = lane & ~(G - 1);
+        const unsigned low = (G == 32) ? 0xffffffffu : ((1u << G) - 1u);
+        const unsigned gmask = low << gbase;
+        for (int r = gi; r < R; r += ngroups) {
+            const uint32_t agg = (uint32_t)excl[r];
+            uint32_t ex = 0;
+            if (tile > 0) {
+                int p_hi = tile - 1;
+                uint64_t deadline = 0;
+                while (true) {
+                    const int p = p_hi - gl;
+                    const uint64_t w = (p >= 0) ? ld_relaxed_gpu_u64(tile_status + (size_t)p * R + r) : kFlagInclusive;
+                    const uint64_t flag = w & 0xffffffff00000000ull;
+                    const unsigned pm = (__ballot_sync(gmask, flag == kFlagInclusive) >> gbase) & low;
+                    const unsigned zm = (__ballot_sync(gmask, flag == 0) >> gbase) & low;
+                    const int fp = pm ? __ffs(pm) - 1 : G;                 // nearest inclusive in the window
+                    const unsigned need = (fp >= 31) ? low : ((2u << fp) - 1u) & low;
+                    if (zm & need) {                                      // a needed predecessor is not ready
+                        const uint64_t now = globaltimer_ns();
+                        if (deadline == 0) {
+                            deadline = now + a.timeout_ns;
+                        } else if (now > deadline) {
+                            if (gl == 0) report(a.status, MOE_ERR_TIMEOUT);
+                            break;
+                        }
+                        continue;
                     }
-                    continue;
+                    uint32_t v = (gl <= fp) ? (uint32_t)w : 0u;
+                    for (int o = G >> 1; o >= 1; o >>= 1) v += __shfl_xor_sync(gmask, v, o);
+                    ex += v;
+                    if (fp < G) break;
+                    p_hi -= G;
                 }
-                ex += (uint32_t)w;
-                if (flag == kFlagInclusive) break;
-                --p;
+                if (publish && gl == 0) st_relaxed_gpu_u64(my_status + r, kFlagInclusive | (ex + agg));
             }
-            if (publish) st_relaxed_gpu_u64(my_status + r, kFlagInclusive | (ex + agg));
+            if (gl == 0) excl[r] = (int32_t)ex;
         }
-        excl[r] = (int32_t)ex;
     }
     __syncthreads();
 
@@ -229,24 +260,6 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
     for (int e = threadIdx.x; e < E; e += kThreads) {
         const int h = hist[e];
         if (h) atomicAdd(ws_expert + e, h);
-    }
-
-    // ---- pass 2: in-rank positions of the owning lanes
-    for (int base = warp * tpp; base < tcount; base += kWarps * tpp) {
-        const int tl = base + sub;
-        const bool act = lane_used && tl < tcount;
-        int r = -1;
-        if (act) r = lane_route(a, ld_nc_i64(a.topk + (int64_t)(t0 + tl) * k + j), nullptr, false);
-        const int key = (r >= 0) ? (sub * R + r) : -(lane + 1);
-        const unsigned peers = __match_any_sync(0xffffffffu, key);
-        if (act) {
-            int32_t v = -1;
-            if (r >= 0 && (__ffs(peers) - 1) == lane) {
-                const uint32_t word = bitmap[r * kWords + (tl >> 5)];
-                v = excl[r] + wprefix[r * kWords + (tl >> 5)] + __popc(word & ((1u << (tl & 31)) - 1u));
-            }
-            a.token_dst_row[(int64_t)(t0 + tl) * k + j] = v;
-        }
     }
 
     // ---- is_token_in_rank rows of this tile, expanded from the bitmap
@@ -274,18 +287,58 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
     __syncthreads();
     if (threadIdx.x == 0) s_last = (atomicAdd(&hdr->done, 1u) == (unsigned)(a.num_tiles - 1));
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const uint64_t *last_status = tile_status + (size_t)(a.num_tiles - 1) * R;
-    for (int r = threadIdx.x; r < R; r += kThreads) {
-        const uint64_t w = ld_relaxed_gpu_u64(last_status + r);
-        if ((w & 0xffffffff00000000ull) != kFlagInclusive) report(a.status, MOE_ERR_TIMEOUT);
-        a.num_tokens_per_rank[r] = (int32_t)(uint32_t)w;
+    if (s_last) {
+        __threadfence();
+        const uint64_t *last_status = tile_status + (size_t)(a.num_tiles - 1) * R;
+        for (int r = threadIdx.x; r < R; r += kThreads) {
+            const uint64_t w = ld_relaxed_gpu_u64(last_status + r);
+            if ((w & 0xffffffff00000000ull) != kFlagInclusive) report(a.status, MOE_ERR_TIMEOUT);
+            a.num_tokens_per_rank[r] = (int32_t)(uint32_t)w;
+        }
+        __threadfence();
+        __syncthreads();
+        block_exclusive_scan(a.num_tokens_per_rank, R, nullptr, a.rank_prefix);
+        block_exclusive_scan(ws_expert, E, a.num_tokens_per_expert, a.expert_prefix);
+        if (kCooperative) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) st_release_gpu_u32(&hdr->ready, 1u);
+        }
     }
-    __syncthreads();
-    __threadfence_block();
-    block_exclusive_scan(a.num_tokens_per_rank, R, nullptr, a.rank_prefix, true);
-    block_exclusive_scan(ws_expert, E, a.num_tokens_per_expert, a.expert_prefix, true);
+
+    // ---- pass 2: receive rows of the owning entries
+    if (kCooperative) {
+        // wait (bounded) for the prefixes, then global rows directly
+        if (threadIdx.x == 0) {
+            int ok = 1;
+            uint64_t deadline = 0;
+            while (ld_acquire_gpu_u32(&hdr->ready) == 0u) {
+                const uint64_t now = globaltimer_ns();
+                if (deadline == 0) {
+                    deadline = now + a.timeout_ns;
+                } else if (now > deadline) {
+                    report(a.status, MOE_ERR_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+            }
+            s_ok = ok;
+        }
+        __syncthreads();
+        if (s_ok)
+            for (int r = threadIdx.x; r < R; r += kThreads) excl[r] += __ldcg(a.rank_prefix + r);
+        __syncthreads();
+    }
+    for (int i = threadIdx.x; i < tcount * k; i += kThreads) {
+        const int r = own[i];
+        int32_t v = -1;
+        if (r >= 0) {
+            const int tl = i / k;
+            const uint32_t word = bitmap[r * kWords + (tl >> 5)];
+            v = excl[r] + wprefix[r * kWords + (tl >> 5)] + __popc(word & ((1u << (tl & 31)) - 1u));
+        }
+        a.token_dst_row[(int64_t)t0 * k + i] = v;
+    }
 }
 
 __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, int m,
@@ -294,6 +347,34 @@ __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, 
         const int32_t v = token_dst_row[i];
         if (v >= 0) token_dst_row[i] = v + rank_prefix[(int)(topk[i] / m)];
     }
+}
+
+// Largest power of two <= min(32, kThreads / R), at least 1.
+int lookback_group(int R) {
+    int g = 1;
+    while (g * 2 <= 32 && g * 2 * R <= kThreads) g *= 2;
+    return g;
+}
+
+// How many tiles can be co-resident (cooperative launch bound), cached per (device, smem).
+int cooperative_capacity(size_t smem) {
+    static std::mutex mu;
+    static int dev_cached[64] = {0};
+    static size_t smem_cached[64] = {0};
+    static int cap_cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev_cached[dev] && smem_cached[dev] == smem) return cap_cached[dev];
+    int coop = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_tiles_kernel<true>, kThreads, smem) !=
+        cudaSuccess)
+        return 0;
+    dev_cached[dev] = 1;
+    smem_cached[dev] = smem;
+    cap_cached[dev] = per_sm * device_sm_count();
+    return cap_cached[dev];
 }
 
 }  // namespace
@@ -319,6 +400,7 @@ int launch_layout(const LayoutLaunch &L) {
     a.topk = L.topk_idx;
     a.T = T; a.k = k; a.E = E; a.R = R; a.m = E / R;
     a.num_tiles = (T + kTile - 1) / kTile;
+    a.group = lookback_group(R);
     a.is_token_in_rank = o.is_token_in_rank;
     a.token_dst_row = o.token_dst_row;
     a.num_tokens_per_rank = o.num_tokens_per_rank;
@@ -332,14 +414,31 @@ int launch_layout(const LayoutLaunch &L) {
     a.timeout_ns = L.timeout_ns > 0 ? (uint64_t)L.timeout_ns : kDefaultWaitNs;
     a.unpublished_tile = L.unpublished_tile;
 
-    const size_t smem = smem_bytes(E, R);
-    if (ensure_dynamic_smem((const void *)layout_tiles_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
-    layout_tiles_kernel<<<a.num_tiles, kThreads, smem, s>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t smem = smem_layout(E, R, k).total;
+    if (ensure_dynamic_smem((const void *)layout_tiles_kernel<true>, smem) != MOE_OK ||
+        ensure_dynamic_smem((const void *)layout_tiles_kernel<false>, smem) != MOE_OK)
+        return MOE_ERR_CUDA;
 
+    if (a.num_tiles <= cooperative_capacity(smem)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)a.num_tiles);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, layout_tiles_kernel<true>, a) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+
+    layout_tiles_kernel<false><<<a.num_tiles, kThreads, smem, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     const int64_t n = (int64_t)T * k;
     const int threads = 256;
-    int blocks = (int)std::min<int64_t>((n + threads - 1) / threads, (int64_t)device_sm_count() * 8);
+    const int blocks = (int)std::min<int64_t>((n + threads - 1) / threads, (int64_t)device_sm_count() * 8);
     layout_rows_kernel<<<blocks, threads, 0, s>>>(L.topk_idx, n, a.m, o.rank_prefix, o.token_dst_row);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;

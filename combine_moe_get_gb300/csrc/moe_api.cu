@@ -104,9 +104,13 @@ const Tuning &tuning() {
         x.dispatch_warps = env_int("MOE_TUNE_DISPATCH_WARPS", 8);
         x.dispatch_stages = env_int("MOE_TUNE_DISPATCH_STAGES", 3);
         x.dispatch_chunk = env_int("MOE_TUNE_DISPATCH_CHUNK", 8192);
-        x.combine_warps = env_int("MOE_TUNE_COMBINE_WARPS", 4);
-        x.combine_stages = env_int("MOE_TUNE_COMBINE_STAGES", 3);
-        x.combine_stage_bytes = env_int("MOE_TUNE_COMBINE_STAGE_BYTES", 16384);
+        x.combine_warps = env_int("MOE_TUNE_COMBINE_WARPS", 8);
+        x.combine_chunk = env_int("MOE_TUNE_COMBINE_CHUNK", 8192);
+        x.combine_ring_bytes = env_int("MOE_TUNE_COMBINE_RING_BYTES", 224 << 10);
+        x.fp8_rows = env_int("MOE_TUNE_FP8_ROWS", 1) == 1;
+        x.fp8_in_slots = env_int("MOE_TUNE_FP8_IN_SLOTS", 8);
+        x.fp8_out_slots = env_int("MOE_TUNE_FP8_OUT_SLOTS", 8);
+        x.fp8_quant_warps = env_int("MOE_TUNE_FP8_QUANT_WARPS", 12);
         x.ctas_per_sm = env_int("MOE_TUNE_CTAS_PER_SM", 0);
         x.l2_hints = env_int("MOE_TUNE_L2_HINTS", 1) & 3;
         return x;

@@ -21,7 +21,8 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 // Tuning knobs, read once from MOE_TUNE_* environment variables (0 = default).
 struct Tuning {
     int dispatch_warps, dispatch_stages, dispatch_chunk;
-    int combine_warps, combine_stages, combine_stage_bytes;
+    int combine_warps, combine_chunk, combine_ring_bytes;   // consumer warps, max chunk, ring budget
+    int fp8_rows, fp8_in_slots, fp8_out_slots, fp8_quant_warps;   // FP8 row pipeline
     int ctas_per_sm;
     int l2_hints;  // bit 0: evict-first on single-use loads; bit 1: evict-first on stores
 };

@@ -230,6 +230,45 @@ def test_dispatch_fp8_special_blocks(moe):
     check_dispatch(moe, inp, E, R, True)
 
 
+def _e4m3_midpoints():
+    vals = []
+    for code in range(1, 126):
+        e, m = code >> 3, code & 7
+        lo = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+        c2 = code + 1
+        e2, m2 = c2 >> 3, c2 & 7
+        hi = (m2 / 8.0) * 2.0 ** -6 if e2 == 0 else (1 + m2 / 8.0) * 2.0 ** (e2 - 7)
+        vals.append((lo + hi) / 2)
+    return torch.tensor(vals, dtype=torch.float64)
+
+
+def test_dispatch_fp8_rounding_boundaries(moe):
+    # blocks whose quotients x / scale land on or next to E4M3 rounding midpoints, for
+    # scales that are powers of two (exact ties) and scales that are not
+    g = torch.Generator().manual_seed(11)
+    mids = _e4m3_midpoints()
+    amaxes = [1.75, 3.5, 2.625, 0.4375, 5.25, 1.3125, 2.0 ** -3 * 1.75, 448.0, 7.0, 0.21875, 3.0, 1.0]
+    T, H = 96, 1024
+    x = torch.zeros(T, H, dtype=torch.float64)
+    for t in range(T):
+        for b in range(H // 128):
+            amax = amaxes[(t * 8 + b) % len(amaxes)]
+            s = amax / 448.0
+            pick = mids[torch.randint(0, len(mids), (127,), generator=g)]
+            sign = torch.where(torch.rand(127, generator=g) < 0.5, -1.0, 1.0)
+            blk = (pick * s * sign).to(torch.bfloat16).to(torch.float64)
+            # nudge some entries one bf16 step either way
+            nud = torch.randint(-1, 2, (127,), generator=g)
+            bits = blk.to(torch.bfloat16).view(torch.int16).to(torch.int32) + nud * (blk != 0).to(torch.int32)
+            blk = bits.to(torch.int16).view(torch.bfloat16).to(torch.float64).clamp(-amax, amax)
+            x[t, b * 128:(b + 1) * 128 - 1] = blk
+            x[t, (b + 1) * 128 - 1] = amax
+    E, R, k = 64, 8, 4
+    topk = wl.make_topk_uniform(g, T, E, k)
+    inp = wl.Inputs(None, x.to(torch.bfloat16), topk, wl.make_weights(g, T, k), None)
+    check_dispatch(moe, inp, E, R, True)
+
+
 def test_dispatch_capacity_overflow_writes_nothing_beyond(moe):
     w = wl.CONFIGS["tiny"]
     inp = wl.make_inputs(w, with_partial=False)
