@@ -61,52 +61,87 @@ struct DispatchArgs {
     uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+// Block scale RN(amax / 448) without a division: q0 = RN(amax * C) with
+// C = RN(1/448), r = amax - q0 * 448 (exact by FMA), s = RN(r * C + q0).
+// amax is a bf16 value, and for every non-negative finite bf16 value this
+// equals the IEEE quotient (checked exhaustively with exact arithmetic).
+__device__ __forceinline__ float block_scale(float amax) {
+    const float C = __uint_as_float(0x3b124925u);   // RN(1 / 448)
+    const float q0 = __fmul_rn(amax, C);
+    const float r = __fmaf_rn(-q0, 448.0f, amax);
+    return __fmaf_rn(r, C, q0);
+}
 
-// x / scale as the IEEE fp32 quotient, as far as its E4M3 code can tell.
-// q0 = RN(x * RN(1/scale)) is within 3 fp32 ulps of RN(x / scale) (two
-// roundings of relative size <= 2^-24 each against one). E4M3 rounding (3
-// mantissa bits, RNE) is a step function of its fp32 argument whose steps sit
-// at midpoints, whose fp32 mantissa has low 20 bits == 0x80000 in the normal
-// range. So when q0 is more than 4 ulps from a midpoint and |q0| >= 2^-6 (below
-// that the E4M3 quantum is fixed), q0 and RN(x / scale) get the same code;
-// otherwise the quotient must be taken with the IEEE division.
-__device__ __forceinline__ bool e4m3_needs_exact(float q0) {
-    const uint32_t b = __float_as_uint(q0) & 0x7fffffffu;
-    const uint32_t m = b & 0xfffffu;
-    return ((m + 4u - 0x80000u) <= 8u) || (b < 0x3c800000u);   // |m - 0x80000| <= 4, or |q0| < 2^-6
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));   // max error 1 ulp (relative <= 2^-23)
+    return r;
+}
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// E4M3 codes of x / scale with the quotient taken as the IEEE fp32 quotient.
+// q0 = RN(x * rcp_approx(scale)) is within 5 fp32 ulps of RN(x / scale)
+// (relative errors <= 2^-23 for the reciprocal and 2^-24 for each rounding).
+// E4M3 rounding (3 mantissa bits, RNE, saturating) is a step function of its
+// fp32 argument whose steps sit at midpoints, whose fp32 mantissa has low 20
+// bits == 0x80000 in the normal range; below 2^-6 the E4M3 quantum is fixed.
+// So when every q0 of the lane is more than 16 ulps from a midpoint and at
+// least 2^-6 in magnitude, the q0 give the same codes as the IEEE quotients;
+// otherwise the flagged quotients are taken with the IEEE division.
+constexpr uint32_t kMidWindow = 16;
+
+__device__ __forceinline__ bool near_midpoint(float q) {
+    return ((__float_as_uint(q) + kMidWindow - 0x80000u) & 0xfffffu) <= 2 * kMidWindow;
 }
 
 // Quantise one 128-channel block held by a half-warp (16 lanes x 8 values).
 // Returns the block's scale; writes the 8 codes of this lane to `q8`.
 __device__ __forceinline__ float quantize_lane8(const uint4 v, uint2 &q8) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float f[8];
-    f[0] = bf16_bits_to_float(v.x & 0xffffu); f[1] = bf16_bits_to_float(v.x >> 16);
-    f[2] = bf16_bits_to_float(v.y & 0xffffu); f[3] = bf16_bits_to_float(v.y >> 16);
-    f[4] = bf16_bits_to_float(v.z & 0xffffu); f[5] = bf16_bits_to_float(v.z >> 16);
-    f[6] = bf16_bits_to_float(v.w & 0xffffu); f[7] = bf16_bits_to_float(v.w >> 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-    const float scale = amax / 448.0f;   // IEEE division (no fast-math)
+    const float scale = block_scale(amax);
     uint32_t c[4];
     if (scale == 0.0f) {
         c[0] = c[1] = c[2] = c[3] = 0u;
     } else {
-        const float rcp = __frcp_rn(scale);
+        const float rcp = rcp_approx(scale);
+        const uint64_t rr = (uint64_t)__float_as_uint(rcp) | ((uint64_t)__float_as_uint(rcp) << 32);
         float q[8];
-        unsigned exact = 0;
+        uint32_t dmin = 0xffffffffu;
+        float qmin = INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint64_t xy;                     // {f[2i], f[2i+1]} as one f32x2 operand
+            asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "r"(w[i] << 16), "r"(w[i] & 0xffff0000u));
+            const uint64_t p = mul_f32x2(xy, rr);
+            q[2 * i] = __uint_as_float((uint32_t)p);
+            q[2 * i + 1] = __uint_as_float((uint32_t)(p >> 32));
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            q[i] = f[i] * rcp;
-            exact |= e4m3_needs_exact(q[i]) ? (1u << i) : 0u;
+            dmin = min(dmin, (__float_as_uint(q[i]) + kMidWindow - 0x80000u) & 0xfffffu);
+            qmin = fminf(qmin, fabsf(q[i]));
         }
-        if (exact) {                         // rare: near a rounding midpoint or tiny
+        // scale >= 2^-100 keeps 1/scale finite; tinier scales take the IEEE path throughout
+        if (dmin <= 2 * kMidWindow || qmin < 0.015625f || scale < 7.8886090522e-31f) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                if ((exact >> i) & 1u) q[i] = f[i] / scale;
+                if (near_midpoint(q[i]) || fabsf(q[i]) < 0.015625f || scale < 7.8886090522e-31f) q[i] = f[i] / scale;
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -115,6 +150,60 @@ __device__ __forceinline__ float quantize_lane8(const uint4 v, uint2 &q8) {
     }
     q8.x = c[0] | (c[1] << 16);
     q8.y = c[2] | (c[3] << 16);
+    return scale;
+}
+
+// Quantise one 128-channel block held by a quarter-warp (8 lanes x 16 values;
+// `lo`, `hi` are the lane's 32 contiguous bytes). Same arithmetic as
+// quantize_lane8. Returns the block's scale; writes the 16 codes to `q16`.
+__device__ __forceinline__ float quantize_lane16(const uint4 lo, const uint4 hi, uint4 &q16) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    const float scale = block_scale(amax);
+    uint32_t c[8];
+    if (scale == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = 0u;
+    } else {
+        const float rcp = rcp_approx(scale);
+        const uint64_t rr = (uint64_t)__float_as_uint(rcp) | ((uint64_t)__float_as_uint(rcp) << 32);
+        float q[16];
+        uint32_t dmin = 0xffffffffu;
+        float qmin = INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint64_t xy;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "r"(w[i] << 16), "r"(w[i] & 0xffff0000u));
+            const uint64_t p = mul_f32x2(xy, rr);
+            q[2 * i] = __uint_as_float((uint32_t)p);
+            q[2 * i + 1] = __uint_as_float((uint32_t)(p >> 32));
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            dmin = min(dmin, (__float_as_uint(q[i]) + kMidWindow - 0x80000u) & 0xfffffu);
+            qmin = fminf(qmin, fabsf(q[i]));
+        }
+        if (dmin <= 2 * kMidWindow || qmin < 0.015625f || scale < 7.8886090522e-31f) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float f = __uint_as_float((i & 1) ? (w[i >> 1] & 0xffff0000u) : (w[i >> 1] << 16));
+                if (near_midpoint(q[i]) || fabsf(q[i]) < 0.015625f || scale < 7.8886090522e-31f) q[i] = f / scale;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(q[2 * i], q[2 * i + 1]), __NV_SATFINITE,
+                                                      __NV_E4M3);   // .x -> low byte
+    }
+    q16.x = c[0] | (c[1] << 16);
+    q16.y = c[2] | (c[3] << 16);
+    q16.z = c[4] | (c[5] << 16);
+    q16.w = c[6] | (c[7] << 16);
     return scale;
 }
 
@@ -228,22 +317,30 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
             out_off = off / 2;
         }
 
-        unsigned mm = dmask;
-        while (mm) {
-            const int jd = __ffs(mm) - 1;
-            mm &= mm - 1;
-            const int rowd = __shfl_sync(kFull, row, jd);
+        // every bulk store of this chunk first, then the per-row metadata
+        for (unsigned mm = dmask; mm; mm &= mm - 1) {
+            const int rowd = __shfl_sync(kFull, row, __ffs(mm) - 1);
             if (lane == 0)
                 bulk_store(a.recv_x + (int64_t)rowd * a.recv_row_bytes + out_off, src, (uint32_t)out_bytes, pol_store);
+        }
+        if (lane == 0) bulk_commit();
+        // rank of this lane's expert (-1 if masked or invalid) and its index within the rank
+        int rl = -1, el = 0;
+        if (c == 0 && e >= 0 && e < a.E) {
+            rl = (int)e / a.m;
+            el = (int)e - rl * a.m;
+        }
+        for (unsigned mm = dmask; mm; mm &= mm - 1) {
+            const int jd = __ffs(mm) - 1;
+            const int rowd = __shfl_sync(kFull, row, jd);
             if constexpr (kFP8) {
                 for (int b = lane; b < nblk; b += 32) a.recv_scales[(int64_t)rowd * a.nb + c * cpb + b] = sc[b];
             }
             if (c == 0) {
-                const int64_t ed = __shfl_sync(kFull, e, jd);
-                const int rd = (int)(ed / a.m);
+                const int rd = __shfl_sync(kFull, rl, jd);
                 if (lane < a.k) {
-                    const bool local = e >= 0 && e < a.E && (int)(e / a.m) == rd;
-                    if (a.recv_topk_idx) a.recv_topk_idx[(int64_t)rowd * a.k + lane] = local ? e - (int64_t)rd * a.m : -1;
+                    const bool local = rl == rd;
+                    if (a.recv_topk_idx) a.recv_topk_idx[(int64_t)rowd * a.k + lane] = local ? (int64_t)el : -1;
                     if (a.recv_topk_w) a.recv_topk_w[(int64_t)rowd * a.k + lane] = local ? wgt : 0.0f;
                 }
                 if (lane == 0 && a.recv_src) a.recv_src[rowd] = (int32_t)t;
@@ -254,7 +351,6 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
                 for (int b = lane; b < nblk; b += 32) a.x_scales[t * a.nb + c * cpb + b] = sc[b];
         }
         if (lane == 0) {
-            bulk_commit();
             // the stage stored one unit ago is free once its bulk stores have read it
             if (i >= 1 && i - 1 + S < n_w) {
                 bulk_wait_read<1>();
@@ -268,20 +364,26 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
 
 // ------------------------------------------------------------------ FP8 dispatch, row pipeline
 //
-// FP8 dispatch does real arithmetic per element, so it runs as a CTA-level
-// pipeline over whole rows. One CTA per SM owns a contiguous token range:
-//   producer warp    one cp.async.bulk per token row (bf16, 14 KB at H=7168)
-//                    into an input ring;
-//   quantiser warps  (row, slice) items round-robin, a slice being up to 8
-//                    blocks of 128 channels; each half-warp quantises one block
-//                    (amax, scale = amax/448, E4M3 codes) into an output ring
-//                    slot holding the row's codes followed by its scales;
-//   store warp       one cp.async.bulk of the code row (and of the scale row
-//                    when its pitch is a multiple of 16 bytes) per destination
-//                    rank, plus the per-row metadata.
-// Ring slots are handed back through mbarriers; every wait is bounded.
+// FP8 dispatch does arithmetic per element and writes rows half as wide as
+// it reads, so it runs as a CTA-level pipeline over whole rows. One CTA per
+// SM owns a contiguous token range:
+//   producer warp  one cp.async.bulk per token row (bf16, 14 KB at H=7168)
+//                  into an input ring;
+//   worker warps   (row, slice) items round-robin, a slice being up to 8
+//                  blocks of 128 channels. Each quarter-warp quantises one
+//                  block (amax, scale = amax/448, E4M3 codes; 16 values per
+//                  lane) and stores its 128 code bytes straight from
+//                  registers to every destination row (16 bytes per lane,
+//                  one full 128-byte line per quarter-warp store); the
+//                  slice's scales go out as one coalesced 32-byte store per
+//                  destination. The worker of slice 0 also writes the row
+//                  metadata.
+// There is no output staging and no single store warp, so the many small
+// scattered writes (scales, metadata) spread over all worker warps. Input
+// slots are handed back through mbarriers; every wait is bounded.
 
 constexpr int kFp8MaxSlots = 16;
+constexpr int kFp8SliceBlocks = 8;
 
 struct Fp8Args {
     const uint8_t *x;
@@ -299,10 +401,8 @@ struct Fp8Args {
     int32_t *recv_src;
     float *x_scales;
     int32_t *status;
-    int n_in, n_out;             // ring slots
-    int slice_blocks, num_slices;
-    int out_slot_bytes;          // H + scale bytes, rounded to 16
-    int scales_bulk;             // scale rows can be bulk-stored (nb * 4 % 16 == 0)
+    int n_in;                    // input ring slots
+    int num_slices;
     int l2_hints;
     uint64_t timeout_ns;
 };
@@ -311,17 +411,14 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__global__ void __launch_bounds__(32 * 18, 1) dispatch_fp8_rows_kernel(const Fp8Args a) {
+__global__ void __launch_bounds__(32 * 21, 1) dispatch_fp8_rows_kernel(const Fp8Args a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *in_full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *in_empty = in_full + kFp8MaxSlots;
-    uint64_t *out_full = in_empty + kFp8MaxSlots;
-    uint64_t *out_empty = out_full + kFp8MaxSlots;
-    uint8_t *in_ring = smem + 4 * kFp8MaxSlots * 8;
-    uint8_t *out_ring = in_ring + (size_t)a.n_in * a.row_bytes;
+    uint8_t *in_ring = smem + 2 * kFp8MaxSlots * 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int quantizers = (blockDim.x >> 5) - 2;
-    const int NI = a.n_in, NO = a.n_out, nsl = a.num_slices;
+    const int workers = (blockDim.x >> 5) - 1;
+    const int NI = a.n_in, nsl = a.num_slices;
 
     const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
     const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
@@ -331,10 +428,6 @@ __global__ void __launch_bounds__(32 * 18, 1) dispatch_fp8_rows_kernel(const Fp8
         for (int i = 0; i < NI; ++i) {
             mbar_init(&in_full[i], 1);
             mbar_init(&in_empty[i], (uint32_t)nsl);
-        }
-        for (int i = 0; i < NO; ++i) {
-            mbar_init(&out_full[i], (uint32_t)nsl);
-            mbar_init(&out_empty[i], 1);
         }
         fence_barrier_init();
     }
@@ -359,123 +452,90 @@ __global__ void __launch_bounds__(32 * 18, 1) dispatch_fp8_rows_kernel(const Fp8
         return;
     }
 
-    if (warp == 1) {
-        // ------------------------------------------------------------ store warp
-        const uint64_t pol = (a.l2_hints & 2) ? policy_evict_first() : policy_evict_normal();
-        const int scale_bytes = a.nb * 4;
-        int row_n = -1;
-        int64_t e_n = -1;
-        float w_n = 0.0f;
-        if (lane < a.k) {
-            const int64_t base = (int64_t)t_begin * a.k + lane;
-            row_n = a.dst_row[base];
-            e_n = a.topk[base];
-            if (a.topk_w) w_n = a.topk_w[base];
-        }
-        bool failed = false;
-        for (int j = 0; j < n; ++j) {
-            const int t = t_begin + j;
-            const int o = j % NO;
-            int row = row_n;
-            const int64_t e = e_n;
-            const float wgt = w_n;
-            if (j + 1 < n && lane < a.k) {
-                const int64_t base = (int64_t)(t + 1) * a.k + lane;
-                row_n = a.dst_row[base];
-                e_n = a.topk[base];
-                if (a.topk_w) w_n = a.topk_w[base];
-            }
-            if (row >= a.capacity) {
-                report(a.status, MOE_ERR_CAPACITY);
-                row = -1;
-            }
-            const unsigned dmask = __ballot_sync(kFull, row >= 0);
-            const bool ok = mbar_wait_bounded(&out_full[o], (uint32_t)((j / NO) & 1), a.timeout_ns);
-            if (!__all_sync(kFull, ok)) {
-                if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
-                failed = true;
-                break;
-            }
-            const uint8_t *codes = out_ring + (size_t)o * a.out_slot_bytes;
-            const float *sc = reinterpret_cast<const float *>(codes + a.H);
-            unsigned mm = dmask;
-            while (mm) {
-                const int jd = __ffs(mm) - 1;
-                mm &= mm - 1;
-                const int rowd = __shfl_sync(kFull, row, jd);
-                if (lane == 0) {
-                    bulk_store(a.recv_x + (int64_t)rowd * a.H, codes, (uint32_t)a.H, pol);
-                    if (a.scales_bulk)
-                        bulk_store(a.recv_scales + (int64_t)rowd * a.nb, sc, (uint32_t)scale_bytes, pol);
-                }
-                if (!a.scales_bulk)
-                    for (int b = lane; b < a.nb; b += 32) a.recv_scales[(int64_t)rowd * a.nb + b] = sc[b];
-                const int64_t ed = __shfl_sync(kFull, e, jd);
-                const int rd = (int)(ed / a.m);
-                if (lane < a.k) {
-                    const bool local = e >= 0 && e < a.E && (int)(e / a.m) == rd;
-                    if (a.recv_topk_idx) a.recv_topk_idx[(int64_t)rowd * a.k + lane] = local ? e - (int64_t)rd * a.m : -1;
-                    if (a.recv_topk_w) a.recv_topk_w[(int64_t)rowd * a.k + lane] = local ? wgt : 0.0f;
-                }
-                if (lane == 0 && a.recv_src) a.recv_src[rowd] = (int32_t)t;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                bulk_commit();
-                if (j >= 1) {                    // the previous row's stores have read their slot
-                    bulk_wait_read<1>();
-                    mbar_arrive_plain(&out_empty[(j - 1) % NO]);
-                }
-            }
-            __syncwarp();
-        }
-        if (lane == 0) {
-            bulk_wait_all();
-            if (!failed) mbar_arrive_plain(&out_empty[(n - 1) % NO]);
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------------- quantiser warps
-    const int qw = warp - 2;
-    const int half = lane >> 4, hl = lane & 15;
+    // ---------------------------------------------------------------- worker warps
+    const int wk = warp - 1;
     const int64_t n_items = (int64_t)n * nsl;
-    for (int64_t q = qw; q < n_items; q += quantizers) {
+    // destination rows of an item's token, lanes < k (prefetched one item ahead)
+    auto fetch_rows = [&](int64_t q) -> int {
+        const int t = t_begin + (int)(q / nsl);
+        return (q < n_items && lane < a.k) ? a.dst_row[(int64_t)t * a.k + lane] : -1;
+    };
+    int row_next = fetch_rows(wk);
+    for (int64_t q = wk; q < n_items; q += workers) {
         const int j = (int)(q / nsl);
         const int sl = (int)(q - (int64_t)j * nsl);
         const int t = t_begin + j;
-        const int si = j % NI, so = j % NO;
-        bool ok = mbar_wait_bounded(&in_full[si], (uint32_t)((j / NI) & 1), a.timeout_ns);
-        if (ok && j >= NO) ok = mbar_wait_bounded(&out_empty[so], (uint32_t)(((j / NO) - 1) & 1), a.timeout_ns);
+        const int si = j % NI;
+        int row = row_next;
+        row_next = fetch_rows(q + workers);
+        if (row >= a.capacity) {
+            if (sl == 0) report(a.status, MOE_ERR_CAPACITY);
+            row = -1;
+        }
+        const unsigned dmask = __ballot_sync(kFull, row >= 0);
+        const bool ok = mbar_wait_bounded(&in_full[si], (uint32_t)((j / NI) & 1), a.timeout_ns);
         if (!__all_sync(kFull, ok)) {
             if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
             break;
         }
         const uint8_t *src = in_ring + (size_t)si * a.row_bytes;
-        uint8_t *codes = out_ring + (size_t)so * a.out_slot_bytes;
-        float *sc = reinterpret_cast<float *>(codes + a.H);
-        const int b_begin = sl * a.slice_blocks;
-        const int b_end = min(a.nb, b_begin + a.slice_blocks);
-        for (int b0 = b_begin; b0 < b_end; b0 += 2) {
-            const int b = b0 + half;
+        const int b_begin = sl * kFp8SliceBlocks;
+        const int b_end = min(a.nb, b_begin + kFp8SliceBlocks);
+        const int quarter = lane >> 3, ql = lane & 7;
+        float my_scale = 0.0f;            // lane l < blocks of the slice: scale of block b_begin + l
+        for (int b0 = b_begin; b0 < b_end; b0 += 4) {
+            const int b = b0 + quarter;
             const bool act = b < b_end;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (act) v = *reinterpret_cast<const uint4 *>(src + (size_t)b * 256 + hl * 16);
-            uint2 q8;
-            const float scale = quantize_lane8(v, q8);
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
             if (act) {
-                *reinterpret_cast<uint2 *>(codes + (size_t)b * 128 + hl * 8) = q8;
-                if (hl == 0) {
-                    sc[b] = scale;
-                    if (a.x_scales) a.x_scales[(int64_t)t * a.nb + b] = scale;
-                }
+                lo = *reinterpret_cast<const uint4 *>(src + (size_t)b * 256 + ql * 32);
+                hi = *reinterpret_cast<const uint4 *>(src + (size_t)b * 256 + ql * 32 + 16);
+            }
+            uint4 q16;
+            const float scale = quantize_lane16(lo, hi, q16);
+            // block b0 + i's scale sits in lane 8 i; lane (b0 - b_begin) + i keeps it
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float si_ = __shfl_sync(kFull, scale, 8 * i);
+                if (lane == b0 - b_begin + i) my_scale = si_;
+            }
+            for (unsigned mm = dmask; mm; mm &= mm - 1) {
+                const int rowd = __shfl_sync(kFull, row, __ffs(mm) - 1);
+                if (act) *reinterpret_cast<uint4 *>(a.recv_x + (int64_t)rowd * a.H + (size_t)b * 128 + ql * 16) = q16;
             }
         }
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive_plain(&in_empty[si]);
-            mbar_arrive_plain(&out_full[so]);
+        if (lane == 0) mbar_arrive_plain(&in_empty[si]);   // the row's slice has been read
+        // scales of the slice: one coalesced store per destination row (and the source-side copy)
+        const int nblk = b_end - b_begin;
+        for (unsigned mm = dmask; mm; mm &= mm - 1) {
+            const int rowd = __shfl_sync(kFull, row, __ffs(mm) - 1);
+            if (lane < nblk) a.recv_scales[(int64_t)rowd * a.nb + b_begin + lane] = my_scale;
+        }
+        if (a.x_scales && lane < nblk) a.x_scales[(int64_t)t * a.nb + b_begin + lane] = my_scale;
+        // row metadata, written by the worker of slice 0
+        if (sl == 0) {
+            int rl = -1, el = 0;
+            float wgt = 0.0f;
+            if (lane < a.k) {
+                const int64_t e = a.topk[(int64_t)t * a.k + lane];
+                if (e >= 0 && e < a.E) {
+                    rl = (int)e / a.m;
+                    el = (int)e - rl * a.m;
+                }
+                if (a.topk_w) wgt = a.topk_w[(int64_t)t * a.k + lane];
+            }
+            for (unsigned mm = dmask; mm; mm &= mm - 1) {
+                const int jd = __ffs(mm) - 1;
+                const int rowd = __shfl_sync(kFull, row, jd);
+                const int rd = __shfl_sync(kFull, rl, jd);
+                if (lane < a.k) {
+                    const bool local = rl == rd;
+                    if (a.recv_topk_idx) a.recv_topk_idx[(int64_t)rowd * a.k + lane] = local ? (int64_t)el : -1;
+                    if (a.recv_topk_w) a.recv_topk_w[(int64_t)rowd * a.k + lane] = local ? wgt : 0.0f;
+                }
+                if (lane == 0 && a.recv_src) a.recv_src[rowd] = (int32_t)t;
+            }
         }
     }
 }
@@ -524,28 +584,22 @@ int launch_dispatch(const DispatchLaunch &L) {
         f.recv_x = a.recv_x; f.recv_scales = a.recv_scales; f.recv_topk_idx = a.recv_topk_idx;
         f.recv_topk_w = a.recv_topk_w; f.recv_src = a.recv_src; f.x_scales = a.x_scales;
         f.status = a.status;
-        f.slice_blocks = 8;
-        f.num_slices = (f.nb + f.slice_blocks - 1) / f.slice_blocks;
-        f.out_slot_bytes = (int)round_up((int64_t)f.H + (int64_t)f.nb * 4, 16);
-        f.scales_bulk = ((f.nb * 4) % 16 == 0) ? 1 : 0;
+        f.num_slices = (f.nb + kFp8SliceBlocks - 1) / kFp8SliceBlocks;
         f.l2_hints = a.l2_hints;
         f.timeout_ns = a.timeout_ns;
-        const size_t head = 4 * kFp8MaxSlots * 8;
+        const size_t head = 2 * kFp8MaxSlots * 8;
         const size_t optin = device_smem_optin();
-        f.n_out = std::max(2, std::min(kFp8MaxSlots, tu.fp8_out_slots));
         f.n_in = std::max(2, std::min(kFp8MaxSlots, tu.fp8_in_slots));
-        // shrink the rings until they fit (the input ring first, keeping at least two slots each)
-        while (head + (size_t)f.n_in * f.row_bytes + (size_t)f.n_out * f.out_slot_bytes > optin && f.n_in > 2) --f.n_in;
-        while (head + (size_t)f.n_in * f.row_bytes + (size_t)f.n_out * f.out_slot_bytes > optin && f.n_out > 2) --f.n_out;
-        const size_t smem = head + (size_t)f.n_in * f.row_bytes + (size_t)f.n_out * f.out_slot_bytes;
-        if (smem <= optin) {
+        while (head + (size_t)f.n_in * f.row_bytes > optin && f.n_in > 2) --f.n_in;
+        const size_t smem = head + (size_t)f.n_in * f.row_bytes;
+        if (smem <= optin && f.row_bytes < (1 << 20)) {
             if (ensure_dynamic_smem((const void *)dispatch_fp8_rows_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
-            const int qwarps = std::max(1, std::min(16, tu.fp8_quant_warps));
+            const int workers = std::max(1, std::min(20, tu.fp8_quant_warps));
             const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
-            dispatch_fp8_rows_kernel<<<grid, (qwarps + 2) * 32, smem, st>>>(f);
+            dispatch_fp8_rows_kernel<<<grid, (workers + 1) * 32, smem, st>>>(f);
             return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
         }
-        // rows too large for the rings: fall through to the chunked kernel
+        // rows too large for the ring: fall through to the chunked kernel
     }
 
     // chunking: equal chunks no larger than the tuned maximum

@@ -23,15 +23,17 @@
 //           Each (tile, rank) status is one 64-bit word {flag:32 | value:32},
 //           written in one store, so value and flag change together. Waits
 //           are bounded (MOE_ERR_TIMEOUT).
-//   last    the last CTA to finish (done counter) writes per-rank and
-//           per-expert counts and their exclusive prefixes.
 //   pass 2  the owning entries get their receive rows.
+//   last    the last CTA to finish (done counter) writes the per-expert counts
+//           and their exclusive prefix.
 // When every tile fits on the GPU at once, the kernel is launched
-// cooperatively (all CTAs co-resident, tile = blockIdx): after the last CTA
-// publishes the prefixes, every tile waits (bounded) for them and writes final
-// global rows -- one launch. Otherwise tiles are claimed by an atomic ticket
-// (so every predecessor of a tile is already resident), pass 2 writes in-rank
-// positions, and a second small kernel adds rank_prefix[r].
+// cooperatively (all CTAs co-resident, tile = blockIdx): the last tile's
+// inclusive prefix is the vector of rank totals, so every tile waits
+// (bounded) for it, scans it in shared memory into rank_prefix and writes
+// final global rows -- one launch. Otherwise tiles are claimed by an atomic
+// ticket (so every predecessor of a tile is already resident), pass 2 writes
+// in-rank positions, the last CTA also writes the rank counts and prefix, and
+// a second small kernel adds rank_prefix[r].
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -54,8 +56,7 @@ constexpr uint64_t kFlagInclusive = 2ull << 32;
 struct WsHeader {
     uint32_t ticket;
     uint32_t done;
-    uint32_t ready;      // cooperative mode: prefixes published
-    uint32_t pad[29];
+    uint32_t pad[30];
 };
 static_assert(sizeof(WsHeader) == 128, "header is one 128-byte line");
 
@@ -75,19 +76,59 @@ inline WsLayout ws_layout(int T, int E, int R) {
 }
 
 // Shared memory: bitmap u32 [R][kWords] | word prefix u16 [R][kWords] |
-// exclusive prefix i32 [R] | expert histogram i32 [E] | owned rank i16 [kTile * k]
+// exclusive prefix i32 [R] | tile aggregate i32 [R] | rank totals i32 [R] |
+// expert histogram i32 [E] | owned rank i16 [kTile * k]
 struct SmemLayout {
-    size_t wprefix, excl, hist, own, total;
+    size_t wprefix, excl, agg, tot, hist, own, total;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int E, int R, int k) {
     SmemLayout s;
     s.wprefix = align_up((size_t)R * kWords * 4, 16);
     s.excl = s.wprefix + align_up((size_t)R * kWords * 2, 16);
-    s.hist = s.excl + align_up((size_t)R * 4, 16);
+    s.agg = s.excl + align_up((size_t)R * 4, 16);
+    s.tot = s.agg + align_up((size_t)R * 4, 16);
+    s.hist = s.tot + align_up((size_t)R * 4, 16);
     s.own = s.hist + align_up((size_t)E * 4, 16);
     s.total = s.own + align_up((size_t)kTile * k * 2, 16);
     return s;
+}
+
+// In-place exclusive scan of n int32 values in shared memory; returns the total.
+__device__ int32_t smem_exclusive_scan(int32_t *v, int n) {
+    __shared__ int32_t warp_sums[kWarps];
+    __shared__ int32_t total;
+    const int per = (n + kThreads - 1) / kThreads;
+    const int lo = min(n, (int)threadIdx.x * per), hi = min(n, lo + per);
+    int32_t local = 0;
+    for (int i = lo; i < hi; ++i) local += v[i];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int32_t run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int32_t t = warp_sums[w];
+            warp_sums[w] = run;
+            run += t;
+        }
+        total = run;
+    }
+    __syncthreads();
+    int32_t run = warp_sums[warp] + incl - local;
+    for (int i = lo; i < hi; ++i) {
+        const int32_t x = v[i];
+        v[i] = run;
+        run += x;
+    }
+    __syncthreads();
+    return total;
 }
 
 // Exclusive scan of n int32 counts (read from `in`, copied to `copy_out` when
@@ -151,11 +192,12 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem);
     uint16_t *wprefix = reinterpret_cast<uint16_t *>(smem + sl.wprefix);
     int32_t *excl = reinterpret_cast<int32_t *>(smem + sl.excl);
+    int32_t *aggs = reinterpret_cast<int32_t *>(smem + sl.agg);
+    int32_t *tot = reinterpret_cast<int32_t *>(smem + sl.tot);
     int32_t *hist = reinterpret_cast<int32_t *>(smem + sl.hist);
     int16_t *own = reinterpret_cast<int16_t *>(smem + sl.own);
     __shared__ int s_tile;
     __shared__ int s_last;
-    __shared__ int s_ok;
 
     WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
     int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
@@ -182,7 +224,7 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
         if (act) {
             const int64_t e = ld_nc_i64(a.topk + (int64_t)(t0 + tl) * k + j);
             if (e >= 0 && e < E) {
-                r = (int)(e / a.m);
+                r = (int)e / a.m;
                 atomicAdd(&hist[(int)e], 1);
             } else if (e != -1) {
                 report(a.status, MOE_ERR_BAD_TOPK);
@@ -207,6 +249,7 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
             run += __popc(bitmap[r * kWords + w]);
         }
         excl[r] = (int32_t)run;   // holds the aggregate until the lookback below
+        aggs[r] = (int32_t)run;
         if (publish) st_relaxed_gpu_u64(my_status + r, (tile == 0 ? kFlagInclusive : kFlagAggregate) | run);
     }
     __syncthreads();
@@ -282,53 +325,41 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
         }
     }
 
-    // ---- the last CTA to finish writes counts and prefixes
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(&hdr->done, 1u) == (unsigned)(a.num_tiles - 1));
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
+    if (kCooperative) {
+        // ---- rank totals = inclusive prefix of the last tile (read as it is published)
         const uint64_t *last_status = tile_status + (size_t)(a.num_tiles - 1) * R;
         for (int r = threadIdx.x; r < R; r += kThreads) {
-            const uint64_t w = ld_relaxed_gpu_u64(last_status + r);
-            if ((w & 0xffffffff00000000ull) != kFlagInclusive) report(a.status, MOE_ERR_TIMEOUT);
-            a.num_tokens_per_rank[r] = (int32_t)(uint32_t)w;
+            int32_t v = excl[r] + aggs[r];
+            if (tile != a.num_tiles - 1) {
+                uint64_t w = ld_relaxed_gpu_u64(last_status + r), deadline = 0;
+                while ((w & 0xffffffff00000000ull) != kFlagInclusive) {
+                    const uint64_t now = globaltimer_ns();
+                    if (deadline == 0) {
+                        deadline = now + a.timeout_ns;
+                    } else if (now > deadline) {
+                        report(a.status, MOE_ERR_TIMEOUT);
+                        break;
+                    }
+                    w = ld_relaxed_gpu_u64(last_status + r);
+                }
+                v = (int32_t)(uint32_t)w;
+            }
+            tot[r] = v;
         }
-        __threadfence();
         __syncthreads();
-        block_exclusive_scan(a.num_tokens_per_rank, R, nullptr, a.rank_prefix);
-        block_exclusive_scan(ws_expert, E, a.num_tokens_per_expert, a.expert_prefix);
-        if (kCooperative) {
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) st_release_gpu_u32(&hdr->ready, 1u);
+        if (tile == a.num_tiles - 1)
+            for (int r = threadIdx.x; r < R; r += kThreads) a.num_tokens_per_rank[r] = tot[r];
+        const int32_t n_recv = smem_exclusive_scan(tot, R);   // tot -> rank_prefix
+        for (int r = threadIdx.x; r < R; r += kThreads) {
+            excl[r] += tot[r];
+            if (tile == a.num_tiles - 1) a.rank_prefix[r] = tot[r];
         }
+        if (tile == a.num_tiles - 1 && threadIdx.x == 0) a.rank_prefix[R] = n_recv;
+        __syncthreads();
     }
 
-    // ---- pass 2: receive rows of the owning entries
-    if (kCooperative) {
-        // wait (bounded) for the prefixes, then global rows directly
-        if (threadIdx.x == 0) {
-            int ok = 1;
-            uint64_t deadline = 0;
-            while (ld_acquire_gpu_u32(&hdr->ready) == 0u) {
-                const uint64_t now = globaltimer_ns();
-                if (deadline == 0) {
-                    deadline = now + a.timeout_ns;
-                } else if (now > deadline) {
-                    report(a.status, MOE_ERR_TIMEOUT);
-                    ok = 0;
-                    break;
-                }
-            }
-            s_ok = ok;
-        }
-        __syncthreads();
-        if (s_ok)
-            for (int r = threadIdx.x; r < R; r += kThreads) excl[r] += __ldcg(a.rank_prefix + r);
-        __syncthreads();
-    }
+    // ---- pass 2: receive rows of the owning entries (global rows when cooperative,
+    //      in-rank positions otherwise)
     for (int i = threadIdx.x; i < tcount * k; i += kThreads) {
         const int r = own[i];
         int32_t v = -1;
@@ -339,13 +370,36 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
         }
         a.token_dst_row[(int64_t)t0 * k + i] = v;
     }
+
+    // ---- the last CTA to finish writes the expert counts and prefix (and, when
+    //      not cooperative, the rank counts and prefix)
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&hdr->done, 1u) == (unsigned)(a.num_tiles - 1));
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (!kCooperative) {
+        const uint64_t *last_status = tile_status + (size_t)(a.num_tiles - 1) * R;
+        for (int r = threadIdx.x; r < R; r += kThreads) {
+            const uint64_t w = ld_relaxed_gpu_u64(last_status + r);
+            if ((w & 0xffffffff00000000ull) != kFlagInclusive) report(a.status, MOE_ERR_TIMEOUT);
+            a.num_tokens_per_rank[r] = (int32_t)(uint32_t)w;
+        }
+        __threadfence();
+        __syncthreads();
+        block_exclusive_scan(a.num_tokens_per_rank, R, nullptr, a.rank_prefix);
+    } else if (a.unpublished_tile == a.num_tiles - 1) {
+        report(a.status, MOE_ERR_TIMEOUT);   // test hook: the last tile never published its totals
+    }
+    block_exclusive_scan(ws_expert, E, a.num_tokens_per_expert, a.expert_prefix);
 }
 
 __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, int m,
                                    const int32_t *__restrict__ rank_prefix, int32_t *__restrict__ token_dst_row) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t v = token_dst_row[i];
-        if (v >= 0) token_dst_row[i] = v + rank_prefix[(int)(topk[i] / m)];
+        if (v >= 0) token_dst_row[i] = v + rank_prefix[(int)topk[i] / m];
     }
 }
 

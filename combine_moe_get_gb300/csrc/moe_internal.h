@@ -22,7 +22,7 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 struct Tuning {
     int dispatch_warps, dispatch_stages, dispatch_chunk;
     int combine_warps, combine_chunk, combine_ring_bytes;   // consumer warps, max chunk, ring budget
-    int fp8_rows, fp8_in_slots, fp8_out_slots, fp8_quant_warps;   // FP8 row pipeline
+    int fp8_rows, fp8_in_slots, fp8_quant_warps;   // FP8 row pipeline: on/off, input ring slots, worker warps
     int ctas_per_sm;
     int l2_hints;  // bit 0: evict-first on single-use loads; bit 1: evict-first on stores
 };
