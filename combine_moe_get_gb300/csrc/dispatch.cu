@@ -411,7 +411,8 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__global__ void __launch_bounds__(32 * 21, 1) dispatch_fp8_rows_kernel(const Fp8Args a) {
+// 80 registers (no spills) allow 1 producer + 24 worker warps per SM
+__global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *in_full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *in_empty = in_full + kFp8MaxSlots;
@@ -594,7 +595,16 @@ int launch_dispatch(const DispatchLaunch &L) {
         const size_t smem = head + (size_t)f.n_in * f.row_bytes;
         if (smem <= optin && f.row_bytes < (1 << 20)) {
             if (ensure_dynamic_smem((const void *)dispatch_fp8_rows_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
-            const int workers = std::max(1, std::min(20, tu.fp8_quant_warps));
+            // as many of the requested workers as the kernel's register use allows in one CTA
+            static int max_threads[64] = {0};
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+            if (max_threads[dev] == 0) {
+                cudaFuncAttributes fa;
+                if (cudaFuncGetAttributes(&fa, (const void *)dispatch_fp8_rows_kernel) != cudaSuccess) return MOE_ERR_CUDA;
+                max_threads[dev] = fa.maxThreadsPerBlock;
+            }
+            const int workers = std::max(1, std::min({24, tu.fp8_quant_warps, max_threads[dev] / 32 - 1}));
             const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
             dispatch_fp8_rows_kernel<<<grid, (workers + 1) * 32, smem, st>>>(f);
             return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
