@@ -12,7 +12,7 @@
 // One CTA per tile of kTile tokens:
 //   pass 1  lanes hold one top-k entry each; __match_any_sync de-duplicates the
 //           (token, rank) pairs, the lowest lane owning each; a shared bitmap
-//           [rank][token-word] records membership, a shared histogram counts
+//           [token-word][rank] records membership, a shared histogram counts
 //           experts, and each entry's owned rank (or -1) is kept in shared
 //           memory for pass 2.
 //   scan    per rank, popcounts give the tile aggregate, published for all
@@ -75,7 +75,7 @@ inline WsLayout ws_layout(int T, int E, int R) {
     return w;
 }
 
-// Shared memory: bitmap u32 [R][kWords] | word prefix u16 [R][kWords] |
+// Shared memory: bitmap u32 [kWords][R] | word prefix u16 [R][kWords] |
 // exclusive prefix i32 [R] | tile aggregate i32 [R] | rank totals i32 [R] |
 // expert histogram i32 [E] | owned rank i16 [kTile * k]
 struct SmemLayout {
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
         const int key = (r >= 0) ? (sub * R + r) : -(lane + 1);
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         const bool owner = r >= 0 && (__ffs(peers) - 1) == lane;
-        if (owner) atomicOr(&bitmap[r * kWords + (tl >> 5)], 1u << (tl & 31));
+        if (owner) atomicOr(&bitmap[(tl >> 5) * R + r], 1u << (tl & 31));
         if (act) own[tl * k + j] = (int16_t)(owner ? r : -1);
     }
     __syncthreads();
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
 #pragma unroll
         for (int w = 0; w < kWords; ++w) {
             wprefix[r * kWords + w] = (uint16_t)run;
-            run += __popc(bitmap[r * kWords + w]);
+            run += __popc(bitmap[w * R + r]);
         }
         excl[r] = (int32_t)run;   // holds the aggregate until the lookback below
         aggs[r] = (int32_t)run;
@@ -305,24 +305,29 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
         if (h) atomicAdd(ws_expert + e, h);
     }
 
-    // ---- is_token_in_rank rows of this tile, expanded from the bitmap
-    uint8_t *dst = a.is_token_in_rank + (int64_t)t0 * R;
-    const int nbytes = tcount * R;
-    if ((R & 3) == 0) {
-        uint32_t *dst4 = reinterpret_cast<uint32_t *>(dst);
-        for (int i = threadIdx.x; i < nbytes / 4; i += kThreads) {
-            const int tl = (i * 4) / R, r0 = (i * 4) - tl * R;
-            uint32_t v = 0;
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                v |= ((bitmap[(r0 + b) * kWords + (tl >> 5)] >> (tl & 31)) & 1u) << (8 * b);
-            dst4[i] = v;
+    // ---- the last CTA to finish its histogram writes the expert counts and prefix
+    //      (and, when not cooperative, the rank counts and prefix); the other
+    //      tiles go on meanwhile
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&hdr->done, 1u) == (unsigned)(a.num_tiles - 1));
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        if (!kCooperative) {
+            const uint64_t *last_status = tile_status + (size_t)(a.num_tiles - 1) * R;
+            for (int r = threadIdx.x; r < R; r += kThreads) {
+                const uint64_t w = ld_relaxed_gpu_u64(last_status + r);
+                if ((w & 0xffffffff00000000ull) != kFlagInclusive) report(a.status, MOE_ERR_TIMEOUT);
+                a.num_tokens_per_rank[r] = (int32_t)(uint32_t)w;
+            }
+            __threadfence();
+            __syncthreads();
+            block_exclusive_scan(a.num_tokens_per_rank, R, nullptr, a.rank_prefix);
+        } else if (a.unpublished_tile == a.num_tiles - 1) {
+            report(a.status, MOE_ERR_TIMEOUT);   // test hook: the last tile never published its totals
         }
-    } else {
-        for (int i = threadIdx.x; i < nbytes; i += kThreads) {
-            const int tl = i / R, r = i - tl * R;
-            dst[i] = (uint8_t)((bitmap[r * kWords + (tl >> 5)] >> (tl & 31)) & 1u);
-        }
+        block_exclusive_scan(ws_expert, E, a.num_tokens_per_expert, a.expert_prefix);
     }
 
     if (kCooperative) {
@@ -365,34 +370,32 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
         int32_t v = -1;
         if (r >= 0) {
             const int tl = i / k;
-            const uint32_t word = bitmap[r * kWords + (tl >> 5)];
+            const uint32_t word = bitmap[(tl >> 5) * R + r];
             v = excl[r] + wprefix[r * kWords + (tl >> 5)] + __popc(word & ((1u << (tl & 31)) - 1u));
         }
         a.token_dst_row[(int64_t)t0 * k + i] = v;
     }
 
-    // ---- the last CTA to finish writes the expert counts and prefix (and, when
-    //      not cooperative, the rank counts and prefix)
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(&hdr->done, 1u) == (unsigned)(a.num_tiles - 1));
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (!kCooperative) {
-        const uint64_t *last_status = tile_status + (size_t)(a.num_tiles - 1) * R;
-        for (int r = threadIdx.x; r < R; r += kThreads) {
-            const uint64_t w = ld_relaxed_gpu_u64(last_status + r);
-            if ((w & 0xffffffff00000000ull) != kFlagInclusive) report(a.status, MOE_ERR_TIMEOUT);
-            a.num_tokens_per_rank[r] = (int32_t)(uint32_t)w;
+    // ---- is_token_in_rank rows of this tile, expanded from the bitmap
+    uint8_t *dst = a.is_token_in_rank + (int64_t)t0 * R;
+    const int nbytes = tcount * R;
+    if ((R & 3) == 0) {
+        uint32_t *dst4 = reinterpret_cast<uint32_t *>(dst);
+        for (int i = threadIdx.x; i < nbytes / 4; i += kThreads) {
+            const int tl = (i * 4) / R, r0 = (i * 4) - tl * R;
+            uint32_t v = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                v |= ((bitmap[(tl >> 5) * R + r0 + b] >> (tl & 31)) & 1u) << (8 * b);
+            dst4[i] = v;
         }
-        __threadfence();
-        __syncthreads();
-        block_exclusive_scan(a.num_tokens_per_rank, R, nullptr, a.rank_prefix);
-    } else if (a.unpublished_tile == a.num_tiles - 1) {
-        report(a.status, MOE_ERR_TIMEOUT);   // test hook: the last tile never published its totals
+    } else {
+        for (int i = threadIdx.x; i < nbytes; i += kThreads) {
+            const int tl = i / R, r = i - tl * R;
+            dst[i] = (uint8_t)((bitmap[(tl >> 5) * R + r] >> (tl & 31)) & 1u);
+        }
     }
-    block_exclusive_scan(ws_expert, E, a.num_tokens_per_expert, a.expert_prefix);
+
 }
 
 __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, int m,
