@@ -252,43 +252,64 @@ def run_ours(args, world, rank, local):
     # attribute setting happens during capture) and replayed, so host-side
     # submission cost never leaves the GPU idle inside the timed events.
     timing = "cuda-graph replay"
+    mean = statistics.fmean
     try:
-        evs_g = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+        # the step alone: events only at its ends (an event between two kernels
+        # adds its own gap to the step)
+        ev_step = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            one(evs_g)
+            ev_step[0].record()
+            one()
+            ev_step[1].record()
+        # the per-kernel breakdown: events between the kernels
+        evs_k = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+        graph_k = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_k):
+            one(evs_k)
         graph.replay()
+        graph_k.replay()
         torch.cuda.synchronize()
     except Exception as exc:  # eager fallback (e.g. no external events in this torch)
-        graph, timing = None, f"eager ({type(exc).__name__})"
+        graph, graph_k, timing = None, None, f"eager ({type(exc).__name__})"
 
-    times = []
+    def timed_step():
+        """One step (after an untimed L2 flush): (step ms, [layout, dispatch, combine] ms or None)."""
+        flush.zero_()
+        if graph is not None:
+            graph.replay()
+            torch.cuda.synchronize()
+            return ev_step[0].elapsed_time(ev_step[1]), None
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        one(ev)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[3]), [ev[j].elapsed_time(ev[j + 1]) for j in (0, 1, 2)]
+
+    step_ms, parts = [], []
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(device.index) as clk:
         for i in range(args.steps):
-            flush.zero_()                       # L2 flush between steps, outside the events
-            if graph is not None:
-                graph.replay()
-                torch.cuda.synchronize()
-                times.append([evs_g[0].elapsed_time(evs_g[j]) for j in (1, 2, 3)] +
-                             [evs_g[j].elapsed_time(evs_g[j + 1]) for j in (0, 1, 2)])
-            else:
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-                one(ev)
-                torch.cuda.synchronize()
-                times.append([ev[0].elapsed_time(ev[j]) for j in (1, 2, 3)] +
-                             [ev[j].elapsed_time(ev[j + 1]) for j in (0, 1, 2)])
+            ms, p = timed_step()
+            step_ms.append(ms)
+            if p:
+                parts.append(p)
         torch.cuda.synchronize()
     barrier(world)
     moe.check_status(st.status, "timed steps")
     clocks = clk.summary()
 
-    step_ms = [t[2] for t in times]
-    lay_ms = [t[3] for t in times]
-    dis_ms = [t[4] for t in times]
-    com_ms = [t[5] for t in times]
-    mean = statistics.fmean
+    # per-kernel breakdown (outside the timed region): the graph with events between kernels
+    if graph_k is not None:
+        for i in range(args.steps):
+            flush.zero_()
+            graph_k.replay()
+            torch.cuda.synchronize()
+            parts.append([evs_k[j].elapsed_time(evs_k[j + 1]) for j in (0, 1, 2)])
+        moe.check_status(st.status, "kernel breakdown")
+    lay_ms = [p[0] for p in parts]
+    dis_ms = [p[1] for p in parts]
+    com_ms = [p[2] for p in parts]
     ms_per_step = max_over_ranks(mean(step_ms), world, device)
     tokens_per_s = world * T / (ms_per_step / 1e3)
 
@@ -354,7 +375,7 @@ def run_ours(args, world, rank, local):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes": bytes_bf16},
         "kernels": kern,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,   # per step: the cooperative layout kernel, dispatch, combine
         "clocks": clocks,
         "e2e": e2e,
     }
