@@ -71,6 +71,8 @@ def _load():
     lib.moe_dispatch.restype = _I
     lib.moe_combine.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
     lib.moe_combine.restype = _I
+    lib.moe_combine_ex.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
+    lib.moe_combine_ex.restype = _I
     return lib
 
 
@@ -166,29 +168,44 @@ class Dispatched:
     x_scales: Optional[torch.Tensor]          # [T, H/128] fp32 (FP8)
 
 
+MOE_DISPATCH_BF16 = 0
+MOE_DISPATCH_QUANTIZE_FP8 = 1
+MOE_DISPATCH_FP8 = 2
+
+
 def moe_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
                  num_experts: int, num_ranks: int, token_dst_row: torch.Tensor, recv_capacity: int, *,
-                 quantize_fp8: bool = False, out: Optional[Dispatched] = None, with_metadata: bool = True,
+                 quantize_fp8: bool = False, x_scales: Optional[torch.Tensor] = None,
+                 out: Optional[Dispatched] = None, with_metadata: bool = True,
                  status: Optional[torch.Tensor] = None, stream=None) -> Dispatched:
-    """Row copies (bf16, or fused E4M3 quantisation) and per-row metadata."""
+    """Row copies and per-row metadata. ``x`` bf16 is copied as is, or quantised
+    to E4M3 with per-128 scales when ``quantize_fp8``; ``x`` uint8 (E4M3 codes)
+    is copied together with its ``x_scales`` [T, H/128]."""
     T, H = x.shape
     k = topk_idx.shape[1]
     dev = x.device
+    fp8_in = x.dtype == torch.uint8
+    mode = MOE_DISPATCH_FP8 if fp8_in else (MOE_DISPATCH_QUANTIZE_FP8 if quantize_fp8 else MOE_DISPATCH_BF16)
+    fp8_out = mode != MOE_DISPATCH_BF16
+    if fp8_in and x_scales is None:
+        raise ValueError("E4M3 input needs its x_scales")
     if out is None:
         nb = H // 128
         out = Dispatched(
-            recv_x=torch.empty(recv_capacity, H, dtype=torch.uint8 if quantize_fp8 else torch.bfloat16, device=dev),
-            recv_x_scales=torch.empty(recv_capacity, nb, dtype=torch.float32, device=dev) if quantize_fp8 else None,
+            recv_x=torch.empty(recv_capacity, H, dtype=torch.uint8 if fp8_out else torch.bfloat16, device=dev),
+            recv_x_scales=torch.empty(recv_capacity, nb, dtype=torch.float32, device=dev) if fp8_out else None,
             recv_topk_idx=torch.empty(recv_capacity, k, dtype=torch.int64, device=dev) if with_metadata else None,
             recv_topk_weights=(torch.empty(recv_capacity, k, dtype=torch.float32, device=dev)
                                if with_metadata else None),
             recv_src_idx=torch.empty(recv_capacity, dtype=torch.int32, device=dev) if with_metadata else None,
-            x_scales=torch.empty(T, nb, dtype=torch.float32, device=dev) if quantize_fp8 else None)
+            x_scales=(x_scales if fp8_in else
+                      (torch.empty(T, nb, dtype=torch.float32, device=dev) if quantize_fp8 else None)))
     status = new_status(dev) if status is None else status
+    scales_arg = x_scales if fp8_in else out.x_scales
     code = LIB.moe_dispatch(_ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), k, num_experts, num_ranks,
-                            _ptr(token_dst_row), recv_capacity, int(bool(quantize_fp8)), _ptr(out.recv_x),
+                            _ptr(token_dst_row), recv_capacity, mode, _ptr(out.recv_x),
                             _ptr(out.recv_x_scales), _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights),
-                            _ptr(out.recv_src_idx), _ptr(out.x_scales), _ptr(status), _stream(stream))
+                            _ptr(out.recv_src_idx), _ptr(scales_arg), _ptr(status), _stream(stream))
     _check(code, "moe_dispatch")
     return out
 
@@ -205,3 +222,23 @@ def moe_combine(partial: torch.Tensor, token_dst_row: torch.Tensor, *, out: Opti
                            _stream(stream))
     _check(code, "moe_combine")
     return out
+
+
+def moe_combine_ex(partial: torch.Tensor, token_dst_row: torch.Tensor, *, row_weights: Optional[torch.Tensor] = None,
+                   recv_topk_weights: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                   combined_topk_weights: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                   stream=None) -> tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Combine with per-row weights (fma per term) and/or the reduction of the
+    received top-k weights back to [T, k]. Returns (out, combined_topk_weights)."""
+    rows, H = partial.shape
+    T, k = token_dst_row.shape
+    dev = partial.device
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev) if out is None else out
+    if recv_topk_weights is not None and combined_topk_weights is None:
+        combined_topk_weights = torch.empty(T, k, dtype=torch.float32, device=dev)
+    status = new_status(dev) if status is None else status
+    code = LIB.moe_combine_ex(_ptr(partial), rows, T, H, k, _ptr(token_dst_row), _ptr(row_weights),
+                              _ptr(recv_topk_weights), _ptr(combined_topk_weights), _ptr(out), _ptr(status),
+                              _stream(stream))
+    _check(code, "moe_combine_ex")
+    return out, combined_topk_weights

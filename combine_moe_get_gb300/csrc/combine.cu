@@ -29,6 +29,9 @@
 //                  packed add.rn.f32x2: 32 independent fp32-pair chains per
 //                  lane), store 16-byte bf16 vectors and arrive on the unit's
 //                  "empty" mbarrier (one arrival per slice).
+// Options (moe_combine_ex): per-row weights turn each add into a single-rounding
+// fused multiply-add (packed fma.rn.f32x2), and the received top-k weights can
+// be reduced back to [T, k] in the same ascending order.
 // Every wait is bounded (MOE_ERR_TIMEOUT on expiry).
 #include <algorithm>
 #include <cstdint>
@@ -44,7 +47,7 @@ namespace {
 
 constexpr int kUnits = 16;       // unit ring entries
 constexpr int kVMax = 8;         // 16-byte vectors per lane per slice -> slice <= 32 * 8 * 16 = 4096 B
-constexpr int kHeadBytes = 512;  // full[kUnits] + empty[kUnits] mbarriers, unit entries
+constexpr int kHeadBytes = 4608; // full[kUnits] + empty[kUnits] mbarriers, unit entries
 constexpr unsigned kFull = 0xffffffffu;
 
 struct CombineArgs {
@@ -53,6 +56,9 @@ struct CombineArgs {
     int num_rows;
     int T, k;
     const int32_t *dst_row;
+    const float *row_weights;        // optional: weight of each receive row
+    const float *recv_topk_weights;  // optional, with combined_topk_weights: [rows, k] -> [T, k]
+    float *combined_topk_weights;
     uint8_t *out;
     int32_t *status;
     int chunk_bytes, num_chunks;
@@ -63,9 +69,12 @@ struct CombineArgs {
 };
 
 struct UnitEntry {
-    int D;       // rows of the unit
-    int start;   // first ring slot (the unit's rows occupy start, start+1, ... mod num_slots)
+    int D;                   // rows of the unit
+    int start;               // first ring slot (the unit's rows occupy start, start+1, ... mod num_slots)
+    float w[MOE_MAX_TOPK];   // weight of the row in slot start + d (weighted combine)
+    int row[MOE_MAX_TOPK];   // receive row in slot start + d
 };
+static_assert(2 * kUnits * 8 + kUnits * sizeof(UnitEntry) <= kHeadBytes, "unit ring header");
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -74,6 +83,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 __device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
 }
 
@@ -100,6 +115,7 @@ __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
     return v;
 }
 
+template <bool kWeighted>
 __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -130,6 +146,7 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
         const uint64_t pol = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
         int64_t head = 0, tail = 0, oldest = 0;
         int row = -1, pos = 0, D = 0;
+        float w_cur = 1.0f;
         int row_next = (lane < a.k) ? a.dst_row[(int64_t)t_begin * a.k + lane] : -1;
         for (int64_t j = 0; j < n_units; ++j) {
             const int tl = (int)(j / nch), c = (int)(j - (int64_t)tl * nch);
@@ -143,6 +160,7 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
                     report(a.status, MOE_ERR_CAPACITY);
                     row = -1;
                 }
+                if (kWeighted && row >= 0) w_cur = a.row_weights[row];   // used after the wait for slots
                 const unsigned vmask = __ballot_sync(kFull, row >= 0);
                 D = __popc(vmask);
                 pos = 0;
@@ -170,9 +188,13 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
             if (lane == 0) {
                 entry[e].D = D;
                 entry[e].start = (int)(head % NS);
-                mbar_arrive_expect_tx(&full[e], (uint32_t)D * nbytes);
+            }
+            if (row >= 0) {
+                entry[e].row[pos] = row;
+                if (kWeighted) entry[e].w[pos] = w_cur;
             }
             __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[e], (uint32_t)D * nbytes);
             if (row >= 0) {
                 const int slot = (int)((head + pos) % NS);
                 bulk_load(ring + (size_t)slot * CH, a.partial + (int64_t)row * a.row_bytes + off, nbytes, &full[e],
@@ -211,17 +233,41 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
             for (int p = 0; p < 4; ++p) acc[v][p] = 0ull;   // +0.0f pairs
         for (int d = 0; d < D; ++d) {
             const uint8_t *base = ring + (size_t)slot * CH + soff + lane * 16;
+            uint64_t ww = 0;
+            if (kWeighted) {
+                const uint32_t wb = __float_as_uint(entry[e].w[d]);
+                ww = (uint64_t)wb | ((uint64_t)wb << 32);
+            }
 #pragma unroll
             for (int v = 0; v < kVMax; ++v) {
                 if (lane + 32 * v < nvec) {
                     const uint4 qv = lds128(base + v * 512);
-                    acc[v][0] = add_f32x2(acc[v][0], widen_bf16x2(qv.x));
-                    acc[v][1] = add_f32x2(acc[v][1], widen_bf16x2(qv.y));
-                    acc[v][2] = add_f32x2(acc[v][2], widen_bf16x2(qv.z));
-                    acc[v][3] = add_f32x2(acc[v][3], widen_bf16x2(qv.w));
+                    if (kWeighted) {   // acc = fma(w, x, acc), one rounding per term
+                        acc[v][0] = fma_f32x2(ww, widen_bf16x2(qv.x), acc[v][0]);
+                        acc[v][1] = fma_f32x2(ww, widen_bf16x2(qv.y), acc[v][1]);
+                        acc[v][2] = fma_f32x2(ww, widen_bf16x2(qv.z), acc[v][2]);
+                        acc[v][3] = fma_f32x2(ww, widen_bf16x2(qv.w), acc[v][3]);
+                    } else {
+                        acc[v][0] = add_f32x2(acc[v][0], widen_bf16x2(qv.x));
+                        acc[v][1] = add_f32x2(acc[v][1], widen_bf16x2(qv.y));
+                        acc[v][2] = add_f32x2(acc[v][2], widen_bf16x2(qv.z));
+                        acc[v][3] = add_f32x2(acc[v][3], widen_bf16x2(qv.w));
+                    }
                 }
             }
             if (++slot == NS) slot = 0;
+        }
+        // received top-k weights back to [T, k]: by the consumer of the first slice of the first chunk
+        if (a.combined_topk_weights != nullptr && c == 0 && sl == 0 && lane < a.k) {
+            float v[MOE_MAX_TOPK];
+#pragma unroll
+            for (int d = 0; d < MOE_MAX_TOPK; ++d)
+                if (d < D) v[d] = a.recv_topk_weights[(int64_t)entry[e].row[d] * a.k + lane];
+            float cw = 0.0f;
+#pragma unroll
+            for (int d = 0; d < MOE_MAX_TOPK; ++d)
+                if (d < D) cw += v[d];
+            a.combined_topk_weights[(int64_t)t * a.k + lane] = cw;
         }
         uint8_t *dst = a.out + (int64_t)t * a.row_bytes + off + soff + lane * 16;
 #pragma unroll
@@ -257,6 +303,9 @@ int launch_combine(const CombineLaunch &L) {
     a.T = L.num_tokens;
     a.k = L.num_topk;
     a.dst_row = L.token_dst_row;
+    a.row_weights = L.row_weights;
+    a.recv_topk_weights = L.recv_topk_weights;
+    a.combined_topk_weights = L.recv_topk_weights ? L.combined_topk_weights : nullptr;
     a.out = static_cast<uint8_t *>(L.out);
     a.status = L.status;
     a.l2_hints = tu.l2_hints;
@@ -278,11 +327,14 @@ int launch_combine(const CombineLaunch &L) {
     a.num_slices = (int)((a.chunk_bytes + 32 * kVMax * 16 - 1) / (32 * kVMax * 16));
     a.slice_bytes = (int)round_up((a.chunk_bytes + a.num_slices - 1) / a.num_slices, 16);
     const size_t smem = kHeadBytes + (size_t)a.num_slots * a.chunk_bytes;
-    if (ensure_dynamic_smem((const void *)combine_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
+    const bool weighted = a.row_weights != nullptr;
+    const void *fn = weighted ? (const void *)combine_kernel<true> : (const void *)combine_kernel<false>;
+    if (ensure_dynamic_smem(fn, smem) != MOE_OK) return MOE_ERR_CUDA;
 
     const int consumers = std::max(1, std::min(8, tu.combine_warps));
     const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
-    combine_kernel<<<grid, (consumers + 1) * 32, smem, st>>>(a);
+    if (weighted) combine_kernel<true><<<grid, (consumers + 1) * 32, smem, st>>>(a);
+    else combine_kernel<false><<<grid, (consumers + 1) * 32, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

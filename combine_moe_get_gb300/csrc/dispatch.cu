@@ -50,6 +50,7 @@ struct DispatchArgs {
     float *recv_topk_w;
     int32_t *recv_src;
     float *x_scales;
+    const float *in_scales;   // E4M3 input: the token's scales, copied to every destination row
     int nb;                   // scale blocks per row (H / 128), FP8
     int32_t *status;
     int chunk_bytes;          // input bytes per unit; multiple of 16 (FP8: of 256)
@@ -336,6 +337,8 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
             if constexpr (kFP8) {
                 for (int b = lane; b < nblk; b += 32) a.recv_scales[(int64_t)rowd * a.nb + c * cpb + b] = sc[b];
             }
+            if (a.in_scales != nullptr && c == 0)
+                for (int b = lane; b < a.nb; b += 32) a.recv_scales[(int64_t)rowd * a.nb + b] = a.in_scales[t * a.nb + b];
             if (c == 0) {
                 const int rd = __shfl_sync(kFull, rl, jd);
                 if (lane < a.k) {
@@ -548,12 +551,13 @@ inline int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 int launch_dispatch(const DispatchLaunch &L) {
     if (L.num_tokens == 0) return MOE_OK;
     const Tuning &tu = tuning();
-    const bool fp8 = L.quantize_fp8 != 0;
+    const bool fp8 = L.mode == MOE_DISPATCH_QUANTIZE_FP8;      // quantise in the kernel
+    const bool fp8_in = L.mode == MOE_DISPATCH_FP8;             // relay E4M3 bytes and their scales
     cudaStream_t st = reinterpret_cast<cudaStream_t>(L.stream);
 
     DispatchArgs a;
     a.x = static_cast<const uint8_t *>(L.x);
-    a.row_bytes = (int64_t)L.hidden * 2;
+    a.row_bytes = fp8_in ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
     a.k = L.num_topk;
     a.m = L.num_experts / L.num_ranks;
     a.E = L.num_experts;
@@ -562,12 +566,13 @@ int launch_dispatch(const DispatchLaunch &L) {
     a.dst_row = L.token_dst_row;
     a.capacity = L.recv_capacity;
     a.recv_x = static_cast<uint8_t *>(L.recv_x);
-    a.recv_row_bytes = fp8 ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
+    a.recv_row_bytes = (fp8 || fp8_in) ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
     a.recv_scales = L.recv_x_scales;
     a.recv_topk_idx = L.recv_topk_idx;
     a.recv_topk_w = L.recv_topk_weights;
     a.recv_src = L.recv_src_idx;
-    a.x_scales = L.x_scales;
+    a.x_scales = fp8 ? L.x_scales : nullptr;
+    a.in_scales = fp8_in ? L.x_scales : nullptr;
     a.nb = L.hidden / 128;
     a.status = L.status;
     a.l2_hints = tu.l2_hints;

@@ -213,17 +213,21 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
 
 MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
                          const float *topk_weights, int num_topk, int num_experts, int num_ranks,
-                         const int32_t *token_dst_row, int recv_capacity, int quantize_fp8, void *recv_x,
+                         const int32_t *token_dst_row, int recv_capacity, int mode, void *recv_x,
                          float *recv_x_scales, int64_t *recv_topk_idx, float *recv_topk_weights,
                          int32_t *recv_src_idx, float *x_scales, int32_t *status, void *stream) {
     const int T = num_tokens, H = hidden;
     if (!shape_ok(T, num_topk, num_experts, num_ranks)) return MOE_ERR_INVALID_ARG;
-    if (recv_capacity < 0 || H < 8 || H % 8 != 0 || (quantize_fp8 && H % 128 != 0)) return MOE_ERR_INVALID_ARG;
+    if (mode != MOE_DISPATCH_BF16 && mode != MOE_DISPATCH_QUANTIZE_FP8 && mode != MOE_DISPATCH_FP8)
+        return MOE_ERR_INVALID_ARG;
+    const bool fp8_out = mode != MOE_DISPATCH_BF16;
+    if (recv_capacity < 0 || H < 8 || H % 8 != 0 || (fp8_out && H % 128 != 0)) return MOE_ERR_INVALID_ARG;
     if (H > (1 << 24)) return MOE_ERR_INVALID_ARG;
     if (!status) return MOE_ERR_INVALID_ARG;
     if (T > 0) {
         if (!x || !topk_idx || !token_dst_row || (recv_capacity > 0 && !recv_x)) return MOE_ERR_INVALID_ARG;
-        if (quantize_fp8 && recv_capacity > 0 && !recv_x_scales) return MOE_ERR_INVALID_ARG;
+        if (fp8_out && recv_capacity > 0 && !recv_x_scales) return MOE_ERR_INVALID_ARG;
+        if (mode == MOE_DISPATCH_FP8 && !x_scales) return MOE_ERR_INVALID_ARG;
         if (!aligned(x, 16) || (recv_x && !aligned(recv_x, 16)) || !aligned(topk_idx, 8) ||
             !aligned(token_dst_row, 4) || !aligned(status, 4) || (topk_weights && !aligned(topk_weights, 4)) ||
             (recv_x_scales && !aligned(recv_x_scales, 4)) || (recv_topk_idx && !aligned(recv_topk_idx, 8)) ||
@@ -242,28 +246,31 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
     L.num_ranks = num_ranks;
     L.token_dst_row = token_dst_row;
     L.recv_capacity = recv_capacity;
-    L.quantize_fp8 = quantize_fp8;
+    L.mode = mode;
     L.recv_x = recv_x;
-    L.recv_x_scales = quantize_fp8 ? recv_x_scales : nullptr;
+    L.recv_x_scales = fp8_out ? recv_x_scales : nullptr;
     L.recv_topk_idx = recv_topk_idx;
     L.recv_topk_weights = recv_topk_weights;
     L.recv_src_idx = recv_src_idx;
-    L.x_scales = quantize_fp8 ? x_scales : nullptr;
+    L.x_scales = fp8_out ? x_scales : nullptr;
     L.status = status;
     L.stream = stream;
     return moe::launch_dispatch(L);
 }
 
-MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
-                        const int32_t *token_dst_row, void *out, int32_t *status, void *stream) {
+static int combine_common(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
+                          const int32_t *token_dst_row, const float *row_weights, const float *recv_topk_weights,
+                          float *combined_topk_weights, void *out, int32_t *status, void *stream) {
     const int T = num_tokens, H = hidden;
     if (T < 0 || num_topk < 1 || num_topk > MOE_MAX_TOPK || num_partial_rows < 0) return MOE_ERR_INVALID_ARG;
     if (H < 8 || H % 8 != 0 || H > (1 << 24) || (int64_t)T * num_topk >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
     if (!status) return MOE_ERR_INVALID_ARG;
+    if ((recv_topk_weights == nullptr) != (combined_topk_weights == nullptr)) return MOE_ERR_INVALID_ARG;
     if (T > 0) {
         if (!token_dst_row || !out || (num_partial_rows > 0 && !partial)) return MOE_ERR_INVALID_ARG;
         if ((partial && !aligned(partial, 16)) || !aligned(out, 16) || !aligned(token_dst_row, 4) ||
-            !aligned(status, 4))
+            !aligned(status, 4) || !aligned(row_weights, 4) || !aligned(recv_topk_weights, 4) ||
+            !aligned(combined_topk_weights, 4))
             return MOE_ERR_MISALIGNED;
     }
     moe::CombineLaunch L;
@@ -273,10 +280,26 @@ MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_token
     L.hidden = H;
     L.num_topk = num_topk;
     L.token_dst_row = token_dst_row;
+    L.row_weights = row_weights;
+    L.recv_topk_weights = recv_topk_weights;
+    L.combined_topk_weights = combined_topk_weights;
     L.out = out;
     L.status = status;
     L.stream = stream;
     return moe::launch_combine(L);
+}
+
+MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
+                        const int32_t *token_dst_row, void *out, int32_t *status, void *stream) {
+    return combine_common(partial, num_partial_rows, num_tokens, hidden, num_topk, token_dst_row, nullptr, nullptr,
+                          nullptr, out, status, stream);
+}
+
+MOE_API int moe_combine_ex(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
+                           const int32_t *token_dst_row, const float *row_weights, const float *recv_topk_weights,
+                           float *combined_topk_weights, void *out, int32_t *status, void *stream) {
+    return combine_common(partial, num_partial_rows, num_tokens, hidden, num_topk, token_dst_row, row_weights,
+                          recv_topk_weights, combined_topk_weights, out, status, stream);
 }
 
 }  // extern "C"

@@ -50,7 +50,7 @@ struct DispatchLaunch {
     int num_topk, num_experts, num_ranks;
     const int32_t *token_dst_row;
     int recv_capacity;
-    int quantize_fp8;
+    int mode;                 // moe_dispatch_mode_t
     void *recv_x;
     float *recv_x_scales;
     int64_t *recv_topk_idx;
@@ -67,6 +67,9 @@ struct CombineLaunch {
     const void *partial;
     int num_partial_rows, num_tokens, hidden, num_topk;
     const int32_t *token_dst_row;
+    const float *row_weights;          // optional
+    const float *recv_topk_weights;    // optional, with combined_topk_weights
+    float *combined_topk_weights;
     void *out;
     int32_t *status;
     void *stream;

@@ -148,27 +148,38 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
  *   recv_topk_weights[row, j] = topk_weights[t, j] if that entry is local, else 0
  * where row = token_dst_row[t, j] >= 0 for the owning entry j and r its rank.
  *
- * FP8 mode (quantize_fp8 != 0; H % 128 == 0): per token and per block of 128
- * channels, amax = max |x|, scale = amax / 448 (fp32, round to nearest),
- * code = E4M3(x / scale) (IEEE fp32 division, round to nearest even,
- * saturating to +-448); a block with amax == 0 has scale 0 and codes 0.
+ * Modes (argument `mode`, H % 128 == 0 for the FP8 modes):
+ *   MOE_DISPATCH_BF16           x bf16 [T, H]; recv_x bf16.
+ *   MOE_DISPATCH_QUANTIZE_FP8   x bf16; recv_x E4M3 codes and recv_x_scales. Per token
+ *                               and block of 128 channels: amax = max |x|, scale =
+ *                               amax / 448 (fp32, round to nearest), code = E4M3(x /
+ *                               scale) (IEEE fp32 division, round to nearest even,
+ *                               saturating to +-448); a block with amax == 0 has scale 0
+ *                               and codes 0. x_scales, if given, receives the scales.
+ *   MOE_DISPATCH_FP8            x already E4M3 [T, H] bytes with its scales x_scales
+ *                               [T, H/128] (input, section 3.4's sf next to the hidden
+ *                               bytes); codes and scales are copied unchanged.
  *
- *   x                  [T, H] bf16, device, 16-byte aligned, H % 8 == 0.
+ *   x                  [T, H] bf16 (E4M3 bytes in MOE_DISPATCH_FP8), device, 16-byte
+ *                      aligned, H % 8 == 0.
  *   topk_idx           [T, k] int64 (the same array given to moe_get_layout).
  *   topk_weights       [T, k] fp32 or NULL (then recv_topk_weights may be NULL).
  *   token_dst_row      [T, k] int32 from moe_get_layout.
  *   recv_capacity      rows available in the receive arrays; rows >= capacity
  *                      raise MOE_ERR_CAPACITY and are skipped. N <= T*min(k, R).
- *   recv_x             [capacity, H] bf16, or [capacity, H] uint8 E4M3 in FP8 mode.
- *   recv_x_scales      [capacity, H/128] fp32 (FP8 mode only, else ignored).
+ *   recv_x             [capacity, H] bf16, or [capacity, H] uint8 E4M3 in the FP8 modes.
+ *   recv_x_scales      [capacity, H/128] fp32 (FP8 modes only, else ignored).
  *   recv_topk_idx      [capacity, k] int64, may be NULL (not written).
  *   recv_topk_weights  [capacity, k] fp32, may be NULL.
  *   recv_src_idx       [capacity] int32, may be NULL.
- *   x_scales           [T, H/128] fp32 source-side scales (FP8 mode), may be NULL.
+ *   x_scales           [T, H/128] fp32: output of MOE_DISPATCH_QUANTIZE_FP8 (may be
+ *                      NULL), input of MOE_DISPATCH_FP8 (required), else ignored.
  */
+typedef enum { MOE_DISPATCH_BF16 = 0, MOE_DISPATCH_QUANTIZE_FP8 = 1, MOE_DISPATCH_FP8 = 2 } moe_dispatch_mode_t;
+
 MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
                          const float *topk_weights, int num_topk, int num_experts, int num_ranks,
-                         const int32_t *token_dst_row, int recv_capacity, int quantize_fp8,
+                         const int32_t *token_dst_row, int recv_capacity, int mode,
                          void *recv_x, float *recv_x_scales, int64_t *recv_topk_idx,
                          float *recv_topk_weights, int32_t *recv_src_idx, float *x_scales,
                          int32_t *status, void *stream);
@@ -224,6 +235,28 @@ MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_token
  */
 MOE_API int moe_get_layout_noalloc(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
                                    int num_ranks, moe_layout_t layout, int32_t *status, void *stream);
+
+/*
+ * moe_combine_ex -- moe_combine with the two combine options of the pages.
+ *
+ *   row_weights           [num_partial_rows] fp32 or NULL. When given, each term
+ *                         is weighted: acc = fma(row_weights[row], float(partial[row]),
+ *                         acc) (one rounding per term), same order and start as
+ *                         moe_combine; NULL gives exactly moe_combine.
+ *   recv_topk_weights     [num_partial_rows, k] fp32 or NULL (e.g. the dispatch's
+ *                         recv_topk_weights) and
+ *   combined_topk_weights [T, k] fp32 output or NULL: the received top-k weights
+ *                         reduced back to the tokens (the combine also returns the
+ *                         weights that travelled with the rows, section 3.5 /
+ *                         the Ascend page's FP32 weights next to the BF16 hidden):
+ *                         combined[t, j] = sum over the rows of t in ascending rank
+ *                         order of recv_topk_weights[row, j], fp32 from +0.0f.
+ * Other arguments, errors and limits as for moe_combine.
+ */
+MOE_API int moe_combine_ex(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
+                           const int32_t *token_dst_row, const float *row_weights,
+                           const float *recv_topk_weights, float *combined_topk_weights, void *out,
+                           int32_t *status, void *stream);
 
 /* Human-readable name of a moe_status_t value (static string). */
 MOE_API const char *moe_status_string(int status);

@@ -39,6 +39,10 @@ def lib():
         _lib.oracle_dispatch_bf16.argtypes = [P, I, I, P, P, I, I, I, P, I, P, P, P, P]
         _lib.oracle_dispatch_fp8.argtypes = [P, I, I, P, P, I, I, I, P, I, P, P, P, P, P, P]
         _lib.oracle_combine.argtypes = [P, I, I, I, I, P, P]
+        _lib.oracle_dispatch_fp8_input.argtypes = [P, P, I, I, P, P, I, I, I, P, I, P, P, P, P, P]
+        _lib.oracle_dispatch_fp8_input.restype = I
+        _lib.oracle_combine_weighted.argtypes = [P, I, I, I, I, P, P, P, P, P]
+        _lib.oracle_combine_weighted.restype = I
         for f in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_combine"):
             getattr(_lib, f).restype = I
         _lib.oracle_bf16_from_float.argtypes = [ctypes.c_float]
@@ -121,6 +125,28 @@ def dispatch(x_bits: np.ndarray, topk_idx: np.ndarray, topk_weights: Optional[np
     return out
 
 
+def dispatch_fp8_input(codes: np.ndarray, scales: np.ndarray, topk_idx: np.ndarray,
+                       topk_weights: Optional[np.ndarray], num_experts: int, num_ranks: int,
+                       token_dst_row: np.ndarray, recv_capacity: int) -> dict:
+    """Copies of E4M3 rows [T, H] (uint8) and their scales [T, H/128] per destination."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    token_dst_row = np.ascontiguousarray(token_dst_row, dtype=np.int32)
+    w = None if topk_weights is None else np.ascontiguousarray(topk_weights, dtype=np.float32)
+    T, H = codes.shape
+    k = topk_idx.shape[1]
+    cap = recv_capacity
+    out = dict(recv_x=np.zeros((cap, H), np.uint8), recv_x_scales=np.zeros((cap, H // 128), np.float32),
+               recv_topk_idx=np.zeros((cap, k), np.int64), recv_topk_weights=np.zeros((cap, k), np.float32),
+               recv_src_idx=np.zeros(cap, np.int32))
+    out["flags"] = lib().oracle_dispatch_fp8_input(
+        _ptr(codes), _ptr(scales), T, H, _ptr(topk_idx), _ptr(w), k, num_experts, num_ranks, _ptr(token_dst_row),
+        cap, _ptr(out["recv_x"]), _ptr(out["recv_x_scales"]), _ptr(out["recv_topk_idx"]),
+        _ptr(out["recv_topk_weights"]), _ptr(out["recv_src_idx"]))
+    return out
+
+
 def combine(partial_bits: np.ndarray, token_dst_row: np.ndarray) -> tuple[np.ndarray, int]:
     """bf16 bit patterns [T, H] of the fp32 ascending-rank sums."""
     partial_bits = np.ascontiguousarray(partial_bits, dtype=np.uint16)
@@ -130,6 +156,22 @@ def combine(partial_bits: np.ndarray, token_dst_row: np.ndarray) -> tuple[np.nda
     out = np.zeros((T, H), np.uint16)
     flags = lib().oracle_combine(_ptr(partial_bits), num_rows, T, H, k, _ptr(token_dst_row), _ptr(out))
     return out, flags
+
+
+def combine_weighted(partial_bits: np.ndarray, token_dst_row: np.ndarray, row_weights: Optional[np.ndarray],
+                     recv_topk_weights: Optional[np.ndarray] = None) -> tuple[np.ndarray, Optional[np.ndarray], int]:
+    """(out bf16 bits [T, H], combined top-k weights [T, k] or None, flags)."""
+    partial_bits = np.ascontiguousarray(partial_bits, dtype=np.uint16)
+    token_dst_row = np.ascontiguousarray(token_dst_row, dtype=np.int32)
+    rw = None if row_weights is None else np.ascontiguousarray(row_weights, dtype=np.float32)
+    rtw = None if recv_topk_weights is None else np.ascontiguousarray(recv_topk_weights, dtype=np.float32)
+    num_rows, H = partial_bits.shape
+    T, k = token_dst_row.shape
+    out = np.zeros((T, H), np.uint16)
+    cw = None if rtw is None else np.zeros((T, k), np.float32)
+    flags = lib().oracle_combine_weighted(_ptr(partial_bits), num_rows, T, H, k, _ptr(token_dst_row), _ptr(rw),
+                                          _ptr(rtw), _ptr(out), _ptr(cw))
+    return out, cw, flags
 
 
 def bf16_from_float(v: float) -> int:

@@ -279,6 +279,32 @@ int oracle_dispatch_fp8(const uint16_t *x, int T, int H,
     return flags;
 }
 
+/* Dispatch of rows that are already E4M3 codes with their per-128 scales
+ * (the scales travel next to the hidden bytes): codes and scales are copied
+ * unchanged, once per distinct destination rank. */
+int oracle_dispatch_fp8_input(const uint8_t *x, const float *x_scales, int T, int H,
+                              const int64_t *topk_idx, const float *topk_weights, int k, int E, int R,
+                              const int32_t *token_dst_row, int recv_capacity,
+                              uint8_t *recv_x, float *recv_x_scales, int64_t *recv_topk_idx,
+                              float *recv_topk_weights, int32_t *recv_src_idx)
+{
+    if (T < 0 || H < 128 || H % 128 != 0 || k < 1 || k > 32 || E % R != 0) return ORACLE_BAD_ARG;
+    int flags = 0, m = E / R, nb = H / 128;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t row = token_dst_row[(int64_t)t * k + j];
+            if (row < 0) continue;
+            if (row >= recv_capacity) { flags |= ORACLE_CAPACITY; continue; }
+            int r = (int)(topk_idx[(int64_t)t * k + j] / m);
+            for (int h = 0; h < H; ++h) recv_x[row * H + h] = x[(int64_t)t * H + h];
+            for (int b = 0; b < nb; ++b) recv_x_scales[row * nb + b] = x_scales[(int64_t)t * nb + b];
+            write_metadata(topk_idx, topk_weights, k, E, m, t, r, row,
+                           recv_topk_idx, recv_topk_weights, recv_src_idx);
+        }
+    }
+    return flags;
+}
+
 /* ------------------------------------------------------------------ */
 /* Combine: partial rows back into token order, fp32 sum, bf16 out.     */
 /* ------------------------------------------------------------------ */
@@ -327,4 +353,49 @@ void oracle_bf16_from_float_n(const float *v, uint16_t *h, int64_t n)
 void oracle_e4m3_from_float_n(const float *v, uint8_t *q, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) q[i] = oracle_e4m3_from_float(v[i]);
+}
+
+/* Combine with per-row weights and the reduction of the received top-k
+ * weights. For token t with receive rows in ascending rank order:
+ *   out[t] = bf16( acc ), acc = +0.0f then acc = fma(w[row], partial[row], acc)
+ *            (single-rounding fused multiply-add per term; w = 1 when
+ *            row_weights is NULL, which is then the plain ascending sum);
+ *   combined_topk_weights[t, j] = sum over the same rows, ascending, of
+ *            recv_topk_weights[row, j] in fp32 from +0.0f. */
+int oracle_combine_weighted(const uint16_t *partial, int num_rows, int T, int H, int k,
+                            const int32_t *token_dst_row, const float *row_weights,
+                            const float *recv_topk_weights, uint16_t *out, float *combined_topk_weights)
+{
+    if (T < 0 || H < 1 || k < 1 || k > 32) return ORACLE_BAD_ARG;
+    int flags = 0;
+    int32_t rows[32];
+    for (int t = 0; t < T; ++t) {
+        int n = 0;
+        for (int j = 0; j < k; ++j) {
+            int32_t row = token_dst_row[(int64_t)t * k + j];
+            if (row < 0) continue;
+            if (row >= num_rows) { flags |= ORACLE_CAPACITY; continue; }
+            rows[n++] = row;
+        }
+        for (int a = 1; a < n; ++a)
+            for (int b = a; b > 0 && rows[b - 1] > rows[b]; --b) {
+                int32_t tmp = rows[b]; rows[b] = rows[b - 1]; rows[b - 1] = tmp;
+            }
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int i = 0; i < n; ++i) {
+                float w = row_weights ? row_weights[rows[i]] : 1.0f;
+                acc = fmaf(w, oracle_bf16_to_float(partial[(int64_t)rows[i] * H + h]), acc);
+            }
+            out[(int64_t)t * H + h] = oracle_bf16_from_float(acc);
+        }
+        if (combined_topk_weights && recv_topk_weights) {
+            for (int j = 0; j < k; ++j) {
+                float acc = 0.0f;
+                for (int i = 0; i < n; ++i) acc += recv_topk_weights[(int64_t)rows[i] * k + j];
+                combined_topk_weights[(int64_t)t * k + j] = acc;
+            }
+        }
+    }
+    return flags;
 }

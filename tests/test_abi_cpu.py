@@ -106,6 +106,7 @@ def _dispatch(lib, x=A, T=128, H=256, topk=A + 0x10000, w=None, k=2, E=16, R=4, 
     (dict(H=12), 1), (dict(H=0), 1), (dict(fp8=1, H=264, scales=A + 0x400000), 1), (dict(fp8=1), 1),
     (dict(k=40), 1), (dict(E=17), 1), (dict(cap=-1), 1), (dict(x=None), 1), (dict(recv=None), 1),
     (dict(status=None), 1), (dict(x=A + 8), 2), (dict(recv=A + 8), 2), (dict(dst=MIS), 2),
+    (dict(fp8=3), 1), (dict(fp8=2, scales=A + 0x400000), 1), (dict(fp8=-1), 1),
 ])
 def test_dispatch_rejects_bad_arguments(lib, kw, code):
     assert _dispatch(lib, **kw) == code

@@ -1,5 +1,5 @@
 """The oracle's pins must be able to fail: plant one plausible mistake at a
-time in a copy of the C oracle (a dropped term, a wrong index or operator, a
+time (at every place the mutated line occurs) in a copy of the C oracle (a dropped term, a wrong index or operator, a
 wrong rounding rule), build that copy, and check that the pin suite rejects it.
 CPU only; nothing here touches the CUDA path."""
 from __future__ import annotations
@@ -27,6 +27,10 @@ MUTATIONS = {
     "localised_index_wrong": ("e - (int64_t)r * m : -1;", "e - (int64_t)r : -1;"),
     "combine_descending": ("rows[b - 1] > rows[b]; --b)", "rows[b - 1] < rows[b]; --b)"),
     "weights_not_masked": ("(local && topk_weights) ?", "(topk_weights) ?"),
+    "weighted_combine_unfused": ("acc = fmaf(w, oracle_bf16_to_float(partial[(int64_t)rows[i] * H + h]), acc);",
+                                 "acc = acc + w * oracle_bf16_to_float(partial[(int64_t)rows[i] * H + h]);"),
+    "combined_weights_wrong_lane": ("acc += recv_topk_weights[(int64_t)rows[i] * k + j];",
+                                    "acc += recv_topk_weights[(int64_t)rows[i] * k + (k - 1 - j)];"),
 }
 
 
@@ -34,7 +38,7 @@ MUTATIONS = {
 def test_pins_reject_planted_mistake(name, tmp_path):
     old, new = MUTATIONS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
     mutated = tmp_path / "moe_oracle_mut.c"
     mutated.write_text(src.replace(old, new))
     lib = tmp_path / "liboracle_mut.so"

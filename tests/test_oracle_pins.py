@@ -460,3 +460,123 @@ def test_oracle_combine_token_without_rows_is_zero():
     partial = bf.f32_to_bf16_bits(np.ones((2, 16), np.float32))
     out, _ = oracle.combine(partial, lay["token_dst_row"])
     assert np.all(out[0] == 0) and np.all(bf.bf16_bits_to_f32(out[1]) == 2.0)
+
+
+# ---------------------------------------------------------------- dispatch of E4M3 input
+
+def test_oracle_fp8_input_dispatch_matches_quantised_dispatch():
+    # quantising inside dispatch and dispatching already-quantised rows with their
+    # scales must land the same bytes in the same receive rows
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=300)
+    topk = inp.topk_idx.numpy()
+    lay = oracle.layout(topk, wk.num_experts, wk.num_ranks)
+    N = lay["num_recv"]
+    q = oracle.dispatch(_bits(inp.x), topk, inp.topk_weights.numpy(), wk.num_experts, wk.num_ranks,
+                        lay["token_dst_row"], N, fp8=True)
+    # the source rows' codes: each token's codes appear in every one of its receive rows
+    src = q["recv_src_idx"]
+    codes = np.zeros((300, wk.hidden), np.uint8)
+    codes[src] = q["recv_x"]
+    c = oracle.dispatch_fp8_input(codes, q["x_scales"], topk, inp.topk_weights.numpy(), wk.num_experts,
+                                  wk.num_ranks, lay["token_dst_row"], N)
+    assert c["flags"] == 0
+    for key in ("recv_x", "recv_topk_idx", "recv_src_idx"):
+        np.testing.assert_array_equal(c[key], q[key], err_msg=key)
+    np.testing.assert_array_equal(c["recv_x_scales"].view(np.uint32), q["recv_x_scales"].view(np.uint32))
+
+
+def test_oracle_fp8_input_dispatch_copies_bytes():
+    g = np.random.default_rng(3)
+    T, H, E, R, k = 64, 256, 16, 4, 3
+    topk = wl.make_topk_uniform(torch.Generator().manual_seed(3), T, E, k).numpy()
+    codes = g.integers(0, 256, (T, H), dtype=np.uint8)
+    scales = g.standard_normal((T, H // 128)).astype(np.float32)
+    lay = oracle.layout(topk, E, R)
+    d = oracle.dispatch_fp8_input(codes, scales, topk, None, E, R, lay["token_dst_row"], lay["num_recv"])
+    src = d["recv_src_idx"]
+    np.testing.assert_array_equal(d["recv_x"], codes[src])
+    np.testing.assert_array_equal(d["recv_x_scales"], scales[src])
+    assert np.all(d["recv_topk_weights"] == 0)
+
+
+# ---------------------------------------------------------------- weighted combine
+
+def _rn32(v):
+    from fractions import Fraction
+    if v == 0:
+        return Fraction(0)
+    sign = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    q = Fraction(2) ** (max(e, -126) - 23)
+    n = a / q
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * fl * q
+
+
+def test_oracle_weighted_combine_vs_exact_fma():
+    # acc = fma(w, x, acc): the exact product plus acc, rounded once to fp32, emulated with rationals
+    from fractions import Fraction
+    g = torch.Generator().manual_seed(4)
+    T, E, R, k, H = 24, 16, 8, 4, 16
+    topk = wl.make_topk_uniform(g, T, E, k)
+    lay = oracle.layout(topk.numpy(), E, R)
+    N = lay["num_recv"]
+    partial = _bits(wl.make_partial(g, N, H))
+    w = (torch.rand(N, generator=g) * 3 - 1).numpy().astype(np.float32)
+    out, _, flags = oracle.combine_weighted(partial, lay["token_dst_row"], w)
+    assert flags == 0
+    pf = bf.bf16_bits_to_f32(partial)
+    ref = np.zeros((T, H), np.float32)
+    for t in range(T):
+        rows = sorted(int(r) for r in lay["token_dst_row"][t] if r >= 0)
+        for h in range(H):
+            acc = Fraction(0)
+            for r in rows:
+                acc = _rn32(Fraction(float(w[r])) * Fraction(float(pf[r, h])) + acc)
+            ref[t, h] = float(acc)
+    np.testing.assert_array_equal(out, bf.f32_to_bf16_bits(ref))
+
+
+def test_oracle_weighted_combine_unit_weights_is_plain_combine():
+    wk = wl.CONFIGS["tiny"]
+    inp = wl.make_inputs(wk)
+    lay = oracle.layout(inp.topk_idx.numpy(), wk.num_experts, wk.num_ranks)
+    partial = _bits(inp.partial)
+    a, _, _ = oracle.combine_weighted(partial, lay["token_dst_row"], np.ones(partial.shape[0], np.float32))
+    b, _ = oracle.combine(partial, lay["token_dst_row"])
+    np.testing.assert_array_equal(a, b)
+
+
+def test_oracle_combined_topk_weights_return_the_routing_weights():
+    # each weight travels in exactly one receive row (its expert's rank), zeros elsewhere,
+    # so reducing the received weights gives the token's weights back
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=256)
+    topk = wl.mask_random_lanes(torch.Generator().manual_seed(9), inp.topk_idx, 0.2).numpy()
+    lay = oracle.layout(topk, wk.num_experts, wk.num_ranks)
+    d = oracle.dispatch(_bits(inp.x), topk, inp.topk_weights.numpy(), wk.num_experts, wk.num_ranks,
+                        lay["token_dst_row"], lay["num_recv"])
+    _, cw, _ = oracle.combine_weighted(d["recv_x"], lay["token_dst_row"], None, d["recv_topk_weights"])
+    expect = np.where(topk >= 0, inp.topk_weights.numpy(), 0.0).astype(np.float32)
+    np.testing.assert_array_equal(cw, expect)
+
+
+def test_oracle_weighted_combine_is_fused():
+    # two rows of one token: acc = wA * 1 exactly, then wB * xB has an inexact fp32
+    # product whose lost part (2^-30) is all that is left after cancellation --
+    # a fused multiply-add keeps it, multiply-then-add loses it
+    topk = np.array([[0, 1]], np.int64)
+    lay = oracle.layout(topk, 2, 2)                     # rows 0 and 1
+    wA = np.float32(-(1 + 2.0 ** -7 + 2.0 ** -23))
+    wB = np.float32(1 + 2.0 ** -23)
+    partial = bf.f32_to_bf16_bits(np.array([[1.0], [1 + 2.0 ** -7]], np.float32))
+    assert float(wA) == -(1 + 2.0 ** -7 + 2.0 ** -23) and float(wB) == 1 + 2.0 ** -23
+    out, _, _ = oracle.combine_weighted(partial, lay["token_dst_row"], np.array([wA, wB], np.float32))
+    assert bf.bf16_bits_to_f32(out)[0, 0] == np.float32(2.0 ** -30)

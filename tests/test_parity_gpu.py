@@ -269,6 +269,47 @@ def test_dispatch_fp8_rounding_boundaries(moe):
     check_dispatch(moe, inp, E, R, True)
 
 
+def check_dispatch_fp8_input(moe, topk, E, R, H, seed, weights=True):
+    g = np.random.default_rng(seed)
+    T, k = topk.shape
+    codes = g.integers(0, 256, (T, H), dtype=np.uint8)          # any byte pattern: this is a copy
+    scales = g.standard_normal((T, H // 128)).astype(np.float32)
+    w = wl.make_weights(torch.Generator().manual_seed(seed), T, k)
+    topk_d = topk.to(DEV)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk_d, E, R, status=status)
+    cap = wl.recv_capacity(T, k, R)
+    d = moe.moe_dispatch(torch.from_numpy(codes).to(DEV), topk_d, w.to(DEV) if weights else None, E, R,
+                         lay.token_dst_row, cap, x_scales=torch.from_numpy(scales).to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_lay = oracle.layout(topk.numpy(), E, R)
+    N = ref_lay["num_recv"]
+    ref = oracle.dispatch_fp8_input(codes, scales, topk.numpy(), w.numpy() if weights else None, E, R,
+                                    ref_lay["token_dst_row"], N)
+    np.testing.assert_array_equal(d.recv_x[:N].cpu().numpy(), ref["recv_x"])
+    np.testing.assert_array_equal(d.recv_x_scales[:N].cpu().numpy().view(np.uint32),
+                                  ref["recv_x_scales"].view(np.uint32))
+    np.testing.assert_array_equal(d.recv_src_idx[:N].cpu().numpy(), ref["recv_src_idx"])
+    np.testing.assert_array_equal(d.recv_topk_idx[:N].cpu().numpy(), ref["recv_topk_idx"])
+    np.testing.assert_array_equal(d.recv_topk_weights[:N].cpu().numpy().view(np.uint32),
+                                  ref["recv_topk_weights"].view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode"])
+def test_dispatch_fp8_input_parity_configs(moe, name):
+    w = wl.CONFIGS[name]
+    check_dispatch_fp8_input(moe, topk_for(w), w.num_experts, w.num_ranks, w.hidden, 17)
+
+
+@pytest.mark.parametrize("T,H,k,E,R", [(1, 128, 2, 16, 4), (129, 384, 8, 256, 256), (300, 16384, 6, 48, 3),
+                                       (77, 7040, 5, 20, 5)])
+def test_dispatch_fp8_input_parity_shapes(moe, T, H, k, E, R):
+    g = torch.Generator().manual_seed(T + H)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
+    check_dispatch_fp8_input(moe, topk, E, R, H, T, weights=(T % 2 == 1))
+
+
 def test_dispatch_capacity_overflow_writes_nothing_beyond(moe):
     w = wl.CONFIGS["tiny"]
     inp = wl.make_inputs(w, with_partial=False)
@@ -326,6 +367,54 @@ def test_combine_parity_shapes(moe, T, H, k, E, R):
     topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
     partial = wl.make_partial(g, wl.recv_capacity(T, k, R), H)
     check_combine(moe, topk, partial, E, R)
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode"])
+def test_combine_ex_parity_configs(moe, name):
+    w = wl.CONFIGS[name]
+    inp = wl.make_inputs(w)
+    g = torch.Generator().manual_seed(5)
+    topk = wl.mask_random_lanes(g, inp.topk_idx, 0.1)
+    topk_d = topk.to(DEV)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk_d, w.num_experts, w.num_ranks, status=status)
+    cap = inp.partial.shape[0]
+    d = moe.moe_dispatch(inp.x.to(DEV), topk_d, inp.topk_weights.to(DEV), w.num_experts, w.num_ranks,
+                         lay.token_dst_row, cap, status=status)
+    row_w = (torch.rand(cap, generator=g) * 2 - 0.5).to(DEV)
+    out, cw = moe.moe_combine_ex(inp.partial.to(DEV), lay.token_dst_row, row_weights=row_w,
+                                 recv_topk_weights=d.recv_topk_weights, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_lay = oracle.layout(topk.numpy(), w.num_experts, w.num_ranks)
+    N = ref_lay["num_recv"]
+    rtw = d.recv_topk_weights.cpu().numpy()
+    rtw[N:] = 0.0
+    ref_out, ref_cw, flags = oracle.combine_weighted(bits16(inp.partial), ref_lay["token_dst_row"],
+                                                     row_w.cpu().numpy(), rtw)
+    assert flags == 0
+    got = bits16(out)
+    g32 = (got.astype(np.uint32) << 16).view(np.float32)
+    r32 = (ref_out.astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_allclose(g32, r32, rtol=1e-2, atol=1e-3)
+    np.testing.assert_array_equal(got, ref_out)
+    np.testing.assert_array_equal(cw.cpu().numpy().view(np.uint32), ref_cw.view(np.uint32))
+    # the combined weights are the routing weights of the valid entries
+    expect = np.where(topk.numpy() >= 0, inp.topk_weights.numpy(), 0.0).astype(np.float32)
+    np.testing.assert_array_equal(cw.cpu().numpy(), expect)
+
+
+def test_combine_ex_without_options_is_combine(moe):
+    w = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(w, num_tokens=1000)
+    topk_d = inp.topk_idx.to(DEV)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk_d, w.num_experts, w.num_ranks, status=status)
+    part = inp.partial.to(DEV)
+    a, cw = moe.moe_combine_ex(part, lay.token_dst_row, status=status)
+    b = moe.moe_combine(part, lay.token_dst_row, status=status)
+    torch.cuda.synchronize()
+    assert cw is None and torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
 def test_combine_partial_rows_short_reports_capacity(moe):
