@@ -200,6 +200,15 @@ class Step:
             recv_topk_idx=self.disp.recv_topk_idx, recv_topk_weights=self.disp.recv_topk_weights,
             recv_src_idx=self.disp.recv_src_idx, x_scales=torch.empty(T, H // 128, dtype=torch.float32, device=device))
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        # E4M3 rows + scales for the pass-through dispatch (codes of x; any bytes would do for a copy)
+        self.x8 = (self.x.view(torch.int16) & 0xFF).to(torch.uint8).contiguous()
+        self.x8_scales = torch.ones(T, H // 128, dtype=torch.float32, device=device)
+        self.disp8in = moe.Dispatched(
+            recv_x=self.disp8.recv_x, recv_x_scales=self.disp8.recv_x_scales,
+            recv_topk_idx=self.disp.recv_topk_idx, recv_topk_weights=self.disp.recv_topk_weights,
+            recv_src_idx=self.disp.recv_src_idx, x_scales=None)
+        self.row_w = torch.rand(self.cap, device=device)
+        self.cw = torch.empty(T, k, dtype=torch.float32, device=device)
 
     def layout(self):
         self.moe.moe_get_layout(self.topk, self.w.num_experts, self.w.num_ranks, out=self.lay, workspace=self.ws,
@@ -209,6 +218,16 @@ class Step:
         self.moe.moe_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks,
                               self.lay.token_dst_row, self.cap, quantize_fp8=fp8,
                               out=self.disp8 if fp8 else self.disp, status=self.status)
+
+    def dispatch_fp8_input(self):
+        self.moe.moe_dispatch(self.x8, self.topk, self.wts, self.w.num_experts, self.w.num_ranks,
+                              self.lay.token_dst_row, self.cap, x_scales=self.x8_scales, out=self.disp8in,
+                              status=self.status)
+
+    def combine_weighted(self):
+        self.moe.moe_combine_ex(self.partial, self.lay.token_dst_row, row_weights=self.row_w,
+                                recv_topk_weights=self.disp.recv_topk_weights, out=self.out,
+                                combined_topk_weights=self.cw, status=self.status)
 
     def combine(self):
         self.moe.moe_combine(self.partial, self.lay.token_dst_row, out=self.out, status=self.status)
@@ -313,47 +332,60 @@ def run_ours(args, world, rank, local):
     ms_per_step = max_over_ranks(mean(step_ms), world, device)
     tokens_per_s = world * T / (ms_per_step / 1e3)
 
-    # FP8 dispatch (fused quantisation), timed alone with the same flush discipline
-    fp8_ms = []
-    a = torch.cuda.Event(enable_timing=True, external=graph is not None)
-    b = torch.cuda.Event(enable_timing=True, external=graph is not None)
-    st.dispatch(fp8=True)                       # first call outside any capture
-    torch.cuda.synchronize()
-    g8 = None
-    if graph is not None:
-        g8 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g8):
-            a.record()
-            st.dispatch(fp8=True)
-            b.record()
-    for i in range(max(3, args.steps // 2) + 2):
-        flush.zero_()
-        if g8 is not None:
-            g8.replay()
-        else:
-            a.record(stream)
-            st.dispatch(fp8=True)
-            b.record(stream)
+    # the other dispatch / combine variants, each timed alone with the same flush discipline
+    def time_alone(fn, reps):
+        fn()                                    # first call outside any capture
         torch.cuda.synchronize()
-        if i >= 2:
-            fp8_ms.append(a.elapsed_time(b))
-    moe.check_status(st.status, "fp8 dispatch")
+        a = torch.cuda.Event(enable_timing=True, external=graph is not None)
+        b = torch.cuda.Event(enable_timing=True, external=graph is not None)
+        g1 = None
+        if graph is not None:
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1):
+                a.record()
+                fn()
+                b.record()
+        ms = []
+        for i in range(reps + 2):
+            flush.zero_()
+            if g1 is not None:
+                g1.replay()
+            else:
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                ms.append(a.elapsed_time(b))
+        return ms
+
+    reps = max(3, args.steps // 2)
+    fp8_ms = time_alone(lambda: st.dispatch(fp8=True), reps)                  # fused E4M3 quantisation
+    fp8in_ms = time_alone(st.dispatch_fp8_input, reps)                        # E4M3 rows + scales relayed
+    wcomb_ms = time_alone(st.combine_weighted, reps)                          # weighted rows + combined weights
+    moe.check_status(st.status, "dispatch / combine variants")
 
     peak, peak_kind = hbm_peak()
     row = H * 2
     bytes_bf16 = T * row + N * row                      # x read once + one row per (token, rank)
     bytes_fp8 = T * row + N * H + N * (H // 128) * 4    # x read + e4m3 rows + scales
+    bytes_fp8in = (T + N) * (H + (H // 128) * 4)        # e4m3 rows + scales read once, written per rank
+    bytes_wcomb = bytes_bf16 + N * 4                    # + one weight per receive row
     kern = {
         "layout_us": mean(lay_ms) * 1e3,
         "dispatch_us": mean(dis_ms) * 1e3,
         "combine_us": mean(com_ms) * 1e3,
         "dispatch_fp8_us": mean(fp8_ms) * 1e3,
+        "dispatch_fp8_input_us": mean(fp8in_ms) * 1e3,
+        "combine_weighted_us": mean(wcomb_ms) * 1e3,
     }
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     kern["dispatch_gbs"] = gbs(bytes_bf16, mean(dis_ms))
     kern["combine_gbs"] = gbs(bytes_bf16, mean(com_ms))
     kern["dispatch_fp8_gbs"] = gbs(bytes_fp8, mean(fp8_ms))
-    for key in ("dispatch", "combine", "dispatch_fp8"):
+    kern["dispatch_fp8_input_gbs"] = gbs(bytes_fp8in, mean(fp8in_ms))
+    kern["combine_weighted_gbs"] = gbs(bytes_wcomb, mean(wcomb_ms))
+    for key in ("dispatch", "combine", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted"):
         kern[f"{key}_frac"] = kern[f"{key}_gbs"] / peak
     dominant = "dispatch" if mean(dis_ms) >= mean(com_ms) else "combine"
     dom_ms = mean(dis_ms) if dominant == "dispatch" else mean(com_ms)
