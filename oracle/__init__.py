@@ -43,6 +43,10 @@ def lib():
         _lib.oracle_dispatch_fp8_input.restype = I
         _lib.oracle_combine_weighted.argtypes = [P, I, I, I, I, P, P, P, P, P]
         _lib.oracle_combine_weighted.restype = I
+        _lib.oracle_expand_layout.argtypes = [P, I, I, I, P, P]
+        _lib.oracle_expand_layout.restype = I
+        _lib.oracle_dispatch_expand.argtypes = [I, P, P, I, I, P, P, I, I, I, P, I, P, P, P, P, P, P]
+        _lib.oracle_dispatch_expand.restype = I
         for f in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_combine"):
             getattr(_lib, f).restype = I
         _lib.oracle_bf16_from_float.argtypes = [ctypes.c_float]
@@ -172,6 +176,51 @@ def combine_weighted(partial_bits: np.ndarray, token_dst_row: np.ndarray, row_we
     flags = lib().oracle_combine_weighted(_ptr(partial_bits), num_rows, T, H, k, _ptr(token_dst_row), _ptr(rw),
                                           _ptr(rtw), _ptr(out), _ptr(cw))
     return out, cw, flags
+
+
+def expand_layout(topk_idx: np.ndarray, num_experts: int) -> dict:
+    """Expand mode: expert_prefix [E+1] and token_expert_row [T, k], one row
+    per valid entry, expert regions in expert order, source order inside."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, k = topk_idx.shape
+    out = dict(expert_prefix=np.zeros(num_experts + 1, np.int32), token_expert_row=np.zeros((T, k), np.int32))
+    out["flags"] = lib().oracle_expand_layout(_ptr(topk_idx), T, k, num_experts, _ptr(out["expert_prefix"]),
+                                              _ptr(out["token_expert_row"]))
+    out["num_recv"] = int(out["expert_prefix"][-1])
+    return out
+
+
+EXPAND_BF16, EXPAND_QUANTIZE_FP8, EXPAND_FP8 = 0, 1, 2
+
+
+def dispatch_expand(mode: int, x: np.ndarray, topk_idx: np.ndarray, topk_weights: Optional[np.ndarray],
+                    num_experts: int, num_ranks: int, token_expert_row: np.ndarray, recv_capacity: int,
+                    x_scales: Optional[np.ndarray] = None, fill_x: int = 0, fill_meta: int = 0) -> dict:
+    """Expand-mode dispatch. ``x`` is bf16 bit patterns (uint16 [T, H]) for
+    modes 0 and 1, E4M3 codes (uint8 [T, H]) with ``x_scales`` for mode 2."""
+    x = np.ascontiguousarray(x, dtype=np.uint8 if mode == EXPAND_FP8 else np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    token_expert_row = np.ascontiguousarray(token_expert_row, dtype=np.int32)
+    w = None if topk_weights is None else np.ascontiguousarray(topk_weights, dtype=np.float32)
+    xs = None if x_scales is None else np.ascontiguousarray(x_scales, dtype=np.float32)
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    cap = recv_capacity
+    nb = H // 128
+    fp8 = mode != EXPAND_BF16
+    out = dict(
+        recv_x=(np.full((cap, H), fill_x & 0xFF, np.uint8) if fp8 else np.full((cap, H), fill_x & 0xFFFF, np.uint16)),
+        recv_x_scales=np.full((cap, max(nb, 1)), fill_meta, np.int32).view(np.float32) if fp8 else None,
+        recv_topk_idx=np.full((cap, k), fill_meta, np.int64),
+        recv_topk_weights=np.full((cap, k), fill_meta, np.int32).view(np.float32),
+        recv_src_idx=np.full(cap, fill_meta, np.int32),
+        x_scales=np.zeros((T, nb), np.float32) if mode == EXPAND_QUANTIZE_FP8 else None,
+    )
+    out["flags"] = lib().oracle_dispatch_expand(
+        mode, _ptr(x), _ptr(xs), T, H, _ptr(topk_idx), _ptr(w), k, num_experts, num_ranks, _ptr(token_expert_row),
+        cap, _ptr(out["recv_x"]), _ptr(out["recv_x_scales"]), _ptr(out["recv_topk_idx"]),
+        _ptr(out["recv_topk_weights"]), _ptr(out["recv_src_idx"]), _ptr(out["x_scales"]))
+    return out
 
 
 def bf16_from_float(v: float) -> int:

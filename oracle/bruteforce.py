@@ -13,6 +13,9 @@ route, so a slip in either shows up as a mismatch.
   bit, saturating above 448. (The C oracle counts quanta per binade.)
 * bf16 rounding: torch's float32 -> bfloat16 cast (round to nearest even).
 * fp32 sums: numpy float32 element-wise adds, one row at a time.
+* Expand layout: list every valid (expert, token, choice) triple and sort it;
+  a triple's index in the sorted list is its row. (The C oracle uses counts,
+  prefix sums and a running counter per expert.)
 """
 from __future__ import annotations
 
@@ -171,3 +174,62 @@ def combine(partial_bits: np.ndarray, token_dst_row: np.ndarray) -> np.ndarray:
             acc = (acc + pf[row]).astype(np.float32)
         out[t] = acc
     return f32_to_bf16_bits(out)
+
+
+def expand_layout(topk_idx, num_experts: int) -> dict:
+    topk = np.asarray(topk_idx, np.int64)
+    T, k = topk.shape if topk.ndim == 2 else (0, 1)
+    triples = sorted((int(topk[t, j]), t, j) for t in range(T) for j in range(k)
+                     if 0 <= int(topk[t, j]) < num_experts)
+    rows = np.full((T, k), -1, np.int32)
+    for row, (_, t, j) in enumerate(triples):
+        rows[t, j] = row
+    prefix = np.zeros(num_experts + 1, np.int32)
+    for e, _, _ in triples:
+        prefix[e + 1:] += 1
+    bad = bool(np.any((topk != -1) & ((topk < 0) | (topk >= num_experts))))
+    return dict(expert_prefix=prefix, token_expert_row=rows, num_recv=len(triples), bad_topk=bad)
+
+
+def dispatch_expand(x_bits: np.ndarray, topk_idx, topk_weights: Optional[np.ndarray], num_experts: int,
+                    num_ranks: int, fp8: bool = False) -> dict:
+    """Expand-mode receive buffers of exactly one row per valid entry."""
+    lay = expand_layout(topk_idx, num_experts)
+    topk = np.asarray(topk_idx)
+    T, k = topk.shape
+    H = x_bits.shape[1]
+    m = num_experts // num_ranks
+    N = lay["num_recv"]
+    rows = lay["token_expert_row"]
+    if fp8:
+        # the token's codes and scales are those of the rank-mode brute force
+        ref = dispatch(x_bits, topk_idx, topk_weights, num_experts, num_ranks, fp8=True)
+        src_rows = layout(topk_idx, num_experts, num_ranks)["token_dst_row"]
+        recv_x = np.zeros((N, H), np.uint8)
+        recv_scales = np.zeros((N, H // 128), np.float32)
+    else:
+        recv_x = np.zeros((N, H), np.uint16)
+    recv_src = np.zeros(N, np.int32)
+    recv_idx = np.full((N, k), -1, np.int64)
+    recv_w = np.zeros((N, k), np.float32)
+    for t in range(T):
+        for j in range(k):
+            row = int(rows[t, j])
+            if row < 0:
+                continue
+            e = int(topk[t, j])
+            recv_src[row] = t
+            recv_idx[row, j] = e % m
+            recv_w[row, j] = 0.0 if topk_weights is None else topk_weights[t, j]
+            if fp8:
+                # any rank-mode row of token t holds its codes
+                r_row = max(int(v) for v in src_rows[t])
+                recv_x[row] = ref["recv_x"][r_row]
+                recv_scales[row] = ref["recv_x_scales"][r_row]
+            else:
+                recv_x[row] = x_bits[t]
+    out = dict(layout=lay, recv_x=recv_x, recv_src_idx=recv_src, recv_topk_idx=recv_idx, recv_topk_weights=recv_w)
+    if fp8:
+        out["recv_x_scales"] = recv_scales
+        out["x_scales"] = ref["x_scales"]
+    return out

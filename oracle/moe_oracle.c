@@ -399,3 +399,105 @@ int oracle_combine_weighted(const uint16_t *partial, int num_rows, int T, int H,
     }
     return flags;
 }
+
+/* ------------------------------------------------------------------ */
+/* Expand mode: one receive row per valid top-k entry, grouped by expert. */
+/* ------------------------------------------------------------------ */
+
+/* The copy epilogue of the DeepEP V2 deep-dive page (section 3.3 stage 3), in
+ * expand mode, takes each received token's destination from a counter per
+ * expert that starts at the exclusive prefix of the per-expert counts
+ * (psum_num_recv_tokens_per_expert) and advances by one per placed token.
+ * Readings: one row per valid top-k entry (the per-expert counts of the
+ * notify stage count entries, so that is what fills each region exactly);
+ * entries are placed in source order -- token ascending, then choice index
+ * ascending -- instead of arrival order. Masked (-1) and invalid entries get
+ * -1 (invalid ones are flagged). Writes expert_prefix [E+1] and
+ * token_expert_row [T, k]. */
+int oracle_expand_layout(const int64_t *topk_idx, int T, int k, int E,
+                         int32_t *expert_prefix, int32_t *token_expert_row)
+{
+    if (T < 0 || k < 1 || k > 32 || E < 1) return ORACLE_BAD_ARG;
+    int flags = 0;
+    int32_t *count = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (int64_t i = 0; i < (int64_t)T * k; ++i) {
+        int64_t e = topk_idx[i];
+        if (e == -1) continue;
+        if (e < 0 || e >= E) { flags |= ORACLE_BAD_TOPK; continue; }
+        count[e] += 1;
+    }
+    expert_prefix[0] = 0;
+    for (int e = 0; e < E; ++e) expert_prefix[e + 1] = expert_prefix[e] + count[e];
+    /* the counter of each expert starts at its region's first row */
+    for (int e = 0; e < E; ++e) count[e] = expert_prefix[e];
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int64_t idx = (int64_t)t * k + j;
+            int64_t e = topk_idx[idx];
+            token_expert_row[idx] = -1;
+            if (e < 0 || e >= E) continue;
+            token_expert_row[idx] = count[e];
+            count[e] += 1;
+        }
+    }
+    free(count);
+    return flags;
+}
+
+/* Dispatch in expand mode. The row of every valid entry (t, j) receives the
+ * token, exactly as in the three dispatch forms above (mode 0: bf16 copy;
+ * mode 1: fused per-128 E4M3 quantisation, with x_scales_out; mode 2: E4M3
+ * codes and their given scales copied). Reading: a row of the expand layout
+ * belongs to one (token, expert) entry, so its metadata keeps that entry only:
+ *   recv_topk_idx[row, jj]     = e - rank(e)*m for jj == j, else -1
+ *   recv_topk_weights[row, jj] = topk_weights[t, j] for jj == j, else 0
+ *   recv_src_idx[row]          = t. */
+int oracle_dispatch_expand(int mode, const void *x, const float *x_scales_in, int T, int H,
+                           const int64_t *topk_idx, const float *topk_weights, int k, int E, int R,
+                           const int32_t *token_expert_row, int recv_capacity,
+                           void *recv_x, float *recv_x_scales, int64_t *recv_topk_idx,
+                           float *recv_topk_weights, int32_t *recv_src_idx, float *x_scales_out)
+{
+    if (T < 0 || H < 1 || k < 1 || k > 32 || E % R != 0 || mode < 0 || mode > 2) return ORACLE_BAD_ARG;
+    if (mode != 0 && (H < 128 || H % 128 != 0)) return ORACLE_BAD_ARG;
+    int flags = 0, m = E / R, nb = H / 128;
+    uint8_t *q = (uint8_t *)malloc((size_t)H);
+    float *s = (float *)malloc(sizeof(float) * (size_t)(nb > 0 ? nb : 1));
+    for (int t = 0; t < T; ++t) {
+        if (mode == 1) {
+            quantize_row((const uint16_t *)x + (int64_t)t * H, H, q, s);
+            if (x_scales_out)
+                for (int b = 0; b < nb; ++b) x_scales_out[(int64_t)t * nb + b] = s[b];
+        }
+        for (int j = 0; j < k; ++j) {
+            int64_t row = token_expert_row[(int64_t)t * k + j];
+            if (row < 0) continue;
+            if (row >= recv_capacity) { flags |= ORACLE_CAPACITY; continue; }
+            if (mode == 0) {
+                const uint16_t *src = (const uint16_t *)x + (int64_t)t * H;
+                uint16_t *dst = (uint16_t *)recv_x + row * H;
+                for (int h = 0; h < H; ++h) dst[h] = src[h];
+            } else if (mode == 1) {
+                uint8_t *dst = (uint8_t *)recv_x + row * H;
+                for (int h = 0; h < H; ++h) dst[h] = q[h];
+                for (int b = 0; b < nb; ++b) recv_x_scales[row * nb + b] = s[b];
+            } else {
+                const uint8_t *src = (const uint8_t *)x + (int64_t)t * H;
+                uint8_t *dst = (uint8_t *)recv_x + row * H;
+                for (int h = 0; h < H; ++h) dst[h] = src[h];
+                for (int b = 0; b < nb; ++b) recv_x_scales[row * nb + b] = x_scales_in[(int64_t)t * nb + b];
+            }
+            int64_t e = topk_idx[(int64_t)t * k + j];
+            int r = (int)(e / m);
+            recv_src_idx[row] = t;
+            for (int jj = 0; jj < k; ++jj) {
+                recv_topk_idx[row * k + jj] = (jj == j) ? e - (int64_t)r * m : -1;
+                if (recv_topk_weights)
+                    recv_topk_weights[row * k + jj] = (jj == j && topk_weights) ? topk_weights[(int64_t)t * k + j] : 0.0f;
+            }
+        }
+    }
+    free(q);
+    free(s);
+    return flags;
+}

@@ -31,6 +31,16 @@ MUTATIONS = {
                                  "acc = acc + w * oracle_bf16_to_float(partial[(int64_t)rows[i] * H + h]);"),
     "combined_weights_wrong_lane": ("acc += recv_topk_weights[(int64_t)rows[i] * k + j];",
                                     "acc += recv_topk_weights[(int64_t)rows[i] * k + (k - 1 - j)];"),
+    "expand_counter_from_zero": ("for (int e = 0; e < E; ++e) count[e] = expert_prefix[e];",
+                                 "for (int e = 0; e < E; ++e) count[e] = 0;"),
+    "expand_metadata_whole_rank": ("recv_topk_idx[row * k + jj] = (jj == j) ? e - (int64_t)r * m : -1;",
+                                   "recv_topk_idx[row * k + jj] = (topk_idx[(int64_t)t * k + jj] >= 0 && "
+                                   "topk_idx[(int64_t)t * k + jj] / m == r) ? topk_idx[(int64_t)t * k + jj] - "
+                                   "(int64_t)r * m : -1;"),
+    "expand_weight_of_other_entries": ("(jj == j && topk_weights) ? topk_weights[(int64_t)t * k + j] : 0.0f;",
+                                       "(topk_weights) ? topk_weights[(int64_t)t * k + jj] : 0.0f;"),
+    "expand_source_token_off_by_one": ("            recv_src_idx[row] = t;\n            for (int jj = 0;",
+                                       "            recv_src_idx[row] = t + 1;\n            for (int jj = 0;"),
 }
 
 

@@ -580,3 +580,153 @@ def test_oracle_weighted_combine_is_fused():
     assert float(wA) == -(1 + 2.0 ** -7 + 2.0 ** -23) and float(wB) == 1 + 2.0 ** -23
     out, _, _ = oracle.combine_weighted(partial, lay["token_dst_row"], np.array([wA, wB], np.float32))
     assert bf.bf16_bits_to_f32(out)[0, 0] == np.float32(2.0 ** -30)
+
+
+# ---------------------------------------------------------------- expand mode (one row per valid entry)
+
+def _cmp_expand(a, b):
+    np.testing.assert_array_equal(a["expert_prefix"], b["expert_prefix"])
+    np.testing.assert_array_equal(a["token_expert_row"], b["token_expert_row"])
+    assert a["num_recv"] == b["num_recv"]
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_oracle_expand_layout_vs_bruteforce_random_small(seed):
+    topk, _, _, E, R = _random_small_case(seed)
+    a = oracle.expand_layout(topk.numpy(), E)
+    assert a["flags"] == 0
+    _cmp_expand(a, bf.expand_layout(topk.numpy(), E))
+
+
+def test_oracle_expand_layout_duplicates_and_bad_entries():
+    # a token naming one expert twice gets two rows; entries outside [-1, E) are flagged and get no row
+    topk = np.array([[1, 1, -1], [0, 7, 1], [-5, 0, 2], [2, 2, 2]], np.int64)
+    a = oracle.expand_layout(topk, 4)
+    assert a["flags"] == oracle.ORACLE_BAD_TOPK
+    _cmp_expand(a, bf.expand_layout(topk, 4))
+    np.testing.assert_array_equal(a["expert_prefix"], [0, 2, 5, 9, 9])
+    np.testing.assert_array_equal(a["token_expert_row"], [[2, 3, -1], [0, -1, 4], [-1, 1, 5], [6, 7, 8]])
+
+
+def test_oracle_expand_layout_empty():
+    a = oracle.expand_layout(np.zeros((0, 4), np.int64), 8)
+    assert a["flags"] == 0 and a["num_recv"] == 0
+    np.testing.assert_array_equal(a["expert_prefix"], np.zeros(9, np.int32))
+
+
+@pytest.mark.parametrize("name", ["dsv3", "skewed", "decode"])
+def test_oracle_expand_layout_invariants_full_configs(name):
+    wk = wl.CONFIGS[name]
+    topk = wl.make_inputs(wk, with_partial=False, num_tokens=min(wk.num_tokens, 2048)).topk_idx.numpy()
+    E = wk.num_experts
+    a = oracle.expand_layout(topk, E)
+    rows = a["token_expert_row"]
+    valid = topk >= 0
+    # one row per valid entry, rows a permutation of [0, number of valid entries)
+    assert np.all((rows >= 0) == valid)
+    np.testing.assert_array_equal(np.sort(rows[valid]), np.arange(int(valid.sum())))
+    # the per-expert prefix is the rank-mode layout's expert_prefix
+    np.testing.assert_array_equal(a["expert_prefix"], oracle.layout(topk, E, wk.num_ranks)["expert_prefix"])
+    # each expert's rows fill its region, in ascending (token, choice) order
+    t_idx, j_idx = np.nonzero(valid)
+    e = topk[t_idx, j_idx]
+    r = rows[t_idx, j_idx]
+    assert np.all(r >= a["expert_prefix"][e]) and np.all(r < a["expert_prefix"][e + 1])
+    order = np.lexsort((j_idx, t_idx, e))
+    np.testing.assert_array_equal(r[order], np.arange(len(r)))
+
+
+def _distinct_topk(seed, T, E, k):
+    return wl.make_topk_uniform(torch.Generator().manual_seed(seed), T, E, k)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_oracle_expand_reduces_to_rank_mode_with_one_expert_per_rank(mode):
+    # with one expert per rank (E == R) and distinct experts per token, every entry is its
+    # rank's only entry: the expand rows, the copies and the metadata are those of rank mode
+    T, E, k, H = 96, 16, 4, 256
+    topk = wl.mask_random_lanes(torch.Generator().manual_seed(3), _distinct_topk(2, T, E, k), 0.2).numpy()
+    w = wl.make_weights(torch.Generator().manual_seed(4), T, k).numpy()
+    x = _bits(wl.make_x(torch.Generator().manual_seed(5), T, H))
+    lay = oracle.layout(topk, E, E)
+    ex = oracle.expand_layout(topk, E)
+    np.testing.assert_array_equal(ex["token_expert_row"], lay["token_dst_row"])
+    N = lay["num_recv"]
+    a = oracle.dispatch(x, topk, w, E, E, lay["token_dst_row"], N, fp8=mode == 1)
+    b = oracle.dispatch_expand(mode, x, topk, w, E, E, ex["token_expert_row"], N)
+    for key in ("recv_x", "recv_topk_idx", "recv_src_idx"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    np.testing.assert_array_equal(a["recv_topk_weights"].view(np.uint32), b["recv_topk_weights"].view(np.uint32))
+    if mode == 1:
+        np.testing.assert_array_equal(a["recv_x_scales"].view(np.uint32), b["recv_x_scales"].view(np.uint32))
+        np.testing.assert_array_equal(a["x_scales"].view(np.uint32), b["x_scales"].view(np.uint32))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("seed", range(12))
+def test_oracle_dispatch_expand_vs_bruteforce_random_small(seed, fp8):
+    topk, w, x, E, R = _random_small_case(seed)
+    ex = oracle.expand_layout(topk.numpy(), E)
+    a = oracle.dispatch_expand(1 if fp8 else 0, _bits(x), topk.numpy(), w.numpy(), E, R, ex["token_expert_row"],
+                               ex["num_recv"])
+    b = bf.dispatch_expand(_bits(x), topk.numpy(), w.numpy(), E, R, fp8=fp8)
+    assert a["flags"] == 0
+    for key in ("recv_x", "recv_src_idx", "recv_topk_idx"):
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+    np.testing.assert_array_equal(a["recv_topk_weights"].view(np.uint32), b["recv_topk_weights"].view(np.uint32))
+    if fp8:
+        np.testing.assert_array_equal(a["recv_x_scales"].view(np.uint32), b["recv_x_scales"].view(np.uint32))
+
+
+def test_oracle_dispatch_expand_fp8_input_matches_quantised():
+    # E4M3 rows dispatched with their scales land the same bytes as quantising inside dispatch
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=64)
+    topk = inp.topk_idx.numpy()
+    ex = oracle.expand_layout(topk, wk.num_experts)
+    N = ex["num_recv"]
+    q = oracle.dispatch_expand(1, _bits(inp.x), topk, inp.topk_weights.numpy(), wk.num_experts, wk.num_ranks,
+                               ex["token_expert_row"], N)
+    # the token's codes: any of its expand rows
+    first = np.array([ex["token_expert_row"][t][ex["token_expert_row"][t] >= 0][0] for t in range(64)])
+    codes, scales = q["recv_x"][first], q["recv_x_scales"][first]
+    np.testing.assert_array_equal(scales.view(np.uint32), q["x_scales"].view(np.uint32))
+    p = oracle.dispatch_expand(2, codes, topk, inp.topk_weights.numpy(), wk.num_experts, wk.num_ranks,
+                               ex["token_expert_row"], N, x_scales=scales)
+    for key in ("recv_x", "recv_topk_idx", "recv_src_idx"):
+        np.testing.assert_array_equal(p[key], q[key], err_msg=key)
+    np.testing.assert_array_equal(p["recv_x_scales"].view(np.uint32), q["recv_x_scales"].view(np.uint32))
+
+
+def test_oracle_expand_dispatch_then_combine_is_count_times_x():
+    # identity experts on the expand rows: every valid entry sends x_t back once, so the
+    # combine returns bf16(n_t * x_t); with k = 4 all valid, n_t = 4 and the sum is exact
+    wk = wl.CONFIGS["dsv3"]
+    T, E, k = 128, wk.num_experts, 4
+    topk = _distinct_topk(7, T, E, k).numpy()
+    x = wl.make_x(torch.Generator().manual_seed(8), T, 256)
+    ex = oracle.expand_layout(topk, E)
+    d = oracle.dispatch_expand(0, _bits(x), topk, None, E, wk.num_ranks, ex["token_expert_row"], ex["num_recv"])
+    out, flags = oracle.combine(d["recv_x"], ex["token_expert_row"])
+    assert flags == 0
+    np.testing.assert_array_equal(out, _bits((x.float() * 4).to(torch.bfloat16)))
+
+
+def test_oracle_expand_weighted_combine_returns_weights_and_mixture():
+    # each entry's weight travels in its own row only, so the reduced weights are the routing
+    # weights; weighting each identity-expert row by its entry weight gives sum_j w_j * x_t
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=128)
+    topk = wl.mask_random_lanes(torch.Generator().manual_seed(11), inp.topk_idx, 0.2).numpy()
+    w = inp.topk_weights.numpy()
+    ex = oracle.expand_layout(topk, wk.num_experts)
+    d = oracle.dispatch_expand(0, _bits(inp.x), topk, w, wk.num_experts, wk.num_ranks, ex["token_expert_row"],
+                               ex["num_recv"])
+    row_w = d["recv_topk_weights"].sum(axis=1).astype(np.float32)     # one non-zero entry per row
+    out, cw, _ = oracle.combine_weighted(d["recv_x"], ex["token_expert_row"], row_w, d["recv_topk_weights"])
+    np.testing.assert_array_equal(cw, np.where(topk >= 0, w, 0.0).astype(np.float32))
+    wsum = np.where(topk >= 0, w, 0.0).astype(np.float64).sum(axis=1)
+    x = inp.x.float().numpy().astype(np.float64)
+    got = bf.bf16_bits_to_f32(out).astype(np.float64)
+    # fp32 fma chain of <= 8 terms then one bf16 rounding
+    assert np.all(np.abs(got - wsum[:, None] * x) <= 2.0 ** -8 * np.abs(wsum[:, None] * x) * 1.01 + 8 * 2.0 ** -24 * np.abs(x))
