@@ -67,6 +67,11 @@ def _load():
     lib.moe_get_layout_ex.argtypes = [_P, _I, _I, _I, _I, MoeLayoutC, _P, ctypes.c_size_t, _P, _P,
                                       ctypes.POINTER(MoeLayoutOptionsC)]
     lib.moe_get_layout_ex.restype = _I
+    lib.moe_get_expand_layout_workspace_size.argtypes = [_I, _I]
+    lib.moe_get_expand_layout_workspace_size.restype = ctypes.c_size_t
+    lib.moe_get_expand_layout.argtypes = [_P, _I, _I, _I, _P, _P, _P, ctypes.c_size_t, _P, _P,
+                                          ctypes.POINTER(MoeLayoutOptionsC)]
+    lib.moe_get_expand_layout.restype = _I
     lib.moe_dispatch.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.moe_dispatch.restype = _I
     lib.moe_combine.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
@@ -158,6 +163,31 @@ def moe_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
     return out
 
 
+def moe_get_expand_layout_workspace_size(num_tokens: int, num_experts: int) -> int:
+    return int(LIB.moe_get_expand_layout_workspace_size(num_tokens, num_experts))
+
+
+def moe_get_expand_layout(topk_idx: torch.Tensor, expert_prefix: torch.Tensor, num_experts: int, *,
+                          out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                          status: Optional[torch.Tensor] = None, stream=None, wait_timeout_ns: int = 0,
+                          test_unpublished_tile: int = -1) -> torch.Tensor:
+    """Expand-mode receive rows [T, k] int32 (one per valid entry, grouped by
+    expert); ``expert_prefix`` is the layout's [E+1] prefix for ``topk_idx``."""
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    out = torch.empty(T, k, dtype=torch.int32, device=dev) if out is None else out
+    ws_bytes = moe_get_expand_layout_workspace_size(T, num_experts)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    status = new_status(dev) if status is None else status
+    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile))
+    code = LIB.moe_get_expand_layout(_ptr(topk_idx), T, k, num_experts, _ptr(expert_prefix), _ptr(out),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+                                     _stream(stream), ctypes.byref(opts))
+    _check(code, "moe_get_expand_layout")
+    return out
+
+
 @dataclasses.dataclass
 class Dispatched:
     recv_x: torch.Tensor                      # [capacity, H] bf16 or uint8 (E4M3 codes)
@@ -171,16 +201,18 @@ class Dispatched:
 MOE_DISPATCH_BF16 = 0
 MOE_DISPATCH_QUANTIZE_FP8 = 1
 MOE_DISPATCH_FP8 = 2
+MOE_DISPATCH_EXPAND = 0x100
 
 
 def moe_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
                  num_experts: int, num_ranks: int, token_dst_row: torch.Tensor, recv_capacity: int, *,
-                 quantize_fp8: bool = False, x_scales: Optional[torch.Tensor] = None,
+                 quantize_fp8: bool = False, x_scales: Optional[torch.Tensor] = None, expand: bool = False,
                  out: Optional[Dispatched] = None, with_metadata: bool = True,
                  status: Optional[torch.Tensor] = None, stream=None) -> Dispatched:
     """Row copies and per-row metadata. ``x`` bf16 is copied as is, or quantised
     to E4M3 with per-128 scales when ``quantize_fp8``; ``x`` uint8 (E4M3 codes)
-    is copied together with its ``x_scales`` [T, H/128]."""
+    is copied together with its ``x_scales`` [T, H/128]. With ``expand``,
+    ``token_dst_row`` is the expand layout's token_expert_row."""
     T, H = x.shape
     k = topk_idx.shape[1]
     dev = x.device
@@ -203,7 +235,8 @@ def moe_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional
     status = new_status(dev) if status is None else status
     scales_arg = x_scales if fp8_in else out.x_scales
     code = LIB.moe_dispatch(_ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), k, num_experts, num_ranks,
-                            _ptr(token_dst_row), recv_capacity, mode, _ptr(out.recv_x),
+                            _ptr(token_dst_row), recv_capacity, mode | (MOE_DISPATCH_EXPAND if expand else 0),
+                            _ptr(out.recv_x),
                             _ptr(out.recv_x_scales), _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights),
                             _ptr(out.recv_src_idx), _ptr(scales_arg), _ptr(status), _stream(stream))
     _check(code, "moe_dispatch")

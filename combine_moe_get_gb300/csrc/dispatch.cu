@@ -1,4 +1,5 @@
-// dispatch.cu -- copy each token's row once per distinct destination rank.
+// dispatch.cu -- copy each token's row once per distinct destination rank
+// (or, in expand mode, once per valid top-k entry).
 //
 // DeepEP V2 deep-dive page ("DeepEP V2 深度深潜"), section 3.3 stage 2: a
 // dispatch warp loads a token's hidden row into shared memory once and stores
@@ -52,6 +53,7 @@ struct DispatchArgs {
     float *x_scales;
     const float *in_scales;   // E4M3 input: the token's scales, copied to every destination row
     int nb;                   // scale blocks per row (H / 128), FP8
+    int expand;               // dst_row holds expand-mode rows: a row's metadata keeps its own entry only
     int32_t *status;
     int chunk_bytes;          // input bytes per unit; multiple of 16 (FP8: of 256)
     int num_chunks;           // units per token
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
             if (c == 0) {
                 const int rd = __shfl_sync(kFull, rl, jd);
                 if (lane < a.k) {
-                    const bool local = rl == rd;
+                    const bool local = a.expand ? (lane == jd && rl >= 0) : rl == rd;
                     if (a.recv_topk_idx) a.recv_topk_idx[(int64_t)rowd * a.k + lane] = local ? (int64_t)el : -1;
                     if (a.recv_topk_w) a.recv_topk_w[(int64_t)rowd * a.k + lane] = local ? wgt : 0.0f;
                 }
@@ -403,6 +405,7 @@ struct Fp8Args {
     float *recv_topk_w;
     int32_t *recv_src;
     float *x_scales;
+    int expand;                  // dst_row holds expand-mode rows (metadata: own entry only)
     int32_t *status;
     int n_in;                    // input ring slots
     int num_slices;
@@ -534,7 +537,7 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
                 const int rowd = __shfl_sync(kFull, row, jd);
                 const int rd = __shfl_sync(kFull, rl, jd);
                 if (lane < a.k) {
-                    const bool local = rl == rd;
+                    const bool local = a.expand ? (lane == jd && rl >= 0) : rl == rd;
                     if (a.recv_topk_idx) a.recv_topk_idx[(int64_t)rowd * a.k + lane] = local ? (int64_t)el : -1;
                     if (a.recv_topk_w) a.recv_topk_w[(int64_t)rowd * a.k + lane] = local ? wgt : 0.0f;
                 }
@@ -574,6 +577,7 @@ int launch_dispatch(const DispatchLaunch &L) {
     a.x_scales = fp8 ? L.x_scales : nullptr;
     a.in_scales = fp8_in ? L.x_scales : nullptr;
     a.nb = L.hidden / 128;
+    a.expand = L.expand ? 1 : 0;
     a.status = L.status;
     a.l2_hints = tu.l2_hints;
     a.timeout_ns = kDefaultWaitNs;
@@ -589,6 +593,7 @@ int launch_dispatch(const DispatchLaunch &L) {
         f.topk = a.topk; f.topk_w = a.topk_w; f.dst_row = a.dst_row; f.capacity = a.capacity;
         f.recv_x = a.recv_x; f.recv_scales = a.recv_scales; f.recv_topk_idx = a.recv_topk_idx;
         f.recv_topk_w = a.recv_topk_w; f.recv_src = a.recv_src; f.x_scales = a.x_scales;
+        f.expand = a.expand;
         f.status = a.status;
         f.num_slices = (f.nb + kFp8SliceBlocks - 1) / kFp8SliceBlocks;
         f.l2_hints = a.l2_hints;

@@ -80,10 +80,10 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes) {
     std::lock_guard<std::mutex> lock(mu);
     size_t &cur = done[d][kernel];
     if (bytes <= cur) return MOE_OK;
-    if (bytes > 48 * 1024) {
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
+    // set even below 48 KB: the default limit covers dynamic plus static shared
+    // memory, so a kernel with static shared memory needs it raised earlier
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return MOE_ERR_CUDA;
     cur = bytes;
     return MOE_OK;
 }
@@ -211,6 +211,41 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
                          workspace_bytes, status, stream, timeout, unpublished);
 }
 
+MOE_API size_t moe_get_expand_layout_workspace_size(int num_tokens, int num_experts) {
+    if (!shape_ok(num_tokens, 1, num_experts, 1)) return 0;
+    return moe::expand_workspace_bytes(num_tokens, num_experts);
+}
+
+MOE_API int moe_get_expand_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                                  const int32_t *expert_prefix, int32_t *token_expert_row, void *workspace,
+                                  size_t workspace_bytes, int32_t *status, void *stream,
+                                  const moe_layout_options_t *options) {
+    const int T = num_tokens, k = num_topk, E = num_experts;
+    if (!shape_ok(T, k, E, 1)) return MOE_ERR_INVALID_ARG;
+    if (!status) return MOE_ERR_INVALID_ARG;
+    if (!aligned(status, 4)) return MOE_ERR_MISALIGNED;
+    if (T > 0) {
+        if (!topk_idx || !expert_prefix || !token_expert_row || !workspace) return MOE_ERR_INVALID_ARG;
+        if (!aligned(topk_idx, 8) || !aligned(expert_prefix, 4) || !aligned(token_expert_row, 4) ||
+            !aligned(workspace, 16))
+            return MOE_ERR_MISALIGNED;
+        if (workspace_bytes < moe::expand_workspace_bytes(T, E)) return MOE_ERR_WORKSPACE;
+    }
+    moe::ExpandLaunch L;
+    L.topk_idx = topk_idx;
+    L.num_tokens = T;
+    L.num_topk = k;
+    L.num_experts = E;
+    L.expert_prefix = expert_prefix;
+    L.token_expert_row = token_expert_row;
+    L.workspace = workspace;
+    L.status = status;
+    L.stream = stream;
+    L.timeout_ns = options ? options->wait_timeout_ns : 0;
+    L.unpublished_tile = options ? options->test_unpublished_tile : -1;
+    return moe::launch_expand_layout(L);
+}
+
 MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
                          const float *topk_weights, int num_topk, int num_experts, int num_ranks,
                          const int32_t *token_dst_row, int recv_capacity, int mode, void *recv_x,
@@ -218,6 +253,8 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
                          int32_t *recv_src_idx, float *x_scales, int32_t *status, void *stream) {
     const int T = num_tokens, H = hidden;
     if (!shape_ok(T, num_topk, num_experts, num_ranks)) return MOE_ERR_INVALID_ARG;
+    const bool expand = (mode & MOE_DISPATCH_EXPAND) != 0;
+    mode &= ~MOE_DISPATCH_EXPAND;
     if (mode != MOE_DISPATCH_BF16 && mode != MOE_DISPATCH_QUANTIZE_FP8 && mode != MOE_DISPATCH_FP8)
         return MOE_ERR_INVALID_ARG;
     const bool fp8_out = mode != MOE_DISPATCH_BF16;
@@ -247,6 +284,7 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
     L.token_dst_row = token_dst_row;
     L.recv_capacity = recv_capacity;
     L.mode = mode;
+    L.expand = expand;
     L.recv_x = recv_x;
     L.recv_x_scales = fp8_out ? recv_x_scales : nullptr;
     L.recv_topk_idx = recv_topk_idx;

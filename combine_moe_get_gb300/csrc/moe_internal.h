@@ -1,5 +1,6 @@
 // moe_internal.h -- host-side interfaces between the C ABI entry points
-// (moe_api.cu) and the kernel launchers (layout.cu, dispatch.cu, combine.cu).
+// (moe_api.cu) and the kernel launchers (layout.cu, expand.cu, dispatch.cu,
+// combine.cu).
 // Arguments reaching a launcher have already been validated.
 #pragma once
 
@@ -42,6 +43,21 @@ struct LayoutLaunch {
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 int launch_layout(const LayoutLaunch &L);
 
+struct ExpandLaunch {
+    const int64_t *topk_idx;
+    int num_tokens, num_topk, num_experts;
+    const int32_t *expert_prefix;
+    int32_t *token_expert_row;
+    void *workspace;
+    int32_t *status;
+    void *stream;
+    int64_t timeout_ns;     // <= 0: default
+    int unpublished_tile;   // test hook, -1 = off
+};
+
+size_t expand_workspace_bytes(int num_tokens, int num_experts);
+int launch_expand_layout(const ExpandLaunch &L);
+
 struct DispatchLaunch {
     const void *x;
     int num_tokens, hidden;
@@ -50,7 +66,8 @@ struct DispatchLaunch {
     int num_topk, num_experts, num_ranks;
     const int32_t *token_dst_row;
     int recv_capacity;
-    int mode;                 // moe_dispatch_mode_t
+    int mode;                 // moe_dispatch_mode_t, without MOE_DISPATCH_EXPAND
+    bool expand;              // token_dst_row holds expand-mode rows
     void *recv_x;
     float *recv_x_scales;
     int64_t *recv_topk_idx;

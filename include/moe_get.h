@@ -133,6 +133,48 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
                               int num_ranks, moe_layout_t layout, void *workspace, size_t workspace_bytes,
                               int32_t *status, void *stream, const moe_layout_options_t *options);
 
+/* Bytes of device workspace moe_get_expand_layout needs (16-byte aligned
+ * pointer required). Host-only; never fails (0 for invalid sizes). */
+MOE_API size_t moe_get_expand_layout_workspace_size(int num_tokens, int num_experts);
+
+/*
+ * moe_get_expand_layout -- receive rows of expand mode: one row per valid
+ * top-k entry, grouped by expert (the layout a grouped expert GEMM reads).
+ *
+ * Page: copy epilogue of the dispatch (section 3.3 stage 3), expand mode: the
+ * destination of a received token is taken from a counter per expert that
+ * starts at the exclusive prefix of the per-expert counts
+ * (psum_num_recv_tokens_per_expert) and advances by one per placed token.
+ * The page advances it with atomicAdd (arrival order); this library places
+ * the entries of each expert in source order instead:
+ *   token_expert_row[t, j] = expert_prefix[e] + #{(t', j') < (t, j) in
+ *                            (token, choice) order : topk_idx[t', j'] == e}
+ * for e = topk_idx[t, j] in [0, E), and -1 for masked or invalid entries.
+ * Expert e's rows are [expert_prefix[e], expert_prefix[e+1]); since experts
+ * are numbered rank by rank, rank r's rows are [expert_prefix[r*m],
+ * expert_prefix[(r+1)*m]). A token naming one expert in two entries gets two
+ * rows. The number of rows is expert_prefix[E] (<= T*k). The in-expert
+ * position is a decoupled-lookback column scan over tiles of 256 tokens
+ * (bounded waits, MOE_ERR_TIMEOUT on expiry).
+ *
+ *   topk_idx          [T, k] int64, device (as for moe_get_layout).
+ *   expert_prefix     [E+1] int32, device, input: moe_get_layout's output for
+ *                     the same topk_idx (enqueued earlier, e.g. on the same stream).
+ *   token_expert_row  [T, k] int32, device, output. Pass it as `token_dst_row`
+ *                     to moe_dispatch with MOE_DISPATCH_EXPAND and to
+ *                     moe_combine / moe_combine_ex.
+ *   workspace         device scratch of at least
+ *                     moe_get_expand_layout_workspace_size() bytes, cleared by the
+ *                     call on `stream`; not shared by calls that overlap on the GPU.
+ *   options           NULL or the options of moe_get_layout_ex; here the test hook
+ *                     names a tile of 256 tokens.
+ * Limits: 1 <= k <= 32, 1 <= E <= 8192, T * k < 2^31.
+ */
+MOE_API int moe_get_expand_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
+                                  const int32_t *expert_prefix, int32_t *token_expert_row, void *workspace,
+                                  size_t workspace_bytes, int32_t *status, void *stream,
+                                  const moe_layout_options_t *options);
+
 /*
  * moe_dispatch -- copy each token once per distinct destination rank.
  *
@@ -159,6 +201,14 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
  *   MOE_DISPATCH_FP8            x already E4M3 [T, H] bytes with its scales x_scales
  *                               [T, H/128] (input, section 3.4's sf next to the hidden
  *                               bytes); codes and scales are copied unchanged.
+ * Any of the three may be OR-ed with MOE_DISPATCH_EXPAND (expand mode, section 3.3
+ * stage 3): `token_dst_row` is then the token_expert_row of moe_get_expand_layout,
+ * the token goes once to the row of every valid entry (t, j), and each row's
+ * metadata keeps that entry only:
+ *   recv_topk_idx[row, jj] = topk_idx[t, j] - r*m for jj == j, else -1;
+ *   recv_topk_weights[row, jj] = topk_weights[t, j] for jj == j, else 0.
+ * (In expand mode a token has several rows on one rank, one per local expert, so
+ * the rank-wide record would repeat its other local entries.)
  *
  *   x                  [T, H] bf16 (E4M3 bytes in MOE_DISPATCH_FP8), device, 16-byte
  *                      aligned, H % 8 == 0.
@@ -166,7 +216,8 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
  *   topk_weights       [T, k] fp32 or NULL (then recv_topk_weights may be NULL).
  *   token_dst_row      [T, k] int32 from moe_get_layout.
  *   recv_capacity      rows available in the receive arrays; rows >= capacity
- *                      raise MOE_ERR_CAPACITY and are skipped. N <= T*min(k, R).
+ *                      raise MOE_ERR_CAPACITY and are skipped. N <= T*min(k, R)
+ *                      (expand mode: expert_prefix[E] <= T*k).
  *   recv_x             [capacity, H] bf16, or [capacity, H] uint8 E4M3 in the FP8 modes.
  *   recv_x_scales      [capacity, H/128] fp32 (FP8 modes only, else ignored).
  *   recv_topk_idx      [capacity, k] int64, may be NULL (not written).
@@ -175,7 +226,12 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
  *   x_scales           [T, H/128] fp32: output of MOE_DISPATCH_QUANTIZE_FP8 (may be
  *                      NULL), input of MOE_DISPATCH_FP8 (required), else ignored.
  */
-typedef enum { MOE_DISPATCH_BF16 = 0, MOE_DISPATCH_QUANTIZE_FP8 = 1, MOE_DISPATCH_FP8 = 2 } moe_dispatch_mode_t;
+typedef enum {
+    MOE_DISPATCH_BF16 = 0,
+    MOE_DISPATCH_QUANTIZE_FP8 = 1,
+    MOE_DISPATCH_FP8 = 2,
+    MOE_DISPATCH_EXPAND = 0x100   /* flag, OR-ed with one of the above */
+} moe_dispatch_mode_t;
 
 MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
                          const float *topk_weights, int num_topk, int num_experts, int num_ranks,
@@ -200,7 +256,9 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
  *
  *   partial          [num_partial_rows, H] bf16, device, 16-byte aligned, H % 8 == 0.
  *   token_dst_row    [T, k] int32 from moe_get_layout; rows >= num_partial_rows
- *                    raise MOE_ERR_CAPACITY and are skipped.
+ *                    raise MOE_ERR_CAPACITY and are skipped. In expand mode, the
+ *                    token_expert_row of moe_get_expand_layout: one partial row per
+ *                    valid entry, summed in ascending row (= expert) order.
  *   out              [T, H] bf16, device, 16-byte aligned.
  */
 MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_tokens, int hidden,

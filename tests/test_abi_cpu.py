@@ -107,6 +107,8 @@ def _dispatch(lib, x=A, T=128, H=256, topk=A + 0x10000, w=None, k=2, E=16, R=4, 
     (dict(k=40), 1), (dict(E=17), 1), (dict(cap=-1), 1), (dict(x=None), 1), (dict(recv=None), 1),
     (dict(status=None), 1), (dict(x=A + 8), 2), (dict(recv=A + 8), 2), (dict(dst=MIS), 2),
     (dict(fp8=3), 1), (dict(fp8=2, scales=A + 0x400000), 1), (dict(fp8=-1), 1),
+    (dict(fp8=0x103), 1), (dict(fp8=0x200), 1), (dict(fp8=0x102), 1), (dict(fp8=0x101, H=264), 1),
+    (dict(fp8=0x100, dst=MIS), 2),
 ])
 def test_dispatch_rejects_bad_arguments(lib, kw, code):
     assert _dispatch(lib, **kw) == code
@@ -123,3 +125,25 @@ def _combine(lib, partial=A, rows=256, T=128, H=256, k=2, dst=A + 0x10000, out=A
 ])
 def test_combine_rejects_bad_arguments(lib, kw, code):
     assert _combine(lib, **kw) == code
+
+
+def test_expand_workspace_size(lib):
+    ws = lib.moe_get_expand_layout_workspace_size
+    assert ws(4096, 256) >= 4096 // 256 * 256 * 8
+    assert ws(0, 256) > 0
+    assert ws(4096, 0) == 0 and ws(4096, 8193) == 0 and ws(-1, 16) == 0
+
+
+def _expand(lib, T=128, k=2, E=16, topk=A, prefix=A + 0x10000, rows=A + 0x20000, ws=A + 0x100000,
+            ws_bytes=1 << 30, status=A + 0x200000):
+    return lib.LIB.moe_get_expand_layout(topk, T, k, E, prefix, rows, ws, ws_bytes, status, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=0), 1), (dict(k=33), 1), (dict(E=0), 1), (dict(E=8193), 1), (dict(T=-1), 1),
+    (dict(status=None), 1), (dict(topk=None), 1), (dict(prefix=None), 1), (dict(rows=None), 1),
+    (dict(ws=None), 1), (dict(topk=MIS), 2), (dict(prefix=MIS), 2), (dict(rows=MIS), 2), (dict(ws=A + 8), 2),
+    (dict(status=MIS), 2), (dict(ws_bytes=64), 7),
+])
+def test_expand_layout_rejects_bad_arguments(lib, kw, code):
+    assert _expand(lib, **kw) == code
