@@ -209,6 +209,17 @@ class Step:
             recv_src_idx=self.disp.recv_src_idx, x_scales=None)
         self.row_w = torch.rand(self.cap, device=device)
         self.cw = torch.empty(T, k, dtype=torch.float32, device=device)
+        # expand mode: one receive row per valid top-k entry, grouped by expert
+        self.xcap = T * k
+        self.xws = torch.empty(moe.moe_get_expand_layout_workspace_size(T, E), dtype=torch.uint8, device=device)
+        self.xrows = torch.empty(T, k, dtype=torch.int32, device=device)
+        self.dispx = moe.Dispatched(
+            recv_x=torch.empty(self.xcap, H, dtype=torch.bfloat16, device=device), recv_x_scales=None,
+            recv_topk_idx=torch.empty(self.xcap, k, dtype=torch.int64, device=device),
+            recv_topk_weights=torch.empty(self.xcap, k, dtype=torch.float32, device=device),
+            recv_src_idx=torch.empty(self.xcap, dtype=torch.int32, device=device), x_scales=None)
+        self.partial_x = (self.partial if self.partial.shape[0] >= self.xcap else
+                          wl.make_partial(torch.Generator().manual_seed(w.seed + 1), self.xcap, H).to(device))
 
     def layout(self):
         self.moe.moe_get_layout(self.topk, self.w.num_experts, self.w.num_ranks, out=self.lay, workspace=self.ws,
@@ -231,6 +242,23 @@ class Step:
 
     def combine(self):
         self.moe.moe_combine(self.partial, self.lay.token_dst_row, out=self.out, status=self.status)
+
+    def expand_layout(self):
+        self.moe.moe_get_expand_layout(self.topk, self.lay.expert_prefix, self.w.num_experts, out=self.xrows,
+                                       workspace=self.xws, status=self.status)
+
+    def dispatch_expand(self):
+        self.moe.moe_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks, self.xrows,
+                              self.xcap, expand=True, out=self.dispx, status=self.status)
+
+    def combine_expand(self):
+        self.moe.moe_combine(self.partial_x, self.xrows, out=self.out, status=self.status)
+
+    def expand_step(self):
+        self.layout()
+        self.expand_layout()
+        self.dispatch_expand()
+        self.combine_expand()
 
 
 def run_ours(args, world, rank, local):
@@ -363,7 +391,12 @@ def run_ours(args, world, rank, local):
     fp8_ms = time_alone(lambda: st.dispatch(fp8=True), reps)                  # fused E4M3 quantisation
     fp8in_ms = time_alone(st.dispatch_fp8_input, reps)                        # E4M3 rows + scales relayed
     wcomb_ms = time_alone(st.combine_weighted, reps)                          # weighted rows + combined weights
+    xlay_ms = time_alone(st.expand_layout, reps)                              # expand mode, each kernel alone
+    xdis_ms = time_alone(st.dispatch_expand, reps)
+    xcom_ms = time_alone(st.combine_expand, reps)
+    xstep_ms = time_alone(st.expand_step, reps)                               # the whole expand-mode step
     moe.check_status(st.status, "dispatch / combine variants")
+    NX = int(st.lay.expert_prefix[-1].item())                                 # expand rows: valid entries
 
     peak, peak_kind = hbm_peak()
     row = H * 2
@@ -371,6 +404,7 @@ def run_ours(args, world, rank, local):
     bytes_fp8 = T * row + N * H + N * (H // 128) * 4    # x read + e4m3 rows + scales
     bytes_fp8in = (T + N) * (H + (H // 128) * 4)        # e4m3 rows + scales read once, written per rank
     bytes_wcomb = bytes_bf16 + N * 4                    # + one weight per receive row
+    bytes_expand = T * row + NX * row                   # x read once + one row per valid entry
     kern = {
         "layout_us": mean(lay_ms) * 1e3,
         "dispatch_us": mean(dis_ms) * 1e3,
@@ -378,6 +412,12 @@ def run_ours(args, world, rank, local):
         "dispatch_fp8_us": mean(fp8_ms) * 1e3,
         "dispatch_fp8_input_us": mean(fp8in_ms) * 1e3,
         "combine_weighted_us": mean(wcomb_ms) * 1e3,
+        "expand_layout_us": mean(xlay_ms) * 1e3,
+        "dispatch_expand_us": mean(xdis_ms) * 1e3,
+        "combine_expand_us": mean(xcom_ms) * 1e3,
+        "expand_step_us": mean(xstep_ms) * 1e3,
+        "expand_step_tokens_per_s": T / (mean(xstep_ms) * 1e-3),
+        "expand_rows": NX,
     }
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     kern["dispatch_gbs"] = gbs(bytes_bf16, mean(dis_ms))
@@ -385,7 +425,10 @@ def run_ours(args, world, rank, local):
     kern["dispatch_fp8_gbs"] = gbs(bytes_fp8, mean(fp8_ms))
     kern["dispatch_fp8_input_gbs"] = gbs(bytes_fp8in, mean(fp8in_ms))
     kern["combine_weighted_gbs"] = gbs(bytes_wcomb, mean(wcomb_ms))
-    for key in ("dispatch", "combine", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted"):
+    kern["dispatch_expand_gbs"] = gbs(bytes_expand, mean(xdis_ms))
+    kern["combine_expand_gbs"] = gbs(bytes_expand, mean(xcom_ms))
+    for key in ("dispatch", "combine", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted", "dispatch_expand",
+                "combine_expand"):
         kern[f"{key}_frac"] = kern[f"{key}_gbs"] / peak
     dominant = "dispatch" if mean(dis_ms) >= mean(com_ms) else "combine"
     dom_ms = mean(dis_ms) if dominant == "dispatch" else mean(com_ms)
