@@ -74,6 +74,9 @@ def _load():
     lib.moe_get_expand_layout.restype = _I
     lib.moe_dispatch.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.moe_dispatch.restype = _I
+    lib.moe_layout_dispatch.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, MoeLayoutC, _P, ctypes.c_size_t, _I, _I, _P,
+                                        _P, _P, _P, _P, _P, _P, _P]
+    lib.moe_layout_dispatch.restype = _I
     lib.moe_combine.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P]
     lib.moe_combine.restype = _I
     lib.moe_combine_ex.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
@@ -241,6 +244,47 @@ def moe_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional
                             _ptr(out.recv_src_idx), _ptr(scales_arg), _ptr(status), _stream(stream))
     _check(code, "moe_dispatch")
     return out
+
+
+def moe_layout_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional[torch.Tensor],
+                        num_experts: int, num_ranks: int, recv_capacity: int, *, quantize_fp8: bool = False,
+                        x_scales: Optional[torch.Tensor] = None, layout: Optional[Layout] = None,
+                        workspace: Optional[torch.Tensor] = None, out: Optional[Dispatched] = None,
+                        with_metadata: bool = True, status: Optional[torch.Tensor] = None,
+                        stream=None) -> tuple[Layout, Dispatched]:
+    """moe_get_layout + moe_dispatch in one call (one launch for small batches)."""
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    dev = x.device
+    fp8_in = x.dtype == torch.uint8
+    mode = MOE_DISPATCH_FP8 if fp8_in else (MOE_DISPATCH_QUANTIZE_FP8 if quantize_fp8 else MOE_DISPATCH_BF16)
+    fp8_out = mode != MOE_DISPATCH_BF16
+    if fp8_in and x_scales is None:
+        raise ValueError("E4M3 input needs its x_scales")
+    layout = layout or Layout.empty(T, k, num_experts, num_ranks, dev)
+    ws_bytes = moe_get_layout_workspace_size(T, num_experts, num_ranks)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    if out is None:
+        nb = H // 128
+        out = Dispatched(
+            recv_x=torch.empty(recv_capacity, H, dtype=torch.uint8 if fp8_out else torch.bfloat16, device=dev),
+            recv_x_scales=torch.empty(recv_capacity, nb, dtype=torch.float32, device=dev) if fp8_out else None,
+            recv_topk_idx=torch.empty(recv_capacity, k, dtype=torch.int64, device=dev) if with_metadata else None,
+            recv_topk_weights=(torch.empty(recv_capacity, k, dtype=torch.float32, device=dev)
+                               if with_metadata else None),
+            recv_src_idx=torch.empty(recv_capacity, dtype=torch.int32, device=dev) if with_metadata else None,
+            x_scales=(x_scales if fp8_in else
+                      (torch.empty(T, nb, dtype=torch.float32, device=dev) if quantize_fp8 else None)))
+    status = new_status(dev) if status is None else status
+    scales_arg = x_scales if fp8_in else out.x_scales
+    code = LIB.moe_layout_dispatch(_ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), k, num_experts, num_ranks,
+                                   layout.c(), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   recv_capacity, mode, _ptr(out.recv_x), _ptr(out.recv_x_scales),
+                                   _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights), _ptr(out.recv_src_idx),
+                                   _ptr(scales_arg), _ptr(status), _stream(stream))
+    _check(code, "moe_layout_dispatch")
+    return layout, out
 
 
 def moe_combine(partial: torch.Tensor, token_dst_row: torch.Tensor, *, out: Optional[torch.Tensor] = None,

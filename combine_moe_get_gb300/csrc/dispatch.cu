@@ -62,6 +62,11 @@ struct DispatchArgs {
     int warp_smem;
     int l2_hints;
     uint64_t timeout_ns;
+    // fused launch (layout computed by every CTA in shared memory, dst_row unused)
+    int T, R;                 // tokens, ranks
+    int fl_words;             // bitmap words per rank: ceil(T / 32)
+    size_t fl_off;            // byte offset of the layout region in dynamic shared memory
+    moe_layout_t fl_out;      // layout outputs, written by CTA 0
 };
 
 // Block scale RN(amax / 448) without a division: q0 = RN(amax * C) with
@@ -210,7 +215,172 @@ __device__ __forceinline__ float quantize_lane16(const uint4 lo, const uint4 hi,
     return scale;
 }
 
-template <bool kFP8>
+// ------------------------------------------------------------------ fused layout (small batches)
+//
+// For a small batch every CTA of the fused launch computes the whole layout
+// itself in shared memory, the same definition as layout.cu: per token the
+// entries are de-duplicated by rank (__match_any_sync, lowest entry owns
+// the rank), a bitmap [word][rank] records membership, per-rank popcounts
+// give the counts and word prefixes, and an exclusive scan over ranks gives
+// the rank regions. Receive row of (t, r) = rank_prefix[r] + #{t' < t in r}.
+// No CTA waits on another. CTA 0 writes the counts and prefixes (and counts
+// experts); every CTA writes is_token_in_rank and token_dst_row for its own
+// slice of tokens.
+
+// Shared memory of the fused layout: bitmap u32 [W][R] | word prefix u16 [R][W] |
+// rank prefix i32 [R+1] | expert histogram i32 [E+1] | expert ids i16 [T*k] |
+// rank ids i16 [T*k]
+struct FusedSmem {
+    size_t wprefix, rprefix, hist, eid, rid, total;
+};
+
+__host__ __device__ inline FusedSmem fused_smem(int T, int R, int E, int k) {
+    const size_t W = (size_t)((T + 31) / 32);
+    FusedSmem f;
+    f.wprefix = (W * R * 4 + 15) / 16 * 16;
+    f.rprefix = f.wprefix + (W * R * 2 + 15) / 16 * 16;
+    f.hist = f.rprefix + ((size_t)(R + 1) * 4 + 15) / 16 * 16;
+    f.eid = f.hist + ((size_t)(E + 1) * 4 + 15) / 16 * 16;
+    f.rid = f.eid + ((size_t)T * k * 2 + 15) / 16 * 16;
+    f.total = f.rid + ((size_t)T * k * 2 + 15) / 16 * 16;
+    return f;
+}
+
+// In-place exclusive scan of n int32 in shared memory by one warp; v[n] = total.
+__device__ void warp_exclusive_scan(int32_t *v, int n, int lane) {
+    const int per = (n + 31) / 32;
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    int32_t local = 0;
+    for (int i = lo; i < hi; ++i) local += v[i];
+    int32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int32_t run = incl - local;
+    for (int i = lo; i < hi; ++i) {
+        const int32_t x = v[i];
+        v[i] = run;
+        run += x;
+    }
+    if (lane == 31) v[n] = incl;
+}
+
+// The (token, rank) owner of entry j of token t, and its receive row (-1 if not an owner).
+__device__ __forceinline__ int fused_row(const DispatchArgs &a, const uint32_t *bitmap, const uint16_t *wprefix,
+                                         const int32_t *rprefix, int t, int r, int lane, unsigned peers) {
+    if (r < 0 || (__ffs(peers) - 1) != lane) return -1;
+    const uint32_t word = bitmap[(t >> 5) * a.R + r];
+    return rprefix[r] + wprefix[r * a.fl_words + (t >> 5)] + __popc(word & ((1u << (t & 31)) - 1u));
+}
+
+// Every thread of the CTA calls this once.
+__device__ void fused_layout(const DispatchArgs &a, uint8_t *region) {
+    const FusedSmem fs = fused_smem(a.T, a.R, a.E, a.k);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(region);
+    uint16_t *wprefix = reinterpret_cast<uint16_t *>(region + fs.wprefix);
+    int32_t *rprefix = reinterpret_cast<int32_t *>(region + fs.rprefix);
+    int32_t *hist = reinterpret_cast<int32_t *>(region + fs.hist);
+    int16_t *eid = reinterpret_cast<int16_t *>(region + fs.eid);
+    int16_t *rid = reinterpret_cast<int16_t *>(region + fs.rid);
+    const int R = a.R, W = a.fl_words, k = a.k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, warps = blockDim.x >> 5;
+    const bool cta0 = blockIdx.x == 0;
+    for (int i = threadIdx.x; i < W * R; i += blockDim.x) bitmap[i] = 0u;
+    if (cta0)
+        for (int i = threadIdx.x; i < a.E; i += blockDim.x) hist[i] = 0;
+    // the batch's top-k entries as expert ids (-1: masked or invalid), 8 loads in flight per thread
+    const int n_ent = a.T * k;
+    for (int base = threadIdx.x; base < n_ent; base += 8 * blockDim.x) {
+        int64_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * blockDim.x;
+            v[u] = i < n_ent ? ld_nc_i64(a.topk + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * blockDim.x;
+            if (i < n_ent) {
+                const bool ok = v[u] >= 0 && v[u] < a.E;
+                if (!ok && v[u] != -1 && cta0) report(a.status, MOE_ERR_BAD_TOPK);
+                eid[i] = ok ? (int16_t)v[u] : (int16_t)-1;
+                rid[i] = ok ? (int16_t)((int)v[u] / a.m) : (int16_t)-1;
+            }
+        }
+    }
+    __syncthreads();
+    // one thread per token: each rank of the token once (its lowest entry), membership bits
+    for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
+        const int16_t *tr = rid + t * k;
+        for (int j = 0; j < k; ++j) {
+            const int r = tr[j];
+            if (r < 0) continue;
+            if (cta0) atomicAdd(&hist[eid[t * k + j]], 1);
+            bool first = true;
+            for (int jj = 0; jj < j; ++jj) first = first && tr[jj] != r;
+            if (first) atomicOr(&bitmap[(t >> 5) * R + r], 1u << (t & 31));
+        }
+    }
+    __syncthreads();
+    const int tpp = 32 / k, sub = lane / k, j = lane - sub * k;
+    const bool lane_used = sub < tpp;
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        uint32_t run = 0;
+        for (int w = 0; w < W; ++w) {
+            wprefix[r * W + w] = (uint16_t)run;
+            run += __popc(bitmap[w * R + r]);
+        }
+        rprefix[r] = (int32_t)run;
+    }
+    __syncthreads();
+    if (warp == 0) warp_exclusive_scan(rprefix, R, lane);
+    if (cta0 && warp == (warps > 1 ? 1 : 0)) {
+        for (int e = lane; e < a.E; e += 32) a.fl_out.num_tokens_per_expert[e] = hist[e];
+        __syncwarp();
+        warp_exclusive_scan(hist, a.E, lane);
+        __syncwarp();
+        for (int e = lane; e <= a.E; e += 32) a.fl_out.expert_prefix[e] = hist[e];
+    }
+    __syncthreads();
+    // ---- layout outputs: counts and prefixes by CTA 0, membership and rows by token slice
+    if (cta0) {
+        for (int r = threadIdx.x; r < R; r += blockDim.x) {
+            a.fl_out.num_tokens_per_rank[r] = rprefix[r + 1] - rprefix[r];
+            a.fl_out.rank_prefix[r] = rprefix[r];
+        }
+        if (threadIdx.x == 0) a.fl_out.rank_prefix[R] = rprefix[R];
+    }
+    const int t_lo = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
+    const int t_hi = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
+    uint8_t *in_rank = a.fl_out.is_token_in_rank + (int64_t)t_lo * R;
+    const int nbytes = (t_hi - t_lo) * R;
+    if ((R & 3) == 0) {
+        for (int i = threadIdx.x; i < nbytes / 4; i += blockDim.x) {
+            const int tl = (i * 4) / R, r0 = i * 4 - tl * R, t = t_lo + tl;
+            uint32_t v = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v |= ((bitmap[(t >> 5) * R + r0 + b] >> (t & 31)) & 1u) << (8 * b);
+            reinterpret_cast<uint32_t *>(in_rank)[i] = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < nbytes; i += blockDim.x) {
+            const int tl = i / R, r = i - tl * R, t = t_lo + tl;
+            in_rank[i] = (uint8_t)((bitmap[(t >> 5) * R + r] >> (t & 31)) & 1u);
+        }
+    }
+    for (int base = t_lo + warp * tpp; base < t_hi; base += warps * tpp) {
+        const int t = base + sub;
+        const bool act = lane_used && t < t_hi;
+        const int r = act ? (int)rid[t * k + j] : -1;
+        const unsigned peers = __match_any_sync(kFull, r >= 0 ? sub * R + r : -(lane + 1));
+        const int row = fused_row(a, bitmap, wprefix, rprefix, t, r, lane, peers);
+        if (act) a.fl_out.token_dst_row[(int64_t)t * k + j] = row;
+    }
+}
+
+template <bool kFP8, bool kFused>
 __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -225,8 +395,8 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
 
     const int64_t gw = (int64_t)blockIdx.x * warps + warp;
     const int64_t GW = (int64_t)gridDim.x * warps;
-    if (gw >= a.num_units) return;
-    const int64_t n_w = (a.num_units - 1 - gw) / GW + 1;
+    if (!kFused && gw >= a.num_units) return;
+    const int64_t n_w = gw < a.num_units ? (a.num_units - 1 - gw) / GW + 1 : 0;
 
     const uint64_t pol_load = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
     const uint64_t pol_store = (a.l2_hints & 2) ? policy_evict_first() : policy_evict_normal();
@@ -249,17 +419,45 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
     if (lane == 0)
         for (int64_t i = 0; i < min((int64_t)S, n_w); ++i) issue_load(i);
 
+    // fused launch: the layout, computed while the first loads are in flight
+    const uint32_t *fl_bitmap = nullptr;
+    const uint16_t *fl_wprefix = nullptr;
+    const int32_t *fl_rprefix = nullptr;
+    const int16_t *fl_eid = nullptr, *fl_rid = nullptr;
+    if constexpr (kFused) {
+        fused_layout(a, smem + a.fl_off);
+        const FusedSmem fs = fused_smem(a.T, a.R, a.E, a.k);
+        fl_bitmap = reinterpret_cast<const uint32_t *>(smem + a.fl_off);
+        fl_wprefix = reinterpret_cast<const uint16_t *>(smem + a.fl_off + fs.wprefix);
+        fl_rprefix = reinterpret_cast<const int32_t *>(smem + a.fl_off + fs.rprefix);
+        fl_eid = reinterpret_cast<const int16_t *>(smem + a.fl_off + fs.eid);
+        fl_rid = reinterpret_cast<const int16_t *>(smem + a.fl_off + fs.rid);
+        if (n_w == 0) return;
+    }
+
     // receive rows (and, for the first chunk, the routing) of the next unit, prefetched one unit ahead
     auto fetch = [&](int64_t i, int &row, int64_t &e, float &w) {
         const int64_t u = gw + i * GW;
         const int64_t t = u / a.num_chunks;
         const bool first = (u - t * a.num_chunks) == 0;
         row = -1; e = -1; w = 0.0f;
-        if (lane < a.k) {
-            row = a.dst_row[t * a.k + lane];
-            if (first) {
-                e = a.topk[t * a.k + lane];
-                if (a.topk_w) w = a.topk_w[t * a.k + lane];
+        if constexpr (kFused) {
+            int r = -1;
+            if (lane < a.k) {
+                e = fl_eid[t * a.k + lane];
+                r = fl_rid[t * a.k + lane];
+                if (first && a.topk_w) w = a.topk_w[t * a.k + lane];
+            }
+            const unsigned peers = __match_any_sync(kFull, r >= 0 ? r : -(lane + 1));
+            row = fused_row(a, fl_bitmap, fl_wprefix, fl_rprefix, (int)t, r, lane, peers);
+            if (!first) e = -1;
+        } else {
+            if (lane < a.k) {
+                row = a.dst_row[t * a.k + lane];
+                if (first) {
+                    e = a.topk[t * a.k + lane];
+                    if (a.topk_w) w = a.topk_w[t * a.k + lane];
+                }
             }
         }
     };
@@ -549,16 +747,14 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
 
 inline int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
-}  // namespace
+constexpr int kFusedMaxTokens = 1024;   // largest batch whose layout every CTA of a fused launch computes
 
-int launch_dispatch(const DispatchLaunch &L) {
-    if (L.num_tokens == 0) return MOE_OK;
+// Fields shared by every dispatch launch.
+DispatchArgs base_args(const DispatchLaunch &L) {
     const Tuning &tu = tuning();
     const bool fp8 = L.mode == MOE_DISPATCH_QUANTIZE_FP8;      // quantise in the kernel
     const bool fp8_in = L.mode == MOE_DISPATCH_FP8;             // relay E4M3 bytes and their scales
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(L.stream);
-
-    DispatchArgs a;
+    DispatchArgs a = {};
     a.x = static_cast<const uint8_t *>(L.x);
     a.row_bytes = fp8_in ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
     a.k = L.num_topk;
@@ -581,6 +777,67 @@ int launch_dispatch(const DispatchLaunch &L) {
     a.status = L.status;
     a.l2_hints = tu.l2_hints;
     a.timeout_ns = kDefaultWaitNs;
+    a.T = L.num_tokens;
+    a.R = L.num_ranks;
+    return a;
+}
+
+// Chunking, per-warp shared memory, warps per CTA and grid of the chunked
+// relay kernel; `extra` bytes of shared memory follow the warps' regions.
+int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int &warps, size_t &smem, int &grid) {
+    const Tuning &tu = tuning();
+    const int64_t align = fp8 ? 256 : 16;
+    const int64_t max_chunk = std::max<int64_t>(align, std::min<int64_t>(65536, tu.dispatch_chunk) / align * align);
+    int64_t chunk_cap = max_chunk;
+    // a small batch: smaller chunks (down to 2 KB) until there are 4 units per SM
+    while (tu.spread_small && chunk_cap > 2048 &&
+           (int64_t)num_tokens * ((a.row_bytes + chunk_cap - 1) / chunk_cap) < 4LL * device_sm_count())
+        chunk_cap = std::max<int64_t>(2048, chunk_cap / 2 / align * align);
+    const int64_t nch = (a.row_bytes + chunk_cap - 1) / chunk_cap;
+    a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
+    a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
+    a.num_units = (int64_t)num_tokens * a.num_chunks;
+    a.stages = std::min(kMaxStages, std::max(2, tu.dispatch_stages));
+
+    int64_t per_warp = kBarBytes + (int64_t)a.stages * a.chunk_bytes;
+    if (fp8) per_warp += (int64_t)a.stages * (a.chunk_bytes / 2) + round_up((int64_t)a.stages * (a.chunk_bytes / 256) * 4, 128);
+    per_warp = round_up(per_warp, 128);
+    a.warp_smem = (int)per_warp;
+    // as many of the requested warps as fit in one CTA's shared memory
+    const int64_t room = (int64_t)device_smem_optin() - (int64_t)round_up((int64_t)extra, 128);
+    const int fit = (int)std::min<int64_t>(16, room / per_warp);
+    if (fit < 1) return MOE_ERR_INVALID_ARG;
+    warps = std::max(1, std::min(fit, tu.dispatch_warps));
+    // a small batch: fewer warps per CTA, so that its units spread over every SM
+    if (tu.spread_small) {
+        const int64_t per_sm = (a.num_units + device_sm_count() - 1) / device_sm_count();
+        warps = (int)std::max<int64_t>(1, std::min<int64_t>(warps, per_sm));
+    }
+    smem = (size_t)per_warp * warps + (extra ? (size_t)round_up((int64_t)extra, 128) : 0);
+    a.fl_off = (size_t)per_warp * warps;
+    int ctas_per_sm = (int)std::max<size_t>(1, device_smem_per_sm() / (smem + 1024));
+    if (tu.ctas_per_sm > 0) ctas_per_sm = std::min(ctas_per_sm, tu.ctas_per_sm);
+    const int64_t want = (a.num_units + warps - 1) / warps;
+    grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)device_sm_count() * ctas_per_sm));
+    return MOE_OK;
+}
+
+template <bool kFP8, bool kFused>
+int launch_chunked(const DispatchArgs &a, int warps, size_t smem, int grid, cudaStream_t st) {
+    const void *fn = (const void *)dispatch_kernel<kFP8, kFused>;
+    if (ensure_dynamic_smem(fn, smem) != MOE_OK) return MOE_ERR_CUDA;
+    dispatch_kernel<kFP8, kFused><<<grid, warps * 32, smem, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_dispatch(const DispatchLaunch &L) {
+    if (L.num_tokens == 0) return MOE_OK;
+    const Tuning &tu = tuning();
+    const bool fp8 = L.mode == MOE_DISPATCH_QUANTIZE_FP8;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(L.stream);
+    DispatchArgs a = base_args(L);
 
     if (fp8 && tu.fp8_rows) {
         Fp8Args f;
@@ -622,35 +879,35 @@ int launch_dispatch(const DispatchLaunch &L) {
         // rows too large for the ring: fall through to the chunked kernel
     }
 
-    // chunking: equal chunks no larger than the tuned maximum
-    const int64_t align = fp8 ? 256 : 16;
-    const int64_t max_chunk = std::max<int64_t>(align, std::min<int64_t>(65536, tu.dispatch_chunk) / align * align);
-    const int64_t nch = (a.row_bytes + max_chunk - 1) / max_chunk;
-    a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
-    a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
-    a.num_units = (int64_t)L.num_tokens * a.num_chunks;
-    a.stages = std::min(kMaxStages, std::max(2, tu.dispatch_stages));
+    int warps = 0, grid = 0;
+    size_t smem = 0;
+    const int rc = chunked_config(a, fp8, L.num_tokens, 0, warps, smem, grid);
+    if (rc != MOE_OK) return rc;
+    return fp8 ? launch_chunked<true, false>(a, warps, smem, grid, st)
+               : launch_chunked<false, false>(a, warps, smem, grid, st);
+}
 
-    int64_t per_warp = kBarBytes + (int64_t)a.stages * a.chunk_bytes;
-    if (fp8) per_warp += (int64_t)a.stages * (a.chunk_bytes / 2) + round_up((int64_t)a.stages * (a.chunk_bytes / 256) * 4, 128);
-    per_warp = round_up(per_warp, 128);
-    a.warp_smem = (int)per_warp;
-    // as many of the requested warps as fit in one CTA's shared memory
-    const int fit = (int)std::min<int64_t>(16, (int64_t)device_smem_optin() / per_warp);
-    if (fit < 1) return MOE_ERR_INVALID_ARG;
-    const int warps = std::max(1, std::min(fit, tu.dispatch_warps));
-    const size_t smem = (size_t)per_warp * warps;
-
-    const void *fn = fp8 ? (const void *)dispatch_kernel<true> : (const void *)dispatch_kernel<false>;
-    if (ensure_dynamic_smem(fn, smem) != MOE_OK) return MOE_ERR_CUDA;
-    int ctas_per_sm = (int)std::max<size_t>(1, device_smem_per_sm() / (smem + 1024));
-    if (tu.ctas_per_sm > 0) ctas_per_sm = std::min(ctas_per_sm, tu.ctas_per_sm);
-    const int64_t want = (a.num_units + warps - 1) / warps;
-    const int grid = (int)std::min<int64_t>(want, (int64_t)device_sm_count() * ctas_per_sm);
-
-    if (fp8) dispatch_kernel<true><<<grid, warps * 32, smem, st>>>(a);
-    else dispatch_kernel<false><<<grid, warps * 32, smem, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+int launch_layout_dispatch(const LayoutLaunch &Ll, const DispatchLaunch &L) {
+    const int T = L.num_tokens;
+    const bool fp8 = L.mode == MOE_DISPATCH_QUANTIZE_FP8;
+    const Tuning &tu = tuning();
+    bool fused = tu.fused_small && T > 0 && T <= kFusedMaxTokens && !L.expand;
+    DispatchArgs a = base_args(L);
+    int warps = 0, grid = 0;
+    size_t smem = 0;
+    if (fused) {
+        a.fl_words = (T + 31) / 32;
+        a.fl_out = Ll.out;
+        const size_t extra = fused_smem(T, L.num_ranks, L.num_experts, L.num_topk).total;
+        fused = chunked_config(a, fp8, T, extra, warps, smem, grid) == MOE_OK;
+    }
+    if (!fused) {   // two launches: layout, then dispatch
+        const int rc = launch_layout(Ll);
+        return rc != MOE_OK ? rc : launch_dispatch(L);
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(L.stream);
+    return fp8 ? launch_chunked<true, true>(a, warps, smem, grid, st)
+               : launch_chunked<false, true>(a, warps, smem, grid, st);
 }
 
 }  // namespace moe

@@ -112,6 +112,8 @@ const Tuning &tuning() {
         x.fp8_quant_warps = env_int("MOE_TUNE_FP8_QUANT_WARPS", 24);
         x.ctas_per_sm = env_int("MOE_TUNE_CTAS_PER_SM", 0);
         x.l2_hints = env_int("MOE_TUNE_L2_HINTS", 1) & 3;
+        x.spread_small = env_int("MOE_TUNE_SPREAD_SMALL", 1) == 1;
+        x.fused_small = env_int("MOE_TUNE_FUSED_SMALL", 1) == 1;
         return x;
     }();
     return t;
@@ -159,9 +161,9 @@ MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, in
     return moe::layout_workspace_bytes(num_tokens, num_experts, num_ranks);
 }
 
-static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
-                         size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
-                         int unpublished_tile) {
+static int layout_prepare(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
+                          size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
+                          int unpublished_tile, moe::LayoutLaunch &L) {
     if (!shape_ok(T, k, E, R)) return MOE_ERR_INVALID_ARG;
     if ((int64_t)T * R >= (int64_t)1 << 40) return MOE_ERR_INVALID_ARG;
     if (!status || !o.num_tokens_per_rank || !o.num_tokens_per_expert || !o.rank_prefix || !o.expert_prefix)
@@ -176,7 +178,6 @@ static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, mo
             return MOE_ERR_MISALIGNED;
         if (workspace_bytes < moe::layout_workspace_bytes(T, E, R)) return MOE_ERR_WORKSPACE;
     }
-    moe::LayoutLaunch L;
     L.topk_idx = topk_idx;
     L.num_tokens = T;
     L.num_topk = k;
@@ -188,7 +189,16 @@ static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, mo
     L.stream = stream;
     L.timeout_ns = timeout_ns;
     L.unpublished_tile = unpublished_tile;
-    return moe::launch_layout(L);
+    return MOE_OK;
+}
+
+static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
+                         size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
+                         int unpublished_tile) {
+    moe::LayoutLaunch L;
+    const int rc = layout_prepare(topk_idx, T, k, E, R, o, workspace, workspace_bytes, status, stream, timeout_ns,
+                                  unpublished_tile, L);
+    return rc != MOE_OK ? rc : moe::launch_layout(L);
 }
 
 MOE_API int moe_get_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts, int num_ranks,
@@ -246,11 +256,14 @@ MOE_API int moe_get_expand_layout(const int64_t *topk_idx, int num_tokens, int n
     return moe::launch_expand_layout(L);
 }
 
-MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
-                         const float *topk_weights, int num_topk, int num_experts, int num_ranks,
-                         const int32_t *token_dst_row, int recv_capacity, int mode, void *recv_x,
-                         float *recv_x_scales, int64_t *recv_topk_idx, float *recv_topk_weights,
-                         int32_t *recv_src_idx, float *x_scales, int32_t *status, void *stream) {
+// Validation of a dispatch; `need_rows` is false when the receive rows come from
+// the same call (moe_layout_dispatch).
+static int dispatch_prepare(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                            const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                            const int32_t *token_dst_row, int recv_capacity, int mode, void *recv_x,
+                            float *recv_x_scales, int64_t *recv_topk_idx, float *recv_topk_weights,
+                            int32_t *recv_src_idx, float *x_scales, int32_t *status, void *stream,
+                            moe::DispatchLaunch &L) {
     const int T = num_tokens, H = hidden;
     if (!shape_ok(T, num_topk, num_experts, num_ranks)) return MOE_ERR_INVALID_ARG;
     const bool expand = (mode & MOE_DISPATCH_EXPAND) != 0;
@@ -272,7 +285,6 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
             (x_scales && !aligned(x_scales, 4)))
             return MOE_ERR_MISALIGNED;
     }
-    moe::DispatchLaunch L;
     L.x = x;
     L.num_tokens = T;
     L.hidden = H;
@@ -293,7 +305,37 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
     L.x_scales = fp8_out ? x_scales : nullptr;
     L.status = status;
     L.stream = stream;
-    return moe::launch_dispatch(L);
+    return MOE_OK;
+}
+
+MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                         const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                         const int32_t *token_dst_row, int recv_capacity, int mode, void *recv_x,
+                         float *recv_x_scales, int64_t *recv_topk_idx, float *recv_topk_weights,
+                         int32_t *recv_src_idx, float *x_scales, int32_t *status, void *stream) {
+    moe::DispatchLaunch L;
+    const int rc = dispatch_prepare(x, num_tokens, hidden, topk_idx, topk_weights, num_topk, num_experts, num_ranks,
+                                    token_dst_row, recv_capacity, mode, recv_x, recv_x_scales, recv_topk_idx,
+                                    recv_topk_weights, recv_src_idx, x_scales, status, stream, L);
+    return rc != MOE_OK ? rc : moe::launch_dispatch(L);
+}
+
+MOE_API int moe_layout_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                                const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                                moe_layout_t layout, void *workspace, size_t workspace_bytes, int recv_capacity,
+                                int mode, void *recv_x, float *recv_x_scales, int64_t *recv_topk_idx,
+                                float *recv_topk_weights, int32_t *recv_src_idx, float *x_scales, int32_t *status,
+                                void *stream) {
+    if (mode & MOE_DISPATCH_EXPAND) return MOE_ERR_INVALID_ARG;
+    moe::LayoutLaunch Ll;
+    int rc = layout_prepare(topk_idx, num_tokens, num_topk, num_experts, num_ranks, layout, workspace,
+                            workspace_bytes, status, stream, 0, -1, Ll);
+    if (rc != MOE_OK) return rc;
+    moe::DispatchLaunch L;
+    rc = dispatch_prepare(x, num_tokens, hidden, topk_idx, topk_weights, num_topk, num_experts, num_ranks,
+                          layout.token_dst_row, recv_capacity, mode, recv_x, recv_x_scales, recv_topk_idx,
+                          recv_topk_weights, recv_src_idx, x_scales, status, stream, L);
+    return rc != MOE_OK ? rc : moe::launch_layout_dispatch(Ll, L);
 }
 
 static int combine_common(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,

@@ -26,6 +26,8 @@ struct Tuning {
     int fp8_rows, fp8_in_slots, fp8_quant_warps;   // FP8 row pipeline: on/off, input ring slots, worker warps
     int ctas_per_sm;
     int l2_hints;  // bit 0: evict-first on single-use loads; bit 1: evict-first on stores
+    int spread_small;   // small batches: fewer dispatch warps per CTA, more CTAs
+    int fused_small;    // moe_layout_dispatch: one fused launch for small batches
 };
 const Tuning &tuning();
 
@@ -79,6 +81,8 @@ struct DispatchLaunch {
 };
 
 int launch_dispatch(const DispatchLaunch &L);
+// Layout and dispatch: one fused launch for small batches, else the two launches.
+int launch_layout_dispatch(const LayoutLaunch &Ll, const DispatchLaunch &L);
 
 struct CombineLaunch {
     const void *partial;

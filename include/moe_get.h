@@ -241,6 +241,34 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
                          int32_t *status, void *stream);
 
 /*
+ * moe_layout_dispatch -- moe_get_layout followed by moe_dispatch, in one
+ * launch for small batches (decode).
+ *
+ * Page: the dispatch kernel runs its notify warps (counts, prefix sums) and
+ * its dispatch warps in one launch (section 3.5, data-flow figure). Here, for
+ * T <= 1024 (and the layout's shared memory fitting
+ * beside the copy pipeline), every CTA of the dispatch grid computes the whole
+ * layout itself in shared memory -- no CTA waits on another -- while its first
+ * row loads are in flight, then stores the rows; the layout outputs are written
+ * to `layout` as moe_get_layout writes them. Larger batches (or when the tuning
+ * switch MOE_TUNE_FUSED_SMALL=2 is set) take the two launches. Outputs, order,
+ * metadata and errors are exactly those of moe_get_layout + moe_dispatch with
+ * the same arguments.
+ *
+ *   layout, workspace, workspace_bytes   as for moe_get_layout (the workspace is
+ *                      only used by the two-launch path but is always required).
+ *   token_dst_row      not an argument: layout.token_dst_row receives the rows.
+ *   other arguments    as for moe_dispatch; `mode` may not include
+ *                      MOE_DISPATCH_EXPAND (MOE_ERR_INVALID_ARG).
+ */
+MOE_API int moe_layout_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                                const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                                moe_layout_t layout, void *workspace, size_t workspace_bytes, int recv_capacity,
+                                int mode, void *recv_x, float *recv_x_scales, int64_t *recv_topk_idx,
+                                float *recv_topk_weights, int32_t *recv_src_idx, float *x_scales, int32_t *status,
+                                void *stream);
+
+/*
  * moe_combine -- gather the per-rank partial rows of each token back into
  * token order and reduce them.
  *

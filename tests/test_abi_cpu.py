@@ -147,3 +147,18 @@ def _expand(lib, T=128, k=2, E=16, topk=A, prefix=A + 0x10000, rows=A + 0x20000,
 ])
 def test_expand_layout_rejects_bad_arguments(lib, kw, code):
     assert _expand(lib, **kw) == code
+
+
+def _layout_dispatch(lib, x=A, T=128, H=256, topk=A + 0x10000, k=2, E=16, R=4, ws=A + 0x300000, ws_bytes=1 << 30,
+                     cap=256, mode=0, recv=A + 0x100000, status=A + 0x200000):
+    return lib.LIB.moe_layout_dispatch(x, T, H, topk, None, k, E, R, _layout_struct(lib, A + 0x400000), ws, ws_bytes,
+                                       cap, mode, recv, None, None, None, None, None, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mode=0x100), 1), (dict(mode=3), 1), (dict(H=12), 1), (dict(k=33), 1), (dict(E=15), 1),
+    (dict(ws=None), 1), (dict(ws_bytes=16), 7), (dict(x=A + 8), 2), (dict(topk=MIS), 2), (dict(status=None), 1),
+    (dict(recv=None), 1), (dict(cap=-1), 1),
+])
+def test_layout_dispatch_rejects_bad_arguments(lib, kw, code):
+    assert _layout_dispatch(lib, **kw) == code

@@ -1,0 +1,183 @@
+"""Parity of moe_layout_dispatch (layout + dispatch; one fused launch for
+batches of at most 1024 tokens, two launches beyond) through the C ABI with
+the CPU oracle: every layout output and every receive output bit for bit, in
+all three dispatch modes, on both sides of the 1024-token limit, with masked,
+duplicate and invalid routing, ranks that are not a multiple of 4 (byte-wise
+membership writes), the largest rank count, capacity overflow and an empty
+batch."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_moe_get_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+POISON_BF16 = 0x7FBF
+LAYOUT_KEYS = ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "rank_prefix",
+               "expert_prefix", "token_dst_row")
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from combine_moe_get_gb300 import binding
+    return binding
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def run_fused(moe, x, topk, w, E, R, mode, scales=None, cap=None):
+    T, H = x.shape
+    k = topk.shape[1]
+    cap = wl.recv_capacity(T, k, R) if cap is None else cap
+    fp8_out = mode != "bf16"
+    rows = cap + 8
+    lay = moe.Layout.empty(T, k, E, R, DEV)
+    for t in (lay.token_dst_row, lay.is_token_in_rank, lay.num_tokens_per_rank, lay.num_tokens_per_expert,
+              lay.rank_prefix, lay.expert_prefix):
+        t.fill_(0x55)          # poison: the call must write every layout output
+    out = moe.Dispatched(
+        recv_x=(torch.full((rows, H), 0xEE, dtype=torch.uint8, device=DEV) if fp8_out else
+                torch.full((rows, H), POISON_BF16, dtype=torch.int16, device=DEV).view(torch.bfloat16)),
+        recv_x_scales=torch.full((rows, H // 128), -1.0, device=DEV) if fp8_out else None,
+        recv_topk_idx=torch.full((rows, k), -7, dtype=torch.int64, device=DEV),
+        recv_topk_weights=torch.full((rows, k), -7.0, device=DEV),
+        recv_src_idx=torch.full((rows,), -7, dtype=torch.int32, device=DEV),
+        x_scales=(torch.full((T, H // 128), -1.0, device=DEV) if mode == "quantize_fp8" else
+                  (scales.to(DEV) if mode == "fp8" else None)))
+    status = moe.new_status(DEV)
+    moe.moe_layout_dispatch(x.to(DEV), topk.to(DEV), None if w is None else w.to(DEV), E, R, cap,
+                            quantize_fp8=mode == "quantize_fp8", x_scales=out.x_scales, layout=lay, out=out,
+                            status=status)
+    torch.cuda.synchronize()
+    return lay, out, int(status.item())
+
+
+def check_fused(moe, topk, E, R, H, mode, seed, weights=True, cap=None):
+    T, k = topk.shape
+    g = torch.Generator().manual_seed(seed)
+    w = wl.make_weights(g, T, k) if weights else None
+    if mode == "fp8":
+        rng = np.random.default_rng(seed)
+        x_np = rng.integers(0, 256, (T, H), dtype=np.uint8)
+        scales = torch.from_numpy(rng.standard_normal((T, H // 128)).astype(np.float32))
+        x = torch.from_numpy(x_np)
+    else:
+        scales = None
+        x = wl.make_x(g, T, H)
+    lay, out, st = run_fused(moe, x, topk, w, E, R, mode, scales, cap)
+    ref_lay = oracle.layout(topk.numpy(), E, R)
+    for key in LAYOUT_KEYS:
+        np.testing.assert_array_equal(getattr(lay, key).cpu().numpy(), ref_lay[key], err_msg=key)
+    N = ref_lay["num_recv"]
+    cap = out.recv_x.shape[0] - 8 if cap is None else cap
+    wn = None if w is None else w.numpy()
+    if mode == "fp8":
+        ref = oracle.dispatch_fp8_input(x.numpy(), scales.numpy(), topk.numpy(), wn, E, R, ref_lay["token_dst_row"],
+                                        cap)
+    else:
+        ref = oracle.dispatch(bits16(x), topk.numpy(), wn, E, R, ref_lay["token_dst_row"], cap,
+                              fp8=mode == "quantize_fp8")
+    expect_status = 0
+    if ref_lay["flags"] & oracle.ORACLE_BAD_TOPK:
+        expect_status = moe.MOE_ERR_BAD_TOPK
+    elif ref["flags"] & oracle.ORACLE_CAPACITY:
+        expect_status = moe.MOE_ERR_CAPACITY
+    assert st == expect_status
+    n = min(N, cap)
+    if mode == "bf16":
+        np.testing.assert_array_equal(bits16(out.recv_x[:n]), ref["recv_x"][:n])
+        assert np.all(bits16(out.recv_x[n:]) == POISON_BF16)
+    else:
+        np.testing.assert_array_equal(out.recv_x[:n].cpu().numpy(), ref["recv_x"][:n])
+        np.testing.assert_array_equal(out.recv_x_scales[:n].cpu().numpy().view(np.uint32),
+                                      ref["recv_x_scales"][:n].view(np.uint32))
+        assert np.all(out.recv_x[n:].cpu().numpy() == 0xEE)
+        if mode == "quantize_fp8":
+            np.testing.assert_array_equal(out.x_scales.cpu().numpy().view(np.uint32),
+                                          ref["x_scales"].view(np.uint32))
+    np.testing.assert_array_equal(out.recv_src_idx[:n].cpu().numpy(), ref["recv_src_idx"][:n])
+    np.testing.assert_array_equal(out.recv_topk_idx[:n].cpu().numpy(), ref["recv_topk_idx"][:n])
+    np.testing.assert_array_equal(out.recv_topk_weights[:n].cpu().numpy().view(np.uint32),
+                                  ref["recv_topk_weights"][:n].view(np.uint32))
+    assert np.all(out.recv_src_idx[n:].cpu().numpy() == -7)
+
+
+MODES = ("bf16", "quantize_fp8", "fp8")
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("name", ["decode", "tiny"])
+def test_layout_dispatch_parity_configs(moe, name, mode):
+    w = wl.CONFIGS[name]
+    topk = wl.make_inputs(w, with_partial=False).topk_idx
+    check_fused(moe, topk, w.num_experts, w.num_ranks, w.hidden, mode, 3)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("T,H,k,E,R", [
+    (1, 128, 2, 16, 4), (31, 7168, 8, 256, 256), (33, 384, 8, 256, 8), (255, 1024, 6, 48, 3),
+    (1024, 7168, 8, 256, 8),        # the largest fused batch
+    (1025, 1024, 8, 256, 8),        # two launches
+    (200, 256, 32, 8192, 1024),     # largest rank and expert counts
+    (130, 640, 3, 7, 7),            # R not a multiple of 4
+])
+def test_layout_dispatch_parity_shapes(moe, T, H, k, E, R, mode):
+    g = torch.Generator().manual_seed(T * 3 + H + R)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.25)
+    check_fused(moe, topk, E, R, H, mode, T + k, weights=(T % 2 == 1))
+
+
+@pytest.mark.parametrize("mode", ["bf16", "quantize_fp8"])
+def test_layout_dispatch_duplicates_and_bad_entries(moe, mode):
+    g = torch.Generator().manual_seed(8)
+    T, k, E, R = 300, 8, 64, 8
+    topk = torch.randint(0, E, (T, k), generator=g)
+    topk[::6] = -1
+    topk[7, 1] = E + 3
+    check_fused(moe, topk, E, R, 512, mode, 9)
+
+
+def test_layout_dispatch_capacity_overflow(moe):
+    w = wl.CONFIGS["decode"]
+    topk = wl.make_inputs(w, with_partial=False).topk_idx
+    N = oracle.layout(topk.numpy(), w.num_experts, w.num_ranks)["num_recv"]
+    check_fused(moe, topk, w.num_experts, w.num_ranks, 1024, "bf16", 4, cap=N - 11)
+
+
+def test_layout_dispatch_empty(moe):
+    x = torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV)
+    topk = torch.zeros(0, 8, dtype=torch.int64, device=DEV)
+    status = moe.new_status(DEV)
+    lay, _ = moe.moe_layout_dispatch(x, topk, None, 256, 8, 0, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for key in ("num_tokens_per_rank", "num_tokens_per_expert", "rank_prefix", "expert_prefix"):
+        assert int(getattr(lay, key).abs().sum().item()) == 0, key
+
+
+def test_layout_dispatch_equals_two_calls_twice(moe):
+    # the fused call and the two separate calls give the same bytes, call after call
+    w = wl.CONFIGS["decode"]
+    inp = wl.make_inputs(w, with_partial=False)
+    x, topk, wt = inp.x.to(DEV), inp.topk_idx.to(DEV), inp.topk_weights.to(DEV)
+    cap = wl.recv_capacity(w.num_tokens, w.num_topk, w.num_ranks)
+    status = moe.new_status(DEV)
+    lay2 = moe.moe_get_layout(topk, w.num_experts, w.num_ranks, status=status)
+    ref = moe.moe_dispatch(x, topk, wt, w.num_experts, w.num_ranks, lay2.token_dst_row, cap, status=status)
+    for _ in range(2):
+        lay1, d1 = moe.moe_layout_dispatch(x, topk, wt, w.num_experts, w.num_ranks, cap, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for key in LAYOUT_KEYS:
+            assert torch.equal(getattr(lay1, key), getattr(lay2, key)), key
+        N = int(lay1.rank_prefix[-1].item())
+        assert torch.equal(d1.recv_x[:N].view(torch.int16), ref.recv_x[:N].view(torch.int16))
+        assert torch.equal(d1.recv_topk_idx[:N], ref.recv_topk_idx[:N])
+        assert torch.equal(d1.recv_src_idx[:N], ref.recv_src_idx[:N])
