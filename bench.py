@@ -243,6 +243,10 @@ class Step:
     def combine(self):
         self.moe.moe_combine(self.partial, self.lay.token_dst_row, out=self.out, status=self.status)
 
+    def layout_dispatch(self):
+        self.moe.moe_layout_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks, self.cap,
+                                     layout=self.lay, workspace=self.ws, out=self.disp, status=self.status)
+
     def expand_layout(self):
         self.moe.moe_get_expand_layout(self.topk, self.lay.expert_prefix, self.w.num_experts, out=self.xrows,
                                        workspace=self.xws, status=self.status)
@@ -396,6 +400,17 @@ def run_ours(args, world, rank, local):
     xcom_ms = time_alone(st.combine_expand, reps)
     xstep_ms = time_alone(st.expand_step, reps)                               # the whole expand-mode step
     moe.check_status(st.status, "dispatch / combine variants")
+    # the decode shape (T=128 over R=256): layout + dispatch as two launches and as one
+    wd = wl.CONFIGS["decode"]
+    sd = Step(moe, wd, wl.make_inputs(dataclass_replace_seed(wd, wd.seed + rank)), device)
+    dec = {
+        "decode_layout_dispatch_two_us": mean(time_alone(lambda: (sd.layout(), sd.dispatch()), reps)) * 1e3,
+        "decode_layout_dispatch_fused_us": mean(time_alone(sd.layout_dispatch, reps)) * 1e3,
+        "decode_step_two_us": mean(time_alone(lambda: (sd.layout(), sd.dispatch(), sd.combine()), reps)) * 1e3,
+        "decode_step_fused_us": mean(time_alone(lambda: (sd.layout_dispatch(), sd.combine()), reps)) * 1e3,
+    }
+    moe.check_status(sd.status, "decode shape")
+    del sd
     NX = int(st.lay.expert_prefix[-1].item())                                 # expand rows: valid entries
 
     peak, peak_kind = hbm_peak()
@@ -418,6 +433,7 @@ def run_ours(args, world, rank, local):
         "expand_step_us": mean(xstep_ms) * 1e3,
         "expand_step_tokens_per_s": T / (mean(xstep_ms) * 1e-3),
         "expand_rows": NX,
+        **dec,
     }
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     kern["dispatch_gbs"] = gbs(bytes_bf16, mean(dis_ms))
