@@ -246,27 +246,6 @@ __host__ __device__ inline FusedSmem fused_smem(int T, int R, int E, int k) {
     return f;
 }
 
-// In-place exclusive scan of n int32 in shared memory by one warp; v[n] = total.
-__device__ void warp_exclusive_scan(int32_t *v, int n, int lane) {
-    const int per = (n + 31) / 32;
-    const int lo = min(n, lane * per), hi = min(n, lo + per);
-    int32_t local = 0;
-    for (int i = lo; i < hi; ++i) local += v[i];
-    int32_t incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    int32_t run = incl - local;
-    for (int i = lo; i < hi; ++i) {
-        const int32_t x = v[i];
-        v[i] = run;
-        run += x;
-    }
-    if (lane == 31) v[n] = incl;
-}
-
 // The (token, rank) owner of entry j of token t, and its receive row (-1 if not an owner).
 __device__ __forceinline__ int fused_row(const DispatchArgs &a, const uint32_t *bitmap, const uint16_t *wprefix,
                                          const int32_t *rprefix, int t, int r, int lane, unsigned peers) {
@@ -393,10 +372,15 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
     uint8_t *out_stage = in_stage + (size_t)S * chunk;                                  // FP8 codes
     float *sc_stage = reinterpret_cast<float *>(out_stage + (size_t)S * (chunk / 2));  // FP8 scales
 
-    const int64_t gw = (int64_t)blockIdx.x * warps + warp;
-    const int64_t GW = (int64_t)gridDim.x * warps;
-    if (!kFused && gw >= a.num_units) return;
-    const int64_t n_w = gw < a.num_units ? (a.num_units - 1 - gw) / GW + 1 : 0;
+    // The CTA owns units blockIdx.x + j * gridDim.x; its warps claim them in
+    // order (j) from a shared counter as they refill their stages, so that a
+    // warp whose units had fewer destinations takes more of them.
+    __shared__ int s_next_unit;
+    if (threadIdx.x == 0) s_next_unit = 0;
+    __syncthreads();
+    const int64_t G = gridDim.x;
+    const int64_t cta_units = a.num_units > (int64_t)blockIdx.x ? (a.num_units - 1 - blockIdx.x) / G + 1 : 0;
+    int64_t *ring = reinterpret_cast<int64_t *>(wbase + 64);   // unit of each stage (after the <= 8 barriers)
 
     const uint64_t pol_load = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
     const uint64_t pol_store = (a.l2_hints & 2) ? policy_evict_first() : policy_evict_normal();
@@ -405,19 +389,26 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
     }
-    __syncwarp();
 
-    auto issue_load = [&](int64_t i) {   // lane 0
-        const int64_t u = gw + i * GW;
+    auto claim = [&]() -> int64_t {   // lane 0; -1 once the CTA's units are exhausted
+        const int64_t j = atomicAdd(&s_next_unit, 1);
+        return j < cta_units ? (int64_t)blockIdx.x + j * G : -1;
+    };
+    auto issue_load = [&](int64_t u, int s) {   // lane 0
         const int64_t t = u / a.num_chunks;
         const int64_t off = (u - t * a.num_chunks) * (int64_t)chunk;
         const uint32_t nbytes = (uint32_t)min((int64_t)chunk, a.row_bytes - off);
-        const int s = (int)(i % S);
         mbar_arrive_expect_tx(&bars[s], nbytes);
         bulk_load(in_stage + (size_t)s * chunk, a.x + t * a.row_bytes + off, nbytes, &bars[s], pol_load);
     };
-    if (lane == 0)
-        for (int64_t i = 0; i < min((int64_t)S, n_w); ++i) issue_load(i);
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) {
+            const int64_t u = claim();
+            ring[s] = u;
+            if (u >= 0) issue_load(u, s);
+        }
+    }
+    __syncwarp();
 
     // fused launch: the layout, computed while the first loads are in flight
     const uint32_t *fl_bitmap = nullptr;
@@ -432,12 +423,10 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
         fl_rprefix = reinterpret_cast<const int32_t *>(smem + a.fl_off + fs.rprefix);
         fl_eid = reinterpret_cast<const int16_t *>(smem + a.fl_off + fs.eid);
         fl_rid = reinterpret_cast<const int16_t *>(smem + a.fl_off + fs.rid);
-        if (n_w == 0) return;
     }
 
     // receive rows (and, for the first chunk, the routing) of the next unit, prefetched one unit ahead
-    auto fetch = [&](int64_t i, int &row, int64_t &e, float &w) {
-        const int64_t u = gw + i * GW;
+    auto fetch = [&](int64_t u, int &row, int64_t &e, float &w) {
         const int64_t t = u / a.num_chunks;
         const bool first = (u - t * a.num_chunks) == 0;
         row = -1; e = -1; w = 0.0f;
@@ -461,13 +450,14 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
             }
         }
     };
-    int row_n; int64_t e_n; float w_n;
-    fetch(0, row_n, e_n, w_n);
+    int row_n = -1; int64_t e_n = -1; float w_n = 0.0f;
+    if (ring[0] >= 0) fetch(ring[0], row_n, e_n, w_n);
 
-    for (int64_t i = 0; i < n_w; ++i) {
+    for (int64_t i = 0;; ++i) {
         const int s = (int)(i % S);
         const uint32_t parity = (uint32_t)((i / S) & 1);
-        const int64_t u = gw + i * GW;
+        const int64_t u = ring[s];
+        if (u < 0) break;
         const int64_t t = u / a.num_chunks;
         const int c = (int)(u - t * a.num_chunks);
         const int64_t off = (int64_t)c * chunk;
@@ -476,7 +466,8 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
         int row = row_n;
         const int64_t e = e_n;
         const float wgt = w_n;
-        if (i + 1 < n_w) fetch(i + 1, row_n, e_n, w_n);
+        const int64_t u_next = ring[(i + 1) % S];   // claimed at least one iteration ago (S >= 3)
+        if (u_next >= 0) fetch(u_next, row_n, e_n, w_n);
         if (row >= a.capacity) {
             if (c == 0) report(a.status, MOE_ERR_CAPACITY);
             row = -1;
@@ -554,10 +545,16 @@ __global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
                 for (int b = lane; b < nblk; b += 32) a.x_scales[t * a.nb + c * cpb + b] = sc[b];
         }
         if (lane == 0) {
-            // the stage stored one unit ago is free once its bulk stores have read it
-            if (i >= 1 && i - 1 + S < n_w) {
-                bulk_wait_read<1>();
-                issue_load(i - 1 + S);
+            // the stage stored one unit ago is free once its bulk stores have read it;
+            // it takes the next unit claimed by this warp
+            if (i >= 1) {
+                const int sp = (int)((i - 1) % S);
+                const int64_t un = claim();
+                ring[sp] = un;
+                if (un >= 0) {
+                    bulk_wait_read<1>();
+                    issue_load(un, sp);
+                }
             }
         }
         __syncwarp();
@@ -622,19 +619,20 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     uint64_t *in_empty = in_full + kFp8MaxSlots;
     uint8_t *in_ring = smem + 2 * kFp8MaxSlots * 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int workers = (blockDim.x >> 5) - 1;
     const int NI = a.n_in, nsl = a.num_slices;
 
     const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
     const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
     const int n = t_end - t_begin;
 
+    __shared__ int s_next_item;
     if (threadIdx.x == 0) {
         for (int i = 0; i < NI; ++i) {
             mbar_init(&in_full[i], 1);
             mbar_init(&in_empty[i], (uint32_t)nsl);
         }
         fence_barrier_init();
+        s_next_item = 0;
     }
     __syncthreads();
     if (n <= 0) return;
@@ -658,21 +656,31 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     }
 
     // ---------------------------------------------------------------- worker warps
-    const int wk = warp - 1;
-    const int64_t n_items = (int64_t)n * nsl;
-    // destination rows of an item's token, lanes < k (prefetched one item ahead)
-    auto fetch_rows = [&](int64_t q) -> int {
-        const int t = t_begin + (int)(q / nsl);
+    // Items (row j, slice sl) = q = j * nsl + sl are claimed in order from a
+    // shared counter, each worker claiming its next item when it starts the
+    // current one (so its rows can be prefetched): a worker whose items had
+    // fewer destinations takes more of them.
+    const int n_items = n * nsl;    // < 2^31 (checked on the host)
+    auto claim = [&]() -> int {
+        int q = 0;
+        if (lane == 0) q = atomicAdd(&s_next_item, 1);
+        return __shfl_sync(kFull, q, 0);
+    };
+    // destination rows of an item's token, lanes < k
+    auto fetch_rows = [&](int q) -> int {
+        const int t = t_begin + q / nsl;
         return (q < n_items && lane < a.k) ? a.dst_row[(int64_t)t * a.k + lane] : -1;
     };
-    int row_next = fetch_rows(wk);
-    for (int64_t q = wk; q < n_items; q += workers) {
-        const int j = (int)(q / nsl);
-        const int sl = (int)(q - (int64_t)j * nsl);
+    int q = claim();
+    int row_next = fetch_rows(q);
+    while (q < n_items) {
+        const int q_next = claim();
+        const int j = q / nsl;
+        const int sl = q - j * nsl;
         const int t = t_begin + j;
         const int si = j % NI;
         int row = row_next;
-        row_next = fetch_rows(q + workers);
+        row_next = fetch_rows(q_next);
         if (row >= a.capacity) {
             if (sl == 0) report(a.status, MOE_ERR_CAPACITY);
             row = -1;
@@ -742,6 +750,7 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
                 if (lane == 0 && a.recv_src) a.recv_src[rowd] = (int32_t)t;
             }
         }
+        q = q_next;
     }
 }
 
@@ -797,7 +806,7 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     a.num_units = (int64_t)num_tokens * a.num_chunks;
-    a.stages = std::min(kMaxStages, std::max(2, tu.dispatch_stages));
+    a.stages = std::min(kMaxStages, std::max(3, tu.dispatch_stages));   // the unit ring needs three
 
     int64_t per_warp = kBarBytes + (int64_t)a.stages * a.chunk_bytes;
     if (fp8) per_warp += (int64_t)a.stages * (a.chunk_bytes / 2) + round_up((int64_t)a.stages * (a.chunk_bytes / 256) * 4, 128);
@@ -860,7 +869,8 @@ int launch_dispatch(const DispatchLaunch &L) {
         f.n_in = std::max(2, std::min(kFp8MaxSlots, tu.fp8_in_slots));
         while (head + (size_t)f.n_in * f.row_bytes > optin && f.n_in > 2) --f.n_in;
         const size_t smem = head + (size_t)f.n_in * f.row_bytes;
-        if (smem <= optin && f.row_bytes < (1 << 20)) {
+        const int64_t max_cta_items = ((int64_t)L.num_tokens + device_sm_count() - 1) / device_sm_count() * f.num_slices + 64;
+        if (smem <= optin && f.row_bytes < (1 << 20) && max_cta_items < ((int64_t)1 << 31)) {
             if (ensure_dynamic_smem((const void *)dispatch_fp8_rows_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
             // as many of the requested workers as the kernel's register use allows in one CTA
             static int max_threads[64] = {0};

@@ -62,6 +62,16 @@ static_assert(sizeof(WsHeader) == 128, "header is one 128-byte line");
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Direct mode (few tiles, all co-resident): every tile publishes its rank
+// counts as flagged words and reads all tiles' words itself.
+constexpr int kDirectMaxTiles = 64;
+constexpr int64_t kDirectMaxRankWords = 16384;     // tiles * R
+
+inline bool direct_sizes(int T, int R) {
+    const int64_t tiles = (T + kTile - 1) / kTile;
+    return T > 0 && tiles <= kDirectMaxTiles && tiles * R <= kDirectMaxRankWords;
+}
+
 struct WsLayout {
     size_t expert_off, status_off, total;
 };
@@ -398,6 +408,226 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
 
 }
 
+// Waits (bounded) for the flagged words words[p], p in [0, n) strided over the
+// CTA, 8 loads in flight per thread, and hands each value to consume(p, v).
+template <typename F>
+__device__ void gather_flagged(const uint64_t *words, int n, uint64_t timeout_ns, int32_t *status, F consume) {
+    for (int p0 = threadIdx.x; p0 < n; p0 += 8 * kThreads) {
+        uint64_t w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int p = p0 + u * kThreads;
+            w[u] = p < n ? ld_relaxed_gpu_u64(words + p) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int p = p0 + u * kThreads;
+            if (p >= n) continue;
+            uint64_t x = w[u], deadline = 0;
+            while ((x & 0xffffffff00000000ull) == 0) {
+                const uint64_t now = globaltimer_ns();
+                if (deadline == 0) {
+                    deadline = now + timeout_ns;
+                } else if (now > deadline) {
+                    report(status, MOE_ERR_TIMEOUT);
+                    break;
+                }
+                x = ld_relaxed_gpu_u64(words + p);
+            }
+            consume(p, (int32_t)(uint32_t)x);
+        }
+    }
+}
+
+// Shared memory of the direct kernel: bitmap u32 [kWords][R] | word prefix
+// u16 [R][kWords] | exclusive prefix i32 [R] | rank totals i32 [R+1] |
+// expert histogram i32 [E+1] | entry expert i16 [kTile*k] | entry rank i16 [kTile*k]
+struct DirectSmem {
+    size_t wprefix, excl, tot, hist, ent, rk, total;
+};
+
+__host__ __device__ inline DirectSmem direct_smem(int E, int R, int k) {
+    DirectSmem d;
+    d.wprefix = align_up((size_t)R * kWords * 4, 16);
+    d.excl = d.wprefix + align_up((size_t)R * kWords * 2, 16);
+    d.tot = d.excl + align_up((size_t)R * 4, 16);
+    d.hist = d.tot + align_up((size_t)(R + 1) * 4, 16);
+    d.ent = d.hist + align_up((size_t)(E + 1) * 4, 16);
+    d.rk = d.ent + align_up((size_t)kTile * k * 2, 16);
+    d.total = d.rk + align_up((size_t)kTile * k * 2, 16);
+    return d;
+}
+
+// Direct mode, launched cooperatively with one CTA per tile (few tiles): each
+// tile adds its expert histogram into the global accumulator, then publishes
+// its per-rank counts, then reads every tile's rank words -- the sum over
+// lower tiles is its exclusive prefix, the sum over all tiles the rank totals
+// -- so no tile waits on a chain of predecessors. A tile's rank words are
+// published after a fence that follows its histogram atomics, so once tile 0
+// has seen every tile's words the expert totals are complete; it then writes
+// the expert counts and prefix. A batch of one tile exchanges nothing.
+__global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int R = a.R, E = a.E, k = a.k;
+    const DirectSmem sl = direct_smem(E, R, k);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem);
+    uint16_t *wprefix = reinterpret_cast<uint16_t *>(smem + sl.wprefix);
+    int32_t *excl = reinterpret_cast<int32_t *>(smem + sl.excl);
+    int32_t *tot = reinterpret_cast<int32_t *>(smem + sl.tot);
+    int32_t *hist = reinterpret_cast<int32_t *>(smem + sl.hist);
+    int16_t *ent = reinterpret_cast<int16_t *>(smem + sl.ent);   // expert of each entry, then its owned rank
+    int16_t *rk = reinterpret_cast<int16_t *>(smem + sl.rk);     // rank of each entry
+    uint64_t *rank_words = reinterpret_cast<uint64_t *>(a.ws + a.status_off);
+    int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
+
+    const int tile = blockIdx.x;
+    const bool multi = a.num_tiles > 1;
+    const int t0 = tile * kTile;
+    const int tcount = min(kTile, a.T - t0);
+    const int n_ent = tcount * k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool publish = tile != a.unpublished_tile;
+
+    for (int i = threadIdx.x; i < R * kWords; i += kThreads) bitmap[i] = 0u;
+    for (int i = threadIdx.x; i < E; i += kThreads) hist[i] = 0;
+    for (int r = threadIdx.x; r < R; r += kThreads) excl[r] = 0;
+    // the tile's entries: expert and rank ids (-1: masked or invalid), 8 loads in flight per thread
+    for (int base = threadIdx.x; base < n_ent; base += 8 * kThreads) {
+        int64_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * kThreads;
+            v[u] = i < n_ent ? ld_nc_i64(a.topk + (int64_t)t0 * k + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * kThreads;
+            if (i < n_ent) {
+                const bool ok = v[u] >= 0 && v[u] < E;
+                if (!ok && v[u] != -1) report(a.status, MOE_ERR_BAD_TOPK);
+                ent[i] = ok ? (int16_t)v[u] : (int16_t)-1;
+                rk[i] = ok ? (int16_t)((int)v[u] / a.m) : (int16_t)-1;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- pass 1, lanes over (token, entry): expert histogram, each rank of a token
+    //      once (__match_any_sync; the lowest entry owns it), membership bits;
+    //      ent[] becomes the owned rank (or -1)
+    {
+        const int tpp = 32 / k;
+        const int sub = lane / k, j = lane - sub * k;
+        const bool lane_used = sub < tpp;
+        for (int base = warp * tpp; base < tcount; base += kWarps * tpp) {
+            const int tl = base + sub;
+            const bool act = lane_used && tl < tcount;
+            const int r = act ? (int)rk[tl * k + j] : -1;
+            if (r >= 0) atomicAdd(&hist[ent[tl * k + j]], 1);
+            const unsigned peers = __match_any_sync(0xffffffffu, r >= 0 ? sub * R + r : -(lane + 1));
+            const bool owner = r >= 0 && (__ffs(peers) - 1) == lane;
+            if (owner) atomicOr(&bitmap[(tl >> 5) * R + r], 1u << (tl & 31));
+            if (act) ent[tl * k + j] = (int16_t)(owner ? r : -1);
+        }
+    }
+    __syncthreads();
+
+    // ---- this tile's rank counts (and, with several tiles, the exchange)
+    if (multi) {
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            const int h = hist[e];
+            if (h) atomicAdd(ws_expert + e, h);
+        }
+        __threadfence();
+    }
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+            wprefix[r * kWords + w] = (uint16_t)run;
+            run += __popc(bitmap[w * R + r]);
+        }
+        tot[r] = multi ? 0 : (int32_t)run;
+        if (multi && publish) st_relaxed_gpu_u64(rank_words + (size_t)tile * R + r, kFlagAggregate | run);
+    }
+    __syncthreads();
+    if (multi) {
+        gather_flagged(rank_words, a.num_tiles * R, a.timeout_ns, a.status, [&](int p, int32_t v) {
+            const int b = p / R, r = p - b * R;
+            if (b < tile) atomicAdd(&excl[r], v);
+            atomicAdd(&tot[r], v);
+        });
+        __syncthreads();
+        if (tile == 0) {
+            __threadfence();
+            for (int e = threadIdx.x; e < E; e += kThreads) hist[e] = __ldcg(ws_expert + e);
+        }
+        __syncthreads();
+    }
+
+    // ---- rank regions (warp 0) and, on tile 0, expert counts and prefix (warp 1)
+    if (warp == 0) {
+        if (tile == 0)
+            for (int r = lane; r < R; r += 32) a.num_tokens_per_rank[r] = tot[r];
+        __syncwarp();
+        warp_exclusive_scan(tot, R, lane);
+    } else if (warp == 1 && tile == 0) {
+        for (int e = lane; e < E; e += 32) a.num_tokens_per_expert[e] = hist[e];
+        __syncwarp();
+        warp_exclusive_scan(hist, E, lane);
+        __syncwarp();
+        for (int e = lane; e <= E; e += 32) a.expert_prefix[e] = hist[e];
+    }
+    __syncthreads();
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+        excl[r] += tot[r];
+        if (tile == 0) a.rank_prefix[r] = tot[r];
+    }
+    if (tile == 0 && threadIdx.x == 0) a.rank_prefix[R] = tot[R];
+    __syncthreads();
+
+    // ---- pass 2: global receive rows of the owning entries
+    for (int i = threadIdx.x; i < n_ent; i += kThreads) {
+        const int r = ent[i];
+        int32_t v = -1;
+        if (r >= 0) {
+            const int tl = i / k;
+            const uint32_t word = bitmap[(tl >> 5) * R + r];
+            v = excl[r] + wprefix[r * kWords + (tl >> 5)] + __popc(word & ((1u << (tl & 31)) - 1u));
+        }
+        a.token_dst_row[(int64_t)t0 * k + i] = v;
+    }
+
+    // ---- is_token_in_rank rows: one warp per token row when rows are long, flat otherwise
+    uint8_t *dst = a.is_token_in_rank + (int64_t)t0 * R;
+    if ((R & 3) == 0 && R >= 128) {
+        for (int tl = warp; tl < tcount; tl += kWarps) {
+            const uint32_t *wrow = bitmap + (tl >> 5) * R;
+            const int b = tl & 31;
+            for (int r0 = 4 * lane; r0 < R; r0 += 128) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(wrow + r0);
+                const uint32_t v = ((q.x >> b) & 1u) | (((q.y >> b) & 1u) << 8) | (((q.z >> b) & 1u) << 16) |
+                                   (((q.w >> b) & 1u) << 24);
+                *reinterpret_cast<uint32_t *>(dst + (int64_t)tl * R + r0) = v;
+            }
+        }
+    } else if ((R & 3) == 0) {
+        uint32_t *dst4 = reinterpret_cast<uint32_t *>(dst);
+        for (int i = threadIdx.x; i < tcount * R / 4; i += kThreads) {
+            const int tl = (i * 4) / R, r0 = (i * 4) - tl * R;
+            uint32_t v = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v |= ((bitmap[(tl >> 5) * R + r0 + b] >> (tl & 31)) & 1u) << (8 * b);
+            dst4[i] = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < tcount * R; i += kThreads) {
+            const int tl = i / R, r = i - tl * R;
+            dst[i] = (uint8_t)((bitmap[(tl >> 5) * R + r] >> (tl & 31)) & 1u);
+        }
+    }
+}
+
 __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, int m,
                                    const int32_t *__restrict__ rank_prefix, int32_t *__restrict__ token_dst_row) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -413,25 +643,40 @@ int lookback_group(int R) {
     return g;
 }
 
-// How many tiles can be co-resident (cooperative launch bound), cached per (device, smem).
-int cooperative_capacity(size_t smem) {
+// How many CTAs of `kernel` can be co-resident (cooperative launch bound),
+// cached per (device, kernel, shared memory).
+int cooperative_capacity(const void *kernel, size_t smem) {
+    struct Entry { int dev; const void *fn; size_t smem; int cap; };
     static std::mutex mu;
-    static int dev_cached[64] = {0};
-    static size_t smem_cached[64] = {0};
-    static int cap_cached[64] = {0};
+    static Entry cache[16];
+    static int n_cached = 0;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev_cached[dev] && smem_cached[dev] == smem) return cap_cached[dev];
+    for (int i = 0; i < n_cached; ++i)
+        if (cache[i].dev == dev && cache[i].fn == kernel && cache[i].smem == smem) return cache[i].cap;
     int coop = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_tiles_kernel<true>, kThreads, smem) !=
-        cudaSuccess)
-        return 0;
-    dev_cached[dev] = 1;
-    smem_cached[dev] = smem;
-    cap_cached[dev] = per_sm * device_sm_count();
-    return cap_cached[dev];
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess) return 0;
+    const int cap = per_sm * device_sm_count();
+    cache[n_cached % 16] = Entry{dev, kernel, smem, cap};
+    ++n_cached;
+    return cap;
+}
+
+int launch_cooperative(const void *kernel, int grid, size_t smem, cudaStream_t s, TileArgs &a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {&a};
+    return cudaLaunchKernelExC(&cfg, kernel, args) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
@@ -451,7 +696,10 @@ int launch_layout(const LayoutLaunch &L) {
         return MOE_OK;
     }
     const WsLayout w = ws_layout(T, E, R);
-    if (cudaMemsetAsync(L.workspace, 0, w.total, s) != cudaSuccess) return MOE_ERR_CUDA;
+    const int num_tiles = (T + kTile - 1) / kTile;
+    // a single-tile direct launch uses no workspace
+    if (!(direct_sizes(T, R) && num_tiles == 1) && cudaMemsetAsync(L.workspace, 0, w.total, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
 
     TileArgs a;
     a.topk = L.topk_idx;
@@ -472,24 +720,21 @@ int launch_layout(const LayoutLaunch &L) {
     a.unpublished_tile = L.unpublished_tile;
 
     const size_t smem = smem_layout(E, R, k).total;
-    if (ensure_dynamic_smem((const void *)layout_tiles_kernel<true>, smem) != MOE_OK ||
+    const size_t dsmem = direct_smem(E, R, k).total;
+    const void *direct = (const void *)layout_direct_kernel;
+    const void *coop = (const void *)layout_tiles_kernel<true>;
+    if (ensure_dynamic_smem(direct, dsmem) != MOE_OK || ensure_dynamic_smem(coop, smem) != MOE_OK ||
         ensure_dynamic_smem((const void *)layout_tiles_kernel<false>, smem) != MOE_OK)
         return MOE_ERR_CUDA;
 
-    if (a.num_tiles <= cooperative_capacity(smem)) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)a.num_tiles);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, layout_tiles_kernel<true>, a) != cudaSuccess) return MOE_ERR_CUDA;
-        return MOE_OK;
+    if (direct_sizes(T, R) && a.num_tiles <= cooperative_capacity(direct, dsmem)) {
+        if (a.num_tiles == 1) {     // nothing to exchange: an ordinary launch
+            layout_direct_kernel<<<1, kThreads, dsmem, s>>>(a);
+            return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+        }
+        return launch_cooperative(direct, a.num_tiles, dsmem, s, a);
     }
+    if (a.num_tiles <= cooperative_capacity(coop, smem)) return launch_cooperative(coop, a.num_tiles, smem, s, a);
 
     layout_tiles_kernel<false><<<a.num_tiles, kThreads, smem, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;

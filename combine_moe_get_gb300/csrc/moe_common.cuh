@@ -21,6 +21,28 @@ __device__ __forceinline__ void report(int32_t *status, int code) {
     if (status != nullptr) atomicCAS(reinterpret_cast<int *>(status), 0, code);
 }
 
+// In-place exclusive scan of n int32 in shared memory by one warp (all 32
+// lanes call it); v[n] receives the total.
+__device__ __forceinline__ void warp_exclusive_scan(int32_t *v, int n, int lane) {
+    const int per = (n + 31) / 32;
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    int32_t local = 0;
+    for (int i = lo; i < hi; ++i) local += v[i];
+    int32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int32_t run = incl - local;
+    for (int i = lo; i < hi; ++i) {
+        const int32_t x = v[i];
+        v[i] = run;
+        run += x;
+    }
+    if (lane == 31) v[n] = incl;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
