@@ -92,126 +92,102 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
     return r;
 }
 
-// E4M3 codes of x / scale with the quotient taken as the IEEE fp32 quotient.
-// q0 = RN(x * rcp_approx(scale)) is within 5 fp32 ulps of RN(x / scale)
-// (relative errors <= 2^-23 for the reciprocal and 2^-24 for each rounding).
-// E4M3 rounding (3 mantissa bits, RNE, saturating) is a step function of its
-// fp32 argument whose steps sit at midpoints, whose fp32 mantissa has low 20
-// bits == 0x80000 in the normal range; below 2^-6 the E4M3 quantum is fixed.
-// So when every q0 of the lane is more than 16 ulps from a midpoint and at
-// least 2^-6 in magnitude, the q0 give the same codes as the IEEE quotients;
-// otherwise the flagged quotients are taken with the IEEE division.
-constexpr uint32_t kMidWindow = 16;
+// E4M3 codes of y = RN(x / scale) (the IEEE fp32 quotient) without a division.
+// r = rcp_approx(scale) is within 1 ulp (relative 2^-23) of 1/scale. With
+// r_lo = RN(r * (1 - 2^-20)) and r_hi = RN(r * (1 + 2^-20)), the products
+// RN(x * r_lo) and RN(x * r_hi) lie strictly below and above y in magnitude
+// (each is off 1/scale by at most 2^-20 + 2^-23 + 2 * 2^-24 < 2^-19 relative
+// in one direction and at least 2^-20 - 2^-23 - 2 * 2^-24 > 2^-21 in the
+// same direction, while y is within 2^-24 of x / scale). E4M3 rounding
+// (RNE, saturating) is monotone in its argument, so when the two products
+// give the same code that code is the code of y; otherwise (the quotient is
+// within ~2^-19 of a rounding boundary) y itself is computed by the IEEE
+// division. A scale below 2^-100 (whose reciprocal may overflow) takes the
+// division throughout.
+constexpr float kTinyScale = 7.8886090522e-31f;   // 2^-100
 
-__device__ __forceinline__ bool near_midpoint(float q) {
-    return ((__float_as_uint(q) + kMidWindow - 0x80000u) & 0xfffffu) <= 2 * kMidWindow;
+__device__ __forceinline__ uint32_t cvt_e4m3x2(uint64_t xy) {   // {x, y} -> (code(y) << 8) | code(x)
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(__uint_as_float((uint32_t)xy),
+                                                          __uint_as_float((uint32_t)(xy >> 32))),
+                                              __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ uint64_t bf16x2_as_f32x2(uint32_t w) {   // two bf16 in one word -> {lo, hi} as f32x2
+    uint64_t xy;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "r"(w << 16), "r"(w & 0xffff0000u));
+    return xy;
+}
+
+// Reciprocal bracket of a nonzero block scale (see above).
+struct RcpBracket {
+    uint64_t lo, hi;   // {r_lo, r_lo} and {r_hi, r_hi} as f32x2 operands
+};
+
+__device__ __forceinline__ RcpBracket rcp_bracket(float scale) {
+    const float r = rcp_approx(scale);
+    const float r_lo = __fmul_rn(r, 0.99999904632568359375f);   // 1 - 2^-20
+    const float r_hi = __fmul_rn(r, 1.00000095367431640625f);   // 1 + 2^-20
+    RcpBracket b;
+    b.lo = (uint64_t)__float_as_uint(r_lo) | ((uint64_t)__float_as_uint(r_lo) << 32);
+    b.hi = (uint64_t)__float_as_uint(r_hi) | ((uint64_t)__float_as_uint(r_hi) << 32);
+    return b;
+}
+
+// Codes of one word's two bf16 values divided by scale, (code1 << 8) | code0.
+__device__ __forceinline__ uint32_t e4m3_pair(uint32_t w, float scale, const RcpBracket &b) {
+    const uint64_t xy = bf16x2_as_f32x2(w);
+    const uint32_t lo = cvt_e4m3x2(mul_f32x2(xy, b.lo));
+    const uint32_t hi = cvt_e4m3x2(mul_f32x2(xy, b.hi));
+    if (lo == hi && scale >= kTinyScale) return lo;
+    // within ~2^-19 of a rounding boundary (rare), or a tiny scale: the IEEE quotient
+    const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xffff0000u);
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x0 / scale, x1 / scale), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Codes of the 8 values of one uint4 (4 words), packed 4 codes per 32 bits.
+__device__ __forceinline__ uint2 e4m3_quad(uint4 v, float scale, const RcpBracket &b) {
+    uint2 q;
+    q.x = e4m3_pair(v.x, scale, b) | (e4m3_pair(v.y, scale, b) << 16);
+    q.y = e4m3_pair(v.z, scale, b) | (e4m3_pair(v.w, scale, b) << 16);
+    return q;
+}
+
+__device__ __forceinline__ float bf16x2_absmax(uint32_t w, float m) {
+    return fmaxf(m, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u))));
 }
 
 // Quantise one 128-channel block held by a half-warp (16 lanes x 8 values).
 // Returns the block's scale; writes the 8 codes of this lane to `q8`.
 __device__ __forceinline__ float quantize_lane8(const uint4 v, uint2 &q8) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float f[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    float amax = bf16x2_absmax(v.w, bf16x2_absmax(v.z, bf16x2_absmax(v.y, bf16x2_absmax(v.x, 0.0f))));
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     const float scale = block_scale(amax);
-    uint32_t c[4];
     if (scale == 0.0f) {
-        c[0] = c[1] = c[2] = c[3] = 0u;
+        q8 = make_uint2(0u, 0u);
     } else {
-        const float rcp = rcp_approx(scale);
-        const uint64_t rr = (uint64_t)__float_as_uint(rcp) | ((uint64_t)__float_as_uint(rcp) << 32);
-        float q[8];
-        uint32_t dmin = 0xffffffffu;
-        float qmin = INFINITY;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint64_t xy;                     // {f[2i], f[2i+1]} as one f32x2 operand
-            asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "r"(w[i] << 16), "r"(w[i] & 0xffff0000u));
-            const uint64_t p = mul_f32x2(xy, rr);
-            q[2 * i] = __uint_as_float((uint32_t)p);
-            q[2 * i + 1] = __uint_as_float((uint32_t)(p >> 32));
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            dmin = min(dmin, (__float_as_uint(q[i]) + kMidWindow - 0x80000u) & 0xfffffu);
-            qmin = fminf(qmin, fabsf(q[i]));
-        }
-        // scale >= 2^-100 keeps 1/scale finite; tinier scales take the IEEE path throughout
-        if (dmin <= 2 * kMidWindow || qmin < 0.015625f || scale < 7.8886090522e-31f) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (near_midpoint(q[i]) || fabsf(q[i]) < 0.015625f || scale < 7.8886090522e-31f) q[i] = f[i] / scale;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(q[2 * i], q[2 * i + 1]), __NV_SATFINITE,
-                                                      __NV_E4M3);   // .x -> low byte
+        const RcpBracket b = rcp_bracket(scale);
+        q8 = e4m3_quad(v, scale, b);
     }
-    q8.x = c[0] | (c[1] << 16);
-    q8.y = c[2] | (c[3] << 16);
     return scale;
 }
 
 // Quantise one 128-channel block held by a quarter-warp (8 lanes x 16 values;
-// `lo`, `hi` are the lane's 32 contiguous bytes). Same arithmetic as
-// quantize_lane8. Returns the block's scale; writes the 16 codes to `q16`.
+// `lo`, `hi` are the lane's 32 contiguous bytes). Returns the block's scale;
+// writes the 16 codes to `q16`.
 __device__ __forceinline__ float quantize_lane16(const uint4 lo, const uint4 hi, uint4 &q16) {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+    float amax = bf16x2_absmax(lo.w, bf16x2_absmax(lo.z, bf16x2_absmax(lo.y, bf16x2_absmax(lo.x, 0.0f))));
+    amax = bf16x2_absmax(hi.w, bf16x2_absmax(hi.z, bf16x2_absmax(hi.y, bf16x2_absmax(hi.x, amax))));
 #pragma unroll
     for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     const float scale = block_scale(amax);
-    uint32_t c[8];
     if (scale == 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) c[i] = 0u;
+        q16 = make_uint4(0u, 0u, 0u, 0u);
     } else {
-        const float rcp = rcp_approx(scale);
-        const uint64_t rr = (uint64_t)__float_as_uint(rcp) | ((uint64_t)__float_as_uint(rcp) << 32);
-        float q[16];
-        uint32_t dmin = 0xffffffffu;
-        float qmin = INFINITY;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint64_t xy;
-            asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "r"(w[i] << 16), "r"(w[i] & 0xffff0000u));
-            const uint64_t p = mul_f32x2(xy, rr);
-            q[2 * i] = __uint_as_float((uint32_t)p);
-            q[2 * i + 1] = __uint_as_float((uint32_t)(p >> 32));
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            dmin = min(dmin, (__float_as_uint(q[i]) + kMidWindow - 0x80000u) & 0xfffffu);
-            qmin = fminf(qmin, fabsf(q[i]));
-        }
-        if (dmin <= 2 * kMidWindow || qmin < 0.015625f || scale < 7.8886090522e-31f) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float f = __uint_as_float((i & 1) ? (w[i >> 1] & 0xffff0000u) : (w[i >> 1] << 16));
-                if (near_midpoint(q[i]) || fabsf(q[i]) < 0.015625f || scale < 7.8886090522e-31f) q[i] = f / scale;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(q[2 * i], q[2 * i + 1]), __NV_SATFINITE,
-                                                      __NV_E4M3);   // .x -> low byte
+        const RcpBracket b = rcp_bracket(scale);
+        const uint2 a0 = e4m3_quad(lo, scale, b), a1 = e4m3_quad(hi, scale, b);
+        q16 = make_uint4(a0.x, a0.y, a1.x, a1.y);
     }
-    q16.x = c[0] | (c[1] << 16);
-    q16.y = c[2] | (c[3] << 16);
-    q16.z = c[4] | (c[5] << 16);
-    q16.w = c[6] | (c[7] << 16);
     return scale;
 }
 
@@ -360,7 +336,7 @@ __device__ void fused_layout(const DispatchArgs &a, uint8_t *region) {
 }
 
 template <bool kFP8, bool kFused>
-__global__ void __launch_bounds__(512) dispatch_kernel(const DispatchArgs a) {
+__global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int warps = blockDim.x >> 5;
@@ -626,6 +602,7 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     const int n = t_end - t_begin;
 
     __shared__ int s_next_item;
+    __shared__ volatile int s_rows_issued;   // rows whose load the producer has armed
     if (threadIdx.x == 0) {
         for (int i = 0; i < NI; ++i) {
             mbar_init(&in_full[i], 1);
@@ -633,6 +610,7 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
         }
         fence_barrier_init();
         s_next_item = 0;
+        s_rows_issued = 0;
     }
     __syncthreads();
     if (n <= 0) return;
@@ -650,6 +628,8 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
                 mbar_arrive_expect_tx(&in_full[s], (uint32_t)a.row_bytes);
                 bulk_load(in_ring + (size_t)s * a.row_bytes, a.x + (int64_t)(t_begin + j) * a.row_bytes,
                           (uint32_t)a.row_bytes, &in_full[s], pol);
+                __threadfence_block();
+                s_rows_issued = j + 1;
             }
         }
         return;
@@ -686,7 +666,21 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
             row = -1;
         }
         const unsigned dmask = __ballot_sync(kFull, row >= 0);
-        const bool ok = mbar_wait_bounded(&in_full[si], (uint32_t)((j / NI) & 1), a.timeout_ns);
+        // A slot's barrier is waited on by parity, which only names its current or
+        // previous phase: wait (bounded) until row j's load has been armed, i.e.
+        // the slot has left the phase of row j - NI, before waiting on the barrier.
+        bool ok = true;
+        if (s_rows_issued <= j) {
+            const uint64_t deadline = globaltimer_ns() + a.timeout_ns;
+            while (s_rows_issued <= j) {
+                if (globaltimer_ns() > deadline) {
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        __threadfence_block();
+        ok = ok && mbar_wait_bounded(&in_full[si], (uint32_t)((j / NI) & 1), a.timeout_ns);
         if (!__all_sync(kFull, ok)) {
             if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
             break;
