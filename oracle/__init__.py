@@ -47,6 +47,8 @@ def lib():
         _lib.oracle_expand_layout.restype = I
         _lib.oracle_dispatch_expand.argtypes = [I, P, P, I, I, P, P, I, I, I, P, I, P, P, P, P, P, P]
         _lib.oracle_dispatch_expand.restype = I
+        _lib.oracle_combine_fp8.argtypes = [P, P, I, I, I, I, P, P]
+        _lib.oracle_combine_fp8.restype = I
         for f in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_combine"):
             getattr(_lib, f).restype = I
         _lib.oracle_bf16_from_float.argtypes = [ctypes.c_float]
@@ -221,6 +223,19 @@ def dispatch_expand(mode: int, x: np.ndarray, topk_idx: np.ndarray, topk_weights
         cap, _ptr(out["recv_x"]), _ptr(out["recv_x_scales"]), _ptr(out["recv_topk_idx"]),
         _ptr(out["recv_topk_weights"]), _ptr(out["recv_src_idx"]), _ptr(out["x_scales"]))
     return out
+
+
+def combine_fp8(codes: np.ndarray, scales: np.ndarray, token_dst_row: np.ndarray) -> tuple[np.ndarray, int]:
+    """bf16 bit patterns [T, H] of the ascending fp32 sums of the dequantised
+    E4M3 rows (codes uint8 [rows, H], scales fp32 [rows, H/128])."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    token_dst_row = np.ascontiguousarray(token_dst_row, dtype=np.int32)
+    num_rows, H = codes.shape
+    T, k = token_dst_row.shape
+    out = np.zeros((T, H), np.uint16)
+    flags = lib().oracle_combine_fp8(_ptr(codes), _ptr(scales), num_rows, T, H, k, _ptr(token_dst_row), _ptr(out))
+    return out, flags
 
 
 def bf16_from_float(v: float) -> int:

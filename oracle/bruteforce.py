@@ -233,3 +233,18 @@ def dispatch_expand(x_bits: np.ndarray, topk_idx, topk_weights: Optional[np.ndar
         out["recv_x_scales"] = recv_scales
         out["x_scales"] = ref["x_scales"]
     return out
+
+
+def combine_fp8(codes: np.ndarray, scales: np.ndarray, token_dst_row: np.ndarray) -> np.ndarray:
+    """Dequantise by table lookup times the block scale (numpy float32), then
+    add the token's rows in ascending row order; bf16 by torch's cast."""
+    T, k = token_dst_row.shape
+    H = codes.shape[1]
+    deq = (e4m3_decode(codes).astype(np.float32) * np.repeat(np.asarray(scales, np.float32), 128, axis=1)).astype(np.float32)
+    out = np.zeros((T, H), np.float32)
+    for t in range(T):
+        acc = np.zeros(H, np.float32)
+        for row in sorted(int(v) for v in token_dst_row[t] if v >= 0):
+            acc = (acc + deq[row]).astype(np.float32)
+        out[t] = acc
+    return f32_to_bf16_bits(out)

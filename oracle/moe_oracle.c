@@ -501,3 +501,39 @@ int oracle_dispatch_expand(int mode, const void *x, const float *x_scales_in, in
     free(s);
     return flags;
 }
+
+/* Combine of E4M3 partial rows (codes plus one fp32 scale per 128 channels,
+ * the layout the FP8 dispatch produces). Reading: each element is first
+ * dequantised on its own, v = RN(value(code) * scale) in fp32, and the
+ * token's dequantised rows are then summed as in oracle_combine: ascending
+ * receive row, fp32 from +0.0f, one round-to-nearest-even cast to bf16. */
+int oracle_combine_fp8(const uint8_t *codes, const float *scales, int num_rows, int T, int H, int k,
+                       const int32_t *token_dst_row, uint16_t *out)
+{
+    if (T < 0 || H < 128 || H % 128 != 0 || k < 1 || k > 32) return ORACLE_BAD_ARG;
+    int flags = 0, nb = H / 128;
+    int32_t rows[32];
+    for (int t = 0; t < T; ++t) {
+        int n = 0;
+        for (int j = 0; j < k; ++j) {
+            int32_t row = token_dst_row[(int64_t)t * k + j];
+            if (row < 0) continue;
+            if (row >= num_rows) { flags |= ORACLE_CAPACITY; continue; }
+            rows[n++] = row;
+        }
+        for (int a = 1; a < n; ++a)
+            for (int b = a; b > 0 && rows[b - 1] > rows[b]; --b) {
+                int32_t tmp = rows[b]; rows[b] = rows[b - 1]; rows[b - 1] = tmp;
+            }
+        for (int h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int i = 0; i < n; ++i) {
+                float s = scales[(int64_t)rows[i] * nb + h / 128];
+                float v = oracle_e4m3_to_float(codes[(int64_t)rows[i] * H + h]) * s;
+                acc = acc + v;
+            }
+            out[(int64_t)t * H + h] = oracle_bf16_from_float(acc);
+        }
+    }
+    return flags;
+}

@@ -39,6 +39,10 @@ MUTATIONS = {
                                    "(int64_t)r * m : -1;"),
     "expand_weight_of_other_entries": ("(jj == j && topk_weights) ? topk_weights[(int64_t)t * k + j] : 0.0f;",
                                        "(topk_weights) ? topk_weights[(int64_t)t * k + jj] : 0.0f;"),
+    "fp8_combine_fused": ("                float v = oracle_e4m3_to_float(codes[(int64_t)rows[i] * H + h]) * s;\n                acc = acc + v;",
+                          "                acc = fmaf(oracle_e4m3_to_float(codes[(int64_t)rows[i] * H + h]), s, acc);"),
+    "fp8_combine_wrong_block_scale": ("float s = scales[(int64_t)rows[i] * nb + h / 128];",
+                                      "float s = scales[(int64_t)rows[i] * nb + (h / 128 + 1) % nb];"),
     "expand_source_token_off_by_one": ("            recv_src_idx[row] = t;\n            for (int jj = 0;",
                                        "            recv_src_idx[row] = t + 1;\n            for (int jj = 0;"),
 }

@@ -730,3 +730,62 @@ def test_oracle_expand_weighted_combine_returns_weights_and_mixture():
     got = bf.bf16_bits_to_f32(out).astype(np.float64)
     # fp32 fma chain of <= 8 terms then one bf16 rounding
     assert np.all(np.abs(got - wsum[:, None] * x) <= 2.0 ** -8 * np.abs(wsum[:, None] * x) * 1.01 + 8 * 2.0 ** -24 * np.abs(x))
+
+
+# ---------------------------------------------------------------- combine of E4M3 partial rows
+
+def _random_fp8_rows(seed, rows, H):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 256, (rows, H), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38          # no NaN codes
+    scales = (rng.standard_normal((rows, H // 128)) * 2.0 ** rng.integers(-8, 8, (rows, H // 128))).astype(np.float32)
+    return codes, scales
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_oracle_combine_fp8_vs_bruteforce(seed):
+    topk, _, _, E, R = _random_small_case(seed)
+    lay = oracle.layout(topk.numpy(), E, R)
+    H = 256
+    codes, scales = _random_fp8_rows(seed, max(lay["num_recv"], 1), H)
+    a, flags = oracle.combine_fp8(codes, scales, lay["token_dst_row"])
+    assert flags == 0
+    np.testing.assert_array_equal(a, bf.combine_fp8(codes, scales, lay["token_dst_row"]))
+
+
+def test_oracle_combine_fp8_single_row_is_the_e4m3_value():
+    # one row per token with scale 1: every E4M3 value is a bf16 value, so the output is the table value exactly
+    codes = np.arange(256, dtype=np.uint8).reshape(2, 128)
+    codes[(codes & 0x7F) == 0x7F] = 0
+    dst = np.array([[0, -1], [-1, 1]], np.int32)
+    out, _ = oracle.combine_fp8(codes, np.ones((2, 1), np.float32), dst)
+    np.testing.assert_array_equal(bf.bf16_bits_to_f32(out), bf.e4m3_decode(codes).astype(np.float32))
+
+
+def test_oracle_combine_fp8_rounds_product_then_sum():
+    # row 0: -1.0 * (1.125 + 2^-23) is exact; row 1: 1.125 * (1 + 2^-23) = 1.125 + 2^-23 + 2^-26 rounds to
+    # 1.125 + 2^-23, so the ascending sum is exactly 0; a fused multiply-add would keep 2^-26
+    codes = np.array([[0xB8] * 128, [0x39] * 128], np.uint8)
+    assert bf.e4m3_decode(codes[:, :1]).ravel().tolist() == [-1.0, 1.125]
+    scales = np.array([[1.125 + 2.0 ** -23], [1 + 2.0 ** -23]], np.float32)
+    out, _ = oracle.combine_fp8(codes, scales, np.array([[0, 1]], np.int32))
+    assert np.all(out == 0)
+
+
+def test_oracle_dispatch_fp8_then_combine_fp8_is_d_times_dequantised_x():
+    # identity experts on FP8 rows: every row of a token carries the same codes and scales, so the combine
+    # returns the D-fold sum of the dequantised token, within one bf16 rounding plus the fp32 sum's roundings
+    wk = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(wk, with_partial=False, num_tokens=128)
+    topk = inp.topk_idx.numpy()
+    lay = oracle.layout(topk, wk.num_experts, wk.num_ranks)
+    d = oracle.dispatch(_bits(inp.x), topk, None, wk.num_experts, wk.num_ranks, lay["token_dst_row"], lay["num_recv"],
+                        fp8=True)
+    out, flags = oracle.combine_fp8(d["recv_x"], d["recv_x_scales"], lay["token_dst_row"])
+    assert flags == 0
+    deq = bf.e4m3_decode(d["recv_x"]).astype(np.float64) * np.repeat(d["recv_x_scales"].astype(np.float64), 128, axis=1)
+    D = lay["is_token_in_rank"].sum(axis=1).astype(np.float64)
+    first = np.array([lay["token_dst_row"][t][lay["token_dst_row"][t] >= 0].min() for t in range(128)])
+    ref = D[:, None] * deq[first]
+    got = bf.bf16_bits_to_f32(out).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) * 1.01 + 1e-30)
