@@ -243,6 +243,11 @@ class Step:
     def combine(self):
         self.moe.moe_combine(self.partial, self.lay.token_dst_row, out=self.out, status=self.status)
 
+    def combine_fp8(self):
+        # E4M3 partial rows: the FP8 dispatch's own receive rows and scales
+        self.moe.moe_combine_fp8(self.disp8.recv_x, self.disp8.recv_x_scales, self.lay.token_dst_row, out=self.out,
+                                 status=self.status)
+
     def layout_dispatch(self):
         self.moe.moe_layout_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks, self.cap,
                                      layout=self.lay, workspace=self.ws, out=self.disp, status=self.status)
@@ -395,6 +400,8 @@ def run_ours(args, world, rank, local):
     fp8_ms = time_alone(lambda: st.dispatch(fp8=True), reps)                  # fused E4M3 quantisation
     fp8in_ms = time_alone(st.dispatch_fp8_input, reps)                        # E4M3 rows + scales relayed
     wcomb_ms = time_alone(st.combine_weighted, reps)                          # weighted rows + combined weights
+    st.dispatch(fp8=True)                                                     # E4M3 rows for the FP8 combine
+    fcomb_ms = time_alone(st.combine_fp8, reps)                               # E4M3 partial rows + scales
     xlay_ms = time_alone(st.expand_layout, reps)                              # expand mode, each kernel alone
     xdis_ms = time_alone(st.dispatch_expand, reps)
     xcom_ms = time_alone(st.combine_expand, reps)
@@ -420,6 +427,7 @@ def run_ours(args, world, rank, local):
     bytes_fp8in = (T + N) * (H + (H // 128) * 4)        # e4m3 rows + scales read once, written per rank
     bytes_wcomb = bytes_bf16 + N * 4                    # + one weight per receive row
     bytes_expand = T * row + NX * row                   # x read once + one row per valid entry
+    bytes_fcomb = N * (H + (H // 128) * 4) + T * row    # e4m3 rows + scales read, bf16 out written
     kern = {
         "layout_us": mean(lay_ms) * 1e3,
         "dispatch_us": mean(dis_ms) * 1e3,
@@ -427,6 +435,7 @@ def run_ours(args, world, rank, local):
         "dispatch_fp8_us": mean(fp8_ms) * 1e3,
         "dispatch_fp8_input_us": mean(fp8in_ms) * 1e3,
         "combine_weighted_us": mean(wcomb_ms) * 1e3,
+        "combine_fp8_us": mean(fcomb_ms) * 1e3,
         "expand_layout_us": mean(xlay_ms) * 1e3,
         "dispatch_expand_us": mean(xdis_ms) * 1e3,
         "combine_expand_us": mean(xcom_ms) * 1e3,
@@ -441,10 +450,11 @@ def run_ours(args, world, rank, local):
     kern["dispatch_fp8_gbs"] = gbs(bytes_fp8, mean(fp8_ms))
     kern["dispatch_fp8_input_gbs"] = gbs(bytes_fp8in, mean(fp8in_ms))
     kern["combine_weighted_gbs"] = gbs(bytes_wcomb, mean(wcomb_ms))
+    kern["combine_fp8_gbs"] = gbs(bytes_fcomb, mean(fcomb_ms))
     kern["dispatch_expand_gbs"] = gbs(bytes_expand, mean(xdis_ms))
     kern["combine_expand_gbs"] = gbs(bytes_expand, mean(xcom_ms))
-    for key in ("dispatch", "combine", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted", "dispatch_expand",
-                "combine_expand"):
+    for key in ("dispatch", "combine", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted", "combine_fp8",
+                "dispatch_expand", "combine_expand"):
         kern[f"{key}_frac"] = kern[f"{key}_gbs"] / peak
     dominant = "dispatch" if mean(dis_ms) >= mean(com_ms) else "combine"
     dom_ms = mean(dis_ms) if dominant == "dispatch" else mean(com_ms)

@@ -32,10 +32,16 @@
 // Options (moe_combine_ex): per-row weights turn each add into a single-rounding
 // fused multiply-add (packed fma.rn.f32x2), and the received top-k weights can
 // be reduced back to [T, k] in the same ascending order.
+// E4M3 partial rows (moe_combine_fp8): a slot holds a chunk of codes followed
+// by its per-128 scales (two bulk copies per row); each element is
+// dequantised on its own -- E4M3 -> f16 -> f32 (both exact), times its
+// block's scale (mul.rn) -- and then added in the same ascending order.
 // Every wait is bounded (MOE_ERR_TIMEOUT on expiry).
 #include <algorithm>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "moe_common.cuh"
@@ -52,7 +58,11 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct CombineArgs {
     const uint8_t *partial;
-    int64_t row_bytes;   // H * 2
+    int64_t row_bytes;   // H * 2 (bf16 rows) or H (E4M3 codes)
+    const uint8_t *scales;       // E4M3 rows: fp32 scales [rows, H/128]
+    int64_t scale_row_bytes;     // H / 128 * 4
+    int64_t out_row_bytes;       // H * 2
+    int slot_bytes;              // chunk_bytes, plus chunk_bytes / 32 of scales for E4M3 rows
     int num_rows;
     int T, k;
     const int32_t *dst_row;
@@ -107,6 +117,32 @@ __device__ __forceinline__ uint32_t narrow_bf16x2(uint64_t p) {
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// a + b on each half with scalar add.rn.f32: a packed multiply followed by a
+// packed add can be contracted into a fused multiply-add by the assembler,
+// while a scalar add with an explicit rounding mode is kept separate, so the
+// product is rounded before it is added
+__device__ __forceinline__ uint64_t add_rn_halves(uint64_t a, uint64_t b) {
+    float r0, r1;
+    asm("add.rn.f32 %0, %1, %2;" : "=f"(r0) : "f"(__uint_as_float((uint32_t)a)), "f"(__uint_as_float((uint32_t)b)));
+    asm("add.rn.f32 %0, %1, %2;"
+        : "=f"(r1)
+        : "f"(__uint_as_float((uint32_t)(a >> 32))), "f"(__uint_as_float((uint32_t)(b >> 32))));
+    return pack2(__float_as_uint(r0), __float_as_uint(r1));
+}
+
+// two E4M3 codes (lo byte, hi byte) -> two fp32 {lo, hi}; exact (E4M3 is a subset of f16)
+__device__ __forceinline__ uint64_t widen_e4m3x2(uint32_t b16) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)b16, __NV_E4M3);
+    const float2 f = __half22float2(__half2(h));
+    return pack2(__float_as_uint(f.x), __float_as_uint(f.y));
+}
+
 __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -115,7 +151,7 @@ __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
     return v;
 }
 
-template <bool kWeighted>
+template <bool kWeighted, bool kFP8>
 __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -124,7 +160,7 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
     uint8_t *ring = smem + kHeadBytes;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int consumers = (blockDim.x >> 5) - 1;
-    const int NS = a.num_slots, CH = a.chunk_bytes, nch = a.num_chunks;
+    const int NS = a.num_slots, CH = a.chunk_bytes, SB = a.slot_bytes, nch = a.num_chunks;
 
     // contiguous token range of this CTA
     const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
@@ -194,11 +230,15 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
                 if (kWeighted) entry[e].w[pos] = w_cur;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_expect_tx(&full[e], (uint32_t)D * nbytes);
+            const uint32_t sbytes = kFP8 ? nbytes / 32 : 0u;   // the chunk's scales (4 B per 128 codes)
+            if (lane == 0) mbar_arrive_expect_tx(&full[e], (uint32_t)D * (nbytes + sbytes));
             if (row >= 0) {
                 const int slot = (int)((head + pos) % NS);
-                bulk_load(ring + (size_t)slot * CH, a.partial + (int64_t)row * a.row_bytes + off, nbytes, &full[e],
+                bulk_load(ring + (size_t)slot * SB, a.partial + (int64_t)row * a.row_bytes + off, nbytes, &full[e],
                           pol);
+                if (kFP8)
+                    bulk_load(ring + (size_t)slot * SB + CH, a.scales + (int64_t)row * a.scale_row_bytes + off / 32,
+                              sbytes, &full[e], pol);
             }
             head += D;
         }
@@ -226,59 +266,105 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
         }
         const int D = entry[e].D;
         int slot = entry[e].start;
-        uint64_t acc[kVMax][4];
+        if constexpr (kFP8) {
+            constexpr int kV8 = kVMax / 2;   // 16 codes per 16-byte vector
+            uint64_t acc[kV8][8];
 #pragma unroll
-        for (int v = 0; v < kVMax; ++v)
+            for (int v = 0; v < kV8; ++v)
 #pragma unroll
-            for (int p = 0; p < 4; ++p) acc[v][p] = 0ull;   // +0.0f pairs
-        for (int d = 0; d < D; ++d) {
-            const uint8_t *base = ring + (size_t)slot * CH + soff + lane * 16;
-            uint64_t ww = 0;
-            if (kWeighted) {
-                const uint32_t wb = __float_as_uint(entry[e].w[d]);
-                ww = (uint64_t)wb | ((uint64_t)wb << 32);
+                for (int p = 0; p < 8; ++p) acc[v][p] = 0ull;   // +0.0f pairs
+            for (int d = 0; d < D; ++d) {
+                const uint8_t *sbase = ring + (size_t)slot * SB;
+                const float *sc = reinterpret_cast<const float *>(sbase + CH);
+#pragma unroll
+                for (int v = 0; v < kV8; ++v) {
+                    if (lane + 32 * v < nvec) {
+                        const int pos = soff + lane * 16 + v * 512;   // code index in the chunk
+                        const uint4 qv = lds128(sbase + pos);
+                        const float sf = sc[pos >> 7];
+                        const uint64_t ss = pack2(__float_as_uint(sf), __float_as_uint(sf));
+                        const uint32_t wq[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {   // value = RN(code * scale), then acc = RN(acc + value)
+                            acc[v][2 * i] = add_rn_halves(acc[v][2 * i], mul_f32x2(widen_e4m3x2(wq[i] & 0xffffu), ss));
+                            acc[v][2 * i + 1] = add_rn_halves(acc[v][2 * i + 1], mul_f32x2(widen_e4m3x2(wq[i] >> 16), ss));
+                        }
+                    }
+                }
+                if (++slot == NS) slot = 0;
             }
+            uint8_t *dst = a.out + (int64_t)t * a.out_row_bytes + (off + soff + lane * 16) * 2;
+#pragma unroll
+            for (int v = 0; v < kV8; ++v) {
+                if (lane + 32 * v < nvec) {
+                    uint4 o0, o1;
+                    o0.x = narrow_bf16x2(acc[v][0]);
+                    o0.y = narrow_bf16x2(acc[v][1]);
+                    o0.z = narrow_bf16x2(acc[v][2]);
+                    o0.w = narrow_bf16x2(acc[v][3]);
+                    o1.x = narrow_bf16x2(acc[v][4]);
+                    o1.y = narrow_bf16x2(acc[v][5]);
+                    o1.z = narrow_bf16x2(acc[v][6]);
+                    o1.w = narrow_bf16x2(acc[v][7]);
+                    *reinterpret_cast<uint4 *>(dst + v * 1024) = o0;
+                    *reinterpret_cast<uint4 *>(dst + v * 1024 + 16) = o1;
+                }
+            }
+        } else {
+            uint64_t acc[kVMax][4];
+#pragma unroll
+            for (int v = 0; v < kVMax; ++v)
+#pragma unroll
+                for (int p = 0; p < 4; ++p) acc[v][p] = 0ull;   // +0.0f pairs
+            for (int d = 0; d < D; ++d) {
+                const uint8_t *base = ring + (size_t)slot * SB + soff + lane * 16;
+                uint64_t ww = 0;
+                if (kWeighted) {
+                    const uint32_t wb = __float_as_uint(entry[e].w[d]);
+                    ww = (uint64_t)wb | ((uint64_t)wb << 32);
+                }
+#pragma unroll
+                for (int v = 0; v < kVMax; ++v) {
+                    if (lane + 32 * v < nvec) {
+                        const uint4 qv = lds128(base + v * 512);
+                        if (kWeighted) {   // acc = fma(w, x, acc), one rounding per term
+                            acc[v][0] = fma_f32x2(ww, widen_bf16x2(qv.x), acc[v][0]);
+                            acc[v][1] = fma_f32x2(ww, widen_bf16x2(qv.y), acc[v][1]);
+                            acc[v][2] = fma_f32x2(ww, widen_bf16x2(qv.z), acc[v][2]);
+                            acc[v][3] = fma_f32x2(ww, widen_bf16x2(qv.w), acc[v][3]);
+                        } else {
+                            acc[v][0] = add_f32x2(acc[v][0], widen_bf16x2(qv.x));
+                            acc[v][1] = add_f32x2(acc[v][1], widen_bf16x2(qv.y));
+                            acc[v][2] = add_f32x2(acc[v][2], widen_bf16x2(qv.z));
+                            acc[v][3] = add_f32x2(acc[v][3], widen_bf16x2(qv.w));
+                        }
+                    }
+                }
+                if (++slot == NS) slot = 0;
+            }
+            // received top-k weights back to [T, k]: by the consumer of the first slice of the first chunk
+            if (a.combined_topk_weights != nullptr && c == 0 && sl == 0 && lane < a.k) {
+                float v[MOE_MAX_TOPK];
+#pragma unroll
+                for (int d = 0; d < MOE_MAX_TOPK; ++d)
+                    if (d < D) v[d] = a.recv_topk_weights[(int64_t)entry[e].row[d] * a.k + lane];
+                float cw = 0.0f;
+#pragma unroll
+                for (int d = 0; d < MOE_MAX_TOPK; ++d)
+                    if (d < D) cw += v[d];
+                a.combined_topk_weights[(int64_t)t * a.k + lane] = cw;
+            }
+            uint8_t *dst = a.out + (int64_t)t * a.out_row_bytes + off + soff + lane * 16;
 #pragma unroll
             for (int v = 0; v < kVMax; ++v) {
                 if (lane + 32 * v < nvec) {
-                    const uint4 qv = lds128(base + v * 512);
-                    if (kWeighted) {   // acc = fma(w, x, acc), one rounding per term
-                        acc[v][0] = fma_f32x2(ww, widen_bf16x2(qv.x), acc[v][0]);
-                        acc[v][1] = fma_f32x2(ww, widen_bf16x2(qv.y), acc[v][1]);
-                        acc[v][2] = fma_f32x2(ww, widen_bf16x2(qv.z), acc[v][2]);
-                        acc[v][3] = fma_f32x2(ww, widen_bf16x2(qv.w), acc[v][3]);
-                    } else {
-                        acc[v][0] = add_f32x2(acc[v][0], widen_bf16x2(qv.x));
-                        acc[v][1] = add_f32x2(acc[v][1], widen_bf16x2(qv.y));
-                        acc[v][2] = add_f32x2(acc[v][2], widen_bf16x2(qv.z));
-                        acc[v][3] = add_f32x2(acc[v][3], widen_bf16x2(qv.w));
-                    }
+                    uint4 o;
+                    o.x = narrow_bf16x2(acc[v][0]);
+                    o.y = narrow_bf16x2(acc[v][1]);
+                    o.z = narrow_bf16x2(acc[v][2]);
+                    o.w = narrow_bf16x2(acc[v][3]);
+                    *reinterpret_cast<uint4 *>(dst + v * 512) = o;
                 }
-            }
-            if (++slot == NS) slot = 0;
-        }
-        // received top-k weights back to [T, k]: by the consumer of the first slice of the first chunk
-        if (a.combined_topk_weights != nullptr && c == 0 && sl == 0 && lane < a.k) {
-            float v[MOE_MAX_TOPK];
-#pragma unroll
-            for (int d = 0; d < MOE_MAX_TOPK; ++d)
-                if (d < D) v[d] = a.recv_topk_weights[(int64_t)entry[e].row[d] * a.k + lane];
-            float cw = 0.0f;
-#pragma unroll
-            for (int d = 0; d < MOE_MAX_TOPK; ++d)
-                if (d < D) cw += v[d];
-            a.combined_topk_weights[(int64_t)t * a.k + lane] = cw;
-        }
-        uint8_t *dst = a.out + (int64_t)t * a.row_bytes + off + soff + lane * 16;
-#pragma unroll
-        for (int v = 0; v < kVMax; ++v) {
-            if (lane + 32 * v < nvec) {
-                uint4 o;
-                o.x = narrow_bf16x2(acc[v][0]);
-                o.y = narrow_bf16x2(acc[v][1]);
-                o.z = narrow_bf16x2(acc[v][2]);
-                o.w = narrow_bf16x2(acc[v][3]);
-                *reinterpret_cast<uint4 *>(dst + v * 512) = o;
             }
         }
         fence_proxy_async_smem();
@@ -296,9 +382,13 @@ int launch_combine(const CombineLaunch &L) {
     const Tuning &tu = tuning();
     cudaStream_t st = reinterpret_cast<cudaStream_t>(L.stream);
 
+    const bool fp8 = L.fp8;    // E4M3 rows with per-128 scales
     CombineArgs a;
     a.partial = static_cast<const uint8_t *>(L.partial);
-    a.row_bytes = (int64_t)L.hidden * 2;
+    a.row_bytes = fp8 ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
+    a.scales = reinterpret_cast<const uint8_t *>(L.partial_scales);
+    a.scale_row_bytes = (int64_t)(L.hidden / 128) * 4;
+    a.out_row_bytes = (int64_t)L.hidden * 2;
     a.num_rows = L.num_partial_rows;
     a.T = L.num_tokens;
     a.k = L.num_topk;
@@ -311,30 +401,37 @@ int launch_combine(const CombineLaunch &L) {
     a.l2_hints = tu.l2_hints;
     a.timeout_ns = kDefaultWaitNs;
 
-    // equal chunks no larger than the tuned maximum, small enough that the
-    // ring holds a unit of k rows with room to spare (k + 4 slots)
+    // equal chunks no larger than the tuned maximum (E4M3 rows: of 512 codes, so
+    // that each chunk's scales are whole 16-byte pieces), small enough that
+    // the ring holds a unit of k rows with room to spare (k + 4 slots)
+    const int64_t align = fp8 ? 512 : 16;
     const size_t budget = std::min<size_t>(device_smem_optin(), (size_t)std::max(64 << 10, tu.combine_ring_bytes));
     int64_t nch = (a.row_bytes + tu.combine_chunk - 1) / std::max(16, tu.combine_chunk);
     while (true) {
-        a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, 16);
-        if ((int64_t)(budget - kHeadBytes) / a.chunk_bytes >= (int64_t)a.k + 4 || a.chunk_bytes <= 16) break;
+        a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
+        a.slot_bytes = fp8 ? a.chunk_bytes + a.chunk_bytes / 32 : a.chunk_bytes;
+        if ((int64_t)(budget - kHeadBytes) / a.slot_bytes >= (int64_t)a.k + 4 || a.chunk_bytes <= align) break;
         ++nch;
     }
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
-    a.num_slots = (int)((budget - kHeadBytes) / (size_t)a.chunk_bytes);
+    a.num_slots = (int)((budget - kHeadBytes) / (size_t)a.slot_bytes);
     if (a.num_slots < a.k) return MOE_ERR_INVALID_ARG;   // a unit of k rows must fit in the ring
-    // consumer slices: equal pieces of at most 32 lanes x kVMax x 16 B
-    a.num_slices = (int)((a.chunk_bytes + 32 * kVMax * 16 - 1) / (32 * kVMax * 16));
+    // consumer slices: equal pieces of at most 32 lanes x kVMax x 16 B of bf16
+    // (E4M3: 32 lanes x kVMax / 2 x 16 codes), multiples of 16 B
+    const int slice_max = fp8 ? 32 * (kVMax / 2) * 16 : 32 * kVMax * 16;
+    a.num_slices = (a.chunk_bytes + slice_max - 1) / slice_max;
     a.slice_bytes = (int)round_up((a.chunk_bytes + a.num_slices - 1) / a.num_slices, 16);
-    const size_t smem = kHeadBytes + (size_t)a.num_slots * a.chunk_bytes;
+    const size_t smem = kHeadBytes + (size_t)a.num_slots * a.slot_bytes;
     const bool weighted = a.row_weights != nullptr;
-    const void *fn = weighted ? (const void *)combine_kernel<true> : (const void *)combine_kernel<false>;
+    const void *fn = fp8 ? (const void *)combine_kernel<false, true>
+                         : (weighted ? (const void *)combine_kernel<true, false> : (const void *)combine_kernel<false, false>);
     if (ensure_dynamic_smem(fn, smem) != MOE_OK) return MOE_ERR_CUDA;
 
     const int consumers = std::max(1, std::min(8, tu.combine_warps));
     const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
-    if (weighted) combine_kernel<true><<<grid, (consumers + 1) * 32, smem, st>>>(a);
-    else combine_kernel<false><<<grid, (consumers + 1) * 32, smem, st>>>(a);
+    if (fp8) combine_kernel<false, true><<<grid, (consumers + 1) * 32, smem, st>>>(a);
+    else if (weighted) combine_kernel<true, false><<<grid, (consumers + 1) * 32, smem, st>>>(a);
+    else combine_kernel<false, false><<<grid, (consumers + 1) * 32, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -382,4 +382,36 @@ MOE_API int moe_combine_ex(const void *partial, int num_partial_rows, int num_to
                           recv_topk_weights, combined_topk_weights, out, status, stream);
 }
 
+MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scales, int num_partial_rows,
+                            int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
+                            int32_t *status, void *stream) {
+    const int T = num_tokens, H = hidden;
+    if (T < 0 || num_topk < 1 || num_topk > MOE_MAX_TOPK || num_partial_rows < 0) return MOE_ERR_INVALID_ARG;
+    if (H < 512 || H % 512 != 0 || H > (1 << 24) || (int64_t)T * num_topk >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
+    if (!status) return MOE_ERR_INVALID_ARG;
+    if (T > 0) {
+        if (!token_dst_row || !out || (num_partial_rows > 0 && (!partial_codes || !partial_scales)))
+            return MOE_ERR_INVALID_ARG;
+        if ((partial_codes && !aligned(partial_codes, 16)) || (partial_scales && !aligned(partial_scales, 16)) ||
+            !aligned(out, 16) || !aligned(token_dst_row, 4) || !aligned(status, 4))
+            return MOE_ERR_MISALIGNED;
+    }
+    moe::CombineLaunch L;
+    L.partial = partial_codes;
+    L.fp8 = true;
+    L.partial_scales = partial_scales;
+    L.num_partial_rows = num_partial_rows;
+    L.num_tokens = T;
+    L.hidden = H;
+    L.num_topk = num_topk;
+    L.token_dst_row = token_dst_row;
+    L.row_weights = nullptr;
+    L.recv_topk_weights = nullptr;
+    L.combined_topk_weights = nullptr;
+    L.out = out;
+    L.status = status;
+    L.stream = stream;
+    return moe::launch_combine(L);
+}
+
 }  // extern "C"

@@ -85,7 +85,9 @@ int launch_dispatch(const DispatchLaunch &L);
 int launch_layout_dispatch(const LayoutLaunch &Ll, const DispatchLaunch &L);
 
 struct CombineLaunch {
-    const void *partial;
+    const void *partial;                     // bf16 rows, or E4M3 codes (fp8)
+    bool fp8 = false;                        // E4M3 rows with per-128 scales
+    const float *partial_scales = nullptr;   // E4M3 rows: fp32 scales [rows, H/128]
     int num_partial_rows, num_tokens, hidden, num_topk;
     const int32_t *token_dst_row;
     const float *row_weights;          // optional

@@ -293,6 +293,28 @@ MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_token
                         int num_topk, const int32_t *token_dst_row, void *out, int32_t *status,
                         void *stream);
 
+/*
+ * moe_combine_fp8 -- moe_combine for partial rows held as E4M3 codes with one
+ * fp32 scale per 128 channels (the layout MOE_DISPATCH_QUANTIZE_FP8 writes).
+ *
+ * Pages: the FP8 path of the intra/inter-node page carries x_scales next to
+ * the hidden bytes; the combine reduces the partial rows as moe_combine does.
+ * Each element is dequantised on its own, v = RN(value(code) * scale) in fp32
+ * (no fused multiply-add), and the token's values are summed as in
+ * moe_combine: ascending row, fp32 from +0.0f, one RNE cast to bf16.
+ *
+ *   partial_codes   [num_partial_rows, H] uint8 E4M3, device, 16-byte aligned.
+ *   partial_scales  [num_partial_rows, H/128] fp32, device, 16-byte aligned.
+ *   token_dst_row   [T, k] int32 (either row map); rows >= num_partial_rows
+ *                   raise MOE_ERR_CAPACITY and are skipped.
+ *   out             [T, H] bf16, device, 16-byte aligned.
+ * Limits: H % 512 == 0 (so that a row's scales are whole 16-byte pieces),
+ * H <= 2^24, 1 <= k <= 32.
+ */
+MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scales, int num_partial_rows,
+                            int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
+                            int32_t *status, void *stream);
+
 /* Size of the library's own layout scratch (bytes), used by moe_get_layout_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
 

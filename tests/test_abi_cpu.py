@@ -162,3 +162,17 @@ def _layout_dispatch(lib, x=A, T=128, H=256, topk=A + 0x10000, k=2, E=16, R=4, w
 ])
 def test_layout_dispatch_rejects_bad_arguments(lib, kw, code):
     assert _layout_dispatch(lib, **kw) == code
+
+
+def _combine_fp8(lib, codes=A, scales=A + 0x80000, rows=256, T=128, H=1024, k=2, dst=A + 0x10000, out=A + 0x100000,
+                 status=A + 0x200000):
+    return lib.LIB.moe_combine_fp8(codes, scales, rows, T, H, k, dst, out, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=256), 1), (dict(H=640), 1), (dict(k=0), 1), (dict(rows=-1), 1), (dict(scales=None), 1),
+    (dict(codes=None), 1), (dict(out=None), 1), (dict(status=None), 1), (dict(scales=A + 4), 2),
+    (dict(codes=A + 8), 2), (dict(out=A + 8), 2),
+])
+def test_combine_fp8_rejects_bad_arguments(lib, kw, code):
+    assert _combine_fp8(lib, **kw) == code

@@ -450,3 +450,66 @@ def test_dispatch_then_combine_identity_expert(moe):
     assert torch.equal(y2.view(torch.int16), (x * D[:, None]).to(torch.bfloat16).view(torch.int16))
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+
+
+# ------------------------------------------------------------------ combine of E4M3 partial rows
+
+def _fp8_rows(seed, rows, H):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 256, (rows, H), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x38          # no NaN codes
+    scales = (rng.standard_normal((rows, H // 128)) * 2.0 ** rng.integers(-6, 6, (rows, H // 128))).astype(np.float32)
+    return codes, scales
+
+
+def check_combine_fp8(moe, topk, E, R, H, seed):
+    topk_d = topk.to(DEV)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk_d, E, R, status=status)
+    rows = wl.recv_capacity(topk.shape[0], topk.shape[1], R)
+    codes, scales = _fp8_rows(seed, max(rows, 1), H)
+    out = moe.moe_combine_fp8(torch.from_numpy(codes).to(DEV), torch.from_numpy(scales).to(DEV), lay.token_dst_row,
+                              status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref_lay = oracle.layout(topk.numpy(), E, R)
+    ref, flags = oracle.combine_fp8(codes, scales, ref_lay["token_dst_row"])
+    assert flags == 0
+    got = bits16(out)
+    g32 = (got.astype(np.uint32) << 16).view(np.float32)
+    r32 = (ref.astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_allclose(g32, r32, rtol=1e-2, atol=1e-3)
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("name", ["dsv3", "skewed", "decode"])
+def test_combine_fp8_parity_configs(moe, name):
+    w = wl.CONFIGS[name]
+    check_combine_fp8(moe, topk_for(w), w.num_experts, w.num_ranks, w.hidden, 23)
+
+
+@pytest.mark.parametrize("T,H,k,E,R", [(1, 512, 2, 16, 4), (33, 7168, 8, 256, 8), (129, 1024, 8, 256, 256),
+                                       (1000, 1536, 6, 48, 3), (300, 4096, 32, 64, 8), (64, 16384, 8, 256, 8)])
+def test_combine_fp8_parity_shapes(moe, T, H, k, E, R):
+    g = torch.Generator().manual_seed(3 * T + H)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
+    check_combine_fp8(moe, topk, E, R, H, T + k)
+
+
+def test_fp8_dispatch_then_fp8_combine(moe):
+    # identity experts on FP8 rows: the GPU result equals the oracle's combine of the oracle's dispatch
+    w = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(w, with_partial=False, num_tokens=1024)
+    lay, out, st = run_dispatch(moe, inp, w.num_experts, w.num_ranks, True)
+    assert st == 0
+    N = int(lay.rank_prefix[-1].item())
+    status = moe.new_status(DEV)
+    y = moe.moe_combine_fp8(out.recv_x[:N].contiguous(), out.recv_x_scales[:N].contiguous(), lay.token_dst_row,
+                            status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    topk = inp.topk_idx.numpy()
+    ref_lay = oracle.layout(topk, w.num_experts, w.num_ranks)
+    d = oracle.dispatch(bits16(inp.x), topk, None, w.num_experts, w.num_ranks, ref_lay["token_dst_row"], N, fp8=True)
+    ref, _ = oracle.combine_fp8(d["recv_x"], d["recv_x_scales"], ref_lay["token_dst_row"])
+    np.testing.assert_array_equal(bits16(y), ref)
