@@ -801,13 +801,17 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     a.num_units = (int64_t)num_tokens * a.num_chunks;
     a.stages = std::min(kMaxStages, std::max(3, tu.dispatch_stages));   // the unit ring needs three
-
-    int64_t per_warp = kBarBytes + (int64_t)a.stages * a.chunk_bytes;
-    if (fp8) per_warp += (int64_t)a.stages * (a.chunk_bytes / 2) + round_up((int64_t)a.stages * (a.chunk_bytes / 256) * 4, 128);
-    per_warp = round_up(per_warp, 128);
+    const int64_t room = (int64_t)device_smem_optin() - (int64_t)round_up((int64_t)extra, 128);
+    auto warp_bytes = [&](int stages) {
+        int64_t b = kBarBytes + (int64_t)stages * a.chunk_bytes;
+        if (fp8) b += (int64_t)stages * (a.chunk_bytes / 2) + round_up((int64_t)stages * (a.chunk_bytes / 256) * 4, 128);
+        return round_up(b, 128);
+    };
+    // fewer stages (down to three) before fewer warps than requested
+    while (a.stages > 3 && room / warp_bytes(a.stages) < tu.dispatch_warps) --a.stages;
+    const int64_t per_warp = warp_bytes(a.stages);
     a.warp_smem = (int)per_warp;
     // as many of the requested warps as fit in one CTA's shared memory
-    const int64_t room = (int64_t)device_smem_optin() - (int64_t)round_up((int64_t)extra, 128);
     const int fit = (int)std::min<int64_t>(16, room / per_warp);
     if (fit < 1) return MOE_ERR_INVALID_ARG;
     warps = std::max(1, std::min(fit, tu.dispatch_warps));

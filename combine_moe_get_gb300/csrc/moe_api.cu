@@ -102,8 +102,8 @@ const Tuning &tuning() {
     static const Tuning t = [] {
         Tuning x;
         x.dispatch_warps = env_int("MOE_TUNE_DISPATCH_WARPS", 8);
-        x.dispatch_stages = env_int("MOE_TUNE_DISPATCH_STAGES", 3);
-        x.dispatch_chunk = env_int("MOE_TUNE_DISPATCH_CHUNK", 8192);
+        x.dispatch_stages = env_int("MOE_TUNE_DISPATCH_STAGES", 4);
+        x.dispatch_chunk = env_int("MOE_TUNE_DISPATCH_CHUNK", 16384);
         x.combine_warps = env_int("MOE_TUNE_COMBINE_WARPS", 8);
         x.combine_chunk = env_int("MOE_TUNE_COMBINE_CHUNK", 8192);
         x.combine_ring_bytes = env_int("MOE_TUNE_COMBINE_RING_BYTES", 224 << 10);
