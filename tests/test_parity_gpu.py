@@ -122,6 +122,19 @@ def test_layout_deterministic_and_reuses_workspace(moe):
         assert_layout_equal(o, outs[0])
 
 
+@pytest.mark.parametrize("T", [65536, 1 << 20])
+def test_layout_lookback_modes_report_timeout(moe, T):
+    # 512 tiles (too many for the direct sweep: cooperative lookback) and 8192 tiles (more than fit on the GPU:
+    # ticket lookback); one tile never publishes, the bounded waits expire, the context stays usable
+    k, E, R = 8, 256, 8
+    topk = wl.make_topk_uniform(torch.Generator().manual_seed(T % 997), T, E, k)
+    _, _, st = gpu_layout(moe, topk, E, R, wait_timeout_ns=20_000_000, test_unpublished_tile=3)
+    assert st == moe.MOE_ERR_TIMEOUT
+    _, got, st = gpu_layout(moe, topk, E, R)
+    assert st == 0
+    assert_layout_equal(got, oracle.layout(topk.numpy(), E, R))
+
+
 def test_layout_bounded_wait_reports_timeout(moe):
     # one tile never publishes its scan status: the tiles after it give up after
     # the bounded wait and report MOE_ERR_TIMEOUT; the context stays usable
@@ -308,6 +321,17 @@ def test_dispatch_fp8_input_parity_shapes(moe, T, H, k, E, R):
     g = torch.Generator().manual_seed(T + H)
     topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
     check_dispatch_fp8_input(moe, topk, E, R, H, T, weights=(T % 2 == 1))
+
+
+@pytest.mark.parametrize("T,H", [(4096, 1024), (8192, 512), (3000, 384)])
+def test_dispatch_fp8_many_rows_per_cta_small_rows(moe, T, H):
+    # one slice per row and tens of rows per CTA: workers claim items several input-ring slots ahead
+    # of the producer, so every wait must first see the row's load armed
+    g = torch.Generator().manual_seed(T + H)
+    E, R, k = 64, 8, 8
+    topk = wl.make_topk_uniform(g, T, E, k)
+    inp = wl.Inputs(None, wl.make_x(g, T, H), topk, wl.make_weights(g, T, k), None)
+    check_dispatch(moe, inp, E, R, True)
 
 
 def test_dispatch_capacity_overflow_writes_nothing_beyond(moe):
