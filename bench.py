@@ -35,6 +35,7 @@ import torch  # noqa: E402
 from combine_moe_get_gb300 import workloads as wl  # noqa: E402
 
 WORKLOAD = "dsv3"
+HBM_SPEC_GBS = 7900.0   # nominal HBM3e bandwidth of a GB300, for context next to the measured peak
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of peak), DSv3 shape"
 FALLBACK_HBM_GBS = 6800.0
 
@@ -428,8 +429,14 @@ def run_ours(args, world, rank, local):
     bytes_wcomb = bytes_bf16 + N * 4                    # + one weight per receive row
     bytes_expand = T * row + NX * row                   # x read once + one row per valid entry
     bytes_fcomb = N * (H + (H // 128) * 4) + T * row    # e4m3 rows + scales read, bf16 out written
+    med = statistics.median
     kern = {
         "layout_us": mean(lay_ms) * 1e3,
+        "layout_median_us": med(lay_ms) * 1e3,
+        "dispatch_median_us": med(dis_ms) * 1e3,
+        "combine_median_us": med(com_ms) * 1e3,
+        # dispatch + combine alone, T / (t_dispatch + t_combine)
+        "dispatch_combine_tokens_per_s": T / ((mean(dis_ms) + mean(com_ms)) * 1e-3),
         "dispatch_us": mean(dis_ms) * 1e3,
         "combine_us": mean(com_ms) * 1e3,
         "dispatch_fp8_us": mean(fp8_ms) * 1e3,
@@ -456,6 +463,7 @@ def run_ours(args, world, rank, local):
     for key in ("dispatch", "combine", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted", "combine_fp8",
                 "dispatch_expand", "combine_expand"):
         kern[f"{key}_frac"] = kern[f"{key}_gbs"] / peak
+        kern[f"{key}_frac_of_spec"] = kern[f"{key}_gbs"] / HBM_SPEC_GBS
     dominant = "dispatch" if mean(dis_ms) >= mean(com_ms) else "combine"
     dom_ms = mean(dis_ms) if dominant == "dispatch" else mean(com_ms)
     achieved = gbs(bytes_bf16, dom_ms)
@@ -474,7 +482,8 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world} (independent token shards, no collective)"},
         "roofline": {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes": bytes_bf16},
+                     "algorithmic_bytes": bytes_bf16, "spec_peak": HBM_SPEC_GBS,
+                     "frac_of_spec": achieved / HBM_SPEC_GBS},
         "kernels": kern,
         "gpu_launches": 3 * args.steps,   # per step: the cooperative layout kernel, dispatch, combine
         "clocks": clocks,
