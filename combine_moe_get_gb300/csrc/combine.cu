@@ -183,20 +183,35 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
         int64_t head = 0, tail = 0, oldest = 0;
         int row = -1, pos = 0, D = 0;
         float w_cur = 1.0f;
-        int row_next = (lane < a.k) ? a.dst_row[(int64_t)t_begin * a.k + lane] : -1;
+        // the next kPre tokens' receive rows, loaded ahead (lanes < k), so that the
+        // row lists' load latency does not stall the issue of bulk loads
+        constexpr int kPre = 8;
+        int rq[kPre];
+#pragma unroll
+        for (int i = 0; i < kPre; ++i) {
+            const int tt = t_begin + i;
+            rq[i] = (tt < t_end && lane < a.k) ? a.dst_row[(int64_t)tt * a.k + lane] : -1;
+        }
+        // weighted: the weight of each row of the next token, loaded one token ahead
+        float w_next = (kWeighted && rq[0] >= 0 && rq[0] < a.num_rows) ? a.row_weights[rq[0]] : 1.0f;
         for (int64_t j = 0; j < n_units; ++j) {
             const int tl = (int)(j / nch), c = (int)(j - (int64_t)tl * nch);
             const int t = t_begin + tl;
             const int64_t off = (int64_t)c * CH;
             const uint32_t nbytes = (uint32_t)min((int64_t)CH, a.row_bytes - off);
             if (c == 0) {
-                row = row_next;
-                if (t + 1 < t_end && lane < a.k) row_next = a.dst_row[(int64_t)(t + 1) * a.k + lane];
+                row = rq[0];
+#pragma unroll
+                for (int i = 0; i < kPre - 1; ++i) rq[i] = rq[i + 1];
+                rq[kPre - 1] = (t + kPre < t_end && lane < a.k) ? a.dst_row[(int64_t)(t + kPre) * a.k + lane] : -1;
                 if (row >= a.num_rows) {
                     report(a.status, MOE_ERR_CAPACITY);
                     row = -1;
                 }
-                if (kWeighted && row >= 0) w_cur = a.row_weights[row];   // used after the wait for slots
+                if (kWeighted) {
+                    w_cur = w_next;
+                    w_next = (rq[0] >= 0 && rq[0] < a.num_rows) ? a.row_weights[rq[0]] : 1.0f;
+                }
                 const unsigned vmask = __ballot_sync(kFull, row >= 0);
                 D = __popc(vmask);
                 pos = 0;
