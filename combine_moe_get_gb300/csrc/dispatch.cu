@@ -647,12 +647,22 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
         return __shfl_sync(kFull, q, 0);
     };
     // destination rows of an item's token, lanes < k
-    auto fetch_rows = [&](int q) -> int {
-        const int t = t_begin + q / nsl;
+    // and, for the item of slice 0, the token's routing (written as the rows' metadata)
+    auto fetch_rows = [&](int q, int64_t &e, float &w) -> int {
+        const int jq = q / nsl;
+        const int t = t_begin + jq;
+        e = -1;
+        w = 0.0f;
+        if (q < n_items && lane < a.k && q - jq * nsl == 0) {
+            e = a.topk[(int64_t)t * a.k + lane];
+            if (a.topk_w) w = a.topk_w[(int64_t)t * a.k + lane];
+        }
         return (q < n_items && lane < a.k) ? a.dst_row[(int64_t)t * a.k + lane] : -1;
     };
     int q = claim();
-    int row_next = fetch_rows(q);
+    int64_t e_next;
+    float w_next;
+    int row_next = fetch_rows(q, e_next, w_next);
     while (q < n_items) {
         const int q_next = claim();
         const int j = q / nsl;
@@ -660,7 +670,9 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
         const int t = t_begin + j;
         const int si = j % NI;
         int row = row_next;
-        row_next = fetch_rows(q_next);
+        const int64_t e_cur = e_next;
+        const float w_cur = w_next;
+        row_next = fetch_rows(q_next, e_next, w_next);
         if (row >= a.capacity) {
             if (sl == 0) report(a.status, MOE_ERR_CAPACITY);
             row = -1;
@@ -723,14 +735,10 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
         // row metadata, written by the worker of slice 0
         if (sl == 0) {
             int rl = -1, el = 0;
-            float wgt = 0.0f;
-            if (lane < a.k) {
-                const int64_t e = a.topk[(int64_t)t * a.k + lane];
-                if (e >= 0 && e < a.E) {
-                    rl = (int)e / a.m;
-                    el = (int)e - rl * a.m;
-                }
-                if (a.topk_w) wgt = a.topk_w[(int64_t)t * a.k + lane];
+            const float wgt = w_cur;
+            if (lane < a.k && e_cur >= 0 && e_cur < a.E) {
+                rl = (int)e_cur / a.m;
+                el = (int)e_cur - rl * a.m;
             }
             for (unsigned mm = dmask; mm; mm &= mm - 1) {
                 const int jd = __ffs(mm) - 1;
@@ -801,7 +809,10 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     a.num_units = (int64_t)num_tokens * a.num_chunks;
     a.stages = std::min(kMaxStages, std::max(3, tu.dispatch_stages));   // the unit ring needs three
-    const int64_t room = (int64_t)device_smem_optin() - (int64_t)round_up((int64_t)extra, 128);
+    // stages take at most ~200 KB, so that some L1 cache is left (a full 227 KB of
+    // stages measured slower)
+    const int64_t room = std::min<int64_t>((int64_t)device_smem_optin(), (int64_t)tu.dispatch_smem) -
+                         (int64_t)round_up((int64_t)extra, 128);
     auto warp_bytes = [&](int stages) {
         int64_t b = kBarBytes + (int64_t)stages * a.chunk_bytes;
         if (fp8) b += (int64_t)stages * (a.chunk_bytes / 2) + round_up((int64_t)stages * (a.chunk_bytes / 256) * 4, 128);

@@ -104,11 +104,12 @@ const Tuning &tuning() {
         x.dispatch_warps = env_int("MOE_TUNE_DISPATCH_WARPS", 8);
         x.dispatch_stages = env_int("MOE_TUNE_DISPATCH_STAGES", 4);
         x.dispatch_chunk = env_int("MOE_TUNE_DISPATCH_CHUNK", 16384);
+        x.dispatch_smem = env_int("MOE_TUNE_DISPATCH_SMEM", 200 << 10);
         x.combine_warps = env_int("MOE_TUNE_COMBINE_WARPS", 8);
         x.combine_chunk = env_int("MOE_TUNE_COMBINE_CHUNK", 8192);
         x.combine_ring_bytes = env_int("MOE_TUNE_COMBINE_RING_BYTES", 224 << 10);
         x.fp8_rows = env_int("MOE_TUNE_FP8_ROWS", 1) == 1;
-        x.fp8_in_slots = env_int("MOE_TUNE_FP8_IN_SLOTS", 6);
+        x.fp8_in_slots = env_int("MOE_TUNE_FP8_IN_SLOTS", 8);
         x.fp8_quant_warps = env_int("MOE_TUNE_FP8_QUANT_WARPS", 24);
         x.ctas_per_sm = env_int("MOE_TUNE_CTAS_PER_SM", 0);
         x.l2_hints = env_int("MOE_TUNE_L2_HINTS", 1) & 3;

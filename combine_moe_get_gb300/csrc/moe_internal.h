@@ -22,6 +22,7 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 // Tuning knobs, read once from MOE_TUNE_* environment variables (0 = default).
 struct Tuning {
     int dispatch_warps, dispatch_stages, dispatch_chunk;
+    int dispatch_smem;                                       // shared-memory budget of a chunked dispatch CTA
     int combine_warps, combine_chunk, combine_ring_bytes;   // consumer warps, max chunk, ring budget
     int fp8_rows, fp8_in_slots, fp8_quant_warps;   // FP8 row pipeline: on/off, input ring slots, worker warps
     int ctas_per_sm;
