@@ -498,14 +498,32 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
             rl = (int)e / a.m;
             el = (int)e - rl * a.m;
         }
+        // E4M3 input: the token's scales, read once (up to 4 per lane, nb <= 128) for every destination
+        constexpr int kInScales = 4;
+        float isc[kInScales];
+        const bool in_sc = a.in_scales != nullptr && c == 0 && a.nb <= 32 * kInScales;
+        if (in_sc) {
+#pragma unroll
+            for (int i = 0; i < kInScales; ++i) {
+                const int b = lane + 32 * i;
+                isc[i] = b < a.nb ? a.in_scales[t * a.nb + b] : 0.0f;
+            }
+        }
         for (unsigned mm = dmask; mm; mm &= mm - 1) {
             const int jd = __ffs(mm) - 1;
             const int rowd = __shfl_sync(kFull, row, jd);
             if constexpr (kFP8) {
                 for (int b = lane; b < nblk; b += 32) a.recv_scales[(int64_t)rowd * a.nb + c * cpb + b] = sc[b];
             }
-            if (a.in_scales != nullptr && c == 0)
+            if (in_sc) {
+#pragma unroll
+                for (int i = 0; i < kInScales; ++i) {
+                    const int b = lane + 32 * i;
+                    if (b < a.nb) a.recv_scales[(int64_t)rowd * a.nb + b] = isc[i];
+                }
+            } else if (a.in_scales != nullptr && c == 0) {
                 for (int b = lane; b < a.nb; b += 32) a.recv_scales[(int64_t)rowd * a.nb + b] = a.in_scales[t * a.nb + b];
+            }
             if (c == 0) {
                 const int rd = __shfl_sync(kFull, rl, jd);
                 if (lane < a.k) {
