@@ -151,8 +151,10 @@ __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
     return v;
 }
 
+// E4M3 rows cost more instructions per byte (dequantisation), so that variant
+// runs more consumer warps.
 template <bool kWeighted, bool kFP8>
-__global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(const CombineArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kUnits;
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(32 * 9, 1) combine_kernel(const CombineArgs a)
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (n_units == 0) return;
 
     if (warp == 0) {
@@ -442,12 +446,13 @@ int launch_combine(const CombineLaunch &L) {
                          : (weighted ? (const void *)combine_kernel<true, false> : (const void *)combine_kernel<false, false>);
     if (ensure_dynamic_smem(fn, smem) != MOE_OK) return MOE_ERR_CUDA;
 
-    const int consumers = std::max(1, std::min(8, tu.combine_warps));
+    const int consumers = fp8 ? std::max(1, std::min(12, tu.combine_fp8_warps)) : std::max(1, std::min(8, tu.combine_warps));
     const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
-    if (fp8) combine_kernel<false, true><<<grid, (consumers + 1) * 32, smem, st>>>(a);
-    else if (weighted) combine_kernel<true, false><<<grid, (consumers + 1) * 32, smem, st>>>(a);
-    else combine_kernel<false, false><<<grid, (consumers + 1) * 32, smem, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    void (*kernel)(const CombineArgs) =
+        fp8 ? combine_kernel<false, true> : (weighted ? combine_kernel<true, false> : combine_kernel<false, false>);
+    return launch_kernel(kernel, dim3(grid), dim3((consumers + 1) * 32), smem, st, tu.overlap != 0, a) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

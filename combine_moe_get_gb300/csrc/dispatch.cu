@@ -354,6 +354,8 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
     __shared__ int s_next_unit;
     if (threadIdx.x == 0) s_next_unit = 0;
     __syncthreads();
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t G = gridDim.x;
     const int64_t cta_units = a.num_units > (int64_t)blockIdx.x ? (a.num_units - 1 - blockIdx.x) / G + 1 : 0;
     int64_t *ring = reinterpret_cast<int64_t *>(wbase + 64);   // unit of each stage (after the <= 8 barriers)
@@ -631,6 +633,8 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
         s_rows_issued = 0;
     }
     __syncthreads();
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (n <= 0) return;
 
     if (warp == 0) {
@@ -862,8 +866,10 @@ template <bool kFP8, bool kFused>
 int launch_chunked(const DispatchArgs &a, int warps, size_t smem, int grid, cudaStream_t st) {
     const void *fn = (const void *)dispatch_kernel<kFP8, kFused>;
     if (ensure_dynamic_smem(fn, smem) != MOE_OK) return MOE_ERR_CUDA;
-    dispatch_kernel<kFP8, kFused><<<grid, warps * 32, smem, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_kernel(dispatch_kernel<kFP8, kFused>, dim3(grid), dim3(warps * 32), smem, st, tuning().overlap != 0,
+                         a) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 }  // namespace
@@ -910,8 +916,10 @@ int launch_dispatch(const DispatchLaunch &L) {
             }
             const int workers = std::max(1, std::min({24, tu.fp8_quant_warps, max_threads[dev] / 32 - 1}));
             const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
-            dispatch_fp8_rows_kernel<<<grid, (workers + 1) * 32, smem, st>>>(f);
-            return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+            return launch_kernel(dispatch_fp8_rows_kernel, dim3(grid), dim3((workers + 1) * 32), smem, st,
+                                 tu.overlap != 0, f) == cudaSuccess
+                       ? MOE_OK
+                       : MOE_ERR_CUDA;
         }
         // rows too large for the ring: fall through to the chunked kernel
     }

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kXThreads) layout_expand_kernel(const ExpandAr
     uint32_t *ticket = reinterpret_cast<uint32_t *>(a.ws);
     uint64_t *tile_status = reinterpret_cast<uint64_t *>(a.ws + kHeaderBytes);
 
+    grid_dependency_wait();
     if (threadIdx.x == 0) s_tile = (int)atomicAdd(ticket, 1u);
     for (int i = threadIdx.x; i < kXWarps * E / 2; i += kXThreads) reinterpret_cast<uint32_t *>(cnt)[i] = 0u;
     __syncthreads();
@@ -231,8 +232,10 @@ int launch_expand_layout(const ExpandLaunch &L) {
     const size_t smem = xsmem(E, k).total;
     if (smem > device_smem_optin()) return MOE_ERR_INVALID_ARG;
     if (ensure_dynamic_smem((const void *)layout_expand_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
-    layout_expand_kernel<<<a.num_tiles, kXThreads, smem, s>>>(a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_kernel(layout_expand_kernel, dim3(a.num_tiles), dim3(kXThreads), smem, s, tuning().overlap != 0, a) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

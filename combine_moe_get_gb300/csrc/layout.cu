@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
     WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
     int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
     uint64_t *tile_status = reinterpret_cast<uint64_t *>(a.ws + a.status_off);
+    grid_dependency_wait();
 
     if (threadIdx.x == 0) s_tile = kCooperative ? (int)blockIdx.x : (int)atomicAdd(&hdr->ticket, 1u);
     for (int i = threadIdx.x; i < R * kWords; i += kThreads) bitmap[i] = 0u;
@@ -487,6 +488,7 @@ __global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
     const int n_ent = tcount * k;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool publish = tile != a.unpublished_tile;
+    grid_dependency_wait();
 
     for (int i = threadIdx.x; i < R * kWords; i += kThreads) bitmap[i] = 0u;
     for (int i = threadIdx.x; i < E; i += kThreads) hist[i] = 0;
@@ -630,6 +632,7 @@ __global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
 
 __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, int m,
                                    const int32_t *__restrict__ rank_prefix, int32_t *__restrict__ token_dst_row) {
+    grid_dependency_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t v = token_dst_row[i];
         if (v >= 0) token_dst_row[i] = v + rank_prefix[(int)topk[i] / m];
@@ -729,20 +732,24 @@ int launch_layout(const LayoutLaunch &L) {
 
     if (direct_sizes(T, R) && a.num_tiles <= cooperative_capacity(direct, dsmem)) {
         if (a.num_tiles == 1) {     // nothing to exchange: an ordinary launch
-            layout_direct_kernel<<<1, kThreads, dsmem, s>>>(a);
-            return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+            return launch_kernel(layout_direct_kernel, dim3(1), dim3(kThreads), dsmem, s, tuning().overlap != 0, a) ==
+                           cudaSuccess
+                       ? MOE_OK
+                       : MOE_ERR_CUDA;
         }
         return launch_cooperative(direct, a.num_tiles, dsmem, s, a);
     }
     if (a.num_tiles <= cooperative_capacity(coop, smem)) return launch_cooperative(coop, a.num_tiles, smem, s, a);
 
-    layout_tiles_kernel<false><<<a.num_tiles, kThreads, smem, s>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_kernel(layout_tiles_kernel<false>, dim3(a.num_tiles), dim3(kThreads), smem, s, tuning().overlap != 0, a) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
     const int64_t n = (int64_t)T * k;
     const int threads = 256;
     const int blocks = (int)std::min<int64_t>((n + threads - 1) / threads, (int64_t)device_sm_count() * 8);
-    layout_rows_kernel<<<blocks, threads, 0, s>>>(L.topk_idx, n, a.m, o.rank_prefix, o.token_dst_row);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_kernel(layout_rows_kernel, dim3(blocks), dim3(threads), 0, s, tuning().overlap != 0, L.topk_idx, n, a.m,
+                      (const int32_t *)o.rank_prefix, o.token_dst_row) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
 

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "../../include/moe_get.h"
@@ -13,6 +14,46 @@ namespace moe {
 
 // Default bound on any spin or barrier wait inside a kernel.
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s
+
+// ------------------------------------------------------------------ launch overlap
+//
+// Programmatic dependent launch (PTX griddepcontrol, sm_90+). A grid launched
+// with programmatic stream serialization may be scheduled while the grid
+// before it on the stream is still running. Every kernel here calls
+// grid_dependency_wait() before its first global memory access, read or
+// write: it returns once the previous grid has completed and its writes are
+// visible, so reads see the producer's results and writes cannot overtake
+// the previous grid's reads. grid_launch_dependents() then lets the next
+// grid's CTAs be placed as this grid's CTAs retire, so that its launch and
+// prologue (barrier set-up) overlap this grid's tail. Only the dispatch and
+// combine kernels call it: a layout kernel leaves the trigger to its exit,
+// because dispatch CTAs placed beside a running layout and waiting there
+// slowed the layout down. In a grid launched without the attribute both are
+// no-ops.
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel`, allowed to overlap the previous grid on the stream when
+// `overlap` is set (cudaLaunchAttributeProgrammaticStreamSerialization).
+template <typename... Params, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 bool overlap, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------------ status
 

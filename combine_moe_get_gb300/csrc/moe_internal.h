@@ -24,11 +24,13 @@ struct Tuning {
     int dispatch_warps, dispatch_stages, dispatch_chunk;
     int dispatch_smem;                                       // shared-memory budget of a chunked dispatch CTA
     int combine_warps, combine_chunk, combine_ring_bytes;   // consumer warps, max chunk, ring budget
+    int combine_fp8_warps;                                   // consumer warps for E4M3 partial rows
     int fp8_rows, fp8_in_slots, fp8_quant_warps;   // FP8 row pipeline: on/off, input ring slots, worker warps
     int ctas_per_sm;
     int l2_hints;  // bit 0: evict-first on single-use loads; bit 1: evict-first on stores
     int spread_small;   // small batches: fewer dispatch warps per CTA, more CTAs
     int fused_small;    // moe_layout_dispatch: one fused launch for small batches
+    int overlap;        // programmatic dependent launch of every non-cooperative kernel
 };
 const Tuning &tuning();
 
