@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
         // ------------------------------------------------------------ producer
         const uint64_t pol = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
         int64_t head = 0, tail = 0, oldest = 0;
+        int head_slot = 0;   // head % NS, kept without 64-bit division
         int row = -1, pos = 0, D = 0;
         float w_cur = 1.0f;
         // the next kPre tokens' receive rows, loaded ahead (lanes < k), so that the
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
         // weighted: the weight of each row of the next token, loaded one token ahead
         float w_next = (kWeighted && rq[0] >= 0 && rq[0] < a.num_rows) ? a.row_weights[rq[0]] : 1.0f;
         for (int64_t j = 0; j < n_units; ++j) {
-            const int tl = (int)(j / nch), c = (int)(j - (int64_t)tl * nch);
+            const int tl = (int)div_count(j, nch), c = (int)(j - (int64_t)tl * nch);
             const int t = t_begin + tl;
             const int64_t off = (int64_t)c * CH;
             const uint32_t nbytes = (uint32_t)min((int64_t)CH, a.row_bytes - off);
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             __syncwarp();   // every lane has read entry[eo] before lane 0 rewrites an entry
             if (lane == 0) {
                 entry[e].D = D;
-                entry[e].start = (int)(head % NS);
+                entry[e].start = head_slot;
             }
             if (row >= 0) {
                 entry[e].row[pos] = row;
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             const uint32_t sbytes = kFP8 ? nbytes / 32 : 0u;   // the chunk's scales (4 B per 128 codes)
             if (lane == 0) mbar_arrive_expect_tx(&full[e], (uint32_t)D * (nbytes + sbytes));
             if (row >= 0) {
-                const int slot = (int)((head + pos) % NS);
+                const int slot = head_slot + pos < NS ? head_slot + pos : head_slot + pos - NS;
                 bulk_load(ring + (size_t)slot * SB, a.partial + (int64_t)row * a.row_bytes + off, nbytes, &full[e],
                           pol);
                 if (kFP8)
@@ -260,6 +261,8 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
                               sbytes, &full[e], pol);
             }
             head += D;
+            head_slot += D;
+            if (head_slot >= NS) head_slot -= NS;
         }
         return;
     }
@@ -269,9 +272,9 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
     const int nsl = a.num_slices, SL = a.slice_bytes;
     const int64_t n_items = n_units * nsl;
     for (int64_t q = cw; q < n_items; q += consumers) {
-        const int64_t j = q / nsl;
+        const int64_t j = div_count(q, nsl);
         const int sl = (int)(q - j * nsl);
-        const int tl = (int)(j / nch), c = (int)(j - (int64_t)tl * nch);
+        const int tl = (int)div_count(j, nch), c = (int)(j - (int64_t)tl * nch);
         const int t = t_begin + tl;
         const int64_t off = (int64_t)c * CH;                       // chunk offset in the row
         const int cbytes = (int)min((int64_t)CH, a.row_bytes - off);

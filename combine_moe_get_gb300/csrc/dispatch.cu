@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         return j < cta_units ? (int64_t)blockIdx.x + j * G : -1;
     };
     auto issue_load = [&](int64_t u, int s) {   // lane 0
-        const int64_t t = u / a.num_chunks;
+        const int64_t t = div_count(u, a.num_chunks);
         const int64_t off = (u - t * a.num_chunks) * (int64_t)chunk;
         const uint32_t nbytes = (uint32_t)min((int64_t)chunk, a.row_bytes - off);
         mbar_arrive_expect_tx(&bars[s], nbytes);
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
 
     // receive rows (and, for the first chunk, the routing) of the next unit, prefetched one unit ahead
     auto fetch = [&](int64_t u, int &row, int64_t &e, float &w) {
-        const int64_t t = u / a.num_chunks;
+        const int64_t t = div_count(u, a.num_chunks);
         const bool first = (u - t * a.num_chunks) == 0;
         row = -1; e = -1; w = 0.0f;
         if constexpr (kFused) {
@@ -431,12 +431,12 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
     int row_n = -1; int64_t e_n = -1; float w_n = 0.0f;
     if (ring[0] >= 0) fetch(ring[0], row_n, e_n, w_n);
 
-    for (int64_t i = 0;; ++i) {
-        const int s = (int)(i % S);
-        const uint32_t parity = (uint32_t)((i / S) & 1);
+    int s = 0;              // stage of iteration i (i % S)
+    uint32_t parity = 0;    // phase parity of that stage ((i / S) & 1)
+    for (int64_t i = 0;; ++i, s = (s + 1 == S) ? 0 : s + 1, parity ^= (s == 0) ? 1u : 0u) {
         const int64_t u = ring[s];
         if (u < 0) break;
-        const int64_t t = u / a.num_chunks;
+        const int64_t t = div_count(u, a.num_chunks);
         const int c = (int)(u - t * a.num_chunks);
         const int64_t off = (int64_t)c * chunk;
         const int nbytes = (int)min((int64_t)chunk, a.row_bytes - off);
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         int row = row_n;
         const int64_t e = e_n;
         const float wgt = w_n;
-        const int64_t u_next = ring[(i + 1) % S];   // claimed at least one iteration ago (S >= 3)
+        const int64_t u_next = ring[s + 1 == S ? 0 : s + 1];   // claimed at least one iteration ago (S >= 3)
         if (u_next >= 0) fetch(u_next, row_n, e_n, w_n);
         if (row >= a.capacity) {
             if (c == 0) report(a.status, MOE_ERR_CAPACITY);
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
             // the stage stored one unit ago is free once its bulk stores have read it;
             // it takes the next unit claimed by this warp
             if (i >= 1) {
-                const int sp = (int)((i - 1) % S);
+                const int sp = s == 0 ? S - 1 : s - 1;
                 const int64_t un = claim();
                 ring[sp] = un;
                 if (un >= 0) {

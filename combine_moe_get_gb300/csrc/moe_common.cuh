@@ -55,6 +55,16 @@ inline cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 bloc
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// ------------------------------------------------------------------ index arithmetic
+
+// u / n for a non-negative unit counter and n >= 1: no division when n == 1
+// and 32-bit division while u fits (a 64-bit division is a long dependent
+// instruction sequence, which matters in a single warp's issue loop).
+__device__ __forceinline__ int64_t div_count(int64_t u, int n) {
+    if (n == 1) return u;
+    return u <= 0x7fffffff ? (int64_t)((uint32_t)u / (uint32_t)n) : u / n;
+}
+
 // ------------------------------------------------------------------ status
 
 // First data error wins; later ones are dropped.
