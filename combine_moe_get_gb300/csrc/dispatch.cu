@@ -67,6 +67,7 @@ struct DispatchArgs {
     int fl_words;             // bitmap words per rank: ceil(T / 32)
     size_t fl_off;            // byte offset of the layout region in dynamic shared memory
     moe_layout_t fl_out;      // layout outputs, written by CTA 0
+    int loads_before_wait;    // first stage loads (input rows only) before the dependency wait
 };
 
 // Block scale RN(amax / 448) without a division: q0 = RN(amax * C) with
@@ -354,8 +355,7 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
     __shared__ int s_next_unit;
     if (threadIdx.x == 0) s_next_unit = 0;
     __syncthreads();
-    grid_dependency_wait();
-    grid_launch_dependents();
+    if (!a.loads_before_wait) grid_dependency_wait();
     const int64_t G = gridDim.x;
     const int64_t cta_units = a.num_units > (int64_t)blockIdx.x ? (a.num_units - 1 - blockIdx.x) / G + 1 : 0;
     int64_t *ring = reinterpret_cast<int64_t *>(wbase + 64);   // unit of each stage (after the <= 8 barriers)
@@ -387,6 +387,10 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         }
     }
     __syncwarp();
+    // launched right behind this library's layout, the input rows were complete
+    // before this grid could launch; the layout's outputs are read only from here
+    if (a.loads_before_wait) grid_dependency_wait();
+    grid_launch_dependents();
 
     // fused launch: the layout, computed while the first loads are in flight
     const uint32_t *fl_bitmap = nullptr;
@@ -602,6 +606,7 @@ struct Fp8Args {
     int num_slices;
     int l2_hints;
     uint64_t timeout_ns;
+    int loads_before_wait;       // the producer (input rows only) skips the dependency wait
 };
 
 __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
@@ -633,7 +638,10 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
         s_rows_issued = 0;
     }
     __syncthreads();
-    grid_dependency_wait();
+    // launched right behind this library's layout, the input rows were complete
+    // before this grid could launch: the producer, which reads nothing else,
+    // starts at once; the workers read the layout's outputs and wait
+    if (!(a.loads_before_wait && warp == 0)) grid_dependency_wait();
     grid_launch_dependents();
     if (n <= 0) return;
 
@@ -796,6 +804,7 @@ DispatchArgs base_args(const DispatchLaunch &L) {
     a.topk = L.topk_idx;
     a.topk_w = L.topk_weights;
     a.dst_row = L.token_dst_row;
+    a.loads_before_wait = L.loads_before_wait ? 1 : 0;
     a.capacity = L.recv_capacity;
     a.recv_x = static_cast<uint8_t *>(L.recv_x);
     a.recv_row_bytes = (fp8 || fp8_in) ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
@@ -896,6 +905,7 @@ int launch_dispatch(const DispatchLaunch &L) {
         f.status = a.status;
         f.num_slices = (f.nb + kFp8SliceBlocks - 1) / kFp8SliceBlocks;
         f.l2_hints = a.l2_hints;
+        f.loads_before_wait = a.loads_before_wait;
         f.timeout_ns = a.timeout_ns;
         const size_t head = 2 * kFp8MaxSlots * 8;
         const size_t optin = device_smem_optin();
@@ -946,9 +956,13 @@ int launch_layout_dispatch(const LayoutLaunch &Ll, const DispatchLaunch &L) {
         const size_t extra = fused_smem(T, L.num_ranks, L.num_experts, L.num_topk).total;
         fused = chunked_config(a, fp8, T, extra, warps, smem, grid) == MOE_OK;
     }
-    if (!fused) {   // two launches: layout, then dispatch
-        const int rc = launch_layout(Ll);
-        return rc != MOE_OK ? rc : launch_dispatch(L);
+    if (!fused) {   // two launches: layout, then dispatch, which loads input rows while the layout runs
+        LayoutLaunch l2 = Ll;
+        DispatchLaunch d2 = L;
+        l2.early_dependents = tu.overlap != 0;
+        d2.loads_before_wait = tu.overlap != 0;
+        const int rc = launch_layout(l2);
+        return rc != MOE_OK ? rc : launch_dispatch(d2);
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(L.stream);
     return fp8 ? launch_chunked<true, true>(a, warps, smem, grid, st)

@@ -192,6 +192,7 @@ struct TileArgs {
     int32_t *status;
     uint64_t timeout_ns;
     int unpublished_tile;  // test hook: this tile never publishes its status (-1 = none)
+    int early_dependents;  // trigger the next grid's launch right after the dependency wait
 };
 
 template <bool kCooperative>
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
     int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
     uint64_t *tile_status = reinterpret_cast<uint64_t *>(a.ws + a.status_off);
     grid_dependency_wait();
+    if (a.early_dependents) grid_launch_dependents();
 
     if (threadIdx.x == 0) s_tile = kCooperative ? (int)blockIdx.x : (int)atomicAdd(&hdr->ticket, 1u);
     for (int i = threadIdx.x; i < R * kWords; i += kThreads) bitmap[i] = 0u;
@@ -489,6 +491,7 @@ __global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool publish = tile != a.unpublished_tile;
     grid_dependency_wait();
+    if (a.early_dependents) grid_launch_dependents();
 
     for (int i = threadIdx.x; i < R * kWords; i += kThreads) bitmap[i] = 0u;
     for (int i = threadIdx.x; i < E; i += kThreads) hist[i] = 0;
@@ -721,6 +724,7 @@ int launch_layout(const LayoutLaunch &L) {
     a.status = L.status;
     a.timeout_ns = L.timeout_ns > 0 ? (uint64_t)L.timeout_ns : kDefaultWaitNs;
     a.unpublished_tile = L.unpublished_tile;
+    a.early_dependents = L.early_dependents ? 1 : 0;
 
     const size_t smem = smem_layout(E, R, k).total;
     const size_t dsmem = direct_smem(E, R, k).total;

@@ -43,6 +43,9 @@ struct LayoutLaunch {
     void *stream;
     int64_t timeout_ns;     // <= 0: default
     int unpublished_tile;   // test hook, -1 = off
+    // let the next grid on the stream launch as soon as every CTA has passed its
+    // dependency wait (the next launch is this library's dispatch)
+    bool early_dependents = false;
 };
 
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
@@ -81,6 +84,10 @@ struct DispatchLaunch {
     float *x_scales;
     int32_t *status;
     void *stream;
+    // the launch before this one is the layout of the same call, which passed its
+    // own dependency wait before letting this grid launch: the input rows are
+    // complete, so the first stage loads may be issued before the wait
+    bool loads_before_wait = false;
 };
 
 int launch_dispatch(const DispatchLaunch &L);
