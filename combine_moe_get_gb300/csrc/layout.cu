@@ -63,13 +63,21 @@ static_assert(sizeof(WsHeader) == 128, "header is one 128-byte line");
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Direct mode (few tiles, all co-resident): every tile publishes its rank
-// counts as flagged words and reads all tiles' words itself.
-constexpr int kDirectMaxTiles = 64;
+// counts as flagged words and reads all tiles' words itself. A batch of at
+// most kTile tokens is one tile of kTile (nothing to exchange); larger ones
+// use tiles of kDirectTile tokens, which halves each CTA's serial work for
+// the price of more (cheap) exchange words.
+constexpr int kDirectTile = 64;
+constexpr int kDirectMaxTiles = 128;
 constexpr int64_t kDirectMaxRankWords = 16384;     // tiles * R
 
-inline bool direct_sizes(int T, int R) {
-    const int64_t tiles = (T + kTile - 1) / kTile;
-    return T > 0 && tiles <= kDirectMaxTiles && tiles * R <= kDirectMaxRankWords;
+// Tokens per tile of the direct mode for this batch, or 0 when the batch
+// takes a lookback mode.
+inline int direct_tile(int T, int R) {
+    if (T <= 0) return 0;
+    if (T <= kTile) return kTile;
+    const int64_t tiles = (T + kDirectTile - 1) / kDirectTile;
+    return tiles <= kDirectMaxTiles && tiles * R <= kDirectMaxRankWords ? kDirectTile : 0;
 }
 
 struct WsLayout {
@@ -78,7 +86,8 @@ struct WsLayout {
 
 inline WsLayout ws_layout(int T, int E, int R) {
     WsLayout w;
-    size_t tiles = (size_t)((T + kTile - 1) / kTile);
+    const int dt = direct_tile(T, R);
+    size_t tiles = (size_t)((T + (dt ? dt : kTile) - 1) / (dt ? dt : kTile));
     w.expert_off = sizeof(WsHeader);
     w.status_off = align_up(w.expert_off + (size_t)E * 4, 128);
     w.total = align_up(w.status_off + tiles * (size_t)R * 8, 128);
@@ -449,15 +458,17 @@ struct DirectSmem {
     size_t wprefix, excl, tot, hist, ent, rk, total;
 };
 
+template <int TILE>
 __host__ __device__ inline DirectSmem direct_smem(int E, int R, int k) {
+    constexpr int kWords = TILE / 32;
     DirectSmem d;
     d.wprefix = align_up((size_t)R * kWords * 4, 16);
     d.excl = d.wprefix + align_up((size_t)R * kWords * 2, 16);
     d.tot = d.excl + align_up((size_t)R * 4, 16);
     d.hist = d.tot + align_up((size_t)(R + 1) * 4, 16);
     d.ent = d.hist + align_up((size_t)(E + 1) * 4, 16);
-    d.rk = d.ent + align_up((size_t)kTile * k * 2, 16);
-    d.total = d.rk + align_up((size_t)kTile * k * 2, 16);
+    d.rk = d.ent + align_up((size_t)TILE * k * 2, 16);
+    d.total = d.rk + align_up((size_t)TILE * k * 2, 16);
     return d;
 }
 
@@ -469,10 +480,13 @@ __host__ __device__ inline DirectSmem direct_smem(int E, int R, int k) {
 // published after a fence that follows its histogram atomics, so once tile 0
 // has seen every tile's words the expert totals are complete; it then writes
 // the expert counts and prefix. A batch of one tile exchanges nothing.
+template <int TILE>
 __global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
+    constexpr int kTile = TILE;            // tokens per tile of this instance
+    constexpr int kWords = TILE / 32;
     extern __shared__ __align__(16) uint8_t smem[];
     const int R = a.R, E = a.E, k = a.k;
-    const DirectSmem sl = direct_smem(E, R, k);
+    const DirectSmem sl = direct_smem<TILE>(E, R, k);
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem);
     uint16_t *wprefix = reinterpret_cast<uint16_t *>(smem + sl.wprefix);
     int32_t *excl = reinterpret_cast<int32_t *>(smem + sl.excl);
@@ -702,15 +716,26 @@ int launch_layout(const LayoutLaunch &L) {
         return MOE_OK;
     }
     const WsLayout w = ws_layout(T, E, R);
-    const int num_tiles = (T + kTile - 1) / kTile;
-    // a single-tile direct launch uses no workspace
-    if (!(direct_sizes(T, R) && num_tiles == 1) && cudaMemsetAsync(L.workspace, 0, w.total, s) != cudaSuccess)
+    const size_t smem = smem_layout(E, R, k).total;
+    // direct mode: tile size, kernel instance and whether all its tiles fit on the GPU at once
+    int dt = direct_tile(T, R);
+    const void *direct = dt == kDirectTile ? (const void *)layout_direct_kernel<kDirectTile>
+                                           : (const void *)layout_direct_kernel<kTile>;
+    const size_t dsmem = dt == kDirectTile ? direct_smem<kDirectTile>(E, R, k).total : direct_smem<kTile>(E, R, k).total;
+    const void *coop = (const void *)layout_tiles_kernel<true>;
+    if (ensure_dynamic_smem(direct, dsmem) != MOE_OK || ensure_dynamic_smem(coop, smem) != MOE_OK ||
+        ensure_dynamic_smem((const void *)layout_tiles_kernel<false>, smem) != MOE_OK)
         return MOE_ERR_CUDA;
+    if (dt && (T + dt - 1) / dt > cooperative_capacity(direct, dsmem)) dt = 0;
+    const int tile_tokens = dt ? dt : kTile;
+    const int num_tiles = (T + tile_tokens - 1) / tile_tokens;
+    // a single-tile direct launch uses no workspace
+    if (!(dt && num_tiles == 1) && cudaMemsetAsync(L.workspace, 0, w.total, s) != cudaSuccess) return MOE_ERR_CUDA;
 
     TileArgs a;
     a.topk = L.topk_idx;
     a.T = T; a.k = k; a.E = E; a.R = R; a.m = E / R;
-    a.num_tiles = (T + kTile - 1) / kTile;
+    a.num_tiles = num_tiles;
     a.group = lookback_group(R);
     a.is_token_in_rank = o.is_token_in_rank;
     a.token_dst_row = o.token_dst_row;
@@ -726,18 +751,10 @@ int launch_layout(const LayoutLaunch &L) {
     a.unpublished_tile = L.unpublished_tile;
     a.early_dependents = L.early_dependents ? 1 : 0;
 
-    const size_t smem = smem_layout(E, R, k).total;
-    const size_t dsmem = direct_smem(E, R, k).total;
-    const void *direct = (const void *)layout_direct_kernel;
-    const void *coop = (const void *)layout_tiles_kernel<true>;
-    if (ensure_dynamic_smem(direct, dsmem) != MOE_OK || ensure_dynamic_smem(coop, smem) != MOE_OK ||
-        ensure_dynamic_smem((const void *)layout_tiles_kernel<false>, smem) != MOE_OK)
-        return MOE_ERR_CUDA;
-
-    if (direct_sizes(T, R) && a.num_tiles <= cooperative_capacity(direct, dsmem)) {
-        if (a.num_tiles == 1) {     // nothing to exchange: an ordinary launch
-            return launch_kernel(layout_direct_kernel, dim3(1), dim3(kThreads), dsmem, s, tuning().overlap != 0, a) ==
-                           cudaSuccess
+    if (dt) {
+        if (a.num_tiles == 1) {     // nothing to exchange: an ordinary launch (dt == kTile)
+            return launch_kernel(layout_direct_kernel<kTile>, dim3(1), dim3(kThreads), dsmem, s, tuning().overlap != 0,
+                                 a) == cudaSuccess
                        ? MOE_OK
                        : MOE_ERR_CUDA;
         }
