@@ -68,6 +68,11 @@ struct DispatchArgs {
     size_t fl_off;            // byte offset of the layout region in dynamic shared memory
     moe_layout_t fl_out;      // layout outputs, written by CTA 0
     int loads_before_wait;    // first stage loads (input rows only) before the dependency wait
+    // tail balancing: units [0, static_units) are dealt round-robin to the CTAs;
+    // the rest form a pool claimed through *pool (zeroed by the caller), so that
+    // CTAs on faster SMs take more of them (nullptr: every unit is dealt)
+    unsigned int *pool;
+    int64_t static_units;
 };
 
 // Block scale RN(amax / 448) without a division: q0 = RN(amax * C) with
@@ -357,7 +362,8 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
     __syncthreads();
     if (!a.loads_before_wait) grid_dependency_wait();
     const int64_t G = gridDim.x;
-    const int64_t cta_units = a.num_units > (int64_t)blockIdx.x ? (a.num_units - 1 - blockIdx.x) / G + 1 : 0;
+    const int64_t dealt = a.pool ? a.static_units : a.num_units;
+    const int64_t cta_units = dealt > (int64_t)blockIdx.x ? (dealt - 1 - blockIdx.x) / G + 1 : 0;
     int64_t *ring = reinterpret_cast<int64_t *>(wbase + 64);   // unit of each stage (after the <= 8 barriers)
 
     const uint64_t pol_load = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
@@ -368,9 +374,12 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         fence_barrier_init();
     }
 
-    auto claim = [&]() -> int64_t {   // lane 0; -1 once the CTA's units are exhausted
+    auto claim = [&]() -> int64_t {   // lane 0; -1 once the CTA's units (and the pool) are exhausted
         const int64_t j = atomicAdd(&s_next_unit, 1);
-        return j < cta_units ? (int64_t)blockIdx.x + j * G : -1;
+        if (j < cta_units) return (int64_t)blockIdx.x + j * G;
+        if (a.pool == nullptr) return -1;
+        const int64_t p = dealt + (int64_t)atomicAdd(a.pool, 1u);
+        return p < a.num_units ? p : -1;
     };
     auto issue_load = [&](int64_t u, int s) {   // lane 0
         const int64_t t = div_count(u, a.num_chunks);
@@ -805,6 +814,7 @@ DispatchArgs base_args(const DispatchLaunch &L) {
     a.topk_w = L.topk_weights;
     a.dst_row = L.token_dst_row;
     a.loads_before_wait = L.loads_before_wait ? 1 : 0;
+    a.pool = L.pool;
     a.capacity = L.recv_capacity;
     a.recv_x = static_cast<uint8_t *>(L.recv_x);
     a.recv_row_bytes = (fp8 || fp8_in) ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
@@ -839,6 +849,13 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     a.num_units = (int64_t)num_tokens * a.num_chunks;
+    const int pool_pct = tu.dispatch_pool;
+    if (a.pool != nullptr && pool_pct > 0 && pool_pct < 100) {
+        a.static_units = a.num_units * (100 - pool_pct) / 100;
+    } else {
+        a.pool = nullptr;
+        a.static_units = a.num_units;
+    }
     a.stages = std::min(kMaxStages, std::max(3, tu.dispatch_stages));   // the unit ring needs three
     // stages take at most ~200 KB, so that some L1 cache is left (a full 227 KB of
     // stages measured slower)
@@ -961,6 +978,7 @@ int launch_layout_dispatch(const LayoutLaunch &Ll, const DispatchLaunch &L) {
         DispatchLaunch d2 = L;
         l2.early_dependents = tu.overlap != 0;
         d2.loads_before_wait = tu.overlap != 0;
+        d2.pool = layout_spare_counter(l2);
         const int rc = launch_layout(l2);
         return rc != MOE_OK ? rc : launch_dispatch(d2);
     }

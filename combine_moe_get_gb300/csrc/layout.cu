@@ -703,6 +703,11 @@ int launch_cooperative(const void *kernel, int grid, size_t smem, cudaStream_t s
 
 size_t layout_workspace_bytes(int T, int E, int R) { return ws_layout(T, E, R).total; }
 
+unsigned int *layout_spare_counter(const LayoutLaunch &L) {
+    if (L.num_tokens <= kTile || L.workspace == nullptr) return nullptr;   // one tile (or none): no clear
+    return &static_cast<WsHeader *>(L.workspace)->pad[0];
+}
+
 int launch_layout(const LayoutLaunch &L) {
     const int T = L.num_tokens, k = L.num_topk, E = L.num_experts, R = L.num_ranks;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(L.stream);

@@ -110,6 +110,7 @@ const Tuning &tuning() {
         x.combine_ring_bytes = env_int("MOE_TUNE_COMBINE_RING_BYTES", 224 << 10);
         x.combine_fp8_warps = env_int("MOE_TUNE_COMBINE_FP8_WARPS", 10);
         x.overlap = env_int("MOE_TUNE_OVERLAP", 1) == 1;   // any other value: ordinary launches
+        x.dispatch_pool = env_int("MOE_TUNE_DISPATCH_POOL", 50);
         x.fp8_rows = env_int("MOE_TUNE_FP8_ROWS", 1) == 1;
         x.fp8_in_slots = env_int("MOE_TUNE_FP8_IN_SLOTS", 8);
         x.fp8_quant_warps = env_int("MOE_TUNE_FP8_QUANT_WARPS", 24);

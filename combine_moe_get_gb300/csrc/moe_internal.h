@@ -31,6 +31,7 @@ struct Tuning {
     int spread_small;   // small batches: fewer dispatch warps per CTA, more CTAs
     int fused_small;    // moe_layout_dispatch: one fused launch for small batches
     int overlap;        // programmatic dependent launch of every non-cooperative kernel
+    int dispatch_pool;  // % of dispatch units left to a shared pool when a cleared counter is at hand (>= 100: off)
 };
 const Tuning &tuning();
 
@@ -50,6 +51,10 @@ struct LayoutLaunch {
 
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 int launch_layout(const LayoutLaunch &L);
+// A 32-bit word of the layout workspace that launch_layout(L) clears and then
+// leaves alone, free for the next launch of the same call; nullptr when the
+// launch clears nothing (a batch of one tile).
+unsigned int *layout_spare_counter(const LayoutLaunch &L);
 
 struct ExpandLaunch {
     const int64_t *topk_idx;
@@ -88,6 +93,8 @@ struct DispatchLaunch {
     // own dependency wait before letting this grid launch: the input rows are
     // complete, so the first stage loads may be issued before the wait
     bool loads_before_wait = false;
+    // optional zeroed counter for tail balancing (a pool of units shared by all CTAs)
+    unsigned int *pool = nullptr;
 };
 
 int launch_dispatch(const DispatchLaunch &L);

@@ -130,8 +130,12 @@ def test_steps_eager_on_side_stream(moe, T, H, k, E, R):
     p.check()
 
 
-def test_fused_steps_in_one_graph(moe):
-    p = Pipeline(moe, 128, 7168, 8, 256, 8, False, 3, 5)
+@pytest.mark.parametrize("T,fp8", [(128, False), (2000, False), (2000, True)])
+def test_layout_dispatch_steps_in_one_graph(moe, T, fp8):
+    # moe_layout_dispatch: one fused launch (T <= 1024), or the layout and then a dispatch
+    # that loads input rows before its dependency wait and balances its tail through a
+    # counter in the layout workspace
+    p = Pipeline(moe, T, 7168, 8, 256, 8, fp8, 3, 5 + T)
     for i in range(3):
         p.step(i, fused=True)
     torch.cuda.synchronize()
@@ -139,5 +143,6 @@ def test_fused_steps_in_one_graph(moe):
     with torch.cuda.graph(g):
         for i in range(3):
             p.step(i, fused=True)
-    g.replay()
-    p.check()
+    for _ in range(2):
+        g.replay()
+        p.check()
