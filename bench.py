@@ -188,6 +188,7 @@ class Step:
         self.wts = inp.topk_weights.to(device)
         self.partial = inp.partial.to(device)
         self.status = moe.new_status(device)
+        self.bal = moe.new_balance_counter(device)
         self.lay = moe.Layout.empty(T, k, E, R, device)
         self.ws = torch.empty(moe.moe_get_layout_workspace_size(T, E, R), dtype=torch.uint8, device=device)
         self.disp = moe.Dispatched(
@@ -239,9 +240,14 @@ class Step:
     def combine_weighted(self):
         self.moe.moe_combine_ex(self.partial, self.lay.token_dst_row, row_weights=self.row_w,
                                 recv_topk_weights=self.disp.recv_topk_weights, out=self.out,
-                                combined_topk_weights=self.cw, status=self.status)
+                                combined_topk_weights=self.cw, balance=self.bal, status=self.status)
 
     def combine(self):
+        # with a balance counter: the last 30% of the tokens go to whichever CTA is free first
+        self.moe.moe_combine_ex(self.partial, self.lay.token_dst_row, out=self.out, balance=self.bal,
+                                status=self.status)
+
+    def combine_unbalanced(self):
         self.moe.moe_combine(self.partial, self.lay.token_dst_row, out=self.out, status=self.status)
 
     def combine_fp8(self):
@@ -262,7 +268,7 @@ class Step:
                               self.xcap, expand=True, out=self.dispx, status=self.status)
 
     def combine_expand(self):
-        self.moe.moe_combine(self.partial_x, self.xrows, out=self.out, status=self.status)
+        self.moe.moe_combine_ex(self.partial_x, self.xrows, out=self.out, balance=self.bal, status=self.status)
 
     def expand_step(self):
         self.layout()
@@ -297,9 +303,10 @@ def run_ours(args, world, rank, local):
 
     def one(events=None):
         """The step through the public API: moe_layout_dispatch (the layout, then
-        the dispatch, which starts loading input rows while the layout runs), then
-        moe_combine. With events, the per-kernel breakdown: the three separate
-        calls with an event between each two."""
+        the dispatch, which starts loading input rows while the layout runs and
+        balances its tail through the layout workspace), then moe_combine_ex with
+        a balance counter. With events, the per-kernel breakdown: moe_get_layout,
+        moe_dispatch and the same combine, with an event between each two."""
         if not events:
             st.layout_dispatch()
             st.combine()
@@ -415,6 +422,8 @@ def run_ours(args, world, rank, local):
         return ms
 
     reps = max(3, args.steps // 2)
+    ld_ms = time_alone(st.layout_dispatch, reps)                              # the step's first call
+    ucomb_ms = time_alone(st.combine_unbalanced, reps)                        # moe_combine: static split only
     fp8_ms = time_alone(lambda: st.dispatch(fp8=True), reps)                  # fused E4M3 quantisation
     fp8in_ms = time_alone(st.dispatch_fp8_input, reps)                        # E4M3 rows + scales relayed
     wcomb_ms = time_alone(st.combine_weighted, reps)                          # weighted rows + combined weights
@@ -456,6 +465,8 @@ def run_ours(args, world, rank, local):
         "dispatch_combine_tokens_per_s": T / ((mean(dis_ms) + mean(com_ms)) * 1e-3),
         "dispatch_us": mean(dis_ms) * 1e3,
         "combine_us": mean(com_ms) * 1e3,
+        "layout_dispatch_us": mean(ld_ms) * 1e3,
+        "combine_unbalanced_us": mean(ucomb_ms) * 1e3,
         "dispatch_fp8_us": mean(fp8_ms) * 1e3,
         "dispatch_fp8_input_us": mean(fp8in_ms) * 1e3,
         "combine_weighted_us": mean(wcomb_ms) * 1e3,
@@ -471,13 +482,14 @@ def run_ours(args, world, rank, local):
     gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     kern["dispatch_gbs"] = gbs(bytes_bf16, mean(dis_ms))
     kern["combine_gbs"] = gbs(bytes_bf16, mean(com_ms))
+    kern["combine_unbalanced_gbs"] = gbs(bytes_bf16, mean(ucomb_ms))
     kern["dispatch_fp8_gbs"] = gbs(bytes_fp8, mean(fp8_ms))
     kern["dispatch_fp8_input_gbs"] = gbs(bytes_fp8in, mean(fp8in_ms))
     kern["combine_weighted_gbs"] = gbs(bytes_wcomb, mean(wcomb_ms))
     kern["combine_fp8_gbs"] = gbs(bytes_fcomb, mean(fcomb_ms))
     kern["dispatch_expand_gbs"] = gbs(bytes_expand, mean(xdis_ms))
     kern["combine_expand_gbs"] = gbs(bytes_expand, mean(xcom_ms))
-    for key in ("dispatch", "combine", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted", "combine_fp8",
+    for key in ("dispatch", "combine", "combine_unbalanced", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted", "combine_fp8",
                 "dispatch_expand", "combine_expand"):
         kern[f"{key}_frac"] = kern[f"{key}_gbs"] / peak
         kern[f"{key}_frac_of_spec"] = kern[f"{key}_gbs"] / HBM_SPEC_GBS
@@ -495,7 +507,8 @@ def run_ours(args, world, rank, local):
         "config": {"workload": "DeepSeek-V3 prefill shape: T=4096, H=7168 bf16, E=256 over R=8 logical ranks, "
                                "top-8 uniform, softmax weights", "tokens": T, "hidden": H,
                    "experts": w.num_experts, "ranks": w.num_ranks, "topk": w.num_topk, "recv_rows": N,
-                   "step": "moe_layout_dispatch (layout, then bf16 dispatch) + moe_combine", "timing": timing, "l2": f"flushed between steps ({flush.numel() >> 20} MiB written, then {flush_src.numel() >> 20} MiB read; untimed)",
+                   "step": "moe_layout_dispatch (layout, then bf16 dispatch) + moe_combine_ex (balance counter)",
+                   "timing": timing, "l2": f"flushed between steps ({flush.numel() >> 20} MiB written, then {flush_src.numel() >> 20} MiB read; untimed)",
                    "parallelism": f"replicas x{world} (independent token shards, no collective)"},
         "roofline": {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,

@@ -81,7 +81,7 @@ def _load():
     lib.moe_combine.restype = _I
     lib.moe_combine_fp8.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]
     lib.moe_combine_fp8.restype = _I
-    lib.moe_combine_ex.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
+    lib.moe_combine_ex.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.moe_combine_ex.restype = _I
     return lib
 
@@ -115,6 +115,11 @@ def _check(code: int, where: str) -> None:
 
 def new_status(device=None) -> torch.Tensor:
     return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def new_balance_counter(device=None) -> torch.Tensor:
+    """Two zeroed uint32 (as int32) for the combine's tail balancing; each call leaves them zero."""
+    return torch.zeros(2, dtype=torch.int32, device=device or "cuda")
 
 
 def check_status(status: torch.Tensor, where: str = "kernel") -> None:
@@ -320,10 +325,13 @@ def moe_combine_fp8(partial_codes: torch.Tensor, partial_scales: torch.Tensor, t
 
 def moe_combine_ex(partial: torch.Tensor, token_dst_row: torch.Tensor, *, row_weights: Optional[torch.Tensor] = None,
                    recv_topk_weights: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-                   combined_topk_weights: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                   combined_topk_weights: Optional[torch.Tensor] = None, balance: Optional[torch.Tensor] = None,
+                   status: Optional[torch.Tensor] = None,
                    stream=None) -> tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Combine with per-row weights (fma per term) and/or the reduction of the
-    received top-k weights back to [T, k]. Returns (out, combined_topk_weights)."""
+    received top-k weights back to [T, k], and optionally a balance counter
+    (new_balance_counter()) that spreads the last tokens over the SMs.
+    Returns (out, combined_topk_weights)."""
     rows, H = partial.shape
     T, k = token_dst_row.shape
     dev = partial.device
@@ -332,7 +340,7 @@ def moe_combine_ex(partial: torch.Tensor, token_dst_row: torch.Tensor, *, row_we
         combined_topk_weights = torch.empty(T, k, dtype=torch.float32, device=dev)
     status = new_status(dev) if status is None else status
     code = LIB.moe_combine_ex(_ptr(partial), rows, T, H, k, _ptr(token_dst_row), _ptr(row_weights),
-                              _ptr(recv_topk_weights), _ptr(combined_topk_weights), _ptr(out), _ptr(status),
-                              _stream(stream))
+                              _ptr(recv_topk_weights), _ptr(combined_topk_weights), _ptr(out), _ptr(balance),
+                              _ptr(status), _stream(stream))
     _check(code, "moe_combine_ex")
     return out, combined_topk_weights

@@ -76,10 +76,16 @@ struct CombineArgs {
     int num_slots;       // ring slots of chunk_bytes
     int l2_hints;
     uint64_t timeout_ns;
+    // tail balancing: tokens [0, static_tokens) are split into contiguous CTA
+    // ranges; the rest form a pool claimed through balance[0] (balance[1]
+    // counts finished CTAs; the last one zeroes both). nullptr: all dealt.
+    unsigned int *balance;
+    int static_tokens;
 };
 
 struct UnitEntry {
-    int D;                   // rows of the unit
+    int D;                   // rows of the unit; -1: no more units
+    int t;                   // token of the unit
     int start;               // first ring slot (the unit's rows occupy start, start+1, ... mod num_slots)
     float w[MOE_MAX_TOPK];   // weight of the row in slot start + d (weighted combine)
     int row[MOE_MAX_TOPK];   // receive row in slot start + d
@@ -164,10 +170,11 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
     const int consumers = (blockDim.x >> 5) - 1;
     const int NS = a.num_slots, CH = a.chunk_bytes, SB = a.slot_bytes, nch = a.num_chunks;
 
-    // contiguous token range of this CTA
-    const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
-    const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
-    const int64_t n_units = (int64_t)(t_end - t_begin) * nch;
+    // contiguous range of the statically dealt tokens for this CTA
+    const int T_st = a.static_tokens;
+    const int s_begin = (int)((int64_t)T_st * blockIdx.x / gridDim.x);
+    const int s_end = (int)((int64_t)T_st * (blockIdx.x + 1) / gridDim.x);
+    const int nsl = a.num_slices;
 
     if (threadIdx.x == 0) {
         for (int e = 0; e < kUnits; ++e) {
@@ -179,54 +186,69 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
     __syncthreads();
     grid_dependency_wait();
     grid_launch_dependents();
-    if (n_units == 0) return;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         const uint64_t pol = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
         int64_t head = 0, tail = 0, oldest = 0;
         int head_slot = 0;   // head % NS, kept without 64-bit division
-        int row = -1, pos = 0, D = 0;
         float w_cur = 1.0f;
-        // the next kPre tokens' receive rows, loaded ahead (lanes < k), so that the
-        // row lists' load latency does not stall the issue of bulk loads
+        // tokens in order: the static range, then pool tokens while the pool lasts (warp-uniform; -1: none left)
+        int s_next = s_begin;
+        bool pool_open = a.balance != nullptr;
+        auto next_token = [&]() -> int {
+            if (s_next < s_end) return s_next++;
+            if (!pool_open) return -1;
+            unsigned p = 0;
+            if (lane == 0) p = atomicAdd(a.balance, 1u);
+            p = __shfl_sync(kFull, p, 0);
+            if ((int64_t)T_st + p < a.T) return T_st + (int)p;
+            pool_open = false;
+            return -1;
+        };
+        // the next kPre tokens and their receive rows (lanes < k), fetched ahead so that
+        // neither a pool claim nor a row list's load stalls the issue of bulk loads
         constexpr int kPre = 8;
-        int rq[kPre];
+        int tq[kPre], rq[kPre];
 #pragma unroll
         for (int i = 0; i < kPre; ++i) {
-            const int tt = t_begin + i;
-            rq[i] = (tt < t_end && lane < a.k) ? a.dst_row[(int64_t)tt * a.k + lane] : -1;
+            tq[i] = next_token();
+            rq[i] = (tq[i] >= 0 && lane < a.k) ? a.dst_row[(int64_t)tq[i] * a.k + lane] : -1;
         }
         // weighted: the weight of each row of the next token, loaded one token ahead
         float w_next = (kWeighted && rq[0] >= 0 && rq[0] < a.num_rows) ? a.row_weights[rq[0]] : 1.0f;
-        for (int64_t j = 0; j < n_units; ++j) {
-            const int tl = (int)div_count(j, nch), c = (int)(j - (int64_t)tl * nch);
-            const int t = t_begin + tl;
+        int64_t j = 0;       // units issued
+        bool ok = true;
+        while (ok) {
+            const int t = tq[0];
+            int row = rq[0];
+            if (t < 0) break;
+#pragma unroll
+            for (int i = 0; i < kPre - 1; ++i) {
+                tq[i] = tq[i + 1];
+                rq[i] = rq[i + 1];
+            }
+            tq[kPre - 1] = next_token();
+            rq[kPre - 1] = (tq[kPre - 1] >= 0 && lane < a.k) ? a.dst_row[(int64_t)tq[kPre - 1] * a.k + lane] : -1;
+            if (row >= a.num_rows) {
+                report(a.status, MOE_ERR_CAPACITY);
+                row = -1;
+            }
+            if (kWeighted) {
+                w_cur = w_next;
+                w_next = (rq[0] >= 0 && rq[0] < a.num_rows) ? a.row_weights[rq[0]] : 1.0f;
+            }
+            const unsigned vmask = __ballot_sync(kFull, row >= 0);
+            const int D = __popc(vmask);
+            int pos = 0;
+            for (int jj = 0; jj < a.k; ++jj) {
+                const int o = __shfl_sync(kFull, row, jj);
+                pos += (row >= 0 && ((vmask >> jj) & 1u) && o < row) ? 1 : 0;
+            }
+          for (int c = 0; c < nch; ++c, ++j) {
             const int64_t off = (int64_t)c * CH;
             const uint32_t nbytes = (uint32_t)min((int64_t)CH, a.row_bytes - off);
-            if (c == 0) {
-                row = rq[0];
-#pragma unroll
-                for (int i = 0; i < kPre - 1; ++i) rq[i] = rq[i + 1];
-                rq[kPre - 1] = (t + kPre < t_end && lane < a.k) ? a.dst_row[(int64_t)(t + kPre) * a.k + lane] : -1;
-                if (row >= a.num_rows) {
-                    report(a.status, MOE_ERR_CAPACITY);
-                    row = -1;
-                }
-                if (kWeighted) {
-                    w_cur = w_next;
-                    w_next = (rq[0] >= 0 && rq[0] < a.num_rows) ? a.row_weights[rq[0]] : 1.0f;
-                }
-                const unsigned vmask = __ballot_sync(kFull, row >= 0);
-                D = __popc(vmask);
-                pos = 0;
-                for (int jj = 0; jj < a.k; ++jj) {
-                    const int o = __shfl_sync(kFull, row, jj);
-                    pos += (row >= 0 && ((vmask >> jj) & 1u) && o < row) ? 1 : 0;
-                }
-            }
             // wait until the unit entry and D slots are free (units are released in order)
-            bool ok = true;
             while (ok && (j - oldest >= kUnits || head + D - tail > NS)) {
                 const int eo = (int)(oldest % kUnits);
                 ok = mbar_wait_bounded(&empty[eo], (uint32_t)((oldest / kUnits) & 1), a.timeout_ns);
@@ -237,12 +259,14 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             }
             if (!__all_sync(kFull, ok)) {
                 if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
+                ok = false;
                 break;
             }
             const int e = (int)(j % kUnits);
             __syncwarp();   // every lane has read entry[eo] before lane 0 rewrites an entry
             if (lane == 0) {
                 entry[e].D = D;
+                entry[e].t = t;
                 entry[e].start = head_slot;
             }
             if (row >= 0) {
@@ -263,23 +287,50 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             head += D;
             head_slot += D;
             if (head_slot >= NS) head_slot -= NS;
+          }
+        }
+        // end markers: the next units carry D = -1, so that each consumer's wait for
+        // its next item ends (consumer cw's next unit is at most (consumers - 1) / nsl
+        // past the last real one)
+        const int markers = (consumers + nsl - 1) / nsl + 1;
+        for (int i = 0; ok && i < markers; ++i, ++j) {
+            while (ok && j - oldest >= kUnits) {
+                const int eo = (int)(oldest % kUnits);
+                ok = mbar_wait_bounded(&empty[eo], (uint32_t)((oldest / kUnits) & 1), a.timeout_ns);
+                if (ok) {
+                    tail += entry[eo].D;
+                    ++oldest;
+                }
+            }
+            if (!__all_sync(kFull, ok)) {
+                if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const int e = (int)(j % kUnits);
+            __syncwarp();
+            if (lane == 0) {
+                entry[e].D = -1;
+                mbar_arrive(&full[e]);   // completes the phase: no bytes expected
+            }
+        }
+        // every claim of this CTA is made: count it finished; the last CTA re-arms the pool
+        if (a.balance != nullptr && lane == 0) {
+            __threadfence();
+            if (atomicAdd(a.balance + 1, 1u) == gridDim.x - 1) {
+                atomicExch(a.balance, 0u);
+                atomicExch(a.balance + 1, 0u);
+            }
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
     const int cw = warp - 1;
-    const int nsl = a.num_slices, SL = a.slice_bytes;
-    const int64_t n_items = n_units * nsl;
-    for (int64_t q = cw; q < n_items; q += consumers) {
+    const int SL = a.slice_bytes;
+    for (int64_t q = cw;; q += consumers) {
         const int64_t j = div_count(q, nsl);
         const int sl = (int)(q - j * nsl);
-        const int tl = (int)div_count(j, nch), c = (int)(j - (int64_t)tl * nch);
-        const int t = t_begin + tl;
-        const int64_t off = (int64_t)c * CH;                       // chunk offset in the row
-        const int cbytes = (int)min((int64_t)CH, a.row_bytes - off);
-        const int soff = sl * SL;                                  // slice offset in the chunk
-        const int nvec = max(0, min(SL, cbytes - soff)) / 16;
         const int e = (int)(j % kUnits);
         const bool ok = mbar_wait_bounded(&full[e], (uint32_t)((j / kUnits) & 1), a.timeout_ns);
         if (!__all_sync(kFull, ok)) {
@@ -287,6 +338,13 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             break;
         }
         const int D = entry[e].D;
+        if (D < 0) break;                                          // no more units
+        const int t = entry[e].t;
+        const int c = (int)(j - div_count(j, nch) * nch);          // units are (token, chunk 0..nch-1) in order
+        const int64_t off = (int64_t)c * CH;                       // chunk offset in the row
+        const int cbytes = (int)min((int64_t)CH, a.row_bytes - off);
+        const int soff = sl * SL;                                  // slice offset in the chunk
+        const int nvec = max(0, min(SL, cbytes - soff)) / 16;
         int slot = entry[e].start;
         if constexpr (kFP8) {
             constexpr int kV8 = kVMax / 2;   // 16 codes per 16-byte vector
@@ -422,6 +480,7 @@ int launch_combine(const CombineLaunch &L) {
     a.status = L.status;
     a.l2_hints = tu.l2_hints;
     a.timeout_ns = kDefaultWaitNs;
+    a.balance = (L.balance != nullptr && tu.combine_pool > 0 && tu.combine_pool < 100) ? L.balance : nullptr;
 
     // equal chunks no larger than the tuned maximum (E4M3 rows: of 512 codes, so
     // that each chunk's scales are whole 16-byte pieces), small enough that
@@ -451,6 +510,10 @@ int launch_combine(const CombineLaunch &L) {
 
     const int consumers = fp8 ? std::max(1, std::min(12, tu.combine_fp8_warps)) : std::max(1, std::min(8, tu.combine_warps));
     const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
+    // the pool pays off only with several tokens per CTA (its claims and the
+    // finishing count cost a few microseconds of latency)
+    if (a.T < 8 * grid) a.balance = nullptr;
+    a.static_tokens = a.balance ? (int)((int64_t)a.T * (100 - tu.combine_pool) / 100) : a.T;
     void (*kernel)(const CombineArgs) =
         fp8 ? combine_kernel<false, true> : (weighted ? combine_kernel<true, false> : combine_kernel<false, false>);
     return launch_kernel(kernel, dim3(grid), dim3((consumers + 1) * 32), smem, st, tu.overlap != 0, a) == cudaSuccess

@@ -111,6 +111,7 @@ const Tuning &tuning() {
         x.combine_fp8_warps = env_int("MOE_TUNE_COMBINE_FP8_WARPS", 10);
         x.overlap = env_int("MOE_TUNE_OVERLAP", 1) == 1;   // any other value: ordinary launches
         x.dispatch_pool = env_int("MOE_TUNE_DISPATCH_POOL", 50);
+        x.combine_pool = env_int("MOE_TUNE_COMBINE_POOL", 30);
         x.fp8_rows = env_int("MOE_TUNE_FP8_ROWS", 1) == 1;
         x.fp8_in_slots = env_int("MOE_TUNE_FP8_IN_SLOTS", 8);
         x.fp8_quant_warps = env_int("MOE_TUNE_FP8_QUANT_WARPS", 24);
@@ -344,7 +345,8 @@ MOE_API int moe_layout_dispatch(const void *x, int num_tokens, int hidden, const
 
 static int combine_common(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
                           const int32_t *token_dst_row, const float *row_weights, const float *recv_topk_weights,
-                          float *combined_topk_weights, void *out, int32_t *status, void *stream) {
+                          float *combined_topk_weights, void *out, uint32_t *balance, int32_t *status,
+                          void *stream) {
     const int T = num_tokens, H = hidden;
     if (T < 0 || num_topk < 1 || num_topk > MOE_MAX_TOPK || num_partial_rows < 0) return MOE_ERR_INVALID_ARG;
     if (H < 8 || H % 8 != 0 || H > (1 << 24) || (int64_t)T * num_topk >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
@@ -357,7 +359,9 @@ static int combine_common(const void *partial, int num_partial_rows, int num_tok
             !aligned(combined_topk_weights, 4))
             return MOE_ERR_MISALIGNED;
     }
+    if (!aligned(balance, 8)) return MOE_ERR_MISALIGNED;
     moe::CombineLaunch L;
+    L.balance = balance;
     L.partial = partial;
     L.num_partial_rows = num_partial_rows;
     L.num_tokens = T;
@@ -376,14 +380,15 @@ static int combine_common(const void *partial, int num_partial_rows, int num_tok
 MOE_API int moe_combine(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
                         const int32_t *token_dst_row, void *out, int32_t *status, void *stream) {
     return combine_common(partial, num_partial_rows, num_tokens, hidden, num_topk, token_dst_row, nullptr, nullptr,
-                          nullptr, out, status, stream);
+                          nullptr, out, nullptr, status, stream);
 }
 
 MOE_API int moe_combine_ex(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
                            const int32_t *token_dst_row, const float *row_weights, const float *recv_topk_weights,
-                           float *combined_topk_weights, void *out, int32_t *status, void *stream) {
+                           float *combined_topk_weights, void *out, uint32_t *balance, int32_t *status,
+                           void *stream) {
     return combine_common(partial, num_partial_rows, num_tokens, hidden, num_topk, token_dst_row, row_weights,
-                          recv_topk_weights, combined_topk_weights, out, status, stream);
+                          recv_topk_weights, combined_topk_weights, out, balance, status, stream);
 }
 
 MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scales, int num_partial_rows,

@@ -32,6 +32,7 @@ struct Tuning {
     int fused_small;    // moe_layout_dispatch: one fused launch for small batches
     int overlap;        // programmatic dependent launch of every non-cooperative kernel
     int dispatch_pool;  // % of dispatch units left to a shared pool when a cleared counter is at hand (>= 100: off)
+    int combine_pool;   // % of combine tokens left to a shared pool when the caller gives a counter (>= 100: off)
 };
 const Tuning &tuning();
 
@@ -113,6 +114,8 @@ struct CombineLaunch {
     void *out;
     int32_t *status;
     void *stream;
+    // optional: two zeroed uint32 of device memory for tail balancing (left zeroed)
+    uint32_t *balance = nullptr;
 };
 
 int launch_combine(const CombineLaunch &L);

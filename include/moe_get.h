@@ -359,12 +359,25 @@ MOE_API int moe_get_layout_noalloc(const int64_t *topk_idx, int num_tokens, int 
  *                         the Ascend page's FP32 weights next to the BF16 hidden):
  *                         combined[t, j] = sum over the rows of t in ascending rank
  *                         order of recv_topk_weights[row, j], fp32 from +0.0f.
+ *   balance               NULL, or a combine balance counter: 2 uint32 of device
+ *                         memory, 8-byte aligned, zero before the first call that
+ *                         uses them; every call leaves them zero again (the last
+ *                         CTA to finish clears them, also after a timeout). With it,
+ *                         70% of the tokens are split statically over the CTAs and
+ *                         the rest are claimed one by one, so that CTAs on SMs with
+ *                         more bandwidth take more of them (SMs do not all get the
+ *                         same HBM bandwidth; at DSv3 they finished 46-57 us apart
+ *                         without it). Batches of fewer than 8 tokens per SM ignore
+ *                         it. Results do not depend on it. Two calls
+ *                         that use the same counter must not run at the same time on
+ *                         the GPU (same stream, or ordered streams).
+ *                         Misaligned: MOE_ERR_MISALIGNED. NULL: static split only.
  * Other arguments, errors and limits as for moe_combine.
  */
 MOE_API int moe_combine_ex(const void *partial, int num_partial_rows, int num_tokens, int hidden, int num_topk,
                            const int32_t *token_dst_row, const float *row_weights,
                            const float *recv_topk_weights, float *combined_topk_weights, void *out,
-                           int32_t *status, void *stream);
+                           uint32_t *balance, int32_t *status, void *stream);
 
 /* Human-readable name of a moe_status_t value (static string). */
 MOE_API const char *moe_status_string(int status);

@@ -176,3 +176,16 @@ def _combine_fp8(lib, codes=A, scales=A + 0x80000, rows=256, T=128, H=1024, k=2,
 ])
 def test_combine_fp8_rejects_bad_arguments(lib, kw, code):
     assert _combine_fp8(lib, **kw) == code
+
+
+def _combine_ex(lib, partial=A, rows=256, T=128, H=256, k=2, dst=A + 0x10000, roww=None, rtw=None, cw=None,
+                out=A + 0x100000, balance=None, status=A + 0x200000):
+    return lib.LIB.moe_combine_ex(partial, rows, T, H, k, dst, roww, rtw, cw, out, balance, status, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=4), 1), (dict(k=0), 1), (dict(status=None), 1), (dict(rtw=A + 0x300000), 1), (dict(cw=A + 0x300000), 1),
+    (dict(balance=A + 4), 2), (dict(roww=A + 2), 2), (dict(partial=A + 4), 2),
+])
+def test_combine_ex_rejects_bad_arguments(lib, kw, code):
+    assert _combine_ex(lib, **kw) == code

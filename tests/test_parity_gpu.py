@@ -393,6 +393,27 @@ def test_combine_parity_shapes(moe, T, H, k, E, R):
     check_combine(moe, topk, partial, E, R)
 
 
+@pytest.mark.parametrize("T,H,k,E,R", [(0, 256, 8, 64, 8), (1, 512, 2, 16, 4), (5, 1024, 8, 256, 8),
+                                       (300, 7168, 8, 256, 8), (4096, 7168, 8, 256, 8), (2000, 1536, 6, 48, 3)])
+def test_combine_balanced_parity(moe, T, H, k, E, R):
+    # a balance counter changes which CTA reduces which token, never a result; each call leaves it zero
+    g = torch.Generator().manual_seed(11 * T + H)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
+    partial = wl.make_partial(g, max(wl.recv_capacity(T, k, R), 1), H)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk.to(DEV), E, R, status=status)
+    bal = moe.new_balance_counter(DEV)
+    ref, flags = oracle.combine(bits16(partial), oracle.layout(topk.numpy(), E, R)["token_dst_row"])
+    assert flags == 0
+    pd = partial.to(DEV)
+    for _ in range(3):
+        out, _ = moe.moe_combine_ex(pd, lay.token_dst_row, balance=bal, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert bal.tolist() == [0, 0]
+        np.testing.assert_array_equal(bits16(out), ref)
+
+
 @pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode"])
 def test_combine_ex_parity_configs(moe, name):
     w = wl.CONFIGS[name]
