@@ -188,7 +188,8 @@ class Step:
         self.wts = inp.topk_weights.to(device)
         self.partial = inp.partial.to(device)
         self.status = moe.new_status(device)
-        self.bal = moe.new_balance_counter(device)
+        self.bal = moe.new_balance_counter(device)     # the combine's
+        self.bal_d = moe.new_balance_counter(device)   # the dispatch's
         self.lay = moe.Layout.empty(T, k, E, R, device)
         self.ws = torch.empty(moe.moe_get_layout_workspace_size(T, E, R), dtype=torch.uint8, device=device)
         self.disp = moe.Dispatched(
@@ -230,12 +231,12 @@ class Step:
     def dispatch(self, fp8=False):
         self.moe.moe_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks,
                               self.lay.token_dst_row, self.cap, quantize_fp8=fp8,
-                              out=self.disp8 if fp8 else self.disp, status=self.status)
+                              out=self.disp8 if fp8 else self.disp, balance=self.bal_d, status=self.status)
 
     def dispatch_fp8_input(self):
         self.moe.moe_dispatch(self.x8, self.topk, self.wts, self.w.num_experts, self.w.num_ranks,
                               self.lay.token_dst_row, self.cap, x_scales=self.x8_scales, out=self.disp8in,
-                              status=self.status)
+                              balance=self.bal_d, status=self.status)
 
     def combine_weighted(self):
         self.moe.moe_combine_ex(self.partial, self.lay.token_dst_row, row_weights=self.row_w,
@@ -265,7 +266,7 @@ class Step:
 
     def dispatch_expand(self):
         self.moe.moe_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks, self.xrows,
-                              self.xcap, expand=True, out=self.dispx, status=self.status)
+                              self.xcap, expand=True, out=self.dispx, balance=self.bal_d, status=self.status)
 
     def combine_expand(self):
         self.moe.moe_combine_ex(self.partial_x, self.xrows, out=self.out, balance=self.bal, status=self.status)

@@ -74,6 +74,8 @@ def _load():
     lib.moe_get_expand_layout.restype = _I
     lib.moe_dispatch.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.moe_dispatch.restype = _I
+    lib.moe_dispatch_ex.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.moe_dispatch_ex.restype = _I
     lib.moe_layout_dispatch.argtypes = [_P, _I, _I, _P, _P, _I, _I, _I, MoeLayoutC, _P, ctypes.c_size_t, _I, _I, _P,
                                         _P, _P, _P, _P, _P, _P, _P]
     lib.moe_layout_dispatch.restype = _I
@@ -218,11 +220,14 @@ def moe_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional
                  num_experts: int, num_ranks: int, token_dst_row: torch.Tensor, recv_capacity: int, *,
                  quantize_fp8: bool = False, x_scales: Optional[torch.Tensor] = None, expand: bool = False,
                  out: Optional[Dispatched] = None, with_metadata: bool = True,
-                 status: Optional[torch.Tensor] = None, stream=None) -> Dispatched:
+                 balance: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                 stream=None) -> Dispatched:
     """Row copies and per-row metadata. ``x`` bf16 is copied as is, or quantised
     to E4M3 with per-128 scales when ``quantize_fp8``; ``x`` uint8 (E4M3 codes)
     is copied together with its ``x_scales`` [T, H/128]. With ``expand``,
-    ``token_dst_row`` is the expand layout's token_expert_row."""
+    ``token_dst_row`` is the expand layout's token_expert_row. ``balance``
+    (new_balance_counter()) calls moe_dispatch_ex, which spreads the last units
+    over the SMs."""
     T, H = x.shape
     k = topk_idx.shape[1]
     dev = x.device
@@ -244,11 +249,13 @@ def moe_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, topk_weights: Optional
                       (torch.empty(T, nb, dtype=torch.float32, device=dev) if quantize_fp8 else None)))
     status = new_status(dev) if status is None else status
     scales_arg = x_scales if fp8_in else out.x_scales
-    code = LIB.moe_dispatch(_ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), k, num_experts, num_ranks,
-                            _ptr(token_dst_row), recv_capacity, mode | (MOE_DISPATCH_EXPAND if expand else 0),
-                            _ptr(out.recv_x),
-                            _ptr(out.recv_x_scales), _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights),
-                            _ptr(out.recv_src_idx), _ptr(scales_arg), _ptr(status), _stream(stream))
+    args = (_ptr(x), T, H, _ptr(topk_idx), _ptr(topk_weights), k, num_experts, num_ranks, _ptr(token_dst_row),
+            recv_capacity, mode | (MOE_DISPATCH_EXPAND if expand else 0), _ptr(out.recv_x), _ptr(out.recv_x_scales),
+            _ptr(out.recv_topk_idx), _ptr(out.recv_topk_weights), _ptr(out.recv_src_idx), _ptr(scales_arg))
+    if balance is None:
+        code = LIB.moe_dispatch(*args, _ptr(status), _stream(stream))
+    else:
+        code = LIB.moe_dispatch_ex(*args, _ptr(balance), _ptr(status), _stream(stream))
     _check(code, "moe_dispatch")
     return out
 

@@ -69,8 +69,10 @@ struct DispatchArgs {
     moe_layout_t fl_out;      // layout outputs, written by CTA 0
     int loads_before_wait;    // first stage loads (input rows only) before the dependency wait
     // tail balancing: units [0, static_units) are dealt round-robin to the CTAs;
-    // the rest form a pool claimed through *pool (zeroed by the caller), so that
-    // CTAs on faster SMs take more of them (nullptr: every unit is dealt)
+    // the rest form a pool claimed through pool[0], so that CTAs on faster SMs
+    // take more of them; pool[1] counts the CTAs whose warps will claim no
+    // more, and the last of them zeroes both (they are zero at launch).
+    // nullptr: every unit is dealt.
     unsigned int *pool;
     int64_t static_units;
 };
@@ -358,7 +360,11 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
     // order (j) from a shared counter as they refill their stages, so that a
     // warp whose units had fewer destinations takes more of them.
     __shared__ int s_next_unit;
-    if (threadIdx.x == 0) s_next_unit = 0;
+    __shared__ int s_retired;   // warps of this CTA that claim no more
+    if (threadIdx.x == 0) {
+        s_next_unit = 0;
+        s_retired = 0;
+    }
     __syncthreads();
     if (!a.loads_before_wait) grid_dependency_wait();
     const int64_t G = gridDim.x;
@@ -374,12 +380,29 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         fence_barrier_init();
     }
 
+    // lane 0: once a claim finds nothing the warp claims no more and counts
+    // itself out; the CTA's last warp counts the CTA out of the pool, and the
+    // last CTA of the grid re-arms it (no tail barrier: the other warps may
+    // still be storing)
+    bool exhausted = false;
+    auto retire = [&]() {
+        exhausted = true;
+        if (a.pool != nullptr && atomicAdd(&s_retired, 1) == (int)(blockDim.x >> 5) - 1 &&
+            atomicAdd(a.pool + 1, 1u) == gridDim.x - 1) {
+            *reinterpret_cast<volatile unsigned int *>(a.pool) = 0u;
+            *reinterpret_cast<volatile unsigned int *>(a.pool + 1) = 0u;
+        }
+    };
     auto claim = [&]() -> int64_t {   // lane 0; -1 once the CTA's units (and the pool) are exhausted
+        if (exhausted) return -1;
         const int64_t j = atomicAdd(&s_next_unit, 1);
         if (j < cta_units) return (int64_t)blockIdx.x + j * G;
-        if (a.pool == nullptr) return -1;
-        const int64_t p = dealt + (int64_t)atomicAdd(a.pool, 1u);
-        return p < a.num_units ? p : -1;
+        if (a.pool != nullptr) {
+            const int64_t p = dealt + (int64_t)atomicAdd(a.pool, 1u);
+            if (p < a.num_units) return p;
+        }
+        retire();
+        return -1;
     };
     auto issue_load = [&](int64_t u, int s) {   // lane 0
         const int64_t t = div_count(u, a.num_chunks);
@@ -568,7 +591,10 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         }
         __syncwarp();
     }
-    if (lane == 0) bulk_wait_all();
+    if (lane == 0) {
+        if (!exhausted) retire();   // a warp that stopped early (timeout) still counts itself out
+        bulk_wait_all();
+    }
 }
 
 // ------------------------------------------------------------------ FP8 dispatch, row pipeline
@@ -849,13 +875,6 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     a.num_units = (int64_t)num_tokens * a.num_chunks;
-    const int pool_pct = tu.dispatch_pool;
-    if (a.pool != nullptr && pool_pct > 0 && pool_pct < 100) {
-        a.static_units = a.num_units * (100 - pool_pct) / 100;
-    } else {
-        a.pool = nullptr;
-        a.static_units = a.num_units;
-    }
     a.stages = std::min(kMaxStages, std::max(3, tu.dispatch_stages));   // the unit ring needs three
     // stages take at most ~200 KB, so that some L1 cache is left (a full 227 KB of
     // stages measured slower)
@@ -885,6 +904,14 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     if (tu.ctas_per_sm > 0) ctas_per_sm = std::min(ctas_per_sm, tu.ctas_per_sm);
     const int64_t want = (a.num_units + warps - 1) / warps;
     grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)device_sm_count() * ctas_per_sm));
+    // tail balancing pays off only with several units per CTA
+    const int pool_pct = tu.dispatch_pool;
+    if (a.pool != nullptr && pool_pct > 0 && pool_pct < 100 && a.num_units >= 8 * (int64_t)grid) {
+        a.static_units = a.num_units * (100 - pool_pct) / 100;
+    } else {
+        a.pool = nullptr;
+        a.static_units = a.num_units;
+    }
     return MOE_OK;
 }
 

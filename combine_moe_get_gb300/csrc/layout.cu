@@ -705,7 +705,7 @@ size_t layout_workspace_bytes(int T, int E, int R) { return ws_layout(T, E, R).t
 
 unsigned int *layout_spare_counter(const LayoutLaunch &L) {
     if (L.num_tokens <= kTile || L.workspace == nullptr) return nullptr;   // one tile (or none): no clear
-    return &static_cast<WsHeader *>(L.workspace)->pad[0];
+    return &static_cast<WsHeader *>(L.workspace)->pad[0];                  // pad[0], pad[1]
 }
 
 int launch_layout(const LayoutLaunch &L) {

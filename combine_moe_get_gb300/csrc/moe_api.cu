@@ -325,6 +325,22 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
     return rc != MOE_OK ? rc : moe::launch_dispatch(L);
 }
 
+MOE_API int moe_dispatch_ex(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                            const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                            const int32_t *token_dst_row, int recv_capacity, int mode, void *recv_x,
+                            float *recv_x_scales, int64_t *recv_topk_idx, float *recv_topk_weights,
+                            int32_t *recv_src_idx, float *x_scales, uint32_t *balance, int32_t *status,
+                            void *stream) {
+    if (!aligned(balance, 8)) return MOE_ERR_MISALIGNED;
+    moe::DispatchLaunch L;
+    const int rc = dispatch_prepare(x, num_tokens, hidden, topk_idx, topk_weights, num_topk, num_experts, num_ranks,
+                                    token_dst_row, recv_capacity, mode, recv_x, recv_x_scales, recv_topk_idx,
+                                    recv_topk_weights, recv_src_idx, x_scales, status, stream, L);
+    if (rc != MOE_OK) return rc;
+    L.pool = balance;
+    return moe::launch_dispatch(L);
+}
+
 MOE_API int moe_layout_dispatch(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
                                 const float *topk_weights, int num_topk, int num_experts, int num_ranks,
                                 moe_layout_t layout, void *workspace, size_t workspace_bytes, int recv_capacity,

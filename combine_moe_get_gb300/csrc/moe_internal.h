@@ -52,9 +52,9 @@ struct LayoutLaunch {
 
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 int launch_layout(const LayoutLaunch &L);
-// A 32-bit word of the layout workspace that launch_layout(L) clears and then
-// leaves alone, free for the next launch of the same call; nullptr when the
-// launch clears nothing (a batch of one tile).
+// Two 32-bit words of the layout workspace that launch_layout(L) clears and
+// then leaves alone, free for the next launch of the same call; nullptr when
+// the launch clears nothing (a batch of one tile).
 unsigned int *layout_spare_counter(const LayoutLaunch &L);
 
 struct ExpandLaunch {
@@ -94,7 +94,8 @@ struct DispatchLaunch {
     // own dependency wait before letting this grid launch: the input rows are
     // complete, so the first stage loads may be issued before the wait
     bool loads_before_wait = false;
-    // optional zeroed counter for tail balancing (a pool of units shared by all CTAs)
+    // optional: two zeroed uint32 for tail balancing (a pool of units shared by all
+    // CTAs); the launch leaves them zeroed
     unsigned int *pool = nullptr;
 };
 

@@ -241,6 +241,30 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
                          int32_t *status, void *stream);
 
 /*
+ * moe_dispatch_ex -- moe_dispatch with a balance counter (a library addition,
+ * as for moe_combine_ex; results do not depend on it).
+ *
+ *   balance   NULL, or 2 uint32 of device memory, 8-byte aligned, zero before
+ *             the first call that uses them; every call leaves them zero again
+ *             (the last CTA to finish clears them, also after a timeout). With
+ *             it, half of the (token, chunk) units are dealt round-robin to the
+ *             CTAs and the rest are claimed one by one, so that CTAs on SMs with
+ *             more bandwidth take more of them (at DSv3 the SMs finished a
+ *             statically split dispatch 39-59 us apart). Used by the bf16,
+ *             pass-through and expand modes; the quantising FP8 row pipeline and
+ *             batches of fewer than 8 units per CTA ignore it. Two calls that use
+ *             the same counter must not run at the same time on the GPU.
+ *             Misaligned: MOE_ERR_MISALIGNED.
+ * Other arguments, errors and limits as for moe_dispatch.
+ */
+MOE_API int moe_dispatch_ex(const void *x, int num_tokens, int hidden, const int64_t *topk_idx,
+                            const float *topk_weights, int num_topk, int num_experts, int num_ranks,
+                            const int32_t *token_dst_row, int recv_capacity, int mode, void *recv_x,
+                            float *recv_x_scales, int64_t *recv_topk_idx, float *recv_topk_weights,
+                            int32_t *recv_src_idx, float *x_scales, uint32_t *balance, int32_t *status,
+                            void *stream);
+
+/*
  * moe_layout_dispatch -- moe_get_layout followed by moe_dispatch, in one
  * launch for small batches (decode).
  *
@@ -251,7 +275,12 @@ MOE_API int moe_dispatch(const void *x, int num_tokens, int hidden, const int64_
  * layout itself in shared memory -- no CTA waits on another -- while its first
  * row loads are in flight, then stores the rows; the layout outputs are written
  * to `layout` as moe_get_layout writes them. Larger batches (or when the tuning
- * switch MOE_TUNE_FUSED_SMALL=2 is set) take the two launches. Outputs, order,
+ * switch MOE_TUNE_FUSED_SMALL=2 is set) take the two launches. On that path
+ * the dispatch is launched to overlap the layout: its CTAs load input rows
+ * while the layout runs (the layout has passed its own dependency wait, so the
+ * rows are complete) and read the layout's outputs only after it ends. It also
+ * balances its tail as moe_dispatch_ex does, with two words of the workspace
+ * that the layout clears as its counter. Outputs, order,
  * metadata and errors are exactly those of moe_get_layout + moe_dispatch with
  * the same arguments.
  *

@@ -189,3 +189,19 @@ def _combine_ex(lib, partial=A, rows=256, T=128, H=256, k=2, dst=A + 0x10000, ro
 ])
 def test_combine_ex_rejects_bad_arguments(lib, kw, code):
     assert _combine_ex(lib, **kw) == code
+
+
+def _dispatch_ex(lib, balance=A + 0x500000, **kw):
+    d = dict(x=A, T=128, H=256, topk=A + 0x10000, w=None, k=2, E=16, R=4, dst=A + 0x20000, cap=256, fp8=0,
+             recv=A + 0x100000, scales=None, status=A + 0x300000)
+    d.update(kw)
+    return lib.LIB.moe_dispatch_ex(d["x"], d["T"], d["H"], d["topk"], d["w"], d["k"], d["E"], d["R"], d["dst"],
+                                   d["cap"], d["fp8"], d["recv"], d["scales"], None, None, None, None, balance,
+                                   d["status"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(balance=A + 4), 2), (dict(H=12), 1), (dict(x=A + 8), 2), (dict(status=None), 1), (dict(fp8=3), 1),
+])
+def test_dispatch_ex_rejects_bad_arguments(lib, kw, code):
+    assert _dispatch_ex(lib, **kw) == code

@@ -334,6 +334,42 @@ def test_dispatch_fp8_many_rows_per_cta_small_rows(moe, T, H):
     check_dispatch(moe, inp, E, R, True)
 
 
+@pytest.mark.parametrize("T,H,k,E,R,mode", [(4096, 7168, 8, 256, 8, "bf16"), (2000, 1024, 8, 256, 8, "fp8in"),
+                                            (3000, 512, 6, 48, 3, "bf16"), (100, 256, 8, 64, 8, "bf16")])
+def test_dispatch_balanced_parity(moe, T, H, k, E, R, mode):
+    # a balance counter changes which CTA copies which unit, never a byte; each call leaves it zero
+    g = torch.Generator().manual_seed(T + H + k)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.15)
+    w = wl.make_weights(g, T, k)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk.to(DEV), E, R, status=status)
+    cap = wl.recv_capacity(T, k, R)
+    ref_lay = oracle.layout(topk.numpy(), E, R)
+    if mode == "fp8in":
+        rng = np.random.default_rng(T)
+        x = torch.from_numpy(rng.integers(0, 256, (T, H), dtype=np.uint8))
+        sc = torch.from_numpy(rng.standard_normal((T, H // 128)).astype(np.float32))
+        ref = oracle.dispatch_fp8_input(x.numpy(), sc.numpy(), topk.numpy(), w.numpy(), E, R, ref_lay["token_dst_row"], cap)
+    else:
+        x, sc = wl.make_x(g, T, H), None
+        ref = oracle.dispatch(bits16(x), topk.numpy(), w.numpy(), E, R, ref_lay["token_dst_row"], cap)
+    bal = moe.new_balance_counter(DEV)
+    N = ref_lay["num_recv"]
+    for _ in range(2):
+        out = moe.moe_dispatch(x.to(DEV), topk.to(DEV), w.to(DEV), E, R, lay.token_dst_row, cap,
+                               x_scales=None if sc is None else sc.to(DEV), balance=bal, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0 and bal.tolist() == [0, 0]
+        if mode == "fp8in":
+            np.testing.assert_array_equal(out.recv_x[:N].cpu().numpy(), ref["recv_x"][:N])
+            np.testing.assert_array_equal(out.recv_x_scales[:N].cpu().numpy().view(np.uint32),
+                                          ref["recv_x_scales"][:N].view(np.uint32))
+        else:
+            np.testing.assert_array_equal(bits16(out.recv_x[:N]), ref["recv_x"][:N])
+        np.testing.assert_array_equal(out.recv_src_idx[:N].cpu().numpy(), ref["recv_src_idx"][:N])
+        np.testing.assert_array_equal(out.recv_topk_idx[:N].cpu().numpy(), ref["recv_topk_idx"][:N])
+
+
 def test_dispatch_capacity_overflow_writes_nothing_beyond(moe):
     w = wl.CONFIGS["tiny"]
     inp = wl.make_inputs(w, with_partial=False)
