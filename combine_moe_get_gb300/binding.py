@@ -40,7 +40,8 @@ class MoeLayoutC(ctypes.Structure):
 
 
 class MoeLayoutOptionsC(ctypes.Structure):
-    _fields_ = [("wait_timeout_ns", ctypes.c_int64), ("test_unpublished_tile", ctypes.c_int32)]
+    _fields_ = [("wait_timeout_ns", ctypes.c_int64), ("test_unpublished_tile", ctypes.c_int32),
+                ("layout_mode", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -158,8 +159,9 @@ def moe_get_layout_workspace_size(num_tokens: int, num_experts: int, num_ranks: 
 def moe_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
                    out: Optional[Layout] = None, workspace: Optional[torch.Tensor] = None,
                    status: Optional[torch.Tensor] = None, stream=None,
-                   wait_timeout_ns: int = 0, test_unpublished_tile: int = -1) -> Layout:
-    """Counts, membership, prefixes and receive rows of ``topk_idx`` [T, k] int64."""
+                   wait_timeout_ns: int = 0, test_unpublished_tile: int = -1, layout_mode: int = 0) -> Layout:
+    """Counts, membership, prefixes and receive rows of ``topk_idx`` [T, k] int64.
+    ``layout_mode`` 1 keeps the call off the cluster mode (same outputs)."""
     T, k = topk_idx.shape
     dev = topk_idx.device
     out = out or Layout.empty(T, k, num_experts, num_ranks, dev)
@@ -167,7 +169,7 @@ def moe_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     status = new_status(dev) if status is None else status
-    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile))
+    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile), int(layout_mode))
     code = LIB.moe_get_layout_ex(_ptr(topk_idx), T, k, num_experts, num_ranks, out.c(), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream),
                                  ctypes.byref(opts))
@@ -192,7 +194,7 @@ def moe_get_expand_layout(topk_idx: torch.Tensor, expert_prefix: torch.Tensor, n
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     status = new_status(dev) if status is None else status
-    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile))
+    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile), 0)
     code = LIB.moe_get_expand_layout(_ptr(topk_idx), T, k, num_experts, _ptr(expert_prefix), _ptr(out),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
                                      _stream(stream), ctypes.byref(opts))

@@ -908,6 +908,10 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     const int pool_pct = tu.dispatch_pool;
     if (a.pool != nullptr && pool_pct > 0 && pool_pct < 100 && a.num_units >= 8 * (int64_t)grid) {
         a.static_units = a.num_units * (100 - pool_pct) / 100;
+        // claims made before the dependency wait (the first stage of every warp) stay in the
+        // dealt units: the pool's counter may be zeroed by the launch before this one
+        if (a.loads_before_wait)
+            a.static_units = std::max(a.static_units, std::min(a.num_units, (int64_t)grid * warps * a.stages));
     } else {
         a.pool = nullptr;
         a.static_units = a.num_units;

@@ -202,6 +202,8 @@ struct TileArgs {
     uint64_t timeout_ns;
     int unpublished_tile;  // test hook: this tile never publishes its status (-1 = none)
     int early_dependents;  // trigger the next grid's launch right after the dependency wait
+    int cl_tile;           // cluster mode: tokens per CTA (a multiple of 32)
+    unsigned int *spare;   // cluster mode: two workspace words to zero for the next launch (the others clear them)
 };
 
 template <bool kCooperative>
@@ -647,6 +649,232 @@ __global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
     }
 }
 
+
+// ------------------------------------------------------------------ cluster mode
+//
+// One thread-block cluster of C CTAs (1024 threads each) covers the whole
+// batch, each CTA a contiguous tile of cl_tile tokens. The tiles exchange their
+// per-rank counts and expert histograms through distributed shared memory
+// between two cluster barriers, so there is no global exchange state: no
+// workspace clear, no flags, no waits that could expire. Everything else is
+// the direct mode's: pass 1 over (token, entry) lanes, word prefixes of the
+// membership bitmap, receive rows from the ranks' exclusive prefixes.
+
+constexpr int kCThreads = 1024;
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kClusterMaxTile = 512;     // tokens per CTA
+constexpr int kClusterMax = 16;          // CTAs per cluster
+
+// Shared memory: bitmap u32 [W][R] | word prefix u16 [R][W] | exclusive prefix
+// i32 [R] | rank totals i32 [R+1] | own rank counts i32 [R] | expert
+// histogram i32 [E+1] | expert totals i32 [E+1] | entry expert i16 [tile*k] |
+// entry rank i16 [tile*k]
+struct ClusterSmem {
+    size_t wprefix, excl, tot, cnt, hist, htot, ent, rk, total;
+};
+
+__host__ __device__ inline ClusterSmem cluster_smem(int tile, int E, int R, int k) {
+    const size_t W = (size_t)tile / 32;
+    ClusterSmem c;
+    c.wprefix = align_up(W * R * 4, 16);
+    c.excl = c.wprefix + align_up(W * R * 2, 16);
+    c.tot = c.excl + align_up((size_t)R * 4, 16);
+    c.cnt = c.tot + align_up((size_t)(R + 1) * 4, 16);
+    c.hist = c.cnt + align_up((size_t)R * 4, 16);
+    c.htot = c.hist + align_up((size_t)(E + 1) * 4, 16);
+    c.ent = c.htot + align_up((size_t)(E + 1) * 4, 16);
+    c.rk = c.ent + align_up((size_t)tile * k * 2, 16);
+    c.total = c.rk + align_up((size_t)tile * k * 2, 16);
+    return c;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32-bit load from the shared memory of CTA `rank` of this cluster, at the
+// offset of `local` in this CTA's shared memory
+__device__ __forceinline__ int32_t ld_cluster_i32(const void *local, uint32_t rank) {
+    uint32_t remote;
+    int32_t v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+__global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int R = a.R, E = a.E, k = a.k, tile = a.cl_tile, W = tile / 32;
+    const ClusterSmem sl = cluster_smem(tile, E, R, k);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem);
+    uint16_t *wprefix = reinterpret_cast<uint16_t *>(smem + sl.wprefix);
+    int32_t *excl = reinterpret_cast<int32_t *>(smem + sl.excl);
+    int32_t *tot = reinterpret_cast<int32_t *>(smem + sl.tot);
+    int32_t *cnt = reinterpret_cast<int32_t *>(smem + sl.cnt);
+    int32_t *hist = reinterpret_cast<int32_t *>(smem + sl.hist);
+    int32_t *htot = reinterpret_cast<int32_t *>(smem + sl.htot);
+    int16_t *ent = reinterpret_cast<int16_t *>(smem + sl.ent);   // expert of each entry, then its owned rank
+    int16_t *rk = reinterpret_cast<int16_t *>(smem + sl.rk);     // rank of each entry
+
+    const int C = (int)gridDim.x;              // one cluster spans the grid
+    const int c = (int)cluster_ctarank();
+    const int t0 = c * tile;
+    const int tcount = max(0, min(tile, a.T - t0));
+    const int n_ent = tcount * k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    grid_dependency_wait();
+    if (a.early_dependents) grid_launch_dependents();
+    if (c == 0 && threadIdx.x == 0 && a.spare != nullptr) {   // the workspace is not cleared in this mode
+        a.spare[0] = 0u;
+        a.spare[1] = 0u;
+    }
+
+    for (int i = threadIdx.x; i < R * W; i += kCThreads) bitmap[i] = 0u;
+    for (int i = threadIdx.x; i <= E; i += kCThreads) hist[i] = 0;
+    for (int r = threadIdx.x; r <= R; r += kCThreads) tot[r] = 0;
+    for (int r = threadIdx.x; r < R; r += kCThreads) excl[r] = 0;
+    // the tile's entries: expert and rank ids (-1: masked or invalid), 8 loads in flight per thread
+    for (int base = threadIdx.x; base < n_ent; base += 8 * kCThreads) {
+        int64_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * kCThreads;
+            v[u] = i < n_ent ? ld_nc_i64(a.topk + (int64_t)t0 * k + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * kCThreads;
+            if (i < n_ent) {
+                const bool ok = v[u] >= 0 && v[u] < E;
+                if (!ok && v[u] != -1) report(a.status, MOE_ERR_BAD_TOPK);
+                ent[i] = ok ? (int16_t)v[u] : (int16_t)-1;
+                rk[i] = ok ? (int16_t)((int)v[u] / a.m) : (int16_t)-1;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- pass 1, lanes over (token, entry): expert histogram, each rank of a token
+    //      once (__match_any_sync; the lowest entry owns it), membership bits;
+    //      ent[] becomes the owned rank (or -1)
+    {
+        const int tpp = 32 / k;
+        const int sub = lane / k, j = lane - sub * k;
+        const bool lane_used = sub < tpp;
+        for (int base = warp * tpp; base < tcount; base += kCWarps * tpp) {
+            const int tl = base + sub;
+            const bool act = lane_used && tl < tcount;
+            const int r = act ? (int)rk[tl * k + j] : -1;
+            if (r >= 0) atomicAdd(&hist[ent[tl * k + j]], 1);
+            const unsigned peers = __match_any_sync(0xffffffffu, r >= 0 ? sub * R + r : -(lane + 1));
+            const bool owner = r >= 0 && (__ffs(peers) - 1) == lane;
+            if (owner) atomicOr(&bitmap[(tl >> 5) * R + r], 1u << (tl & 31));
+            if (act) ent[tl * k + j] = (int16_t)(owner ? r : -1);
+        }
+    }
+    __syncthreads();
+
+    // ---- this tile's rank counts and word prefixes
+    for (int r = threadIdx.x; r < R; r += kCThreads) {
+        uint32_t run = 0;
+        for (int w = 0; w < W; ++w) {
+            wprefix[r * W + w] = (uint16_t)run;
+            run += __popc(bitmap[w * R + r]);
+        }
+        cnt[r] = (int32_t)run;
+    }
+
+    // ---- exchange through distributed shared memory: every tile's counts are
+    //      complete after the first barrier and read before the second
+    cluster_sync_all();
+    for (int idx = threadIdx.x; idx < C * R; idx += kCThreads) {
+        const int cc = idx / R, r = idx - cc * R;
+        const int32_t v = ld_cluster_i32(cnt + r, (uint32_t)cc);
+        if (cc < c) atomicAdd(&excl[r], v);
+        atomicAdd(&tot[r], v);
+    }
+    if (c == 0) {   // expert totals: all C tiles' counts of an expert in flight at once
+        for (int e = threadIdx.x; e < E; e += kCThreads) {
+            int32_t v[kClusterMax];
+#pragma unroll
+            for (int cc = 0; cc < kClusterMax; ++cc) v[cc] = cc < C ? ld_cluster_i32(hist + e, (uint32_t)cc) : 0;
+            int32_t s = 0;
+#pragma unroll
+            for (int cc = 0; cc < kClusterMax; ++cc) s += v[cc];
+            htot[e] = s;
+        }
+    }
+    cluster_sync_all();   // no tile reads another's shared memory after this
+
+    // ---- rank regions (warp 0) and, on tile 0, expert counts and prefix (warp 1)
+    if (warp == 0) {
+        if (c == 0)
+            for (int r = lane; r < R; r += 32) a.num_tokens_per_rank[r] = tot[r];
+        __syncwarp();
+        warp_exclusive_scan(tot, R, lane);
+    } else if (warp == 1 && c == 0) {
+        for (int e = lane; e < E; e += 32) a.num_tokens_per_expert[e] = htot[e];
+        __syncwarp();
+        warp_exclusive_scan(htot, E, lane);
+        __syncwarp();
+        for (int e = lane; e <= E; e += 32) a.expert_prefix[e] = htot[e];
+    }
+    __syncthreads();
+    for (int r = threadIdx.x; r < R; r += kCThreads) {
+        excl[r] += tot[r];
+        if (c == 0) a.rank_prefix[r] = tot[r];
+    }
+    if (c == 0 && threadIdx.x == 0) a.rank_prefix[R] = tot[R];
+    __syncthreads();
+
+    // ---- pass 2: global receive rows of the owning entries
+    for (int i = threadIdx.x; i < n_ent; i += kCThreads) {
+        const int r = ent[i];
+        int32_t v = -1;
+        if (r >= 0) {
+            const int tl = i / k;
+            const uint32_t word = bitmap[(tl >> 5) * R + r];
+            v = excl[r] + wprefix[r * W + (tl >> 5)] + __popc(word & ((1u << (tl & 31)) - 1u));
+        }
+        a.token_dst_row[(int64_t)t0 * k + i] = v;
+    }
+
+    // ---- is_token_in_rank rows: one warp per token row when rows are long, flat otherwise
+    uint8_t *dst = a.is_token_in_rank + (int64_t)t0 * R;
+    if ((R & 3) == 0 && R >= 128) {
+        for (int tl = warp; tl < tcount; tl += kCWarps) {
+            const uint32_t *wrow = bitmap + (tl >> 5) * R;
+            const int b = tl & 31;
+            for (int r0 = 4 * lane; r0 < R; r0 += 128) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(wrow + r0);
+                const uint32_t v = ((q.x >> b) & 1u) | (((q.y >> b) & 1u) << 8) | (((q.z >> b) & 1u) << 16) |
+                                   (((q.w >> b) & 1u) << 24);
+                *reinterpret_cast<uint32_t *>(dst + (int64_t)tl * R + r0) = v;
+            }
+        }
+    } else if ((R & 3) == 0) {
+        uint32_t *dst4 = reinterpret_cast<uint32_t *>(dst);
+        for (int i = threadIdx.x; i < tcount * R / 4; i += kCThreads) {
+            const int tl = (i * 4) / R, r0 = (i * 4) - tl * R;
+            uint32_t v = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v |= ((bitmap[(tl >> 5) * R + r0 + b] >> (tl & 31)) & 1u) << (8 * b);
+            dst4[i] = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < tcount * R; i += kCThreads) {
+            const int tl = i / R, r = i - tl * R;
+            dst[i] = (uint8_t)((bitmap[(tl >> 5) * R + r] >> (tl & 31)) & 1u);
+        }
+    }
+}
+
 __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, int m,
                                    const int32_t *__restrict__ rank_prefix, int32_t *__restrict__ token_dst_row) {
     grid_dependency_wait();
@@ -703,6 +931,73 @@ int launch_cooperative(const void *kernel, int grid, size_t smem, cudaStream_t s
 
 size_t layout_workspace_bytes(int T, int E, int R) { return ws_layout(T, E, R).total; }
 
+namespace {
+
+// Cluster mode for this batch: CTAs and tokens per CTA, or false (the batch is
+// one tile, too large, or clusters of that size cannot be scheduled).
+bool cluster_config(int T, int E, int R, int k, int &C, int &tile, size_t &smem) {
+    const int want = tuning().layout_cluster;
+    if ((want != 8 && want != 16) || T <= kTile || T > want * kClusterMaxTile) return false;
+    C = want;
+    tile = (int)align_up((size_t)((T + C - 1) / C), 32);
+    smem = cluster_smem(tile, E, R, k).total;
+    if (smem > device_smem_optin()) return false;
+    // whether a cluster of C such CTAs fits on this device (cached per device, size and shared memory)
+    struct Entry { int dev, C; size_t smem; bool ok; };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int n_cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < std::min(n_cached, 16); ++i)
+        if (cache[i].dev == dev && cache[i].C == C && cache[i].smem == smem) return cache[i].ok;
+    bool ok = ensure_dynamic_smem((const void *)layout_cluster_kernel, smem) == MOE_OK;
+    if (ok && C > 8)
+        ok = cudaFuncSetAttribute((const void *)layout_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                  1) == cudaSuccess;
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)C);
+        cfg.blockDim = dim3(kCThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        ok = cudaOccupancyMaxActiveClusters(&clusters, (const void *)layout_cluster_kernel, &cfg) == cudaSuccess &&
+             clusters >= 1;
+    }
+    cudaGetLastError();   // a refused attribute or query only means: no cluster mode
+    cache[n_cached % 16] = Entry{dev, C, smem, ok};
+    ++n_cached;
+    return ok;
+}
+
+int launch_cluster(int C, size_t smem, cudaStream_t s, bool overlap, TileArgs &a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)C);
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, layout_cluster_kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
 unsigned int *layout_spare_counter(const LayoutLaunch &L) {
     if (L.num_tokens <= kTile || L.workspace == nullptr) return nullptr;   // one tile (or none): no clear
     return &static_cast<WsHeader *>(L.workspace)->pad[0];                  // pad[0], pad[1]
@@ -721,6 +1016,9 @@ int launch_layout(const LayoutLaunch &L) {
         return MOE_OK;
     }
     const WsLayout w = ws_layout(T, E, R);
+    int cl_C = 0, cl_tile = 0;
+    size_t cl_smem = 0;
+    const bool cluster = !L.no_cluster && cluster_config(T, E, R, k, cl_C, cl_tile, cl_smem);
     const size_t smem = smem_layout(E, R, k).total;
     // direct mode: tile size, kernel instance and whether all its tiles fit on the GPU at once
     int dt = direct_tile(T, R);
@@ -732,10 +1030,12 @@ int launch_layout(const LayoutLaunch &L) {
         ensure_dynamic_smem((const void *)layout_tiles_kernel<false>, smem) != MOE_OK)
         return MOE_ERR_CUDA;
     if (dt && (T + dt - 1) / dt > cooperative_capacity(direct, dsmem)) dt = 0;
+    if (cluster) dt = 0;
     const int tile_tokens = dt ? dt : kTile;
     const int num_tiles = (T + tile_tokens - 1) / tile_tokens;
-    // a single-tile direct launch uses no workspace
-    if (!(dt && num_tiles == 1) && cudaMemsetAsync(L.workspace, 0, w.total, s) != cudaSuccess) return MOE_ERR_CUDA;
+    // a single-tile direct launch and the cluster mode use no workspace
+    if (!cluster && !(dt && num_tiles == 1) && cudaMemsetAsync(L.workspace, 0, w.total, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
 
     TileArgs a;
     a.topk = L.topk_idx;
@@ -755,6 +1055,9 @@ int launch_layout(const LayoutLaunch &L) {
     a.timeout_ns = L.timeout_ns > 0 ? (uint64_t)L.timeout_ns : kDefaultWaitNs;
     a.unpublished_tile = L.unpublished_tile;
     a.early_dependents = L.early_dependents ? 1 : 0;
+    a.cl_tile = cl_tile;
+    a.spare = layout_spare_counter(L);
+    if (cluster) return launch_cluster(cl_C, cl_smem, s, tuning().overlap != 0, a);
 
     if (dt) {
         if (a.num_tiles == 1) {     // nothing to exchange: an ordinary launch (dt == kTile)

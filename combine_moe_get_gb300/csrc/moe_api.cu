@@ -112,6 +112,7 @@ const Tuning &tuning() {
         x.overlap = env_int("MOE_TUNE_OVERLAP", 1) == 1;   // any other value: ordinary launches
         x.dispatch_pool = env_int("MOE_TUNE_DISPATCH_POOL", 50);
         x.combine_pool = env_int("MOE_TUNE_COMBINE_POOL", 30);
+        x.layout_cluster = env_int("MOE_TUNE_LAYOUT_CLUSTER", 16);
         x.fp8_rows = env_int("MOE_TUNE_FP8_ROWS", 1) == 1;
         x.fp8_in_slots = env_int("MOE_TUNE_FP8_IN_SLOTS", 8);
         x.fp8_quant_warps = env_int("MOE_TUNE_FP8_QUANT_WARPS", 24);
@@ -168,7 +169,7 @@ MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, in
 
 static int layout_prepare(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
                           size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
-                          int unpublished_tile, moe::LayoutLaunch &L) {
+                          int unpublished_tile, moe::LayoutLaunch &L, bool no_cluster = false) {
     if (!shape_ok(T, k, E, R)) return MOE_ERR_INVALID_ARG;
     if ((int64_t)T * R >= (int64_t)1 << 40) return MOE_ERR_INVALID_ARG;
     if (!status || !o.num_tokens_per_rank || !o.num_tokens_per_expert || !o.rank_prefix || !o.expert_prefix)
@@ -194,15 +195,16 @@ static int layout_prepare(const int64_t *topk_idx, int T, int k, int E, int R, m
     L.stream = stream;
     L.timeout_ns = timeout_ns;
     L.unpublished_tile = unpublished_tile;
+    L.no_cluster = no_cluster || unpublished_tile >= 0;
     return MOE_OK;
 }
 
 static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
                          size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
-                         int unpublished_tile) {
+                         int unpublished_tile, bool no_cluster = false) {
     moe::LayoutLaunch L;
     const int rc = layout_prepare(topk_idx, T, k, E, R, o, workspace, workspace_bytes, status, stream, timeout_ns,
-                                  unpublished_tile, L);
+                                  unpublished_tile, L, no_cluster);
     return rc != MOE_OK ? rc : moe::launch_layout(L);
 }
 
@@ -218,12 +220,15 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
                               int32_t *status, void *stream, const moe_layout_options_t *options) {
     int64_t timeout = 0;
     int unpublished = -1;
+    bool no_cluster = false;
     if (options) {
         timeout = options->wait_timeout_ns;
         unpublished = options->test_unpublished_tile;
+        if (options->layout_mode != 0 && options->layout_mode != 1) return MOE_ERR_INVALID_ARG;
+        no_cluster = options->layout_mode == 1;
     }
     return layout_common(topk_idx, num_tokens, num_topk, num_experts, num_ranks, layout, workspace,
-                         workspace_bytes, status, stream, timeout, unpublished);
+                         workspace_bytes, status, stream, timeout, unpublished, no_cluster);
 }
 
 MOE_API size_t moe_get_expand_layout_workspace_size(int num_tokens, int num_experts) {

@@ -33,6 +33,7 @@ struct Tuning {
     int overlap;        // programmatic dependent launch of every non-cooperative kernel
     int dispatch_pool;  // % of dispatch units left to a shared pool when a cleared counter is at hand (>= 100: off)
     int combine_pool;   // % of combine tokens left to a shared pool when the caller gives a counter (>= 100: off)
+    int layout_cluster; // CTAs of the cluster-mode layout (8 or 16; other values: off)
 };
 const Tuning &tuning();
 
@@ -48,13 +49,15 @@ struct LayoutLaunch {
     // let the next grid on the stream launch as soon as every CTA has passed its
     // dependency wait (the next launch is this library's dispatch)
     bool early_dependents = false;
+    bool no_cluster = false;   // never the cluster mode
 };
 
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 int launch_layout(const LayoutLaunch &L);
-// Two 32-bit words of the layout workspace that launch_layout(L) clears and
-// then leaves alone, free for the next launch of the same call; nullptr when
-// the launch clears nothing (a batch of one tile).
+// Two 32-bit words of the layout workspace that launch_layout(L) zeroes (with
+// the workspace clear, or from the cluster-mode kernel) and then leaves alone,
+// free for the next launch of the same call -- which may rely on them only
+// after its dependency wait; nullptr for a batch of one tile.
 unsigned int *layout_spare_counter(const LayoutLaunch &L);
 
 struct ExpandLaunch {

@@ -118,11 +118,17 @@ typedef struct {
      * global timer; <= 0 selects the default (1 s). On expiry the kernel writes
      * MOE_ERR_TIMEOUT to *status and finishes without waiting further. */
     int64_t wait_timeout_ns;
-    /* Failure-injection hook for tests: the tile of 128 tokens with this index
-     * never publishes its scan status, so that the tiles after it (and the
-     * final count step) run out of their bounded waits and report
-     * MOE_ERR_TIMEOUT. -1 = off (the only value for production use). */
+    /* Failure-injection hook for tests: the tile with this index (64 or 128
+     * tokens, as the mode sizes it) never publishes its scan status, so that
+     * the tiles after it (and the final count step) run out of their bounded
+     * waits and report MOE_ERR_TIMEOUT. Naming a tile also keeps the call off
+     * the cluster mode, which has no waits. -1 = off (the only value for
+     * production use). */
     int32_t test_unpublished_tile;
+    /* 0: the mode is chosen by size (the cluster mode for 129..4096 tokens
+     * where the device can schedule it); 1: never the cluster mode (the
+     * direct or lookback mode by size). Both give the same outputs. */
+    int32_t layout_mode;
 } moe_layout_options_t;
 
 /*

@@ -205,3 +205,10 @@ def _dispatch_ex(lib, balance=A + 0x500000, **kw):
 ])
 def test_dispatch_ex_rejects_bad_arguments(lib, kw, code):
     assert _dispatch_ex(lib, **kw) == code
+
+
+def test_layout_ex_rejects_unknown_mode(lib):
+    opts = lib.MoeLayoutOptionsC(0, -1, 2)
+    code = lib.LIB.moe_get_layout_ex(A, 128, 2, 16, 4, _layout_struct(lib), A + 0x100000, 1 << 30, A + 0x200000, None,
+                                     ctypes.byref(opts))
+    assert code == 1

@@ -53,11 +53,12 @@ def topk_for(w: wl.Workload, T=None):
 
 # ------------------------------------------------------------------ layout
 
+@pytest.mark.parametrize("layout_mode", [0, 1])   # 1: never the cluster mode
 @pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode", "layout_2048", "layout_2048_1m"])
-def test_layout_parity_configs(moe, name):
+def test_layout_parity_configs(moe, name, layout_mode):
     w = wl.CONFIGS[name]
     topk = topk_for(w)
-    _, got, st = gpu_layout(moe, topk, w.num_experts, w.num_ranks)
+    _, got, st = gpu_layout(moe, topk, w.num_experts, w.num_ranks, layout_mode=layout_mode)
     ref = oracle.layout(topk.numpy(), w.num_experts, w.num_ranks)
     assert st == 0 and ref["flags"] == 0
     assert_layout_equal(got, ref)
@@ -66,18 +67,19 @@ def test_layout_parity_configs(moe, name):
 SHAPES = [  # (T, k, E, R)
     (1, 2, 16, 4), (31, 2, 16, 4), (32, 8, 256, 8), (33, 8, 256, 8), (127, 8, 256, 256), (128, 8, 256, 64),
     (129, 8, 256, 8), (1000, 6, 48, 3), (257, 1, 8, 1), (300, 32, 64, 8), (513, 5, 20, 5), (4097, 8, 256, 8),
-    (200, 32, 8192, 1024), (130, 3, 7, 7),
+    (200, 32, 8192, 1024), (130, 3, 7, 7), (4096, 8, 256, 8), (4095, 4, 16, 4), (3000, 8, 1024, 1024),
 ]
 
 
+@pytest.mark.parametrize("layout_mode", [0, 1])   # 1: never the cluster mode
 @pytest.mark.parametrize("T,k,E,R", SHAPES)
 @pytest.mark.parametrize("mask", [0.0, 0.3])
-def test_layout_parity_shapes(moe, T, k, E, R, mask):
+def test_layout_parity_shapes(moe, T, k, E, R, mask, layout_mode):
     g = torch.Generator().manual_seed(T * 131 + k * 7 + R)
     topk = wl.make_topk_uniform(g, T, E, min(k, E)) if k <= E else None
     if mask:
         topk = wl.mask_random_lanes(g, topk, mask)
-    _, got, st = gpu_layout(moe, topk, E, R)
+    _, got, st = gpu_layout(moe, topk, E, R, layout_mode=layout_mode)
     ref = oracle.layout(topk.numpy(), E, R)
     assert st == 0
     assert_layout_equal(got, ref)
