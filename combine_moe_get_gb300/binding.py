@@ -184,7 +184,7 @@ def moe_get_expand_layout_workspace_size(num_tokens: int, num_experts: int) -> i
 def moe_get_expand_layout(topk_idx: torch.Tensor, expert_prefix: torch.Tensor, num_experts: int, *,
                           out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                           status: Optional[torch.Tensor] = None, stream=None, wait_timeout_ns: int = 0,
-                          test_unpublished_tile: int = -1) -> torch.Tensor:
+                          test_unpublished_tile: int = -1, layout_mode: int = 0) -> torch.Tensor:
     """Expand-mode receive rows [T, k] int32 (one per valid entry, grouped by
     expert); ``expert_prefix`` is the layout's [E+1] prefix for ``topk_idx``."""
     T, k = topk_idx.shape
@@ -194,7 +194,7 @@ def moe_get_expand_layout(topk_idx: torch.Tensor, expert_prefix: torch.Tensor, n
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     status = new_status(dev) if status is None else status
-    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile), 0)
+    opts = MoeLayoutOptionsC(int(wait_timeout_ns), int(test_unpublished_tile), int(layout_mode))
     code = LIB.moe_get_expand_layout(_ptr(topk_idx), T, k, num_experts, _ptr(expert_prefix), _ptr(out),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
                                      _stream(stream), ctypes.byref(opts))

@@ -28,6 +28,7 @@
 //   rows    expert_prefix[e] + tile prefix + warp offset + rank in the warp.
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "moe_common.cuh"
@@ -206,6 +207,165 @@ __global__ void __launch_bounds__(kXThreads) layout_expand_kernel(const ExpandAr
     }
 }
 
+
+// ------------------------------------------------------------------ cluster mode
+//
+// For T <= 16 * 256: one thread-block cluster of 16 CTAs (1024 threads), each a
+// contiguous tile of up to 256 tokens. The per-warp ranks and warp offsets are
+// those of the tiled kernel above; the tiles' per-expert aggregates are
+// exchanged through distributed shared memory between two cluster barriers,
+// so there is no workspace, no clear and no wait that could expire.
+
+constexpr int kXCThreads = 1024;
+constexpr int kXCWarps = kXCThreads / 32;
+constexpr int kXCMax = 16;             // CTAs per cluster
+constexpr int kXCMaxTile = 256;        // tokens per CTA
+constexpr int kXCMaxExperts = 1024;    // per-warp counters: kXCWarps * E * 2 bytes
+
+// Shared memory: warp counters u16 [kXCWarps][E] | tile aggregate i32 [E] |
+// row base i32 [E] | expert ids i16 [tile * k] | rank in warp u16 [tile * k]
+struct XCSmem {
+    size_t agg, base, eid, rank, total;
+};
+
+__host__ __device__ inline XCSmem xcsmem(int tile, int E, int k) {
+    XCSmem s;
+    s.agg = align_up((size_t)kXCWarps * E * 2, 16);
+    s.base = s.agg + align_up((size_t)E * 4, 16);
+    s.eid = s.base + align_up((size_t)E * 4, 16);
+    s.rank = s.eid + align_up((size_t)tile * k * 2, 16);
+    s.total = s.rank + align_up((size_t)tile * k * 2, 16);
+    return s;
+}
+
+__device__ __forceinline__ uint32_t x_cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void x_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ int32_t x_ld_cluster(const void *local, uint32_t rank) {
+    uint32_t remote;
+    int32_t v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+struct ExpandClusterArgs {
+    const int64_t *topk;
+    int T, k, E, tile;
+    const int32_t *expert_prefix;
+    int32_t *token_expert_row;
+    int32_t *status;
+};
+
+__global__ void __launch_bounds__(kXCThreads) layout_expand_cluster_kernel(const ExpandClusterArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int E = a.E, k = a.k, tile = a.tile;
+    const XCSmem sl = xcsmem(tile, E, k);
+    uint16_t *cnt = reinterpret_cast<uint16_t *>(smem);
+    int32_t *agg = reinterpret_cast<int32_t *>(smem + sl.agg);
+    int32_t *base = reinterpret_cast<int32_t *>(smem + sl.base);
+    int16_t *eid = reinterpret_cast<int16_t *>(smem + sl.eid);
+    uint16_t *rank = reinterpret_cast<uint16_t *>(smem + sl.rank);
+
+    const int C = (int)gridDim.x;
+    const int c = (int)x_cluster_ctarank();
+    const int t0 = c * tile;
+    const int tcount = max(0, min(tile, a.T - t0));
+    const int n_ent = tcount * k;
+    const int wtok = tile / kXCWarps;   // tokens walked by one warp (tile is a multiple of kXCWarps)
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    for (int i = threadIdx.x; i < kXCWarps * E / 2; i += kXCThreads) reinterpret_cast<uint32_t *>(cnt)[i] = 0u;
+    // ---- the tile's entries as expert ids (-1: masked or invalid), 8 loads in flight per thread
+    for (int b0 = threadIdx.x; b0 < n_ent; b0 += 8 * kXCThreads) {
+        int64_t v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b0 + u * kXCThreads;
+            v[u] = i < n_ent ? ld_nc_i64(a.topk + (int64_t)t0 * k + i) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = b0 + u * kXCThreads;
+            if (i < n_ent) {
+                int16_t e = -1;
+                if (v[u] >= 0 && v[u] < E) e = (int16_t)v[u];
+                else if (v[u] != -1) report(a.status, MOE_ERR_BAD_TOPK);
+                eid[i] = e;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- each warp ranks its tokens' entries per expert, in (token, choice) order
+    {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int tpp = 32 / k;                 // tokens per pass
+        const int sub = lane / k, j = lane - sub * k;
+        const bool lane_used = sub < tpp;
+        const unsigned lt = (1u << lane) - 1u;
+        uint16_t *my_cnt = cnt + (size_t)warp * E;
+        const int wt0 = warp * wtok;
+        for (int b = 0; b < wtok && wt0 + b < tcount; b += tpp) {
+            const int tw = b + sub;
+            const int tl = wt0 + tw;
+            const bool act = lane_used && tw < wtok && tl < tcount;
+            const int e = act ? (int)eid[tl * k + j] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, e >= 0 ? e : -(lane + 1));
+            const int r = (e >= 0) ? (int)my_cnt[e] + __popc(peers & lt) : 0;
+            __syncwarp();
+            if (e >= 0 && (peers & lt) == 0) my_cnt[e] = (uint16_t)(my_cnt[e] + __popc(peers));
+            __syncwarp();
+            if (act) rank[tl * k + j] = (e >= 0) ? (uint16_t)r : (uint16_t)0xffffu;
+        }
+    }
+    __syncthreads();
+
+    // ---- warp offsets and the tile's aggregate per expert
+    for (int e = threadIdx.x; e < E; e += kXCThreads) {
+        uint32_t run = 0;
+        for (int w = 0; w < kXCWarps; ++w) {
+            const uint32_t cw = cnt[(size_t)w * E + e];
+            cnt[(size_t)w * E + e] = (uint16_t)run;
+            run += cw;
+        }
+        agg[e] = (int32_t)run;
+    }
+
+    // ---- exclusive prefix over the lower tiles, through distributed shared memory
+    x_cluster_sync();
+    for (int e = threadIdx.x; e < E; e += kXCThreads) {
+        int32_t v[kXCMax];
+#pragma unroll
+        for (int cc = 0; cc < kXCMax; ++cc) v[cc] = cc < c ? x_ld_cluster(agg + e, (uint32_t)cc) : 0;
+        int32_t ex = 0;
+#pragma unroll
+        for (int cc = 0; cc < kXCMax; ++cc) ex += v[cc];
+        base[e] = a.expert_prefix[e] + ex;
+    }
+    x_cluster_sync();   // no tile reads another's shared memory after this
+    (void)C;
+
+    // ---- rows
+    for (int i = threadIdx.x; i < n_ent; i += kXCThreads) {
+        const int e = eid[i];
+        int32_t row = -1;
+        if (e >= 0) {
+            const int w = (i / k) / wtok;
+            row = base[e] + (int32_t)cnt[(size_t)w * E + e] + (int32_t)rank[i];
+        }
+        a.token_expert_row[(int64_t)t0 * k + i] = row;
+    }
+}
+
 }  // namespace
 
 size_t expand_workspace_bytes(int T, int E) {
@@ -213,10 +373,78 @@ size_t expand_workspace_bytes(int T, int E) {
     return align_up(kHeaderBytes + tiles * (size_t)E * 8, 128);
 }
 
+namespace {
+
+// Cluster mode for this batch (16 CTAs of up to 256 tokens), or false.
+bool expand_cluster_config(int T, int E, int k, int &tile, size_t &smem) {
+    if (T > kXCMax * kXCMaxTile || E > kXCMaxExperts || tuning().layout_cluster != kXCMax) return false;
+    tile = (int)align_up((size_t)((T + kXCMax - 1) / kXCMax), kXCWarps);
+    smem = xcsmem(tile, E, k).total;
+    if (smem > device_smem_optin()) return false;
+    struct Entry { int dev; size_t smem; bool ok; };
+    static std::mutex mu;
+    static Entry cache[16];
+    static int n_cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < std::min(n_cached, 16); ++i)
+        if (cache[i].dev == dev && cache[i].smem == smem) return cache[i].ok;
+    const void *fn = (const void *)layout_expand_cluster_kernel;
+    bool ok = ensure_dynamic_smem(fn, smem) == MOE_OK &&
+              cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    if (ok) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kXCMax);
+        cfg.blockDim = dim3(kXCThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kXCMax;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        ok = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) == cudaSuccess && clusters >= 1;
+    }
+    cudaGetLastError();   // a refused attribute or query only means: no cluster mode
+    cache[n_cached % 16] = Entry{dev, smem, ok};
+    ++n_cached;
+    return ok;
+}
+
+}  // namespace
+
 int launch_expand_layout(const ExpandLaunch &L) {
     const int T = L.num_tokens, k = L.num_topk, E = L.num_experts;
     if (T == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(L.stream);
+    int tile = 0;
+    size_t csmem = 0;
+    if (L.unpublished_tile < 0 && !L.no_cluster && expand_cluster_config(T, E, k, tile, csmem)) {
+        ExpandClusterArgs c;
+        c.topk = L.topk_idx;
+        c.T = T; c.k = k; c.E = E; c.tile = tile;
+        c.expert_prefix = L.expert_prefix;
+        c.token_expert_row = L.token_expert_row;
+        c.status = L.status;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kXCMax);
+        cfg.blockDim = dim3(kXCThreads);
+        cfg.dynamicSmemBytes = csmem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kXCMax;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = tuning().overlap != 0 ? 2 : 1;
+        return cudaLaunchKernelEx(&cfg, layout_expand_cluster_kernel, c) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
     const size_t ws = expand_workspace_bytes(T, E);
     if (cudaMemsetAsync(L.workspace, 0, ws, s) != cudaSuccess) return MOE_ERR_CUDA;
     ExpandArgs a;

@@ -263,6 +263,8 @@ MOE_API int moe_get_expand_layout(const int64_t *topk_idx, int num_tokens, int n
     L.stream = stream;
     L.timeout_ns = options ? options->wait_timeout_ns : 0;
     L.unpublished_tile = options ? options->test_unpublished_tile : -1;
+    if (options && options->layout_mode != 0 && options->layout_mode != 1) return MOE_ERR_INVALID_ARG;
+    L.no_cluster = options && options->layout_mode == 1;
     return moe::launch_expand_layout(L);
 }
 

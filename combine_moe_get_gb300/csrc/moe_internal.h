@@ -70,6 +70,7 @@ struct ExpandLaunch {
     void *stream;
     int64_t timeout_ns;     // <= 0: default
     int unpublished_tile;   // test hook, -1 = off
+    bool no_cluster = false;   // never the cluster mode
 };
 
 size_t expand_workspace_bytes(int num_tokens, int num_experts);

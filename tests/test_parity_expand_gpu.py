@@ -44,8 +44,8 @@ def gpu_expand(moe, topk_cpu, E, R, **kw):
     return lay, rows, int(status.item())
 
 
-def check_expand_layout(moe, topk, E, R):
-    _, rows, st = gpu_expand(moe, topk, E, R)
+def check_expand_layout(moe, topk, E, R, layout_mode=0):
+    _, rows, st = gpu_expand(moe, topk, E, R, layout_mode=layout_mode)
     ref = oracle.expand_layout(topk.numpy(), E)
     assert st == (moe.MOE_ERR_BAD_TOPK if ref["flags"] & oracle.ORACLE_BAD_TOPK else 0)
     np.testing.assert_array_equal(rows.cpu().numpy(), ref["token_expert_row"])
@@ -53,26 +53,29 @@ def check_expand_layout(moe, topk, E, R):
 
 # ------------------------------------------------------------------ expand layout
 
+@pytest.mark.parametrize("layout_mode", [0, 1])   # 1: never the cluster mode
 @pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode", "layout_2048", "layout_2048_1m"])
-def test_expand_layout_parity_configs(moe, name):
+def test_expand_layout_parity_configs(moe, name, layout_mode):
     w = wl.CONFIGS[name]
-    check_expand_layout(moe, wl.make_inputs(w, with_partial=False).topk_idx, w.num_experts, w.num_ranks)
+    check_expand_layout(moe, wl.make_inputs(w, with_partial=False).topk_idx, w.num_experts, w.num_ranks, layout_mode)
 
 
 EXPAND_SHAPES = [  # (T, k, E, R)
     (1, 2, 16, 4), (255, 8, 256, 8), (256, 8, 256, 64), (257, 8, 256, 256), (511, 6, 48, 3), (513, 1, 8, 1),
     (4097, 8, 256, 8), (300, 32, 64, 8), (200, 32, 8192, 1024), (1030, 3, 7, 7), (2500, 5, 20, 5),
+    (4096, 8, 256, 8), (4096, 32, 1024, 8), (3999, 1, 1024, 1024),
 ]
 
 
+@pytest.mark.parametrize("layout_mode", [0, 1])   # 1: never the cluster mode
 @pytest.mark.parametrize("T,k,E,R", EXPAND_SHAPES)
 @pytest.mark.parametrize("mask", [0.0, 0.3])
-def test_expand_layout_parity_shapes(moe, T, k, E, R, mask):
+def test_expand_layout_parity_shapes(moe, T, k, E, R, mask, layout_mode):
     g = torch.Generator().manual_seed(T * 17 + k * 5 + E)
     topk = wl.make_topk_uniform(g, T, E, k)
     if mask:
         topk = wl.mask_random_lanes(g, topk, mask)
-    check_expand_layout(moe, topk, E, R)
+    check_expand_layout(moe, topk, E, R, layout_mode)
 
 
 def test_expand_layout_duplicates_all_masked_and_bad_entries(moe):
