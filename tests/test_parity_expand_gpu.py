@@ -131,7 +131,7 @@ def test_expand_layout_bounded_wait_reports_timeout(moe):
 MODES = ("bf16", "quantize_fp8", "fp8")
 
 
-def run_expand_dispatch(moe, x, topk, w, E, R, mode, scales=None):
+def run_expand_dispatch(moe, x, topk, w, E, R, mode, scales=None, balance=None):
     T, H = x.shape
     k = topk.shape[1]
     lay, rows, st = gpu_expand(moe, topk, E, R)
@@ -149,12 +149,13 @@ def run_expand_dispatch(moe, x, topk, w, E, R, mode, scales=None):
                   (scales.to(DEV) if mode == "fp8" else None)))
     status = moe.new_status(DEV)
     moe.moe_dispatch(x.to(DEV), topk.to(DEV), None if w is None else w.to(DEV), E, R, rows, cap,
-                     quantize_fp8=mode == "quantize_fp8", x_scales=out.x_scales, expand=True, out=out, status=status)
+                     quantize_fp8=mode == "quantize_fp8", x_scales=out.x_scales, expand=True, out=out,
+                     balance=balance, status=status)
     torch.cuda.synchronize()
     return lay, rows, out, int(status.item())
 
 
-def check_expand_dispatch(moe, topk, E, R, H, mode, seed, weights=True):
+def check_expand_dispatch(moe, topk, E, R, H, mode, seed, weights=True, balance=None):
     T, k = topk.shape
     g = torch.Generator().manual_seed(seed)
     w = wl.make_weights(g, T, k) if weights else None
@@ -168,8 +169,10 @@ def check_expand_dispatch(moe, topk, E, R, H, mode, seed, weights=True):
         scales = None
         x = wl.make_x(g, T, H)
         x_ref = bits16(x)
-    _, rows, out, st = run_expand_dispatch(moe, x, topk, w, E, R, mode, scales)
+    _, rows, out, st = run_expand_dispatch(moe, x, topk, w, E, R, mode, scales, balance)
     assert st == 0
+    if balance is not None:
+        assert balance.tolist() == [0, 0]
     ex = oracle.expand_layout(topk.numpy(), E)
     N = ex["num_recv"]
     ref = oracle.dispatch_expand(MODES.index(mode), x_ref, topk.numpy(), None if w is None else w.numpy(), E, R,
@@ -208,6 +211,16 @@ def test_expand_dispatch_parity_shapes(moe, T, H, k, E, R, mode):
     g = torch.Generator().manual_seed(T + 3 * H + k)
     topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.2)
     check_expand_dispatch(moe, topk, E, R, H, mode, T + H, weights=(T % 2 == 1))
+
+
+@pytest.mark.parametrize("mode", ["bf16", "fp8"])
+def test_expand_dispatch_balanced_parity(moe, mode):
+    # with a balance counter (a pool of units): the same bytes, and the counter left zero
+    w = wl.CONFIGS["dsv3"]
+    topk = wl.make_inputs(w, with_partial=False).topk_idx
+    bal = moe.new_balance_counter(DEV)
+    for seed in (41, 42):
+        check_expand_dispatch(moe, topk, w.num_experts, w.num_ranks, w.hidden, mode, seed, balance=bal)
 
 
 def test_expand_dispatch_duplicate_experts(moe):

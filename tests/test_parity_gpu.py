@@ -452,6 +452,31 @@ def test_combine_balanced_parity(moe, T, H, k, E, R):
         np.testing.assert_array_equal(bits16(out), ref)
 
 
+def test_combine_weighted_balanced_parity(moe):
+    # weighted rows and combined top-k weights with a balance counter: the oracle's results, counter left zero
+    w = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(w)
+    E, R = w.num_experts, w.num_ranks
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(inp.topk_idx.to(DEV), E, R, status=status)
+    N = int(lay.rank_prefix[-1].item())
+    g = torch.Generator().manual_seed(17)
+    row_w = torch.rand(inp.partial.shape[0], generator=g)
+    rtw = torch.rand(inp.partial.shape[0], w.num_topk, generator=g)
+    ref_lay = oracle.layout(inp.topk_idx.numpy(), E, R)
+    ref, cref, flags = oracle.combine_weighted(bits16(inp.partial), ref_lay["token_dst_row"], row_w.numpy(),
+                                               rtw.numpy())
+    assert flags == 0
+    bal = moe.new_balance_counter(DEV)
+    for _ in range(2):
+        out, cw = moe.moe_combine_ex(inp.partial.to(DEV), lay.token_dst_row, row_weights=row_w.to(DEV),
+                                     recv_topk_weights=rtw.to(DEV), balance=bal, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0 and bal.tolist() == [0, 0] and N > 0
+        np.testing.assert_array_equal(bits16(out), ref)
+        np.testing.assert_array_equal(cw.cpu().numpy().view(np.uint32), cref.view(np.uint32))
+
+
 @pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode"])
 def test_combine_ex_parity_configs(moe, name):
     w = wl.CONFIGS[name]
