@@ -248,15 +248,16 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
           for (int c = 0; c < nch; ++c, ++j) {
             const int64_t off = (int64_t)c * CH;
             const uint32_t nbytes = (uint32_t)min((int64_t)CH, a.row_bytes - off);
-            // wait until the unit entry and D slots are free (units are released in order)
-            while (ok && (j - oldest >= kUnits || head + D - tail > NS)) {
+            // wait until the unit entry is free (units are released in order)
+            auto release_oldest = [&]() {
                 const int eo = (int)(oldest % kUnits);
                 ok = mbar_wait_bounded(&empty[eo], (uint32_t)((oldest / kUnits) & 1), a.timeout_ns);
                 if (ok) {
                     tail += entry[eo].D;
                     ++oldest;
                 }
-            }
+            };
+            while (ok && j - oldest >= kUnits) release_oldest();
             if (!__all_sync(kFull, ok)) {
                 if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
                 ok = false;
@@ -276,14 +277,28 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             __syncwarp();
             const uint32_t sbytes = kFP8 ? nbytes / 32 : 0u;   // the chunk's scales (4 B per 128 codes)
             if (lane == 0) mbar_arrive_expect_tx(&full[e], (uint32_t)D * (nbytes + sbytes));
-            if (row >= 0) {
-                const int slot = head_slot + pos < NS ? head_slot + pos : head_slot + pos - NS;
-                bulk_load(ring + (size_t)slot * SB, a.partial + (int64_t)row * a.row_bytes + off, nbytes, &full[e],
-                          pol);
-                if (kFP8)
-                    bulk_load(ring + (size_t)slot * SB + CH, a.scales + (int64_t)row * a.scale_row_bytes + off / 32,
-                              sbytes, &full[e], pol);
+            // the unit's rows take slots head .. head + D - 1; each row's load is issued as soon as
+            // its slot is free, not once all D are (older units release their slots in batches)
+            int issued = 0;
+            while (true) {
+                const int can = min(D, NS - (int)(head - tail));   // rows whose slot is free
+                if (row >= 0 && pos >= issued && pos < can) {
+                    const int slot = head_slot + pos < NS ? head_slot + pos : head_slot + pos - NS;
+                    bulk_load(ring + (size_t)slot * SB, a.partial + (int64_t)row * a.row_bytes + off, nbytes,
+                              &full[e], pol);
+                    if (kFP8)
+                        bulk_load(ring + (size_t)slot * SB + CH,
+                                  a.scales + (int64_t)row * a.scale_row_bytes + off / 32, sbytes, &full[e], pol);
+                }
+                issued = max(issued, can);
+                if (issued >= D || !ok) break;
+                release_oldest();   // an older unit holds the next slot (D <= NS, so one exists)
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
+                    ok = false;
+                }
             }
+            if (!ok) break;
             head += D;
             head_slot += D;
             if (head_slot >= NS) head_slot -= NS;
