@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
                     ++oldest;
                 }
             };
-            while (ok && j - oldest >= kUnits) release_oldest();
+            // E4M3 rows: whole units only (the per-row issue below costs the critical producer
+            // more than it gains when a unit's rows are this short)
+            while (ok && (j - oldest >= kUnits || (kFP8 && head + D - tail > NS))) release_oldest();
             if (!__all_sync(kFull, ok)) {
                 if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
                 ok = false;
@@ -278,7 +280,8 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             const uint32_t sbytes = kFP8 ? nbytes / 32 : 0u;   // the chunk's scales (4 B per 128 codes)
             if (lane == 0) mbar_arrive_expect_tx(&full[e], (uint32_t)D * (nbytes + sbytes));
             // the unit's rows take slots head .. head + D - 1; each row's load is issued as soon as
-            // its slot is free, not once all D are (older units release their slots in batches)
+            // its slot is free, not once all D are (older units release their slots in batches;
+            // for E4M3 rows all D are free here)
             int issued = 0;
             while (true) {
                 const int can = min(D, NS - (int)(head - tail));   // rows whose slot is free
