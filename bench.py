@@ -518,7 +518,7 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes": bytes_bf16, "spec_peak": HBM_SPEC_GBS,
                      "frac_of_spec": achieved / HBM_SPEC_GBS},
         "kernels": kern,
-        "gpu_launches": 3 * args.steps,   # per step: the cooperative layout kernel, dispatch, combine
+        "gpu_launches": 3 * args.steps,   # per step: the layout kernel (one cluster), the dispatch and the combine
         "clocks": clocks,
         "e2e": e2e,
     }
