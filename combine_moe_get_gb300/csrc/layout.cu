@@ -760,10 +760,34 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
     }
     __syncthreads();
 
-    // ---- pass 1, lanes over (token, entry): expert histogram, each rank of a token
-    //      once (__match_any_sync; the lowest entry owns it), membership bits;
-    //      ent[] becomes the owned rank (or -1)
-    {
+    // ---- pass 1: expert histogram, each rank of a token once (the lowest entry
+    //      owns it), membership bits; ent[] becomes the owned rank (or -1)
+    if (R <= 32) {
+        // a lane per token: its ranks as a 32-bit mask, then one ballot per rank
+        // gives a whole bitmap word (32 tokens) without shared-memory atomics
+        const int tpad = (tcount + 31) & ~31;
+        for (int tl = threadIdx.x; tl < tpad; tl += kCThreads) {
+            uint32_t mask = 0u;
+            if (tl < tcount) {
+                for (int j = 0; j < k; ++j) {
+                    const int r = rk[tl * k + j];
+                    int own = -1;
+                    if (r >= 0) {
+                        atomicAdd(&hist[ent[tl * k + j]], 1);
+                        if (!((mask >> r) & 1u)) {
+                            mask |= 1u << r;
+                            own = r;
+                        }
+                    }
+                    ent[tl * k + j] = (int16_t)own;
+                }
+            }
+            for (int r = 0; r < R; ++r) {
+                const unsigned word = __ballot_sync(0xffffffffu, (mask >> r) & 1u);
+                if (lane == 0) bitmap[(tl >> 5) * R + r] = word;
+            }
+        }
+    } else {
         const int tpp = 32 / k;
         const int sub = lane / k, j = lane - sub * k;
         const bool lane_used = sub < tpp;
