@@ -92,18 +92,22 @@ MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, in
  * library fixes a deterministic order instead): rank r's rows occupy
  * [rank_prefix[r], rank_prefix[r+1]) in ascending source-token order, so
  *   token_dst_row[t, j] = rank_prefix[r] + #{t' < t : is_token_in_rank[t', r]}.
- * The in-rank position is a column-wise exclusive scan over tokens, computed by
- * a single-pass decoupled-lookback scan over tiles of tokens (the only
- * inter-CTA wait of the library; bounded, MOE_ERR_TIMEOUT on expiry).
+ * The in-rank position is a column-wise exclusive scan over tokens. For
+ * 129..4096 tokens it is computed inside one 16-CTA thread-block cluster,
+ * whose tiles exchange their counts through distributed shared memory (no
+ * waits, no workspace use). Otherwise it is an all-tile sweep of published
+ * counts (up to 128 tiles of 64 tokens) or a single-pass decoupled-lookback
+ * scan over tiles of 128 tokens; both wait on other CTAs, bounded, with
+ * MOE_ERR_TIMEOUT on expiry.
  *
  *   topk_idx   [T, k] int64, device. -1 = masked; other values outside [0, E)
  *              raise MOE_ERR_BAD_TOPK and are treated as masked.
  *   layout     output arrays (all must be non-null when T > 0; rank_prefix and
  *              expert_prefix, num_tokens_per_* are always written).
  *   workspace  device scratch of at least moe_get_layout_workspace_size()
- *              bytes; contents need not be initialised (the call clears it with
- *              cudaMemsetAsync on `stream`). Must not be shared by calls that
- *              overlap on the GPU.
+ *              bytes; contents need not be initialised (a mode that uses it
+ *              clears it with cudaMemsetAsync on `stream`). Must not be shared
+ *              by calls that overlap on the GPU.
  *   status     device int32, see conventions.
  * Limits: 1 <= k <= 32, 1 <= R <= 1024, E <= 8192, E % R == 0,
  * T * k < 2^31, T * R < 2^40.
@@ -160,8 +164,10 @@ MOE_API size_t moe_get_expand_layout_workspace_size(int num_tokens, int num_expe
  * are numbered rank by rank, rank r's rows are [expert_prefix[r*m],
  * expert_prefix[(r+1)*m]). A token naming one expert in two entries gets two
  * rows. The number of rows is expert_prefix[E] (<= T*k). The in-expert
- * position is a decoupled-lookback column scan over tiles of 256 tokens
- * (bounded waits, MOE_ERR_TIMEOUT on expiry).
+ * position is a column scan over tokens: for T <= 4096 and E <= 1024, inside
+ * one 16-CTA thread-block cluster through distributed shared memory (no
+ * waits, no workspace use); otherwise a decoupled lookback over tiles of 256
+ * tokens (bounded waits, MOE_ERR_TIMEOUT on expiry).
  *
  *   topk_idx          [T, k] int64, device (as for moe_get_layout).
  *   expert_prefix     [E+1] int32, device, input: moe_get_layout's output for
@@ -171,9 +177,11 @@ MOE_API size_t moe_get_expand_layout_workspace_size(int num_tokens, int num_expe
  *                     moe_combine / moe_combine_ex.
  *   workspace         device scratch of at least
  *                     moe_get_expand_layout_workspace_size() bytes, cleared by the
- *                     call on `stream`; not shared by calls that overlap on the GPU.
+ *                     call on `stream` when the lookback mode uses it; not shared
+ *                     by calls that overlap on the GPU.
  *   options           NULL or the options of moe_get_layout_ex; here the test hook
- *                     names a tile of 256 tokens.
+ *                     names a tile of 256 tokens (and keeps the call off the
+ *                     cluster mode, as does layout_mode 1).
  * Limits: 1 <= k <= 32, 1 <= E <= 8192, T * k < 2^31.
  */
 MOE_API int moe_get_expand_layout(const int64_t *topk_idx, int num_tokens, int num_topk, int num_experts,
