@@ -6,7 +6,6 @@
 // description to the kernel launcher of its step.
 #include <atomic>
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
@@ -88,38 +87,30 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes) {
     return MOE_OK;
 }
 
-namespace {
-int env_int(const char *name, int dflt) {
-    const char *v = std::getenv(name);
-    if (v == nullptr || *v == '\0') return dflt;
-    char *end = nullptr;
-    long x = std::strtol(v, &end, 0);
-    return (end && *end == '\0' && x > 0 && x < (1L << 30)) ? (int)x : dflt;
-}
-}  // namespace
-
 const Tuning &tuning() {
+    // Compile-time settings (moe_internal.h): nothing read from the environment,
+    // so every call takes the configuration the parity tests ran.
     static const Tuning t = [] {
         Tuning x;
-        x.dispatch_warps = env_int("MOE_TUNE_DISPATCH_WARPS", 8);
-        x.dispatch_stages = env_int("MOE_TUNE_DISPATCH_STAGES", 4);
-        x.dispatch_chunk = env_int("MOE_TUNE_DISPATCH_CHUNK", 16384);
-        x.dispatch_smem = env_int("MOE_TUNE_DISPATCH_SMEM", 200 << 10);
-        x.combine_warps = env_int("MOE_TUNE_COMBINE_WARPS", 8);
-        x.combine_chunk = env_int("MOE_TUNE_COMBINE_CHUNK", 8192);
-        x.combine_ring_bytes = env_int("MOE_TUNE_COMBINE_RING_BYTES", 224 << 10);
-        x.combine_fp8_warps = env_int("MOE_TUNE_COMBINE_FP8_WARPS", 10);
-        x.overlap = env_int("MOE_TUNE_OVERLAP", 1) == 1;   // any other value: ordinary launches
-        x.dispatch_pool = env_int("MOE_TUNE_DISPATCH_POOL", 50);
-        x.combine_pool = env_int("MOE_TUNE_COMBINE_POOL", 30);
-        x.layout_cluster = env_int("MOE_TUNE_LAYOUT_CLUSTER", 16);
-        x.fp8_rows = env_int("MOE_TUNE_FP8_ROWS", 1) == 1;
-        x.fp8_in_slots = env_int("MOE_TUNE_FP8_IN_SLOTS", 8);
-        x.fp8_quant_warps = env_int("MOE_TUNE_FP8_QUANT_WARPS", 24);
-        x.ctas_per_sm = env_int("MOE_TUNE_CTAS_PER_SM", 0);
-        x.l2_hints = env_int("MOE_TUNE_L2_HINTS", 1) & 3;
-        x.spread_small = env_int("MOE_TUNE_SPREAD_SMALL", 1) == 1;
-        x.fused_small = env_int("MOE_TUNE_FUSED_SMALL", 1) == 1;
+        x.dispatch_warps = MOE_TUNE_DISPATCH_WARPS;
+        x.dispatch_stages = MOE_TUNE_DISPATCH_STAGES;
+        x.dispatch_chunk = MOE_TUNE_DISPATCH_CHUNK;
+        x.dispatch_smem = MOE_TUNE_DISPATCH_SMEM;
+        x.combine_warps = MOE_TUNE_COMBINE_WARPS;
+        x.combine_chunk = MOE_TUNE_COMBINE_CHUNK;
+        x.combine_ring_bytes = MOE_TUNE_COMBINE_RING_BYTES;
+        x.combine_fp8_warps = MOE_TUNE_COMBINE_FP8_WARPS;
+        x.overlap = MOE_TUNE_OVERLAP;
+        x.dispatch_pool = MOE_TUNE_DISPATCH_POOL;
+        x.combine_pool = MOE_TUNE_COMBINE_POOL;
+        x.layout_cluster = MOE_TUNE_LAYOUT_CLUSTER;
+        x.fp8_rows = MOE_TUNE_FP8_ROWS;
+        x.fp8_in_slots = MOE_TUNE_FP8_IN_SLOTS;
+        x.fp8_quant_warps = MOE_TUNE_FP8_QUANT_WARPS;
+        x.ctas_per_sm = MOE_TUNE_CTAS_PER_SM;
+        x.l2_hints = MOE_TUNE_L2_HINTS & 3;
+        x.spread_small = MOE_TUNE_SPREAD_SMALL;
+        x.fused_small = MOE_TUNE_FUSED_SMALL;
         return x;
     }();
     return t;
@@ -141,6 +132,53 @@ bool shape_ok(int T, int k, int E, int R) {
 }
 
 }  // namespace
+
+// ------------------------------------------------------------------ shared layout checks
+
+namespace moe {
+
+int layout_check_args(const int64_t *topk_idx, int T, int k, int E, int R, const moe_layout_t &o,
+                      const int32_t *status) {
+    if (!shape_ok(T, k, E, R)) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * R >= (int64_t)1 << 40) return MOE_ERR_INVALID_ARG;
+    if (!status || !o.num_tokens_per_rank || !o.num_tokens_per_expert || !o.rank_prefix || !o.expert_prefix)
+        return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_idx || !o.is_token_in_rank || !o.token_dst_row)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(status, 4) || !aligned(o.num_tokens_per_rank, 4) || !aligned(o.num_tokens_per_expert, 4) ||
+        !aligned(o.rank_prefix, 4) || !aligned(o.expert_prefix, 4))
+        return MOE_ERR_MISALIGNED;
+    if (T > 0 && (!aligned(topk_idx, 8) || !aligned(o.token_dst_row, 4) || !aligned(o.is_token_in_rank, 4)))
+        return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
+
+int layout_prepare(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
+                   size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns, int unpublished_tile,
+                   LayoutLaunch &L, bool no_cluster) {
+    const int rc = layout_check_args(topk_idx, T, k, E, R, o, status);
+    if (rc != MOE_OK) return rc;
+    if (T > 0) {
+        if (!workspace) return MOE_ERR_INVALID_ARG;
+        if (!aligned(workspace, 16)) return MOE_ERR_MISALIGNED;
+        if (workspace_bytes < layout_workspace_bytes(T, E, R)) return MOE_ERR_WORKSPACE;
+    }
+    L = LayoutLaunch{};
+    L.topk_idx = topk_idx;
+    L.num_tokens = T;
+    L.num_topk = k;
+    L.num_experts = E;
+    L.num_ranks = R;
+    L.out = o;
+    L.workspace = workspace;
+    L.status = status;
+    L.stream = stream;
+    L.timeout_ns = timeout_ns;
+    L.unpublished_tile = unpublished_tile;
+    L.no_cluster = no_cluster || unpublished_tile >= 0;
+    return MOE_OK;
+}
+
+}  // namespace moe
 
 // ------------------------------------------------------------------ C ABI
 
@@ -167,44 +205,12 @@ MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, in
     return moe::layout_workspace_bytes(num_tokens, num_experts, num_ranks);
 }
 
-static int layout_prepare(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
-                          size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
-                          int unpublished_tile, moe::LayoutLaunch &L, bool no_cluster = false) {
-    if (!shape_ok(T, k, E, R)) return MOE_ERR_INVALID_ARG;
-    if ((int64_t)T * R >= (int64_t)1 << 40) return MOE_ERR_INVALID_ARG;
-    if (!status || !o.num_tokens_per_rank || !o.num_tokens_per_expert || !o.rank_prefix || !o.expert_prefix)
-        return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!topk_idx || !o.is_token_in_rank || !o.token_dst_row || !workspace)) return MOE_ERR_INVALID_ARG;
-    if (!aligned(status, 4) || !aligned(o.num_tokens_per_rank, 4) || !aligned(o.num_tokens_per_expert, 4) ||
-        !aligned(o.rank_prefix, 4) || !aligned(o.expert_prefix, 4))
-        return MOE_ERR_MISALIGNED;
-    if (T > 0) {
-        if (!aligned(topk_idx, 8) || !aligned(o.token_dst_row, 4) || !aligned(o.is_token_in_rank, 4) ||
-            !aligned(workspace, 16))
-            return MOE_ERR_MISALIGNED;
-        if (workspace_bytes < moe::layout_workspace_bytes(T, E, R)) return MOE_ERR_WORKSPACE;
-    }
-    L.topk_idx = topk_idx;
-    L.num_tokens = T;
-    L.num_topk = k;
-    L.num_experts = E;
-    L.num_ranks = R;
-    L.out = o;
-    L.workspace = workspace;
-    L.status = status;
-    L.stream = stream;
-    L.timeout_ns = timeout_ns;
-    L.unpublished_tile = unpublished_tile;
-    L.no_cluster = no_cluster || unpublished_tile >= 0;
-    return MOE_OK;
-}
-
 static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
                          size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
                          int unpublished_tile, bool no_cluster = false) {
     moe::LayoutLaunch L;
-    const int rc = layout_prepare(topk_idx, T, k, E, R, o, workspace, workspace_bytes, status, stream, timeout_ns,
-                                  unpublished_tile, L, no_cluster);
+    const int rc = moe::layout_prepare(topk_idx, T, k, E, R, o, workspace, workspace_bytes, status, stream,
+                                       timeout_ns, unpublished_tile, L, no_cluster);
     return rc != MOE_OK ? rc : moe::launch_layout(L);
 }
 
@@ -356,8 +362,8 @@ MOE_API int moe_layout_dispatch(const void *x, int num_tokens, int hidden, const
                                 void *stream) {
     if (mode & MOE_DISPATCH_EXPAND) return MOE_ERR_INVALID_ARG;
     moe::LayoutLaunch Ll;
-    int rc = layout_prepare(topk_idx, num_tokens, num_topk, num_experts, num_ranks, layout, workspace,
-                            workspace_bytes, status, stream, 0, -1, Ll);
+    int rc = moe::layout_prepare(topk_idx, num_tokens, num_topk, num_experts, num_ranks, layout, workspace,
+                                 workspace_bytes, status, stream, 0, -1, Ll, false);
     if (rc != MOE_OK) return rc;
     moe::DispatchLaunch L;
     rc = dispatch_prepare(x, num_tokens, hidden, topk_idx, topk_weights, num_topk, num_experts, num_ranks,

@@ -19,7 +19,67 @@ size_t device_smem_optin();        // max dynamic shared memory per block (bytes
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` (cached).
 int ensure_dynamic_smem(const void *kernel, size_t bytes);
 
-// Tuning knobs, read once from MOE_TUNE_* environment variables (0 = default).
+// Tuning knobs. They are fixed when the library is compiled (the defaults
+// below are the measured best on this GPU and the configuration every parity
+// test runs); a variant build may override one with -DMOE_TUNE_<NAME>=<value>.
+// Nothing is read from the environment at run time.
+#ifndef MOE_TUNE_DISPATCH_WARPS
+#define MOE_TUNE_DISPATCH_WARPS 8
+#endif
+#ifndef MOE_TUNE_DISPATCH_STAGES
+#define MOE_TUNE_DISPATCH_STAGES 4
+#endif
+#ifndef MOE_TUNE_DISPATCH_CHUNK
+#define MOE_TUNE_DISPATCH_CHUNK 16384
+#endif
+#ifndef MOE_TUNE_DISPATCH_SMEM
+#define MOE_TUNE_DISPATCH_SMEM (200 << 10)
+#endif
+#ifndef MOE_TUNE_COMBINE_WARPS
+#define MOE_TUNE_COMBINE_WARPS 8
+#endif
+#ifndef MOE_TUNE_COMBINE_CHUNK
+#define MOE_TUNE_COMBINE_CHUNK 8192
+#endif
+#ifndef MOE_TUNE_COMBINE_RING_BYTES
+#define MOE_TUNE_COMBINE_RING_BYTES (224 << 10)
+#endif
+#ifndef MOE_TUNE_COMBINE_FP8_WARPS
+#define MOE_TUNE_COMBINE_FP8_WARPS 10
+#endif
+#ifndef MOE_TUNE_OVERLAP
+#define MOE_TUNE_OVERLAP 1
+#endif
+#ifndef MOE_TUNE_DISPATCH_POOL
+#define MOE_TUNE_DISPATCH_POOL 50
+#endif
+#ifndef MOE_TUNE_COMBINE_POOL
+#define MOE_TUNE_COMBINE_POOL 30
+#endif
+#ifndef MOE_TUNE_LAYOUT_CLUSTER
+#define MOE_TUNE_LAYOUT_CLUSTER 16
+#endif
+#ifndef MOE_TUNE_FP8_ROWS
+#define MOE_TUNE_FP8_ROWS 1
+#endif
+#ifndef MOE_TUNE_FP8_IN_SLOTS
+#define MOE_TUNE_FP8_IN_SLOTS 8
+#endif
+#ifndef MOE_TUNE_FP8_QUANT_WARPS
+#define MOE_TUNE_FP8_QUANT_WARPS 24
+#endif
+#ifndef MOE_TUNE_CTAS_PER_SM
+#define MOE_TUNE_CTAS_PER_SM 0
+#endif
+#ifndef MOE_TUNE_L2_HINTS
+#define MOE_TUNE_L2_HINTS 1
+#endif
+#ifndef MOE_TUNE_SPREAD_SMALL
+#define MOE_TUNE_SPREAD_SMALL 1
+#endif
+#ifndef MOE_TUNE_FUSED_SMALL
+#define MOE_TUNE_FUSED_SMALL 1
+#endif
 struct Tuning {
     int dispatch_warps, dispatch_stages, dispatch_chunk;
     int dispatch_smem;                                       // shared-memory budget of a chunked dispatch CTA
@@ -54,6 +114,17 @@ struct LayoutLaunch {
 
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);
 int launch_layout(const LayoutLaunch &L);
+
+// Host-side checks of a layout call (moe_api.cu), shared by every layout entry
+// point. layout_check_args: shape, pointers and alignment, but not the
+// workspace. layout_prepare: those checks, then the workspace (present,
+// 16-byte aligned, at least layout_workspace_bytes: else MOE_ERR_WORKSPACE),
+// then the launch description. MOE_OK or the error code; nothing is launched.
+int layout_check_args(const int64_t *topk_idx, int T, int k, int E, int R, const moe_layout_t &o,
+                      const int32_t *status);
+int layout_prepare(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
+                   size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns, int unpublished_tile,
+                   LayoutLaunch &L, bool no_cluster);
 // Two 32-bit words of the layout workspace that launch_layout(L) zeroes (with
 // the workspace clear, or from the cluster-mode kernel) and then leaves alone,
 // free for the next launch of the same call -- which may rely on them only

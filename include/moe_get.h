@@ -288,8 +288,8 @@ MOE_API int moe_dispatch_ex(const void *x, int num_tokens, int hidden, const int
  * beside the copy pipeline), every CTA of the dispatch grid computes the whole
  * layout itself in shared memory -- no CTA waits on another -- while its first
  * row loads are in flight, then stores the rows; the layout outputs are written
- * to `layout` as moe_get_layout writes them. Larger batches (or when the tuning
- * switch MOE_TUNE_FUSED_SMALL=2 is set) take the two launches. On that path
+ * to `layout` as moe_get_layout writes them. Larger batches take the two
+ * launches. On that path
  * the dispatch is launched to overlap the layout: its CTAs load input rows
  * while the layout runs (the layout has passed its own dependency wait, so the
  * rows are complete) and read the layout's outputs only after it ends. It also
@@ -376,6 +376,9 @@ MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scal
  *
  *   - The first call on a device looks up the scratch's device address with
  *     that device current; make that first call before any stream capture.
+ *     The address is kept for the life of the process: after a
+ *     cudaDeviceReset (which unloads the library's device code) it is stale,
+ *     so do not call this entry point on that device again.
  *   - Sizes whose workspace (moe_get_layout_workspace_size) exceeds
  *     MOE_NOALLOC_SCRATCH_BYTES return MOE_ERR_WORKSPACE and launch nothing.
  *   - Every call shares the one scratch array, which keeps the previous
