@@ -925,7 +925,7 @@ int cooperative_capacity(const void *kernel, size_t smem) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < n_cached; ++i)
+    for (int i = 0; i < std::min(n_cached, 16); ++i)
         if (cache[i].dev == dev && cache[i].fn == kernel && cache[i].smem == smem) return cache[i].cap;
     int coop = 0, per_sm = 0;
     if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return 0;
@@ -1148,44 +1148,27 @@ void *noalloc_scratch_address(int *err) {
     return addr[dev];
 }
 
-bool is_aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 }  // namespace moe
 
 extern "C" MOE_API int moe_get_layout_noalloc(const int64_t *topk_idx, int num_tokens, int num_topk,
                                               int num_experts, int num_ranks, moe_layout_t layout,
                                               int32_t *status, void *stream) {
-    const int T = num_tokens, k = num_topk, E = num_experts, R = num_ranks;
-    if (T < 0 || k < 1 || k > MOE_MAX_TOPK || R < 1 || R > MOE_MAX_RANKS || E < 1 || E > MOE_MAX_EXPERTS ||
-        E % R != 0 || (int64_t)T * k >= ((int64_t)1 << 31) || (int64_t)T * R >= ((int64_t)1 << 40))
-        return MOE_ERR_INVALID_ARG;
-    if (!status || !layout.num_tokens_per_rank || !layout.num_tokens_per_expert || !layout.rank_prefix ||
-        !layout.expert_prefix)
-        return MOE_ERR_INVALID_ARG;
-    if (T > 0 && (!topk_idx || !layout.is_token_in_rank || !layout.token_dst_row)) return MOE_ERR_INVALID_ARG;
-    if (!moe::is_aligned(status, 4) || !moe::is_aligned(layout.num_tokens_per_rank, 4) ||
-        !moe::is_aligned(layout.num_tokens_per_expert, 4) || !moe::is_aligned(layout.rank_prefix, 4) ||
-        !moe::is_aligned(layout.expert_prefix, 4))
-        return MOE_ERR_MISALIGNED;
-    if (T > 0 && (!moe::is_aligned(topk_idx, 8) || !moe::is_aligned(layout.token_dst_row, 4) ||
-                  !moe::is_aligned(layout.is_token_in_rank, 4)))
-        return MOE_ERR_MISALIGNED;
-    if (moe::layout_workspace_bytes(T, E, R) > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
-    int err = MOE_OK;
-    void *scratch = moe::noalloc_scratch_address(&err);
-    if (scratch == nullptr) return err;
+    const int T = num_tokens;
+    // the same checks as moe_get_layout, first without the workspace (no CUDA call
+    // for a bad argument), then with the scratch standing in for it, so that a size
+    // beyond the scratch returns MOE_ERR_WORKSPACE before anything is launched
+    int rc = moe::layout_check_args(topk_idx, T, num_topk, num_experts, num_ranks, layout, status);
+    if (rc != MOE_OK) return rc;
+    if (T > 0 && moe::layout_workspace_bytes(T, num_experts, num_ranks) > (size_t)MOE_NOALLOC_SCRATCH_BYTES)
+        return MOE_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (T > 0) {
+        scratch = moe::noalloc_scratch_address(&rc);
+        if (scratch == nullptr) return rc;
+    }
     moe::LayoutLaunch L;
-    L.topk_idx = topk_idx;
-    L.num_tokens = T;
-    L.num_topk = k;
-    L.num_experts = E;
-    L.num_ranks = R;
-    L.out = layout;
-    L.workspace = scratch;
-    L.status = status;
-    L.stream = stream;
-    L.timeout_ns = 0;
-    L.unpublished_tile = -1;
-    return moe::launch_layout(L);
+    rc = moe::layout_prepare(topk_idx, T, num_topk, num_experts, num_ranks, layout, scratch,
+                             (size_t)MOE_NOALLOC_SCRATCH_BYTES, status, stream, 0, -1, L, false);
+    return rc != MOE_OK ? rc : moe::launch_layout(L);
 }

@@ -85,6 +85,20 @@ def test_layout_parity_shapes(moe, T, k, E, R, mask, layout_mode):
     assert_layout_equal(got, ref)
 
 
+def test_layout_many_distinct_shapes_in_one_process(moe):
+    # more distinct (experts, ranks, top-k) shapes than the library's per-shape launch caches hold (16):
+    # each shape's shared memory differs, the caches wrap, and every layout is still the oracle's
+    T = 16384        # 128 tiles of 128 tokens: the cooperative lookback, whose co-residency is cached per shape
+    shapes = [(E, R, k) for (E, R) in ((64, 8), (128, 16), (256, 8), (256, 32), (512, 64)) for k in (2, 4, 6, 8)]
+    assert len(set(shapes)) > 16
+    for i, (E, R, k) in enumerate(shapes + shapes[:3]):     # and back to the first shapes after the wrap
+        g = torch.Generator().manual_seed(1000 + i)
+        topk = wl.make_topk_uniform(g, T, E, k)
+        _, got, st = gpu_layout(moe, topk, E, R)
+        assert st == 0, (E, R, k)
+        assert_layout_equal(got, oracle.layout(topk.numpy(), E, R))
+
+
 def test_layout_duplicates_all_masked_and_bad_entries(moe):
     g = torch.Generator().manual_seed(5)
     T, k, E, R = 700, 8, 64, 8
