@@ -49,6 +49,10 @@ def lib():
         _lib.oracle_dispatch_expand.restype = I
         _lib.oracle_combine_fp8.argtypes = [P, P, I, I, I, I, P, P]
         _lib.oracle_combine_fp8.restype = I
+        _lib.oracle_dispatch_bf16_mt.argtypes = [P, I, I, P, P, I, I, I, P, I, P, P, P, P, I]
+        _lib.oracle_dispatch_bf16_mt.restype = I
+        _lib.oracle_combine_mt.argtypes = [P, I, I, I, I, P, P, I]
+        _lib.oracle_combine_mt.restype = I
         for f in ("oracle_layout", "oracle_dispatch_bf16", "oracle_dispatch_fp8", "oracle_combine"):
             getattr(_lib, f).restype = I
         _lib.oracle_bf16_from_float.argtypes = [ctypes.c_float]
@@ -94,11 +98,12 @@ def layout(topk_idx: np.ndarray, num_experts: int, num_ranks: int) -> dict:
 
 def dispatch(x_bits: np.ndarray, topk_idx: np.ndarray, topk_weights: Optional[np.ndarray],
              num_experts: int, num_ranks: int, token_dst_row: np.ndarray, recv_capacity: int,
-             fp8: bool = False, fill_x: int = 0, fill_meta: int = 0) -> dict:
+             fp8: bool = False, fill_x: int = 0, fill_meta: int = 0, threads: int = 1) -> dict:
     """Row copies (bf16 bit patterns, or E4M3 codes plus per-128 scales) and
     per-row metadata. ``x_bits`` holds bf16 bit patterns as uint16 [T, H].
     Unwritten receive rows keep the fill values, so callers can compare
-    poisoned buffers byte for byte."""
+    poisoned buffers byte for byte. ``threads`` > 1 runs the bf16 copy over
+    token ranges on that many threads (same results; for timing)."""
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
     token_dst_row = np.ascontiguousarray(token_dst_row, dtype=np.int32)
@@ -121,6 +126,12 @@ def dispatch(x_bits: np.ndarray, topk_idx: np.ndarray, topk_weights: Optional[np
                                       _ptr(token_dst_row), cap, _ptr(out["recv_x"]), _ptr(out["recv_x_scales"]),
                                       _ptr(out["recv_topk_idx"]), _ptr(out["recv_topk_weights"]),
                                       _ptr(out["recv_src_idx"]), _ptr(out["x_scales"]))
+    elif threads > 1:
+        out["recv_x"] = np.full((cap, H), fill_x & 0xFFFF, np.uint16)
+        flags = L.oracle_dispatch_bf16_mt(_ptr(x_bits), T, H, _ptr(topk_idx), _ptr(w), k, num_experts, num_ranks,
+                                          _ptr(token_dst_row), cap, _ptr(out["recv_x"]),
+                                          _ptr(out["recv_topk_idx"]), _ptr(out["recv_topk_weights"]),
+                                          _ptr(out["recv_src_idx"]), int(threads))
     else:
         out["recv_x"] = np.full((cap, H), fill_x & 0xFFFF, np.uint16)
         flags = L.oracle_dispatch_bf16(_ptr(x_bits), T, H, _ptr(topk_idx), _ptr(w), k, num_experts, num_ranks,
@@ -153,14 +164,19 @@ def dispatch_fp8_input(codes: np.ndarray, scales: np.ndarray, topk_idx: np.ndarr
     return out
 
 
-def combine(partial_bits: np.ndarray, token_dst_row: np.ndarray) -> tuple[np.ndarray, int]:
-    """bf16 bit patterns [T, H] of the fp32 ascending-rank sums."""
+def combine(partial_bits: np.ndarray, token_dst_row: np.ndarray, threads: int = 1) -> tuple[np.ndarray, int]:
+    """bf16 bit patterns [T, H] of the fp32 ascending-rank sums. ``threads`` > 1
+    runs it over token ranges on that many threads (same results; for timing)."""
     partial_bits = np.ascontiguousarray(partial_bits, dtype=np.uint16)
     token_dst_row = np.ascontiguousarray(token_dst_row, dtype=np.int32)
     num_rows, H = partial_bits.shape
     T, k = token_dst_row.shape
     out = np.zeros((T, H), np.uint16)
-    flags = lib().oracle_combine(_ptr(partial_bits), num_rows, T, H, k, _ptr(token_dst_row), _ptr(out))
+    if threads > 1:
+        flags = lib().oracle_combine_mt(_ptr(partial_bits), num_rows, T, H, k, _ptr(token_dst_row), _ptr(out),
+                                        int(threads))
+    else:
+        flags = lib().oracle_combine(_ptr(partial_bits), num_rows, T, H, k, _ptr(token_dst_row), _ptr(out))
     return out, flags
 
 

@@ -26,6 +26,7 @@
  * Compiled with plain IEEE arithmetic: no -ffast-math, no FMA contraction.
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -206,15 +207,16 @@ static void write_metadata(const int64_t *topk_idx, const float *topk_weights, i
     }
 }
 
-int oracle_dispatch_bf16(const uint16_t *x, int T, int H,
-                         const int64_t *topk_idx, const float *topk_weights, int k, int E, int R,
-                         const int32_t *token_dst_row, int recv_capacity,
-                         uint16_t *recv_x, int64_t *recv_topk_idx, float *recv_topk_weights,
-                         int32_t *recv_src_idx)
+/* The bf16 dispatch of tokens t0 <= t < t1 (every token's rows and metadata
+ * depend on that token alone). */
+static int dispatch_bf16_tokens(const uint16_t *x, int H,
+                                const int64_t *topk_idx, const float *topk_weights, int k, int E, int R,
+                                const int32_t *token_dst_row, int recv_capacity,
+                                uint16_t *recv_x, int64_t *recv_topk_idx, float *recv_topk_weights,
+                                int32_t *recv_src_idx, int t0, int t1)
 {
-    if (T < 0 || H < 1 || k < 1 || k > 32 || E % R != 0) return ORACLE_BAD_ARG;
     int flags = 0, m = E / R;
-    for (int t = 0; t < T; ++t) {
+    for (int t = t0; t < t1; ++t) {
         for (int j = 0; j < k; ++j) {
             int64_t row = token_dst_row[(int64_t)t * k + j];
             if (row < 0) continue;
@@ -226,6 +228,17 @@ int oracle_dispatch_bf16(const uint16_t *x, int T, int H,
         }
     }
     return flags;
+}
+
+int oracle_dispatch_bf16(const uint16_t *x, int T, int H,
+                         const int64_t *topk_idx, const float *topk_weights, int k, int E, int R,
+                         const int32_t *token_dst_row, int recv_capacity,
+                         uint16_t *recv_x, int64_t *recv_topk_idx, float *recv_topk_weights,
+                         int32_t *recv_src_idx)
+{
+    if (T < 0 || H < 1 || k < 1 || k > 32 || E % R != 0) return ORACLE_BAD_ARG;
+    return dispatch_bf16_tokens(x, H, topk_idx, topk_weights, k, E, R, token_dst_row, recv_capacity,
+                                recv_x, recv_topk_idx, recv_topk_weights, recv_src_idx, 0, T);
 }
 
 /* Per-128-channel block quantisation of one token row: amax = max |x| over
@@ -313,13 +326,12 @@ int oracle_dispatch_fp8_input(const uint8_t *x, const float *x_scales, int T, in
  * rank order, of float(partial[row]) ), accumulator starting at +0.0f.
  * Rank regions are laid out in ascending rank order, so ascending rank is
  * ascending row. A token with no rows gets +0. */
-int oracle_combine(const uint16_t *partial, int num_rows, int T, int H, int k,
-                   const int32_t *token_dst_row, uint16_t *out)
+static int combine_tokens(const uint16_t *partial, int num_rows, int H, int k,
+                          const int32_t *token_dst_row, uint16_t *out, int t0, int t1)
 {
-    if (T < 0 || H < 1 || k < 1 || k > 32) return ORACLE_BAD_ARG;
     int flags = 0;
     int32_t rows[32];
-    for (int t = 0; t < T; ++t) {
+    for (int t = t0; t < t1; ++t) {
         int n = 0;
         for (int j = 0; j < k; ++j) {
             int32_t row = token_dst_row[(int64_t)t * k + j];
@@ -339,6 +351,103 @@ int oracle_combine(const uint16_t *partial, int num_rows, int T, int H, int k,
         }
     }
     return flags;
+}
+
+int oracle_combine(const uint16_t *partial, int num_rows, int T, int H, int k,
+                   const int32_t *token_dst_row, uint16_t *out)
+{
+    if (T < 0 || H < 1 || k < 1 || k > 32) return ORACLE_BAD_ARG;
+    return combine_tokens(partial, num_rows, H, k, token_dst_row, out, 0, T);
+}
+
+/* ------------------------------------------------------------------ */
+/* Thread-parallel forms, for timing the oracle on every host core.     */
+/* ------------------------------------------------------------------ */
+
+/* The dispatch and the combine above, run by `threads` POSIX threads over
+ * contiguous token ranges: thread i takes tokens [T*i/n, T*(i+1)/n). Every
+ * token's outputs are computed by exactly the code above, from that token's
+ * inputs alone, into rows no other token writes, so the results are the
+ * single-threaded ones byte for byte (the tests check this); only the wall
+ * time changes. The result flags are OR-ed over the threads. */
+typedef struct {
+    int kind;                                   /* 0: bf16 dispatch, 1: combine */
+    const uint16_t *src;                        /* x or partial */
+    int num_rows, H, k, E, R, recv_capacity;
+    const int64_t *topk_idx;
+    const float *topk_weights;
+    const int32_t *token_dst_row;
+    uint16_t *dst;                              /* recv_x or out */
+    int64_t *recv_topk_idx;
+    float *recv_topk_weights;
+    int32_t *recv_src_idx;
+    int t0, t1, flags;
+} token_job;
+
+static void *run_token_job(void *arg)
+{
+    token_job *j = (token_job *)arg;
+    if (j->kind == 0)
+        j->flags = dispatch_bf16_tokens(j->src, j->H, j->topk_idx, j->topk_weights, j->k, j->E, j->R,
+                                        j->token_dst_row, j->recv_capacity, j->dst, j->recv_topk_idx,
+                                        j->recv_topk_weights, j->recv_src_idx, j->t0, j->t1);
+    else
+        j->flags = combine_tokens(j->src, j->num_rows, j->H, j->k, j->token_dst_row, j->dst, j->t0, j->t1);
+    return NULL;
+}
+
+static int run_token_jobs(const token_job *proto, int T, int threads)
+{
+    if (threads < 1) threads = 1;
+    if (threads > 1024) threads = 1024;
+    token_job *jobs = (token_job *)malloc(sizeof(token_job) * (size_t)threads);
+    pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)threads);
+    int *started = (int *)calloc((size_t)threads, sizeof(int));
+    for (int i = 0; i < threads; ++i) {
+        jobs[i] = *proto;
+        jobs[i].t0 = (int)((int64_t)T * i / threads);
+        jobs[i].t1 = (int)((int64_t)T * (i + 1) / threads);
+        jobs[i].flags = 0;
+        started[i] = (i > 0 && pthread_create(&tids[i], NULL, run_token_job, &jobs[i]) == 0);
+    }
+    run_token_job(&jobs[0]);
+    for (int i = 1; i < threads; ++i) {
+        if (started[i]) pthread_join(tids[i], NULL);
+        else run_token_job(&jobs[i]);            /* no thread could be started: run it here */
+    }
+    int flags = 0;
+    for (int i = 0; i < threads; ++i) flags |= jobs[i].flags;
+    free(jobs);
+    free(tids);
+    free(started);
+    return flags;
+}
+
+int oracle_dispatch_bf16_mt(const uint16_t *x, int T, int H,
+                            const int64_t *topk_idx, const float *topk_weights, int k, int E, int R,
+                            const int32_t *token_dst_row, int recv_capacity,
+                            uint16_t *recv_x, int64_t *recv_topk_idx, float *recv_topk_weights,
+                            int32_t *recv_src_idx, int threads)
+{
+    if (T < 0 || H < 1 || k < 1 || k > 32 || E % R != 0) return ORACLE_BAD_ARG;
+    token_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 0; j.src = x; j.H = H; j.k = k; j.E = E; j.R = R; j.recv_capacity = recv_capacity;
+    j.topk_idx = topk_idx; j.topk_weights = topk_weights; j.token_dst_row = token_dst_row;
+    j.dst = recv_x; j.recv_topk_idx = recv_topk_idx; j.recv_topk_weights = recv_topk_weights;
+    j.recv_src_idx = recv_src_idx;
+    return run_token_jobs(&j, T, threads);
+}
+
+int oracle_combine_mt(const uint16_t *partial, int num_rows, int T, int H, int k,
+                      const int32_t *token_dst_row, uint16_t *out, int threads)
+{
+    if (T < 0 || H < 1 || k < 1 || k > 32) return ORACLE_BAD_ARG;
+    token_job j;
+    memset(&j, 0, sizeof j);
+    j.kind = 1; j.src = partial; j.num_rows = num_rows; j.H = H; j.k = k;
+    j.token_dst_row = token_dst_row; j.dst = out;
+    return run_token_jobs(&j, T, threads);
 }
 
 /* ------------------------------------------------------------------ */

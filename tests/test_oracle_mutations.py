@@ -56,7 +56,7 @@ def test_pins_reject_planted_mistake(name, tmp_path):
     mutated = tmp_path / "moe_oracle_mut.c"
     mutated.write_text(src.replace(old, new))
     lib = tmp_path / "liboracle_mut.so"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-o", str(lib),
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-o", str(lib),
                     str(mutated), "-lm"], check=True)
     env = dict(os.environ, MOE_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
