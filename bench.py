@@ -3,10 +3,14 @@
 the DeepSeek-V3-shaped workload (4096 tokens, hidden 7168 bf16, 256 experts
 over 8 logical ranks, top-8), synthetic inputs resident in HBM.
 
-Prints ONE JSON line (rank 0). Default: 1 GPU, a few hundred ms of timed GPU
-work, plus the CPU oracle timed on the host as a reported baseline.
+Prints ONE JSON line (rank 0). Default: 1 GPU, K timed steps (each after an
+untimed L2 flush), then ~2 s of the same flushed step back to back under the
+clock sampler, every variant and the skewed workload timed alone, the
+end-to-end leg from pinned host buffers, and the CPU oracle timed on the host
+cores (single-threaded and on every core) as a reported baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --profile-kernel combine     # one launch for an ncu capture
 
 Under torchrun each rank runs an independent replica on its own GPU (the
 path shards by tokens and has no exchange step): weak scaling, max-over-ranks
@@ -133,10 +137,13 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def profiled_traffic(kernel: str, source: str):
-    """DRAM bytes per launch recorded in profiles/<kernel>_<workload>.md, if the
-    kernel source has not changed since (its sha256 is recorded beside it)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.md")
+def profiled_traffic(kernel: str, source: str, workload: str = WORKLOAD):
+    """DRAM traffic of one launch recorded in profiles/<kernel>_<workload>.md,
+    if the kernel source has not changed since (its sha256 is recorded beside
+    it): {"in_window": bytes ncu counted inside the kernel, "writeback": bytes
+    of the kernel's output still dirty in L2 when it ended, counted as the
+    writes of the L2-evicting read that follows it}, or None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     src = os.path.join(ROOT, "combine_moe_get_gb300", "csrc", source)
     try:
         text = open(path).read()
@@ -151,31 +158,51 @@ def profiled_traffic(kernel: str, source: str):
     if vals.get("source_sha256") != sha:
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return {"in_window": float(vals["dram_bytes_per_launch"]),
+                "writeback": float(vals["writeback_bytes_after_launch"])}
     except Exception:
         return None
 
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle(inp, w, budget_s: float, min_steps: int = 1, tokens: int = 0):
-    """Oracle steps (layout + dispatch + combine) until `budget_s` elapses, over
-    the whole batch or, with `tokens`, over its first `tokens` tokens."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def time_oracle(inp, w, budget_s: float, min_steps: int = 1, threads: int = 1):
+    """Whole oracle steps (layout, then bf16 dispatch, then combine) over the
+    whole batch until `budget_s` elapses. With `threads` > 1 the dispatch and
+    the combine run over token ranges on that many threads (the same per-token
+    code and results); the layout, a serial scan, stays on one thread."""
     import oracle
-    n = tokens or w.num_tokens
-    topk = inp.topk_idx[:n].numpy()
-    xb = inp.x[:n].view(torch.int16).numpy().view(np.uint16)
-    wts = inp.topk_weights[:n].numpy()
+    topk = inp.topk_idx.numpy()
+    xb = inp.x.view(torch.int16).numpy().view(np.uint16)
+    wts = inp.topk_weights.numpy()
     pb = inp.partial.view(torch.int16).numpy().view(np.uint16)
-    cap = wl.recv_capacity(n, w.num_topk, w.num_ranks)
+    cap = wl.recv_capacity(w.num_tokens, w.num_topk, w.num_ranks)
     steps, t0 = 0, time.perf_counter()
     while steps < min_steps or time.perf_counter() - t0 < budget_s:
         lay = oracle.layout(topk, w.num_experts, w.num_ranks)
-        oracle.dispatch(xb, topk, wts, w.num_experts, w.num_ranks, lay["token_dst_row"], cap)
-        oracle.combine(pb[: lay["num_recv"]], lay["token_dst_row"])
+        oracle.dispatch(xb, topk, wts, w.num_experts, w.num_ranks, lay["token_dst_row"], cap, threads=threads)
+        oracle.combine(pb[: lay["num_recv"]], lay["token_dst_row"], threads=threads)
         steps += 1
     dt = time.perf_counter() - t0
     return steps, dt
+
+
+def workload_config(w, recv_rows: int) -> dict:
+    """The `config` of both arms' lines (identical, so the two are comparable)."""
+    return {"workload": "DeepSeek-V3 prefill shape: T=4096, H=7168 bf16, E=256 over R=8 logical ranks, "
+                        "top-8 uniform, softmax weights",
+            "tokens": w.num_tokens, "hidden": w.hidden, "experts": w.num_experts, "ranks": w.num_ranks,
+            "topk": w.num_topk, "recv_rows": recv_rows,
+            "l2": "GPU arm: L2 flushed before every timed step (a buffer of twice the L2 size written, then another "
+                  "read; untimed); CPU arm: the step's ~1.1 GB working set exceeds every host cache",
+            "parallelism": "independent token shards, one per GPU; no collective"}
 
 
 # ------------------------------------------------------------------ the GPU step
@@ -212,7 +239,7 @@ class Step:
             recv_x=self.disp8.recv_x, recv_x_scales=self.disp8.recv_x_scales,
             recv_topk_idx=self.disp.recv_topk_idx, recv_topk_weights=self.disp.recv_topk_weights,
             recv_src_idx=self.disp.recv_src_idx, x_scales=None)
-        self.row_w = torch.rand(self.cap, device=device)
+        self.row_w = torch.rand(self.cap, generator=torch.Generator().manual_seed(w.seed + 2)).to(device)
         self.cw = torch.empty(T, k, dtype=torch.float32, device=device)
         # expand mode: one receive row per valid top-k entry, grouped by expert
         self.xcap = T * k
@@ -280,6 +307,74 @@ class Step:
         self.combine_expand()
 
 
+
+
+class Flush:
+    """The L2 flush between timed steps: write a buffer twice the size of L2,
+    then read another one. The write evicts everything, and the read evicts the
+    write's dirty lines (written back here, untimed), so the timed kernels start
+    on a cold L2 that holds only clean lines and pay for no write-back but their
+    own."""
+
+    def __init__(self, device):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+        self.src = torch.ones_like(self.buf)
+        self.sum = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self):
+        self.buf.zero_()
+        torch.sum(self.src.view(torch.int64), dim=0, out=self.sum)
+
+    def evict(self):
+        """A read of a clean buffer larger than L2: whatever the kernel before it
+        left dirty in L2 is written back during this read."""
+        torch.sum(self.buf.view(torch.int64), dim=0, out=self.sum)
+
+    def describe(self) -> str:
+        return (f"flushed between steps ({self.buf.numel() >> 20} MiB written, then {self.src.numel() >> 20} MiB "
+                f"read; untimed)")
+
+
+class Timer:
+    """Times a callable alone: captured once in a CUDA graph with an event at
+    each end and replayed after an L2 flush each time (eager calls bracketed by
+    events when graphs are unavailable). Returns the per-call milliseconds."""
+
+    def __init__(self, flush: Flush, stream, use_graph: bool):
+        self.flush, self.stream, self.use_graph = flush, stream, use_graph
+
+    def __call__(self, fn, reps: int):
+        fn()                                    # first call outside any capture
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True, external=self.use_graph)
+        b = torch.cuda.Event(enable_timing=True, external=self.use_graph)
+        g = None
+        if self.use_graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                a.record()
+                fn()
+                b.record()
+        ms = []
+        for i in range(reps + 2):
+            self.flush()
+            if g is not None:
+                g.replay()
+            else:
+                a.record(self.stream)
+                fn()
+                b.record(self.stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                ms.append(a.elapsed_time(b))
+        return ms
+
+
+def gbs(nbytes: float, ms: float) -> float:
+    return nbytes / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, world, rank, local):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
@@ -290,18 +385,7 @@ def run_ours(args, world, rank, local):
     inp = wl.make_inputs(dataclass_replace_seed(w, w.seed + rank))
     st = Step(moe, w, inp, device)
     T, H = w.num_tokens, w.hidden
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
-    flush_src = torch.ones_like(flush)
-    flush_sum = torch.empty((), dtype=torch.int64, device=device)
-
-    def flush_l2():
-        # Write a buffer twice the size of L2, then read another one: the
-        # write evicts everything, and the read evicts the write's dirty lines
-        # (written back here, untimed), so the timed kernels start on a cold L2
-        # holding only clean lines and pay for no write-back but their own.
-        flush.zero_()
-        torch.sum(flush_src.view(torch.int64), dim=0, out=flush_sum)
+    flush_l2 = Flush(device)
     stream = torch.cuda.current_stream(device)
 
     def one(events=None):
@@ -336,7 +420,7 @@ def run_ours(args, world, rank, local):
     # attribute setting happens during capture) and replayed, so host-side
     # submission cost never leaves the GPU idle inside the timed events.
     timing = "cuda-graph replay"
-    mean = statistics.fmean
+    mean, med = statistics.fmean, statistics.median
     try:
         # the step alone: events only at its ends (an event between two kernels
         # adds its own gap to the step)
@@ -369,19 +453,46 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         return ev[0].elapsed_time(ev[3]), [ev[j].elapsed_time(ev[j + 1]) for j in (0, 1, 2)]
 
+    def sustain(seconds: float):
+        """The same step, L2 flushed before each, replayed back to back for about
+        `seconds`, so that the clock sampler sees the GPU under this load: M
+        flushed steps per graph replay, each bracketed by its own events."""
+        if graph is None:
+            return []
+        M = 64
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(M)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for a, b in evs:
+                flush_l2()
+                a.record()
+                one()
+                b.record()
+        ms, t0 = [], time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            g.replay()
+            torch.cuda.synchronize()
+            ms += [a.elapsed_time(b) for a, b in evs]
+        del g
+        return ms
+
     step_ms, parts = [], []
-    barrier(world)
-    torch.cuda.synchronize()
     with ClockSampler(device.index) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
         for i in range(args.steps):
             ms, p = timed_step()
             step_ms.append(ms)
             if p:
                 parts.append(p)
         torch.cuda.synchronize()
-    barrier(world)
+        barrier(world)
+        # after the K timed steps, still under the clock sampler
+        sus_ms = sustain(args.sustain_s)
     moe.check_status(st.status, "timed steps")
     clocks = clk.summary()
+    clocks["window"] = f"the {args.steps} timed steps and the {len(sus_ms)} sustained steps after them"
 
     # per-kernel breakdown (outside the timed region): the graph with events between kernels
     if graph_k is not None:
@@ -396,59 +507,37 @@ def run_ours(args, world, rank, local):
     com_ms = [p[2] for p in parts]
     ms_per_step = max_over_ranks(mean(step_ms), world, device)
     tokens_per_s = world * T / (ms_per_step / 1e3)
+    ref_out = st.out.clone()     # the device-resident step's output, for the end-to-end leg's check
 
     # the other dispatch / combine variants, each timed alone with the same flush discipline
-    def time_alone(fn, reps):
-        fn()                                    # first call outside any capture
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True, external=graph is not None)
-        b = torch.cuda.Event(enable_timing=True, external=graph is not None)
-        g1 = None
-        if graph is not None:
-            g1 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g1):
-                a.record()
-                fn()
-                b.record()
-        ms = []
-        for i in range(reps + 2):
-            flush_l2()
-            if g1 is not None:
-                g1.replay()
-            else:
-                a.record(stream)
-                fn()
-                b.record(stream)
-            torch.cuda.synchronize()
-            if i >= 2:
-                ms.append(a.elapsed_time(b))
-        return ms
-
+    timer = Timer(flush_l2, stream, graph is not None)
     reps = max(3, args.steps // 2)
-    ld_ms = time_alone(st.layout_dispatch, reps)                              # the step's first call
-    ucomb_ms = time_alone(st.combine_unbalanced, reps)                        # moe_combine: static split only
-    fp8_ms = time_alone(lambda: st.dispatch(fp8=True), reps)                  # fused E4M3 quantisation
-    fp8in_ms = time_alone(st.dispatch_fp8_input, reps)                        # E4M3 rows + scales relayed
-    wcomb_ms = time_alone(st.combine_weighted, reps)                          # weighted rows + combined weights
-    st.dispatch(fp8=True)                                                     # E4M3 rows for the FP8 combine
-    fcomb_ms = time_alone(st.combine_fp8, reps)                               # E4M3 partial rows + scales
-    xlay_ms = time_alone(st.expand_layout, reps)                              # expand mode, each kernel alone
-    xdis_ms = time_alone(st.dispatch_expand, reps)
-    xcom_ms = time_alone(st.combine_expand, reps)
-    xstep_ms = time_alone(st.expand_step, reps)                               # the whole expand-mode step
+    ld_ms = timer(st.layout_dispatch, reps)                              # the step's first call
+    bcomb_ms = timer(st.combine, reps)                                   # the step's combine, alone
+    ucomb_ms = timer(st.combine_unbalanced, reps)                        # moe_combine: static split only
+    fp8_ms = timer(lambda: st.dispatch(fp8=True), reps)                  # fused E4M3 quantisation
+    fp8in_ms = timer(st.dispatch_fp8_input, reps)                        # E4M3 rows + scales relayed
+    wcomb_ms = timer(st.combine_weighted, reps)                          # weighted rows + combined weights
+    st.dispatch(fp8=True)                                                # E4M3 rows for the FP8 combine
+    fcomb_ms = timer(st.combine_fp8, reps)                               # E4M3 partial rows + scales
+    xlay_ms = timer(st.expand_layout, reps)                              # expand mode, each kernel alone
+    xdis_ms = timer(st.dispatch_expand, reps)
+    xcom_ms = timer(st.combine_expand, reps)
+    xstep_ms = timer(st.expand_step, reps)                               # the whole expand-mode step
     moe.check_status(st.status, "dispatch / combine variants")
+    NX = int(st.lay.expert_prefix[-1].item())                            # expand rows: valid entries
     # the decode shape (T=128 over R=256): layout + dispatch as two launches and as one
     wd = wl.CONFIGS["decode"]
     sd = Step(moe, wd, wl.make_inputs(dataclass_replace_seed(wd, wd.seed + rank)), device)
     dec = {
-        "decode_layout_dispatch_two_us": mean(time_alone(lambda: (sd.layout(), sd.dispatch()), reps)) * 1e3,
-        "decode_layout_dispatch_fused_us": mean(time_alone(sd.layout_dispatch, reps)) * 1e3,
-        "decode_step_two_us": mean(time_alone(lambda: (sd.layout(), sd.dispatch(), sd.combine()), reps)) * 1e3,
-        "decode_step_fused_us": mean(time_alone(lambda: (sd.layout_dispatch(), sd.combine()), reps)) * 1e3,
+        "decode_layout_dispatch_two_us": mean(timer(lambda: (sd.layout(), sd.dispatch()), reps)) * 1e3,
+        "decode_layout_dispatch_fused_us": mean(timer(sd.layout_dispatch, reps)) * 1e3,
+        "decode_step_two_us": mean(timer(lambda: (sd.layout(), sd.dispatch(), sd.combine()), reps)) * 1e3,
+        "decode_step_fused_us": mean(timer(lambda: (sd.layout_dispatch(), sd.combine()), reps)) * 1e3,
     }
     moe.check_status(sd.status, "decode shape")
     del sd
-    NX = int(st.lay.expert_prefix[-1].item())                                 # expand rows: valid entries
+    skewed = measure_skewed(moe, device, rank, timer, reps)
 
     peak, peak_kind = hbm_peak()
     row = H * 2
@@ -458,7 +547,6 @@ def run_ours(args, world, rank, local):
     bytes_wcomb = bytes_bf16 + N * 4                    # + one weight per receive row
     bytes_expand = T * row + NX * row                   # x read once + one row per valid entry
     bytes_fcomb = N * (H + (H // 128) * 4) + T * row    # e4m3 rows + scales read, bf16 out written
-    med = statistics.median
     kern = {
         "layout_us": mean(lay_ms) * 1e3,
         "layout_median_us": med(lay_ms) * 1e3,
@@ -469,6 +557,7 @@ def run_ours(args, world, rank, local):
         "dispatch_us": mean(dis_ms) * 1e3,
         "combine_us": mean(com_ms) * 1e3,
         "layout_dispatch_us": mean(ld_ms) * 1e3,
+        "combine_alone_us": mean(bcomb_ms) * 1e3,
         "combine_unbalanced_us": mean(ucomb_ms) * 1e3,
         "dispatch_fp8_us": mean(fp8_ms) * 1e3,
         "dispatch_fp8_input_us": mean(fp8in_ms) * 1e3,
@@ -481,10 +570,16 @@ def run_ours(args, world, rank, local):
         "expand_step_tokens_per_s": T / (mean(xstep_ms) * 1e-3),
         "expand_rows": NX,
         **dec,
+        "notes": {
+            "dispatch_us, combine_us": "inside the step (the per-kernel breakdown graph); the in-step combine also "
+                                       "writes back the dispatch's receive rows still dirty in L2",
+            "combine_alone_us": "the step's balanced combine timed alone after an L2 flush",
+            "combine_unbalanced_us": "moe_combine (static split, no balance counter) alone after an L2 flush",
+        },
     }
-    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
     kern["dispatch_gbs"] = gbs(bytes_bf16, mean(dis_ms))
     kern["combine_gbs"] = gbs(bytes_bf16, mean(com_ms))
+    kern["combine_alone_gbs"] = gbs(bytes_bf16, mean(bcomb_ms))
     kern["combine_unbalanced_gbs"] = gbs(bytes_bf16, mean(ucomb_ms))
     kern["dispatch_fp8_gbs"] = gbs(bytes_fp8, mean(fp8_ms))
     kern["dispatch_fp8_input_gbs"] = gbs(bytes_fp8in, mean(fp8in_ms))
@@ -492,54 +587,113 @@ def run_ours(args, world, rank, local):
     kern["combine_fp8_gbs"] = gbs(bytes_fcomb, mean(fcomb_ms))
     kern["dispatch_expand_gbs"] = gbs(bytes_expand, mean(xdis_ms))
     kern["combine_expand_gbs"] = gbs(bytes_expand, mean(xcom_ms))
-    for key in ("dispatch", "combine", "combine_unbalanced", "dispatch_fp8", "dispatch_fp8_input", "combine_weighted", "combine_fp8",
-                "dispatch_expand", "combine_expand"):
+    for key in ("dispatch", "combine", "combine_alone", "combine_unbalanced", "dispatch_fp8", "dispatch_fp8_input",
+                "combine_weighted", "combine_fp8", "dispatch_expand", "combine_expand"):
         kern[f"{key}_frac"] = kern[f"{key}_gbs"] / peak
         kern[f"{key}_frac_of_spec"] = kern[f"{key}_gbs"] / HBM_SPEC_GBS
+    skewed_bytes = skewed.pop("_bytes")
+    for key, nbytes in skewed_bytes.items():
+        skewed[f"{key}_gbs"] = gbs(nbytes, skewed[f"{key}_us"] * 1e-3)
+        skewed[f"{key}_frac"] = skewed[f"{key}_gbs"] / peak
+    kern["skewed"] = skewed
+    if sus_ms:
+        kern["sustained"] = {"steps": len(sus_ms), "ms_per_step_mean": mean(sus_ms),
+                             "ms_per_step_median": med(sus_ms), "tokens_per_s": T / (mean(sus_ms) * 1e-3),
+                             "how": "the timed step, L2 flushed before each, replayed back to back for "
+                                    f"~{args.sustain_s:g} s after the timed steps (64 steps per graph replay, "
+                                    "each bracketed by its own events)"}
     dominant = "dispatch" if mean(dis_ms) >= mean(com_ms) else "combine"
     dom_ms = mean(dis_ms) if dominant == "dispatch" else mean(com_ms)
     achieved = gbs(bytes_bf16, dom_ms)
-    traffic = profiled_traffic(f"{dominant}_kernel", f"{dominant}.cu")
+    prof = profiled_traffic(f"{dominant}_kernel", f"{dominant}.cu")
+    step_gbs = gbs(2 * bytes_bf16, ms_per_step)
 
-    e2e = run_e2e(moe, st, inp, w, device, args)
+    e2e = run_e2e(moe, st, inp, w, device, args, ref_out, N)
 
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 rows, uniform top-8 routing)",
-        "config": {"workload": "DeepSeek-V3 prefill shape: T=4096, H=7168 bf16, E=256 over R=8 logical ranks, "
-                               "top-8 uniform, softmax weights", "tokens": T, "hidden": H,
-                   "experts": w.num_experts, "ranks": w.num_ranks, "topk": w.num_topk, "recv_rows": N,
-                   "step": "moe_layout_dispatch (layout, then bf16 dispatch) + moe_combine_ex (balance counter)",
-                   "timing": timing, "l2": f"flushed between steps ({flush.numel() >> 20} MiB written, then {flush_src.numel() >> 20} MiB read; untimed)",
-                   "parallelism": f"replicas x{world} (independent token shards, no collective)"},
+        "config": workload_config(w, N),
+        "step": "moe_layout_dispatch (layout, then bf16 dispatch) + moe_combine_ex (balance counter)",
+        "timing": timing, "l2": flush_l2.describe(),
         "roofline": {"bound": "hbm", "kernel": f"{dominant}_kernel", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None if prof is None else prof["in_window"] + prof["writeback"],
+                     "traffic_in_window": None if prof is None else prof["in_window"],
+                     "traffic_writeback": None if prof is None else prof["writeback"],
+                     "traffic_scope": "one launch alone after an L2 flush: the DRAM bytes ncu counts inside the "
+                                      "kernel plus the write-back of its output still dirty in L2 when it ends "
+                                      "(the writes of the L2-evicting read that follows it, in the same ncu run)",
                      "algorithmic_bytes": bytes_bf16, "spec_peak": HBM_SPEC_GBS,
-                     "frac_of_spec": achieved / HBM_SPEC_GBS},
+                     "frac_of_spec": achieved / HBM_SPEC_GBS,
+                     "step_achieved": step_gbs, "step_frac": step_gbs / peak,
+                     "step_bytes": 2 * bytes_bf16},
         "kernels": kern,
         "gpu_launches": 3 * args.steps,   # per step: the layout kernel (one cluster), the dispatch and the combine
         "clocks": clocks,
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        steps, dt = time_oracle(inp, w, args.cpu_budget)
-        line["cpu_baseline"] = {"value": steps * T / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{steps} full oracle steps (layout+dispatch+combine) of the same "
-                                          f"workload, {dt:.1f} s single-threaded"}
+        cores = host_cores()
+        s1, d1 = time_oracle(inp, w, args.cpu_budget)
+        sn, dn = time_oracle(inp, w, args.cpu_budget / 2, threads=cores)
+        line["cpu_baseline"] = {
+            "value": sn * T / dn, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "single_thread_value": s1 * T / d1,
+            "sample": f"{sn} full oracle steps of the same workload (layout on one thread; dispatch and combine "
+                      f"over token ranges on {cores} threads) in {dn:.1f} s; single-threaded, {s1} steps in "
+                      f"{d1:.1f} s"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(moe, st, inp, w, device, args):
+def measure_skewed(moe, device, rank, timer, reps):
+    """The skewed workload (8192 tokens over 64 ranks, Zipf expert popularity)
+    with the same kernels and flush discipline: the step and its kernels alone."""
+    ws = wl.CONFIGS["skewed"]
+    sk = Step(moe, ws, wl.make_inputs(dataclass_replace_seed(ws, ws.seed + rank)), device)
+    sk.layout_dispatch()
+    sk.combine()
+    torch.cuda.synchronize()
+    moe.check_status(sk.status, "skewed workload")
+    T, H = ws.num_tokens, ws.hidden
+    N = int(sk.lay.rank_prefix[-1].item())
+    mean = statistics.fmean
+    out = {"tokens": T, "hidden": H, "experts": ws.num_experts, "ranks": ws.num_ranks, "topk": ws.num_topk,
+           "routing": "Zipf(s=1) expert popularity over a random permutation", "recv_rows": N}
+    out["step_us"] = mean(timer(lambda: (sk.layout_dispatch(), sk.combine()), reps)) * 1e3
+    out["layout_us"] = mean(timer(sk.layout, reps)) * 1e3
+    out["layout_dispatch_us"] = mean(timer(sk.layout_dispatch, reps)) * 1e3
+    out["dispatch_us"] = mean(timer(sk.dispatch, reps)) * 1e3
+    out["dispatch_fp8_us"] = mean(timer(lambda: sk.dispatch(fp8=True), reps)) * 1e3
+    out["combine_us"] = mean(timer(sk.combine, reps)) * 1e3
+    out["combine_unbalanced_us"] = mean(timer(sk.combine_unbalanced, reps)) * 1e3
+    out["combine_fp8_us"] = mean(timer(sk.combine_fp8, reps)) * 1e3
+    moe.check_status(sk.status, "skewed workload")
+    out["step_tokens_per_s"] = T / (out["step_us"] * 1e-6)
+    row = H * 2
+    b = T * row + N * row
+    out["_bytes"] = {"step": 2 * b, "dispatch": b, "combine": b, "combine_unbalanced": b,
+                     "dispatch_fp8": T * row + N * H + N * (H // 128) * 4,
+                     "combine_fp8": N * (H + (H // 128) * 4) + T * row}
+    out["notes"] = "every kernel timed alone after an L2 flush (dispatch and combine with balance counters)"
+    del sk
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_e2e(moe, st, inp, w, device, args, ref_out, ref_rows):
     """Same step through the public API from pinned host buffers: H2D of the
     step's inputs, a 4-byte read of the receive count, H2D of the partial rows,
     D2H of the combined output -- every step's copies inside the timed region.
     Two steps are in flight on two sets of device buffers: step i's output D2H
     (its own stream) overlaps step i+1's input H2D, since the host link carries
-    both directions at once; the host waits only for each step's receive count."""
+    both directions at once; the host waits only for each step's receive count.
+    After the timed steps the last output read back to the host is compared bit
+    for bit with the device-resident step's output on the same inputs."""
     T, H = w.num_tokens, w.hidden
     hx = inp.x.pin_memory()
     htopk = inp.topk_idx.pin_memory()
@@ -593,12 +747,18 @@ def run_e2e(moe, st, inp, w, device, args):
     sec = (time.perf_counter() - t0) / K
     for s in bufs:
         moe.check_status(s.status, "e2e")
+    last = houts[(args.warmup + K - 1) % 2]
+    same = ns[-1] == ref_rows and torch.equal(last.view(torch.int16), ref_out.cpu().view(torch.int16))
+    if not same:
+        raise RuntimeError("end-to-end leg: the output read back differs from the device-resident step's")
     n = ns[-1]
     h2d = hx.numel() * 2 + htopk.numel() * 8 + hw.numel() * 4 + n * H * 2
     d2h = 4 + houts[0].numel() * 2
     del bufs[1]
     return {"value": T / sec, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": sec * 1e3, "in_flight": "2 steps: step i's output read-back overlaps step i+1's input copies"}
+            "ms_per_step": sec * 1e3, "in_flight": "2 steps: step i's output read-back overlaps step i+1's input copies",
+            "output_check": "the last step's output read back to the host equals the device-resident step's "
+                            "output on the same inputs, bit for bit (and the same receive-row count)"}
 
 
 def dataclass_replace_seed(w, seed):
@@ -606,36 +766,74 @@ def dataclass_replace_seed(w, seed):
     return dataclasses.replace(w, seed=seed)
 
 
+# ------------------------------------------------------------------ one kernel for an ncu capture
+
+PROFILE_KERNELS = ("layout", "dispatch", "combine", "dispatch_fp8", "combine_fp8", "layout_dispatch", "step")
+
+
+def run_profile(args):
+    """A small run for ncu: the DeepSeek-V3 workload on cuda:0 (about 2.5 GB
+    on the device), a few untimed calls, then, inside the NVTX range
+    "profile", ONE call of the chosen kernel(s) after an L2 flush followed by
+    an L2-evicting read of a clean buffer larger than L2 (whose DRAM writes are
+    the kernel's output left dirty in L2). Capture with
+    `ncu --nvtx --nvtx-include "profile/" ...`. No timing is printed: a
+    number taken under a profiler is not a measurement."""
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from combine_moe_get_gb300 import binding as moe
+    w = wl.CONFIGS[args.profile_workload]
+    st = Step(moe, w, wl.make_inputs(w), device)
+    flush_l2 = Flush(device)
+    st.layout()
+    st.dispatch(fp8=True)                       # E4M3 rows and scales for the FP8 combine's input
+    fn = {"layout": st.layout, "dispatch": st.dispatch, "combine": st.combine,
+          "dispatch_fp8": lambda: st.dispatch(fp8=True), "combine_fp8": st.combine_fp8,
+          "layout_dispatch": st.layout_dispatch,
+          "step": lambda: (st.layout_dispatch(), st.combine())}[args.profile_kernel]
+    for _ in range(2):
+        flush_l2()
+        fn()
+    flush_l2()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("profile")
+    fn()
+    flush_l2.evict()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    moe.check_status(st.status, "profile run")
+    N = int(st.lay.rank_prefix[-1].item())
+    print(json.dumps({"profile_kernel": args.profile_kernel, "workload": w.name, "recv_rows": N}), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 
-REFERENCE_SAMPLE_TOKENS = 1024  # tokens per reference step: a few tenths of a second of oracle work
-
-
 def run_reference(args, world, rank):
-    """The CPU oracle on the workload: each step is layout + dispatch + combine
-    over a bounded sample (the first 1024 of the 4096 tokens, same routing
-    distribution and hidden size), so that the default run (200 steps) ends in
-    about a minute; the rate is tokens of the sample per second."""
+    """The CPU oracle on the same workload: each step is the oracle's layout,
+    bf16 dispatch and combine over all 4096 tokens, the dispatch and the
+    combine over token ranges on every host core (the same per-token code and
+    results as single-threaded). Under torchrun only rank 0 runs it."""
     if rank != 0:
         return
+    import oracle
     w = wl.CONFIGS[WORKLOAD]
     inp = wl.make_inputs(w)
-    S = min(REFERENCE_SAMPLE_TOKENS, w.num_tokens)
-    time_oracle(inp, w, 0.0, min_steps=args.warmup, tokens=S)
-    steps, dt = time_oracle(inp, w, 0.0, min_steps=args.steps, tokens=S)
-    T = S
-    value = steps * T / dt
+    cores = host_cores()
+    time_oracle(inp, w, 0.0, min_steps=args.warmup, threads=cores)
+    steps, dt = time_oracle(inp, w, 0.0, min_steps=args.steps, threads=cores)
+    value = steps * w.num_tokens / dt
+    N = oracle.layout(inp.topk_idx.numpy(), w.num_experts, w.num_ranks)["num_recv"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "DeepSeek-V3 prefill shape: T=4096, H=7168 bf16, E=256 over R=8 logical ranks, "
-                               "top-8 uniform, softmax weights", "tokens": w.num_tokens, "hidden": w.hidden,
-                   "experts": w.num_experts, "ranks": w.num_ranks, "topk": w.num_topk,
-                   "step": "layout + dispatch(bf16) + combine (CPU oracle)"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{steps} oracle steps, each over the first {S} of the {w.num_tokens} tokens "
-                                   f"(same routing and hidden size), single-threaded"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 rows, uniform top-8 routing)",
+        "config": workload_config(w, N),
+        "step": "layout + bf16 dispatch + combine (CPU oracle; dispatch and combine over token ranges on every "
+                "host core)",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{steps} full oracle steps over all {w.num_tokens} tokens of the workload "
+                                   f"(layout on one thread; dispatch and combine on {cores} threads)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -648,10 +846,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of single-threaded oracle work for cpu_baseline (half that threaded)")
+    ap.add_argument("--sustain-s", type=float, default=2.0,
+                    help="seconds of back-to-back flushed steps after the timed ones, under the clock sampler")
+    ap.add_argument("--profile-kernel", choices=PROFILE_KERNELS, default=None,
+                    help="run one call of this kernel for an ncu capture instead of the benchmark")
+    ap.add_argument("--profile-workload", choices=["dsv3", "skewed", "decode"], default=WORKLOAD)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile_kernel:
+        run_profile(args)
+        return
     world, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, world, rank)
