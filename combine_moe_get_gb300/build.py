@@ -47,13 +47,15 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, defines: tuple = ()) -> str:
+    """Compile and link the library in place. `defines` (e.g. ("MOE_TUNE_X=4",))
+    builds a variant with other compile-time settings; the default build has none."""
     if not force and up_to_date():
         return LIB
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     common = [nvcc, *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
-              "-I", INCLUDE, "--expt-relaxed-constexpr"]
+              "-I", INCLUDE, "--expt-relaxed-constexpr", *(f"-D{d}" for d in defines)]
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")

@@ -68,6 +68,10 @@ struct DispatchArgs {
     size_t fl_off;            // byte offset of the layout region in dynamic shared memory
     moe_layout_t fl_out;      // layout outputs, written by CTA 0
     int loads_before_wait;    // first stage loads (input rows only) before the dependency wait
+    // with loads_before_wait: input units per CTA to bring into L2 while the
+    // dependency wait lasts (its next dealt units, then pool units blockIdx +
+    // i * gridDim), kept with an evict-last policy when prefetch_keep is set
+    int prefetch_units, prefetch_keep;
     // tail balancing: units [0, static_units) are dealt round-robin to the CTAs;
     // the rest form a pool claimed through pool[0], so that CTAs on faster SMs
     // take more of them; pool[1] counts the CTAs whose warps will claim no
@@ -419,8 +423,25 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         }
     }
     __syncwarp();
-    // launched right behind this library's layout, the input rows were complete
-    // before this grid could launch; the layout's outputs are read only from here
+    // launched right behind this library's layout (whose outputs are read only
+    // after the wait below), the input rows were complete before this grid
+    // could launch: while the layout runs, bring the rows of this CTA's next
+    // units into L2 as well
+    if (a.loads_before_wait && a.prefetch_units > 0) {
+        const uint64_t pol_pf = a.prefetch_keep ? policy_evict_last() : policy_evict_normal();
+        const int64_t first = (int64_t)warps * S;   // units the stage loads above claimed
+        const int64_t n_dealt = max((int64_t)0, min(cta_units, first + a.prefetch_units) - first);
+        const int64_t pool_units = a.pool ? a.num_units - dealt : 0;
+        const int64_t cta_pool = pool_units > (int64_t)blockIdx.x ? (pool_units - 1 - blockIdx.x) / G + 1 : 0;
+        const int64_t n_pool = min(cta_pool, max((int64_t)0, (int64_t)a.prefetch_units - n_dealt));
+        for (int64_t i = threadIdx.x; i < n_dealt + n_pool; i += blockDim.x) {
+            const int64_t u = i < n_dealt ? (int64_t)blockIdx.x + (first + i) * G
+                                          : dealt + (int64_t)blockIdx.x + (i - n_dealt) * G;
+            const int64_t t = div_count(u, a.num_chunks);
+            const int64_t off = (u - t * a.num_chunks) * (int64_t)chunk;
+            bulk_prefetch_l2(a.x + t * a.row_bytes + off, (uint32_t)min((int64_t)chunk, a.row_bytes - off), pol_pf);
+        }
+    }
     if (a.loads_before_wait) grid_dependency_wait();
     grid_launch_dependents();
 
@@ -493,6 +514,15 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         if (!__all_sync(kFull, ok)) {
             if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
             break;
+        }
+        // input rows brought into L2 with an evict-last policy during the
+        // dependency wait return to normal priority once their load has landed
+        // (lines aligned down to 128 bytes lie in the same page as the row's own)
+        if (a.prefetch_units > 0 && a.prefetch_keep) {
+            const uintptr_t g = reinterpret_cast<uintptr_t>(a.x + t * a.row_bytes + off);
+            const uintptr_t lo = g & ~(uintptr_t)127, hi = (g + (uintptr_t)nbytes - 1) & ~(uintptr_t)127;
+            for (uintptr_t l = lo + (uintptr_t)lane * 128; l <= hi; l += 32 * 128)
+                l2_priority_normal(reinterpret_cast<const void *>(l));
         }
 
         const uint8_t *src = in_stage + (size_t)s * chunk;
@@ -840,6 +870,8 @@ DispatchArgs base_args(const DispatchLaunch &L) {
     a.topk_w = L.topk_weights;
     a.dst_row = L.token_dst_row;
     a.loads_before_wait = L.loads_before_wait ? 1 : 0;
+    a.prefetch_units = L.loads_before_wait ? tu.dispatch_prefetch : 0;
+    a.prefetch_keep = tu.dispatch_prefetch_keep;
     a.pool = L.pool;
     a.capacity = L.recv_capacity;
     a.recv_x = static_cast<uint8_t *>(L.recv_x);

@@ -111,6 +111,8 @@ const Tuning &tuning() {
         x.l2_hints = MOE_TUNE_L2_HINTS & 3;
         x.spread_small = MOE_TUNE_SPREAD_SMALL;
         x.fused_small = MOE_TUNE_FUSED_SMALL;
+        x.dispatch_prefetch = MOE_TUNE_DISPATCH_PREFETCH;
+        x.dispatch_prefetch_keep = MOE_TUNE_DISPATCH_PREFETCH_KEEP;
         return x;
     }();
     return t;

@@ -160,6 +160,25 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Bring `bytes` (a multiple of 16, 16-byte aligned source) of global memory
+// into L2 with a cache policy; nothing is waited for or written.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *gmem_src, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
+                 ::"l"(gmem_src), "r"(bytes), "l"(policy) : "memory");
+}
+
+// Give the 128-byte L2 line at `p` (128-byte aligned) normal eviction
+// priority again, e.g. after an evict-last prefetch has been consumed.
+__device__ __forceinline__ void l2_priority_normal(const void *p) {
+    asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));

@@ -80,6 +80,12 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 #ifndef MOE_TUNE_FUSED_SMALL
 #define MOE_TUNE_FUSED_SMALL 1
 #endif
+#ifndef MOE_TUNE_DISPATCH_PREFETCH
+#define MOE_TUNE_DISPATCH_PREFETCH (1 << 20)
+#endif
+#ifndef MOE_TUNE_DISPATCH_PREFETCH_KEEP
+#define MOE_TUNE_DISPATCH_PREFETCH_KEEP 1
+#endif
 struct Tuning {
     int dispatch_warps, dispatch_stages, dispatch_chunk;
     int dispatch_smem;                                       // shared-memory budget of a chunked dispatch CTA
@@ -94,6 +100,8 @@ struct Tuning {
     int dispatch_pool;  // % of dispatch units left to a shared pool when a cleared counter is at hand (>= 100: off)
     int combine_pool;   // % of combine tokens left to a shared pool when the caller gives a counter (>= 100: off)
     int layout_cluster; // CTAs of the cluster-mode layout (8 or 16; other values: off)
+    int dispatch_prefetch;       // moe_layout_dispatch: input units per CTA prefetched into L2 during the layout
+    int dispatch_prefetch_keep;  // ... with an evict-last policy (else evict-normal)
 };
 const Tuning &tuning();
 
