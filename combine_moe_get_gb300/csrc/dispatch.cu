@@ -164,14 +164,26 @@ __device__ __forceinline__ uint2 e4m3_quad(uint4 v, float scale, const RcpBracke
     return q;
 }
 
-__device__ __forceinline__ float bf16x2_absmax(uint32_t w, float m) {
-    return fmaxf(m, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u))));
+// Per half: the larger of |a| and |b| (two bf16 in a word), in one instruction;
+// the sign bit of each half is the XOR of the inputs' signs and is masked off
+// by the caller. A maximum of bf16 magnitudes is exact, so widening the result
+// gives the same fp32 value as the maximum of the widened magnitudes.
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// max |x| over the bf16 halves of one word, as an fp32
+__device__ __forceinline__ float word_absmax(uint32_t m) {
+    m = absmax_bf16x2(m, m >> 16);   // low half: the larger of the two halves
+    return __uint_as_float((m & 0x7fffu) << 16);
 }
 
 // Quantise one 128-channel block held by a half-warp (16 lanes x 8 values).
 // Returns the block's scale; writes the 8 codes of this lane to `q8`.
 __device__ __forceinline__ float quantize_lane8(const uint4 v, uint2 &q8) {
-    float amax = bf16x2_absmax(v.w, bf16x2_absmax(v.z, bf16x2_absmax(v.y, bf16x2_absmax(v.x, 0.0f))));
+    float amax = word_absmax(absmax_bf16x2(absmax_bf16x2(v.x, v.y), absmax_bf16x2(v.z, v.w)));
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     const float scale = block_scale(amax);
@@ -188,8 +200,8 @@ __device__ __forceinline__ float quantize_lane8(const uint4 v, uint2 &q8) {
 // `lo`, `hi` are the lane's 32 contiguous bytes). Returns the block's scale;
 // writes the 16 codes to `q16`.
 __device__ __forceinline__ float quantize_lane16(const uint4 lo, const uint4 hi, uint4 &q16) {
-    float amax = bf16x2_absmax(lo.w, bf16x2_absmax(lo.z, bf16x2_absmax(lo.y, bf16x2_absmax(lo.x, 0.0f))));
-    amax = bf16x2_absmax(hi.w, bf16x2_absmax(hi.z, bf16x2_absmax(hi.y, bf16x2_absmax(hi.x, amax))));
+    float amax = word_absmax(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(lo.x, lo.y), absmax_bf16x2(lo.z, lo.w)),
+                                           absmax_bf16x2(absmax_bf16x2(hi.x, hi.y), absmax_bf16x2(hi.z, hi.w))));
 #pragma unroll
     for (int o = 4; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
     const float scale = block_scale(amax);
