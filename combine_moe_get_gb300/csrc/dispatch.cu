@@ -68,10 +68,13 @@ struct DispatchArgs {
     size_t fl_off;            // byte offset of the layout region in dynamic shared memory
     moe_layout_t fl_out;      // layout outputs, written by CTA 0
     int loads_before_wait;    // first stage loads (input rows only) before the dependency wait
-    // with loads_before_wait: input units per CTA to bring into L2 while the
-    // dependency wait lasts (its next dealt units, then pool units blockIdx +
-    // i * gridDim), kept with an evict-last policy when prefetch_keep is set
-    int prefetch_units, prefetch_keep;
+    // input units per CTA to bring into L2 right after the first stage loads
+    // (its next dealt units, then pool units blockIdx + i * gridDim), kept with
+    // an evict-last policy when prefetch_keep is set; with loads_before_wait
+    // this happens while the dependency wait lasts. Bounded on the host so that
+    // the grid's evict-last lines take at most a fixed share of L2.
+    int64_t prefetch_units;
+    int prefetch_keep;
     // tail balancing: units [0, static_units) are dealt round-robin to the CTAs;
     // the rest form a pool claimed through pool[0], so that CTAs on faster SMs
     // take more of them; pool[1] counts the CTAs whose warps will claim no
@@ -80,6 +83,24 @@ struct DispatchArgs {
     unsigned int *pool;
     int64_t static_units;
 };
+
+// Whether unit u's input rows were prefetched (evict-last) by the rule of
+// dispatch_kernel: CTA b (of G) prefetches its dealt units b + j * G with
+// first <= j < first + P (j < its dealt count), then, when every CTA's first
+// stage loads took dealt units (dealt >= G * first, so that no pool unit is
+// claimed before all prefetches are issued), pool units dealt + b + m * G for
+// m < P - (the number of dealt units it prefetched).
+__device__ __forceinline__ bool unit_prefetched(int64_t u, int64_t dealt, int64_t G, int64_t first, int64_t P) {
+    if (u < dealt) {
+        const int64_t j = div_count(u, (int)G);
+        return j >= first && j < first + P;
+    }
+    if (dealt < G * first) return false;
+    const int64_t i = u - dealt, m = div_count(i, (int)G), b = i - m * G;
+    const int64_t cta_units = dealt > b ? (dealt - 1 - b) / G + 1 : 0;
+    const int64_t n_dealt = max((int64_t)0, min(cta_units, first + P) - first);
+    return m < P - n_dealt;
+}
 
 // Block scale RN(amax / 448) without a division: q0 = RN(amax * C) with
 // C = RN(1/448), r = amax - q0 * 448 (exact by FMA), s = RN(r * C + q0).
@@ -435,15 +456,15 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         }
     }
     __syncwarp();
-    // launched right behind this library's layout (whose outputs are read only
-    // after the wait below), the input rows were complete before this grid
-    // could launch: while the layout runs, bring the rows of this CTA's next
-    // units into L2 as well
-    if (a.loads_before_wait && a.prefetch_units > 0) {
+    // Bring the rows of this CTA's next units into L2 as well, all at once (the
+    // input rows are complete here: after the dependency wait, or, launched
+    // right behind this library's layout whose outputs are read only after the
+    // wait below, before it, so that the reads overlap the layout)
+    if (a.prefetch_units > 0) {
         const uint64_t pol_pf = a.prefetch_keep ? policy_evict_last() : policy_evict_normal();
         const int64_t first = (int64_t)warps * S;   // units the stage loads above claimed
         const int64_t n_dealt = max((int64_t)0, min(cta_units, first + a.prefetch_units) - first);
-        const int64_t pool_units = a.pool ? a.num_units - dealt : 0;
+        const int64_t pool_units = (a.pool && dealt >= G * first) ? a.num_units - dealt : 0;
         const int64_t cta_pool = pool_units > (int64_t)blockIdx.x ? (pool_units - 1 - blockIdx.x) / G + 1 : 0;
         const int64_t n_pool = min(cta_pool, max((int64_t)0, (int64_t)a.prefetch_units - n_dealt));
         for (int64_t i = threadIdx.x; i < n_dealt + n_pool; i += blockDim.x) {
@@ -453,6 +474,10 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
             const int64_t off = (u - t * a.num_chunks) * (int64_t)chunk;
             bulk_prefetch_l2(a.x + t * a.row_bytes + off, (uint32_t)min((int64_t)chunk, a.row_bytes - off), pol_pf);
         }
+        // every prefetch of the CTA is issued before any of its warps claims a unit
+        // past its stages (a prefetch landing after the unit's own load would keep
+        // its lines evict-last)
+        __syncthreads();
     }
     if (a.loads_before_wait) grid_dependency_wait();
     grid_launch_dependents();
@@ -530,7 +555,8 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         // input rows brought into L2 with an evict-last policy during the
         // dependency wait return to normal priority once their load has landed
         // (lines aligned down to 128 bytes lie in the same page as the row's own)
-        if (a.prefetch_units > 0 && a.prefetch_keep) {
+        if (a.prefetch_units > 0 && a.prefetch_keep &&
+            unit_prefetched(u, dealt, G, (int64_t)warps * S, a.prefetch_units)) {
             const uintptr_t g = reinterpret_cast<uintptr_t>(a.x + t * a.row_bytes + off);
             const uintptr_t lo = g & ~(uintptr_t)127, hi = (g + (uintptr_t)nbytes - 1) & ~(uintptr_t)127;
             for (uintptr_t l = lo + (uintptr_t)lane * 128; l <= hi; l += 32 * 128)
@@ -882,7 +908,7 @@ DispatchArgs base_args(const DispatchLaunch &L) {
     a.topk_w = L.topk_weights;
     a.dst_row = L.token_dst_row;
     a.loads_before_wait = L.loads_before_wait ? 1 : 0;
-    a.prefetch_units = L.loads_before_wait ? tu.dispatch_prefetch : 0;
+    a.prefetch_units = (L.loads_before_wait || tu.dispatch_prefetch_always) ? tu.dispatch_prefetch : 0;
     a.prefetch_keep = tu.dispatch_prefetch_keep;
     a.pool = L.pool;
     a.capacity = L.recv_capacity;
@@ -959,6 +985,17 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     } else {
         a.pool = nullptr;
         a.static_units = a.num_units;
+    }
+    // the L2 prefetch: at most dispatch_prefetch_l2_pct of L2 held evict-last by
+    // the grid, and none at all when the first stage loads already take every
+    // dealt unit and no pool unit would be prefetched (small batches)
+    if (a.prefetch_units > 0) {
+        const int64_t budget = (int64_t)device_l2_bytes() * tu.dispatch_prefetch_l2_pct / 100;
+        a.prefetch_units = std::min<int64_t>(a.prefetch_units, budget / ((int64_t)grid * a.chunk_bytes));
+        const int64_t first = (int64_t)warps * a.stages;
+        const int64_t max_dealt = (a.static_units + grid - 1) / grid;
+        const bool pool_prefetch = a.pool != nullptr && a.static_units >= (int64_t)grid * first;
+        if (max_dealt <= first && !pool_prefetch) a.prefetch_units = 0;
     }
     return MOE_OK;
 }

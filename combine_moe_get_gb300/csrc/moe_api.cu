@@ -25,6 +25,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<long long> g_smem_sm[kMaxDevices];
 std::atomic<long long> g_smem_optin[kMaxDevices];
+std::atomic<long long> g_l2[kMaxDevices];
 
 int current_device() {
     int d = 0;
@@ -72,6 +73,17 @@ size_t device_smem_optin() {
     return (size_t)v;
 }
 
+size_t device_l2_bytes() {
+    const int d = current_device();
+    long long v = g_l2[d].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = query_attr(cudaDevAttrL2CacheSize, d);
+        if (v <= 0) v = 1;
+        g_l2[d].store(v, std::memory_order_relaxed);
+    }
+    return (size_t)v;
+}
+
 int ensure_dynamic_smem(const void *kernel, size_t bytes) {
     static std::mutex mu;
     static std::unordered_map<const void *, size_t> done[kMaxDevices];
@@ -113,6 +125,8 @@ const Tuning &tuning() {
         x.fused_small = MOE_TUNE_FUSED_SMALL;
         x.dispatch_prefetch = MOE_TUNE_DISPATCH_PREFETCH;
         x.dispatch_prefetch_keep = MOE_TUNE_DISPATCH_PREFETCH_KEEP;
+        x.dispatch_prefetch_always = MOE_TUNE_DISPATCH_PREFETCH_ALWAYS;
+        x.dispatch_prefetch_l2_pct = MOE_TUNE_DISPATCH_PREFETCH_L2_PCT;
         return x;
     }();
     return t;

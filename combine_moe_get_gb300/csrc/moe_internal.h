@@ -15,6 +15,7 @@ namespace moe {
 int device_sm_count();             // SMs of the current device
 size_t device_smem_per_sm();       // shared memory per SM (bytes)
 size_t device_smem_optin();        // max dynamic shared memory per block (bytes)
+size_t device_l2_bytes();          // L2 cache size (bytes)
 
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` (cached).
 int ensure_dynamic_smem(const void *kernel, size_t bytes);
@@ -83,6 +84,12 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 #ifndef MOE_TUNE_DISPATCH_PREFETCH
 #define MOE_TUNE_DISPATCH_PREFETCH (1 << 20)
 #endif
+#ifndef MOE_TUNE_DISPATCH_PREFETCH_ALWAYS
+#define MOE_TUNE_DISPATCH_PREFETCH_ALWAYS 1
+#endif
+#ifndef MOE_TUNE_DISPATCH_PREFETCH_L2_PCT
+#define MOE_TUNE_DISPATCH_PREFETCH_L2_PCT 25
+#endif
 #ifndef MOE_TUNE_DISPATCH_PREFETCH_KEEP
 #define MOE_TUNE_DISPATCH_PREFETCH_KEEP 1
 #endif
@@ -100,8 +107,10 @@ struct Tuning {
     int dispatch_pool;  // % of dispatch units left to a shared pool when a cleared counter is at hand (>= 100: off)
     int combine_pool;   // % of combine tokens left to a shared pool when the caller gives a counter (>= 100: off)
     int layout_cluster; // CTAs of the cluster-mode layout (8 or 16; other values: off)
-    int dispatch_prefetch;       // moe_layout_dispatch: input units per CTA prefetched into L2 during the layout
+    int dispatch_prefetch;       // input units per CTA prefetched into L2 (moe_layout_dispatch: during the layout)
     int dispatch_prefetch_keep;  // ... with an evict-last policy (else evict-normal)
+    int dispatch_prefetch_always;  // ... in every chunked dispatch, not only behind the layout
+    int dispatch_prefetch_l2_pct;  // ... holding at most this share of L2 evict-last
 };
 const Tuning &tuning();
 
