@@ -386,6 +386,41 @@ def test_dispatch_balanced_parity(moe, T, H, k, E, R, mode):
         np.testing.assert_array_equal(out.recv_topk_idx[:N].cpu().numpy(), ref["recv_topk_idx"][:N])
 
 
+@pytest.mark.parametrize("T,H,k,E,R,balanced", [
+    (1000, 7168, 8, 256, 8, True),      # pool on, first stage loads spill into the pool: dealt units prefetched only
+    (3000, 7168, 8, 256, 8, True),      # pool on, pool units prefetched too
+    (3000, 7168, 8, 256, 8, False),     # every unit dealt
+    (16384, 7168, 8, 256, 8, True),     # more input than the prefetch budget: part of each CTA's units prefetched
+    (700, 4104, 6, 48, 3, True),        # rows not a multiple of the chunk alignment, ranks not a power of two
+])
+def test_dispatch_l2_prefetch_regimes(moe, T, H, k, E, R, balanced):
+    # the dispatch prefetches its input rows into L2 in every regime of the prefetch rule (with or
+    # without a pool, within or beyond the L2 budget); results are the oracle's, call after call
+    g = torch.Generator().manual_seed(7 * T + H + k)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.1)
+    w = wl.make_weights(g, T, k)
+    x = wl.make_x(g, T, H)
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk.to(DEV), E, R, status=status)
+    cap = wl.recv_capacity(T, k, R)
+    ref_lay = oracle.layout(topk.numpy(), E, R)
+    ref = oracle.dispatch(bits16(x), topk.numpy(), w.numpy(), E, R, ref_lay["token_dst_row"], cap)
+    N = ref_lay["num_recv"]
+    bal = moe.new_balance_counter(DEV) if balanced else None
+    xd, td, wd = x.to(DEV), topk.to(DEV), w.to(DEV)
+    for _ in range(2):
+        out = moe.moe_dispatch(xd, td, wd, E, R, lay.token_dst_row, cap, balance=bal, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        if bal is not None:
+            assert bal.tolist() == [0, 0]
+        np.testing.assert_array_equal(bits16(out.recv_x[:N]), ref["recv_x"][:N])
+        np.testing.assert_array_equal(out.recv_src_idx[:N].cpu().numpy(), ref["recv_src_idx"][:N])
+        np.testing.assert_array_equal(out.recv_topk_idx[:N].cpu().numpy(), ref["recv_topk_idx"][:N])
+        np.testing.assert_array_equal(out.recv_topk_weights[:N].cpu().numpy().view(np.uint32),
+                                      ref["recv_topk_weights"][:N].view(np.uint32))
+
+
 def test_dispatch_capacity_overflow_writes_nothing_beyond(moe):
     w = wl.CONFIGS["tiny"]
     inp = wl.make_inputs(w, with_partial=False)
