@@ -710,6 +710,11 @@ struct Fp8Args {
     int l2_hints;
     uint64_t timeout_ns;
     int loads_before_wait;       // the producer (input rows only) skips the dependency wait
+    // tail balancing: tokens [0, static_tokens) are split into contiguous CTA
+    // ranges; the rest are claimed one by one through pool[0] (pool[1] counts
+    // CTAs that claim no more; the last of them zeroes both). nullptr: all dealt.
+    unsigned int *pool;
+    int static_tokens;
 };
 
 __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
@@ -717,6 +722,7 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
 }
 
 // 80 registers (no spills) allow 1 producer + 24 worker warps per SM
+template <bool kPool>
 __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *in_full = reinterpret_cast<uint64_t *>(smem);
@@ -725,12 +731,16 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int NI = a.n_in, nsl = a.num_slices;
 
-    const int t_begin = (int)((int64_t)a.T * blockIdx.x / gridDim.x);
-    const int t_end = (int)((int64_t)a.T * (blockIdx.x + 1) / gridDim.x);
+    // this CTA's rows: its contiguous range of the dealt tokens, then (with a
+    // pool) tokens claimed one by one
+    const int t_begin = (int)((int64_t)a.static_tokens * blockIdx.x / gridDim.x);
+    const int t_end = (int)((int64_t)a.static_tokens * (blockIdx.x + 1) / gridDim.x);
     const int n = t_end - t_begin;
 
     __shared__ int s_next_item;
     __shared__ volatile int s_rows_issued;   // rows whose load the producer has armed
+    __shared__ volatile int s_rows_total;    // rows of this CTA once the producer claims no more, else -1
+    __shared__ int s_tok[kFp8MaxSlots];      // token of the row in each input slot
     if (threadIdx.x == 0) {
         for (int i = 0; i < NI; ++i) {
             mbar_init(&in_full[i], 1);
@@ -739,6 +749,7 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
         fence_barrier_init();
         s_next_item = 0;
         s_rows_issued = 0;
+        s_rows_total = kPool ? -1 : n;
     }
     __syncthreads();
     // launched right behind this library's layout, the input rows were complete
@@ -746,23 +757,54 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     // starts at once; the workers read the layout's outputs and wait
     if (!(a.loads_before_wait && warp == 0)) grid_dependency_wait();
     grid_launch_dependents();
-    if (n <= 0) return;
+    if (!kPool && n <= 0) return;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol = (a.l2_hints & 1) ? policy_evict_first() : policy_evict_normal();
-            for (int j = 0; j < n; ++j) {
+            bool waited = !a.loads_before_wait;
+            // pool claims are made one row ahead, so that a claim's round trip overlaps
+            // the slot wait and arming of the row before it; the pool's counter is
+            // zeroed by the launch before this one, so the first claim follows the wait
+            int pending = -1;   // pool index claimed for the next row (-1: none)
+            auto claim_ahead = [&]() {
+                if (!waited) {
+                    grid_dependency_wait();
+                    waited = true;
+                }
+                pending = (int)atomicAdd(a.pool, 1u);
+            };
+            if (kPool && n == 0) claim_ahead();
+            int j = 0;
+            for (;; ++j) {
+                int t = -1;
+                if (j < n) t = t_begin + j;
+                else if (pending >= 0 && pending < a.T - a.static_tokens) t = a.static_tokens + pending;
+                if (t < 0) break;
+                pending = -1;
+                if (kPool && j + 1 >= n) claim_ahead();
                 const int s = j % NI;
                 if (j >= NI && !mbar_wait_bounded(&in_empty[s], (uint32_t)(((j / NI) - 1) & 1), a.timeout_ns)) {
                     report(a.status, MOE_ERR_TIMEOUT);
                     break;
                 }
+                if (kPool) s_tok[s] = t;
                 mbar_arrive_expect_tx(&in_full[s], (uint32_t)a.row_bytes);
-                bulk_load(in_ring + (size_t)s * a.row_bytes, a.x + (int64_t)(t_begin + j) * a.row_bytes,
+                bulk_load(in_ring + (size_t)s * a.row_bytes, a.x + (int64_t)t * a.row_bytes,
                           (uint32_t)a.row_bytes, &in_full[s], pol);
                 __threadfence_block();
                 s_rows_issued = j + 1;
+            }
+            __threadfence_block();
+            s_rows_total = j;   // workers waiting on a later row stop
+            // every claim of this CTA is made: count it out; the last CTA re-arms the pool
+            if (kPool) {
+                __threadfence();
+                if (atomicAdd(a.pool + 1, 1u) == gridDim.x - 1) {
+                    atomicExch(a.pool, 0u);
+                    atomicExch(a.pool + 1, 0u);
+                }
             }
         }
         return;
@@ -773,58 +815,80 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     // shared counter, each worker claiming its next item when it starts the
     // current one (so its rows can be prefetched): a worker whose items had
     // fewer destinations takes more of them.
-    const int n_items = n * nsl;    // < 2^31 (checked on the host)
+    // (items < 2^31: checked on the host)
     auto claim = [&]() -> int {
         int q = 0;
         if (lane == 0) q = atomicAdd(&s_next_item, 1);
         return __shfl_sync(kFull, q, 0);
     };
-    // destination rows of an item's token, lanes < k
-    // and, for the item of slice 0, the token's routing (written as the rows' metadata)
-    auto fetch_rows = [&](int q, int64_t &e, float &w) -> int {
-        const int jq = q / nsl;
-        const int t = t_begin + jq;
+    // the token of the CTA's row jq: known in advance for its dealt rows, for a
+    // pool row once the producer has armed it (else -1); warp-uniform
+    auto row_token = [&](int jq) -> int {
+        if (!kPool || jq < n) return jq < n ? t_begin + jq : -1;
+        int t = -1;
+        if (lane == 0 && s_rows_issued > jq) {
+            __threadfence_block();
+            t = s_tok[jq % NI];
+        }
+        return __shfl_sync(kFull, t, 0);
+    };
+    // destination rows of a token, lanes < k, and, for the item of slice 0, the
+    // token's routing (written as the rows' metadata); -1 / none for t < 0
+    auto fetch_rows = [&](int t, bool first, int64_t &e, float &w) -> int {
         e = -1;
         w = 0.0f;
-        if (q < n_items && lane < a.k && q - jq * nsl == 0) {
+        if (t >= 0 && lane < a.k && first) {
             e = a.topk[(int64_t)t * a.k + lane];
             if (a.topk_w) w = a.topk_w[(int64_t)t * a.k + lane];
         }
-        return (q < n_items && lane < a.k) ? a.dst_row[(int64_t)t * a.k + lane] : -1;
+        return (t >= 0 && lane < a.k) ? a.dst_row[(int64_t)t * a.k + lane] : -1;
     };
     int q = claim();
     int64_t e_next;
     float w_next;
-    int row_next = fetch_rows(q, e_next, w_next);
-    while (q < n_items) {
+    int t_next = row_token(q / nsl);   // the next item's token when known ahead (its rows prefetched)
+    int row_next = fetch_rows(t_next, q % nsl == 0, e_next, w_next);
+    while (true) {
         const int q_next = claim();
         const int j = q / nsl;
         const int sl = q - j * nsl;
-        const int t = t_begin + j;
         const int si = j % NI;
+        const int t_pre = t_next;
         int row = row_next;
-        const int64_t e_cur = e_next;
-        const float w_cur = w_next;
-        row_next = fetch_rows(q_next, e_next, w_next);
+        int64_t e_cur = e_next;
+        float w_cur = w_next;
+        t_next = row_token(q_next / nsl);   // prefetched one item ahead (a pool row only once armed)
+        row_next = fetch_rows(t_next, q_next % nsl == 0, e_next, w_next);
+        // A slot's barrier is waited on by parity, which only names its current or
+        // previous phase: wait (bounded) until row j's load has been armed, i.e.
+        // the slot has left the phase of row j - NI, before waiting on the barrier
+        // -- or until the producer has stopped short of row j (no more rows).
+        bool ok = true, done = false;
+        if (!kPool && j >= n) break;   // without a pool the CTA's rows are known in advance
+        if (s_rows_issued <= j) {
+            const uint64_t deadline = globaltimer_ns() + a.timeout_ns;
+            while (s_rows_issued <= j) {
+                const int total = s_rows_total;
+                if (total >= 0 && j >= total) {
+                    done = true;
+                    break;
+                }
+                if (globaltimer_ns() > deadline) {
+                    ok = false;
+                    break;
+                }
+                if (kPool && j >= n) __nanosleep(128);   // a pool row not yet claimed: leave the issue slots to the workers
+            }
+        }
+        if (kPool && __any_sync(kFull, done)) break;
+        __threadfence_block();
+        const int t = (!kPool || j < n) ? t_begin + j : s_tok[si];
+        if (kPool && t_pre < 0) row = fetch_rows(t, sl == 0, e_cur, w_cur);   // a pool row not armed at prefetch time
         if (row >= a.capacity) {
             if (sl == 0) report(a.status, MOE_ERR_CAPACITY);
             row = -1;
         }
         const unsigned dmask = __ballot_sync(kFull, row >= 0);
-        // A slot's barrier is waited on by parity, which only names its current or
-        // previous phase: wait (bounded) until row j's load has been armed, i.e.
-        // the slot has left the phase of row j - NI, before waiting on the barrier.
-        bool ok = true;
-        if (s_rows_issued <= j) {
-            const uint64_t deadline = globaltimer_ns() + a.timeout_ns;
-            while (s_rows_issued <= j) {
-                if (globaltimer_ns() > deadline) {
-                    ok = false;
-                    break;
-                }
-            }
-        }
-        __threadfence_block();
         ok = ok && mbar_wait_bounded(&in_full[si], (uint32_t)((j / NI) & 1), a.timeout_ns);
         if (!__all_sync(kFull, ok)) {
             if (lane == 0) report(a.status, MOE_ERR_TIMEOUT);
@@ -1036,26 +1100,38 @@ int launch_dispatch(const DispatchLaunch &L) {
         f.l2_hints = a.l2_hints;
         f.loads_before_wait = a.loads_before_wait;
         f.timeout_ns = a.timeout_ns;
+        const int grid_rows = std::max(1, std::min(L.num_tokens, device_sm_count()));
+        // tail balancing (a cleared counter at hand, long runs): the last fp8_rows_pool
+        // percent of the tokens are claimed one by one. With fewer rows per CTA the
+        // SMs finish close together and the pool's per-row costs are not repaid
+        // (4096 tokens over 152 SMs: 42.5 against 41.2 us; 8192: 95.2 against 105.5 us).
+        f.pool = (a.pool != nullptr && tu.fp8_rows_pool > 0 && tu.fp8_rows_pool < 100 &&
+                  L.num_tokens >= tu.fp8_rows_pool_min_rows * grid_rows) ? a.pool : nullptr;
+        f.static_tokens = f.pool ? (int)((int64_t)L.num_tokens * (100 - tu.fp8_rows_pool) / 100) : L.num_tokens;
         const size_t head = 2 * kFp8MaxSlots * 8;
         const size_t optin = device_smem_optin();
         f.n_in = std::max(2, std::min(kFp8MaxSlots, tu.fp8_in_slots));
         while (head + (size_t)f.n_in * f.row_bytes > optin && f.n_in > 2) --f.n_in;
         const size_t smem = head + (size_t)f.n_in * f.row_bytes;
-        const int64_t max_cta_items = ((int64_t)L.num_tokens + device_sm_count() - 1) / device_sm_count() * f.num_slices + 64;
+        const int64_t max_cta_items = (f.pool ? (int64_t)L.num_tokens
+                                              : ((int64_t)L.num_tokens + device_sm_count() - 1) / device_sm_count()) *
+                                          f.num_slices + 64;
         if (smem <= optin && f.row_bytes < (1 << 20) && max_cta_items < ((int64_t)1 << 31)) {
-            if (ensure_dynamic_smem((const void *)dispatch_fp8_rows_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
+            void (*rows_kernel)(const Fp8Args) = f.pool ? dispatch_fp8_rows_kernel<true> : dispatch_fp8_rows_kernel<false>;
+            if (ensure_dynamic_smem((const void *)rows_kernel, smem) != MOE_OK) return MOE_ERR_CUDA;
             // as many of the requested workers as the kernel's register use allows in one CTA
-            static int max_threads[64] = {0};
+            static int max_threads[64][2] = {};
             int dev = 0;
             if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-            if (max_threads[dev] == 0) {
+            int &mt = max_threads[dev][f.pool ? 1 : 0];
+            if (mt == 0) {
                 cudaFuncAttributes fa;
-                if (cudaFuncGetAttributes(&fa, (const void *)dispatch_fp8_rows_kernel) != cudaSuccess) return MOE_ERR_CUDA;
-                max_threads[dev] = fa.maxThreadsPerBlock;
+                if (cudaFuncGetAttributes(&fa, (const void *)rows_kernel) != cudaSuccess) return MOE_ERR_CUDA;
+                mt = fa.maxThreadsPerBlock;
             }
-            const int workers = std::max(1, std::min({24, tu.fp8_quant_warps, max_threads[dev] / 32 - 1}));
-            const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
-            return launch_kernel(dispatch_fp8_rows_kernel, dim3(grid), dim3((workers + 1) * 32), smem, st,
+            const int workers = std::max(1, std::min({24, tu.fp8_quant_warps, mt / 32 - 1}));
+            const int grid = grid_rows;
+            return launch_kernel(rows_kernel, dim3(grid), dim3((workers + 1) * 32), smem, st,
                                  tu.overlap != 0, f) == cudaSuccess
                        ? MOE_OK
                        : MOE_ERR_CUDA;

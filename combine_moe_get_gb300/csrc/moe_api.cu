@@ -119,6 +119,8 @@ const Tuning &tuning() {
         x.fp8_rows = MOE_TUNE_FP8_ROWS;
         x.fp8_in_slots = MOE_TUNE_FP8_IN_SLOTS;
         x.fp8_quant_warps = MOE_TUNE_FP8_QUANT_WARPS;
+        x.fp8_rows_pool = MOE_TUNE_FP8_ROWS_POOL;
+        x.fp8_rows_pool_min_rows = MOE_TUNE_FP8_ROWS_POOL_MIN_ROWS;
         x.ctas_per_sm = MOE_TUNE_CTAS_PER_SM;
         x.l2_hints = MOE_TUNE_L2_HINTS & 3;
         x.spread_small = MOE_TUNE_SPREAD_SMALL;

@@ -64,7 +64,13 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 #define MOE_TUNE_FP8_ROWS 1
 #endif
 #ifndef MOE_TUNE_FP8_IN_SLOTS
-#define MOE_TUNE_FP8_IN_SLOTS 8
+#define MOE_TUNE_FP8_IN_SLOTS 12
+#endif
+#ifndef MOE_TUNE_FP8_ROWS_POOL
+#define MOE_TUNE_FP8_ROWS_POOL 50
+#endif
+#ifndef MOE_TUNE_FP8_ROWS_POOL_MIN_ROWS
+#define MOE_TUNE_FP8_ROWS_POOL_MIN_ROWS 40
 #endif
 #ifndef MOE_TUNE_FP8_QUANT_WARPS
 #define MOE_TUNE_FP8_QUANT_WARPS 24
@@ -99,6 +105,8 @@ struct Tuning {
     int combine_warps, combine_chunk, combine_ring_bytes;   // consumer warps, max chunk, ring budget
     int combine_fp8_warps;                                   // consumer warps for E4M3 partial rows
     int fp8_rows, fp8_in_slots, fp8_quant_warps;   // FP8 row pipeline: on/off, input ring slots, worker warps
+    int fp8_rows_pool;  // % of the FP8 row pipeline's tokens left to a pool when a cleared counter is at hand
+    int fp8_rows_pool_min_rows;  // ... only with at least this many rows per CTA
     int ctas_per_sm;
     int l2_hints;  // bit 0: evict-first on single-use loads; bit 1: evict-first on stores
     int spread_small;   // small batches: fewer dispatch warps per CTA, more CTAs
