@@ -281,9 +281,9 @@ class Step:
         self.moe.moe_combine(self.partial, self.lay.token_dst_row, out=self.out, status=self.status)
 
     def combine_fp8(self):
-        # E4M3 partial rows: the FP8 dispatch's own receive rows and scales
+        # E4M3 partial rows: the FP8 dispatch's own receive rows and scales (balance counter: used on long runs)
         self.moe.moe_combine_fp8(self.disp8.recv_x, self.disp8.recv_x_scales, self.lay.token_dst_row, out=self.out,
-                                 status=self.status)
+                                 balance=self.bal, status=self.status)
 
     def layout_dispatch(self):
         self.moe.moe_layout_dispatch(self.x, self.topk, self.wts, self.w.num_experts, self.w.num_ranks, self.cap,

@@ -84,6 +84,8 @@ def _load():
     lib.moe_combine.restype = _I
     lib.moe_combine_fp8.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]
     lib.moe_combine_fp8.restype = _I
+    lib.moe_combine_fp8_ex.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]
+    lib.moe_combine_fp8_ex.restype = _I
     lib.moe_combine_ex.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     lib.moe_combine_ex.restype = _I
     return lib
@@ -318,17 +320,23 @@ def moe_combine(partial: torch.Tensor, token_dst_row: torch.Tensor, *, out: Opti
 
 
 def moe_combine_fp8(partial_codes: torch.Tensor, partial_scales: torch.Tensor, token_dst_row: torch.Tensor, *,
-                    out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                    stream=None) -> torch.Tensor:
-    """out[t] = bf16(fp32 ascending sum over the rows of t of RN(e4m3(code) * scale))."""
+                    out: Optional[torch.Tensor] = None, balance: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[t] = bf16(fp32 ascending sum over the rows of t of RN(e4m3(code) * scale)).
+    With `balance` (new_balance_counter()) this calls moe_combine_fp8_ex."""
     rows, H = partial_codes.shape
     T, k = token_dst_row.shape
     dev = partial_codes.device
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev) if out is None else out
     status = new_status(dev) if status is None else status
-    code = LIB.moe_combine_fp8(_ptr(partial_codes), _ptr(partial_scales), rows, T, H, k, _ptr(token_dst_row),
-                               _ptr(out), _ptr(status), _stream(stream))
-    _check(code, "moe_combine_fp8")
+    if balance is None:
+        code = LIB.moe_combine_fp8(_ptr(partial_codes), _ptr(partial_scales), rows, T, H, k, _ptr(token_dst_row),
+                                   _ptr(out), _ptr(status), _stream(stream))
+        _check(code, "moe_combine_fp8")
+    else:
+        code = LIB.moe_combine_fp8_ex(_ptr(partial_codes), _ptr(partial_scales), rows, T, H, k,
+                                      _ptr(token_dst_row), _ptr(out), _ptr(balance), _ptr(status), _stream(stream))
+        _check(code, "moe_combine_fp8_ex")
     return out
 
 

@@ -529,9 +529,12 @@ int launch_combine(const CombineLaunch &L) {
     const int consumers = fp8 ? std::max(1, std::min(12, tu.combine_fp8_warps)) : std::max(1, std::min(8, tu.combine_warps));
     const int grid = std::max(1, std::min(L.num_tokens, device_sm_count()));
     // the pool pays off only with several tokens per CTA (its claims and the
-    // finishing count cost a few microseconds of latency)
-    if (a.T < 8 * grid) a.balance = nullptr;
-    a.static_tokens = a.balance ? (int)((int64_t)a.T * (100 - tu.combine_pool) / 100) : a.T;
+    // finishing count cost a few microseconds of latency); for E4M3 rows, whose
+    // producer is the critical warp, only with long runs
+    if (a.T < (fp8 ? tu.combine_fp8_pool_min_tokens : 8) * grid) a.balance = nullptr;
+    const int pool_pct = fp8 ? tu.combine_fp8_pool : tu.combine_pool;
+    if (pool_pct <= 0 || pool_pct >= 100) a.balance = nullptr;
+    a.static_tokens = a.balance ? (int)((int64_t)a.T * (100 - pool_pct) / 100) : a.T;
     void (*kernel)(const CombineArgs) =
         fp8 ? combine_kernel<false, true> : (weighted ? combine_kernel<true, false> : combine_kernel<false, false>);
     return launch_kernel(kernel, dim3(grid), dim3((consumers + 1) * 32), smem, st, tu.overlap != 0, a) == cudaSuccess

@@ -112,6 +112,8 @@ const Tuning &tuning() {
         x.combine_chunk = MOE_TUNE_COMBINE_CHUNK;
         x.combine_ring_bytes = MOE_TUNE_COMBINE_RING_BYTES;
         x.combine_fp8_warps = MOE_TUNE_COMBINE_FP8_WARPS;
+        x.combine_fp8_pool = MOE_TUNE_COMBINE_FP8_POOL;
+        x.combine_fp8_pool_min_tokens = MOE_TUNE_COMBINE_FP8_POOL_MIN_TOKENS;
         x.overlap = MOE_TUNE_OVERLAP;
         x.dispatch_pool = MOE_TUNE_DISPATCH_POOL;
         x.combine_pool = MOE_TUNE_COMBINE_POOL;
@@ -438,9 +440,9 @@ MOE_API int moe_combine_ex(const void *partial, int num_partial_rows, int num_to
                           recv_topk_weights, combined_topk_weights, out, balance, status, stream);
 }
 
-MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scales, int num_partial_rows,
-                            int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
-                            int32_t *status, void *stream) {
+static int combine_fp8_common(const void *partial_codes, const float *partial_scales, int num_partial_rows,
+                              int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
+                              uint32_t *balance, int32_t *status, void *stream) {
     const int T = num_tokens, H = hidden;
     if (T < 0 || num_topk < 1 || num_topk > MOE_MAX_TOPK || num_partial_rows < 0) return MOE_ERR_INVALID_ARG;
     if (H < 512 || H % 512 != 0 || H > (1 << 24) || (int64_t)T * num_topk >= (int64_t)1 << 31) return MOE_ERR_INVALID_ARG;
@@ -452,6 +454,7 @@ MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scal
             !aligned(out, 16) || !aligned(token_dst_row, 4) || !aligned(status, 4))
             return MOE_ERR_MISALIGNED;
     }
+    if (!aligned(balance, 8)) return MOE_ERR_MISALIGNED;
     moe::CombineLaunch L;
     L.partial = partial_codes;
     L.fp8 = true;
@@ -467,7 +470,22 @@ MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scal
     L.out = out;
     L.status = status;
     L.stream = stream;
+    L.balance = balance;
     return moe::launch_combine(L);
+}
+
+MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scales, int num_partial_rows,
+                            int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
+                            int32_t *status, void *stream) {
+    return combine_fp8_common(partial_codes, partial_scales, num_partial_rows, num_tokens, hidden, num_topk,
+                              token_dst_row, out, nullptr, status, stream);
+}
+
+MOE_API int moe_combine_fp8_ex(const void *partial_codes, const float *partial_scales, int num_partial_rows,
+                               int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
+                               uint32_t *balance, int32_t *status, void *stream) {
+    return combine_fp8_common(partial_codes, partial_scales, num_partial_rows, num_tokens, hidden, num_topk,
+                              token_dst_row, out, balance, status, stream);
 }
 
 }  // extern "C"

@@ -45,6 +45,12 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 #ifndef MOE_TUNE_COMBINE_RING_BYTES
 #define MOE_TUNE_COMBINE_RING_BYTES (224 << 10)
 #endif
+#ifndef MOE_TUNE_COMBINE_FP8_POOL
+#define MOE_TUNE_COMBINE_FP8_POOL 15
+#endif
+#ifndef MOE_TUNE_COMBINE_FP8_POOL_MIN_TOKENS
+#define MOE_TUNE_COMBINE_FP8_POOL_MIN_TOKENS 40
+#endif
 #ifndef MOE_TUNE_COMBINE_FP8_WARPS
 #define MOE_TUNE_COMBINE_FP8_WARPS 10
 #endif
@@ -104,6 +110,7 @@ struct Tuning {
     int dispatch_smem;                                       // shared-memory budget of a chunked dispatch CTA
     int combine_warps, combine_chunk, combine_ring_bytes;   // consumer warps, max chunk, ring budget
     int combine_fp8_warps;                                   // consumer warps for E4M3 partial rows
+    int combine_fp8_pool, combine_fp8_pool_min_tokens;       // E4M3 rows: pool % and the tokens per CTA it needs
     int fp8_rows, fp8_in_slots, fp8_quant_warps;   // FP8 row pipeline: on/off, input ring slots, worker warps
     int fp8_rows_pool;  // % of the FP8 row pipeline's tokens left to a pool when a cleared counter is at hand
     int fp8_rows_pool_min_rows;  // ... only with at least this many rows per CTA

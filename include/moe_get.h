@@ -358,6 +358,22 @@ MOE_API int moe_combine_fp8(const void *partial_codes, const float *partial_scal
                             int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
                             int32_t *status, void *stream);
 
+/*
+ * moe_combine_fp8_ex -- moe_combine_fp8 with tail balancing, as moe_combine_ex.
+ *
+ *   balance   two zeroed uint32 of device memory (8-byte aligned) or NULL.
+ *             With a counter and a long enough batch (several dozen tokens
+ *             per SM), the last tokens are claimed one by one by whichever
+ *             SM is free first; the counter is left zeroed. Results are
+ *             exactly those of moe_combine_fp8 (each token is reduced by one
+ *             CTA in the same order whichever CTA it is). NULL gives exactly
+ *             moe_combine_fp8.
+ * Other arguments, limits and errors as moe_combine_fp8.
+ */
+MOE_API int moe_combine_fp8_ex(const void *partial_codes, const float *partial_scales, int num_partial_rows,
+                               int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
+                               uint32_t *balance, int32_t *status, void *stream);
+
 /* Size of the library's own layout scratch (bytes), used by moe_get_layout_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
 

@@ -178,6 +178,23 @@ def test_combine_fp8_rejects_bad_arguments(lib, kw, code):
     assert _combine_fp8(lib, **kw) == code
 
 
+def _combine_fp8_ex(lib, balance=A + 0x500000, **kw):
+    d = dict(codes=A, scales=A + 0x80000, rows=256, T=128, H=1024, k=2, dst=A + 0x10000, out=A + 0x100000,
+             status=A + 0x200000)
+    d.update(kw)
+    return lib.LIB.moe_combine_fp8_ex(d["codes"], d["scales"], d["rows"], d["T"], d["H"], d["k"], d["dst"], d["out"],
+                                      balance, d["status"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(balance=A + 4), 2), (dict(H=640), 1), (dict(k=0), 1), (dict(scales=None), 1), (dict(status=None), 1),
+    (dict(codes=A + 8), 2), (dict(out=A + 8), 2),
+])
+def test_combine_fp8_ex_rejects_bad_arguments(lib, kw, code):
+    # the same checks as moe_combine_fp8, plus the balance counter's alignment; nothing is launched
+    assert _combine_fp8_ex(lib, **kw) == code
+
+
 def _combine_ex(lib, partial=A, rows=256, T=128, H=256, k=2, dst=A + 0x10000, roww=None, rtw=None, cw=None,
                 out=A + 0x100000, balance=None, status=A + 0x200000):
     return lib.LIB.moe_combine_ex(partial, rows, T, H, k, dst, roww, rtw, cw, out, balance, status, None)

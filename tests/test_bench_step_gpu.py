@@ -174,6 +174,8 @@ def test_timed_variants_fp8_dispatch_and_fp8_combine(case):
     st.combine_fp8()          # E4M3 partial rows: the FP8 dispatch's own rows and scales
     torch.cuda.synchronize()
     case.moe.check_status(st.status, "fp8 combine")
+    assert st.bal.tolist() == [0, 0], "combine balance counter not left zero"
+    assert st.bal_d.tolist() == [0, 0], "dispatch balance counter not left zero"
     out, flags = oracle.combine_fp8(ref["recv_x"][:n], ref["recv_x_scales"][:n], case.lay["token_dst_row"])
     assert flags == 0
     case.check_combine(out)

@@ -653,6 +653,32 @@ def test_combine_fp8_parity_shapes(moe, T, H, k, E, R):
     check_combine_fp8(moe, topk, E, R, H, T + k)
 
 
+@pytest.mark.parametrize("name", ["skewed", "dsv3", "decode"])
+def test_combine_fp8_balanced_parity(moe, name):
+    # moe_combine_fp8_ex with a balance counter (a pool on the long skewed batch, none on the shorter ones):
+    # the oracle's result bit for bit, the counter left zero, call after call
+    w = wl.CONFIGS[name]
+    topk = topk_for(w)
+    E, R, H = w.num_experts, w.num_ranks, w.hidden
+    lay_ref = oracle.layout(topk.numpy(), E, R)
+    rows = wl.recv_capacity(w.num_tokens, w.num_topk, R)
+    rng = np.random.default_rng(23)
+    codes = rng.integers(0, 256, (rows, H), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x01          # no NaN codes
+    scales = rng.uniform(0.001, 2.0, (rows, H // 128)).astype(np.float32)
+    ref, flags = oracle.combine_fp8(codes, scales, lay_ref["token_dst_row"])
+    assert flags == 0
+    status = moe.new_status(DEV)
+    lay = moe.moe_get_layout(topk.to(DEV), E, R, status=status)
+    bal = moe.new_balance_counter(DEV)
+    cd, sd = torch.from_numpy(codes).to(DEV), torch.from_numpy(scales).to(DEV)
+    for _ in range(2):
+        out = moe.moe_combine_fp8(cd, sd, lay.token_dst_row, balance=bal, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0 and bal.tolist() == [0, 0]
+        np.testing.assert_array_equal(bits16(out), ref)
+
+
 def test_fp8_dispatch_then_fp8_combine(moe):
     # identity experts on FP8 rows: the GPU result equals the oracle's combine of the oracle's dispatch
     w = wl.CONFIGS["dsv3"]
