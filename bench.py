@@ -538,6 +538,7 @@ def run_ours(args, world, rank, local):
     moe.check_status(sd.status, "decode shape")
     del sd
     skewed = measure_skewed(moe, device, rank, timer, reps)
+    small = measure_small_configs(moe, device, rank, timer, reps)
 
     peak, peak_kind = hbm_peak()
     row = H * 2
@@ -596,6 +597,7 @@ def run_ours(args, world, rank, local):
         skewed[f"{key}_gbs"] = gbs(nbytes, skewed[f"{key}_us"] * 1e-3)
         skewed[f"{key}_frac"] = skewed[f"{key}_gbs"] / peak
     kern["skewed"] = skewed
+    kern.update(small)
     if sus_ms:
         kern["sustained"] = {"steps": len(sus_ms), "ms_per_step_mean": mean(sus_ms),
                              "ms_per_step_median": med(sus_ms), "tokens_per_s": T / (mean(sus_ms) * 1e-3),
@@ -681,6 +683,55 @@ def measure_skewed(moe, device, rank, timer, reps):
                      "combine_fp8": N * (H + (H // 128) * 4) + T * row}
     out["notes"] = "every kernel timed alone after an L2 flush (dispatch and combine with balance counters)"
     del sk
+    torch.cuda.empty_cache()
+    return out
+
+
+def expected_distinct_ranks(E: int, R: int, k: int) -> float:
+    """The pages' closed form for the expected number of distinct ranks a token
+    reaches with k experts drawn uniformly without replacement from E experts
+    spread evenly over R ranks: R * (1 - C(E - E/R, k) / C(E, k))."""
+    import math
+    return R * (1.0 - math.comb(E - E // R, k) / math.comb(E, k))
+
+
+def measure_small_configs(moe, device, rank, timer, reps):
+    """The tiny workload's step (two launches and moe_layout_dispatch) and the
+    layout-only 2048-expert / 256-rank runs (128 and 2^20 tokens), each timed
+    alone with the same flush, with the realised mean number of distinct
+    destination ranks per token beside the closed form."""
+    mean = statistics.fmean
+    out = {}
+    wt = wl.CONFIGS["tiny"]
+    st = Step(moe, wt, wl.make_inputs(dataclass_replace_seed(wt, wt.seed + rank)), device)
+    out["tiny"] = {
+        "tokens": wt.num_tokens, "hidden": wt.hidden, "experts": wt.num_experts, "ranks": wt.num_ranks,
+        "topk": wt.num_topk,
+        "step_two_us": mean(timer(lambda: (st.layout(), st.dispatch(), st.combine()), reps)) * 1e3,
+        "step_fused_us": mean(timer(lambda: (st.layout_dispatch(), st.combine()), reps)) * 1e3,
+    }
+    moe.check_status(st.status, "tiny workload")
+    n = int(st.lay.rank_prefix[-1].item())
+    out["tiny"]["mean_distinct_ranks"] = n / wt.num_tokens
+    out["tiny"]["expected_distinct_ranks"] = expected_distinct_ranks(wt.num_experts, wt.num_ranks, wt.num_topk)
+    out["tiny"]["step_fused_tokens_per_s"] = wt.num_tokens / (out["tiny"]["step_fused_us"] * 1e-6)
+    del st
+    for name in ("layout_2048", "layout_2048_1m"):
+        w = wl.CONFIGS[name]
+        topk = wl.make_inputs(dataclass_replace_seed(w, w.seed + rank), with_partial=False).topk_idx.to(device)
+        lay = moe.Layout.empty(w.num_tokens, w.num_topk, w.num_experts, w.num_ranks, device)
+        ws = torch.empty(max(1, moe.moe_get_layout_workspace_size(w.num_tokens, w.num_experts, w.num_ranks)),
+                         dtype=torch.uint8, device=device)
+        status = moe.new_status(device)
+        ms = timer(lambda: moe.moe_get_layout(topk, w.num_experts, w.num_ranks, out=lay, workspace=ws,
+                                              status=status), reps)
+        moe.check_status(status, name)
+        n = int(lay.rank_prefix[-1].item())
+        out[name] = {"tokens": w.num_tokens, "experts": w.num_experts, "ranks": w.num_ranks, "topk": w.num_topk,
+                     "layout_us": mean(ms) * 1e3, "tokens_per_s": w.num_tokens / (mean(ms) * 1e-3),
+                     "mean_distinct_ranks": n / w.num_tokens,
+                     "expected_distinct_ranks": expected_distinct_ranks(w.num_experts, w.num_ranks, w.num_topk)}
+        del topk, lay, ws
     torch.cuda.empty_cache()
     return out
 

@@ -76,3 +76,13 @@ def test_reference_arm_runs_on_rank0_only():
     p.join(timeout=120)
     assert p.exitcode == 0
     assert q.get(timeout=10) == ""
+
+
+@pytest.mark.parametrize("E,R,k", [(2048, 256, 8), (256, 8, 8), (256, 64, 8), (16, 4, 2), (256, 256, 8), (64, 8, 6)])
+def test_bench_expected_distinct_ranks_is_the_closed_form(E, R, k):
+    # the figure bench.py prints beside each layout's realised mean is the pages' closed form
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    from oracle.expected_topk import get_expected_topk
+    assert bench.expected_distinct_ranks(E, R, k) == pytest.approx(get_expected_topk(E, R, k), rel=1e-12, abs=1e-12)
