@@ -163,7 +163,7 @@ def moe_get_layout(topk_idx: torch.Tensor, num_experts: int, num_ranks: int, *,
                    status: Optional[torch.Tensor] = None, stream=None,
                    wait_timeout_ns: int = 0, test_unpublished_tile: int = -1, layout_mode: int = 0) -> Layout:
     """Counts, membership, prefixes and receive rows of ``topk_idx`` [T, k] int64.
-    ``layout_mode`` 1 keeps the call off the cluster mode (same outputs)."""
+    ``layout_mode`` 1 keeps the call off the cluster mode, 2 on the lookback modes (same outputs)."""
     T, k = topk_idx.shape
     dev = topk_idx.device
     out = out or Layout.empty(T, k, num_experts, num_ranks, dev)

@@ -1159,7 +1159,10 @@ int launch_layout_dispatch(const LayoutLaunch &Ll, const DispatchLaunch &L) {
         a.fl_words = (T + 31) / 32;
         a.fl_out = Ll.out;
         const size_t extra = fused_smem(T, L.num_ranks, L.num_experts, L.num_topk).total;
-        fused = chunked_config(a, fp8, T, extra, warps, smem, grid) == MOE_OK;
+        // every CTA computes the whole layout with its own warps: with fewer than
+        // fused_min_warps per CTA that costs more than the separate layout launch
+        // (128 tokens of 512-byte rows: one warp per CTA, 20.6 against 17.7 us)
+        fused = chunked_config(a, fp8, T, extra, warps, smem, grid) == MOE_OK && warps >= tu.fused_min_warps;
     }
     if (!fused) {   // two launches: layout, then dispatch, which loads input rows while the layout runs
         LayoutLaunch l2 = Ll;

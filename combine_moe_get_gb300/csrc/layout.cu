@@ -908,6 +908,147 @@ __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, 
     }
 }
 
+// ------------------------------------------------------------------ scan mode (large batches)
+//
+// For more tiles than fit on the GPU at once, the decoupled lookback becomes a
+// chain through every tile in turn (2^20 tokens over 256 ranks: 8192 tiles,
+// 1.6 ms). The scan mode has no waits at all: three launches, each fully
+// parallel.
+//   count: one CTA per tile of kTile tokens -- the tile's membership rows, each
+//          owning entry's position inside the tile's share of its rank, the
+//          tile's per-rank counts into the workspace (rank-major, [R][tiles+1]),
+//          its expert histogram added into the global accumulator;
+//   scan:  one CTA per rank -- the exclusive scan of that rank's tile counts
+//          (its total lands in slot [tiles]); the last CTA to finish (a done
+//          counter) writes the rank counts and prefix and the expert counts
+//          and prefix;
+//   rows:  every owning entry's position plus its rank's region start plus
+//          its tile's prefix.
+
+__global__ void __launch_bounds__(kThreads) layout_count_kernel(TileArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int R = a.R, E = a.E, k = a.k;
+    const SmemLayout sl = smem_layout(E, R, k);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem);
+    uint16_t *wprefix = reinterpret_cast<uint16_t *>(smem + sl.wprefix);
+    int32_t *hist = reinterpret_cast<int32_t *>(smem + sl.hist);
+    int16_t *own = reinterpret_cast<int16_t *>(smem + sl.own);
+    int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
+    int32_t *counts = reinterpret_cast<int32_t *>(a.ws + a.status_off);   // [R][num_tiles + 1]
+    grid_dependency_wait();
+    for (int i = threadIdx.x; i < R * kWords; i += kThreads) bitmap[i] = 0u;
+    for (int i = threadIdx.x; i < E; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    const int tile = (int)blockIdx.x;
+    const int t0 = tile * kTile;
+    const int tcount = min(kTile, a.T - t0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tpp = 32 / k;
+    const int sub = lane / k, j = lane - sub * k;
+    const bool lane_used = sub < tpp;
+    // ---- membership bitmap, expert histogram, owned ranks (the lowest entry of a rank owns it)
+    for (int base = warp * tpp; base < tcount; base += kWarps * tpp) {
+        const int tl = base + sub;
+        const bool act = lane_used && tl < tcount;
+        int r = -1;
+        if (act) {
+            const int64_t e = ld_nc_i64(a.topk + (int64_t)(t0 + tl) * k + j);
+            if (e >= 0 && e < E) {
+                r = (int)e / a.m;
+                atomicAdd(&hist[(int)e], 1);
+            } else if (e != -1) {
+                report(a.status, MOE_ERR_BAD_TOPK);
+            }
+        }
+        const int key = (r >= 0) ? (sub * R + r) : -(lane + 1);
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const bool owner = r >= 0 && (__ffs(peers) - 1) == lane;
+        if (owner) atomicOr(&bitmap[(tl >> 5) * R + r], 1u << (tl & 31));
+        if (act) own[tl * k + j] = (int16_t)(owner ? r : -1);
+    }
+    __syncthreads();
+    // ---- the tile's word prefixes and per-rank counts
+    const size_t stride = (size_t)a.num_tiles + 1;
+    for (int r = threadIdx.x; r < R; r += kThreads) {
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+            wprefix[r * kWords + w] = (uint16_t)run;
+            run += __popc(bitmap[w * R + r]);
+        }
+        counts[(size_t)r * stride + tile] = (int32_t)run;
+    }
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        const int h = hist[e];
+        if (h) atomicAdd(ws_expert + e, h);
+    }
+    __syncthreads();
+    // ---- positions inside the tile's share of each rank
+    for (int i = threadIdx.x; i < tcount * k; i += kThreads) {
+        const int r = own[i];
+        int32_t v = -1;
+        if (r >= 0) {
+            const int tl = i / k;
+            v = wprefix[r * kWords + (tl >> 5)] + __popc(bitmap[(tl >> 5) * R + r] & ((1u << (tl & 31)) - 1u));
+        }
+        a.token_dst_row[(int64_t)t0 * k + i] = v;
+    }
+    // ---- is_token_in_rank rows of the tile, expanded from the bitmap
+    uint8_t *dst = a.is_token_in_rank + (int64_t)t0 * R;
+    const int nbytes = tcount * R;
+    if ((R & 3) == 0) {
+        uint32_t *dst4 = reinterpret_cast<uint32_t *>(dst);
+        for (int i = threadIdx.x; i < nbytes / 4; i += kThreads) {
+            const int tl = (i * 4) / R, r0 = (i * 4) - tl * R;
+            uint32_t v = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) v |= ((bitmap[(tl >> 5) * R + r0 + b] >> (tl & 31)) & 1u) << (8 * b);
+            dst4[i] = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < nbytes; i += kThreads) {
+            const int tl = i / R, r = i - tl * R;
+            dst[i] = (uint8_t)((bitmap[(tl >> 5) * R + r] >> (tl & 31)) & 1u);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) layout_scan_kernel(TileArgs a) {
+    __shared__ int s_last;
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
+    int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
+    int32_t *counts = reinterpret_cast<int32_t *>(a.ws + a.status_off);
+    grid_dependency_wait();
+    const int r = (int)blockIdx.x;
+    int32_t *row = counts + (size_t)r * ((size_t)a.num_tiles + 1);
+    block_exclusive_scan(row, a.num_tiles, nullptr, row);   // in place; the total lands in row[num_tiles]
+    if (threadIdx.x == 0) a.num_tokens_per_rank[r] = row[a.num_tiles];
+    // the last CTA: rank regions and the expert counts and prefix
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&hdr->done, 1u) == (unsigned)(gridDim.x - 1));
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        block_exclusive_scan(a.num_tokens_per_rank, a.R, nullptr, a.rank_prefix);
+        block_exclusive_scan(ws_expert, a.E, a.num_tokens_per_expert, a.expert_prefix);
+    }
+}
+
+__global__ void layout_rows_scan_kernel(TileArgs a) {
+    grid_dependency_wait();
+    const int64_t n = (int64_t)a.T * a.k;   // < 2^31 (checked on the host)
+    const int32_t *counts = reinterpret_cast<const int32_t *>(a.ws + a.status_off);
+    const size_t stride = (size_t)a.num_tiles + 1;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int32_t v = a.token_dst_row[i];
+        if (v < 0) continue;
+        const int r = (int)a.topk[i] / a.m;   // an owning entry is valid
+        const int tile = (int)(i / a.k) / kTile;
+        a.token_dst_row[i] = v + a.rank_prefix[r] + counts[(size_t)r * stride + tile];
+    }
+}
+
 // Largest power of two <= min(32, kThreads / R), at least 1.
 int lookback_group(int R) {
     int g = 1;
@@ -1051,10 +1192,11 @@ int launch_layout(const LayoutLaunch &L) {
     const size_t dsmem = dt == kDirectTile ? direct_smem<kDirectTile>(E, R, k).total : direct_smem<kTile>(E, R, k).total;
     const void *coop = (const void *)layout_tiles_kernel<true>;
     if (ensure_dynamic_smem(direct, dsmem) != MOE_OK || ensure_dynamic_smem(coop, smem) != MOE_OK ||
-        ensure_dynamic_smem((const void *)layout_tiles_kernel<false>, smem) != MOE_OK)
+        ensure_dynamic_smem((const void *)layout_tiles_kernel<false>, smem) != MOE_OK ||
+        ensure_dynamic_smem((const void *)layout_count_kernel, smem) != MOE_OK)
         return MOE_ERR_CUDA;
     if (dt && (T + dt - 1) / dt > cooperative_capacity(direct, dsmem)) dt = 0;
-    if (cluster) dt = 0;
+    if (cluster || L.lookback_only) dt = 0;
     const int tile_tokens = dt ? dt : kTile;
     const int num_tiles = (T + tile_tokens - 1) / tile_tokens;
     // a single-tile direct launch and the cluster mode use no workspace
@@ -1093,6 +1235,20 @@ int launch_layout(const LayoutLaunch &L) {
         return launch_cooperative(direct, a.num_tiles, dsmem, s, a);
     }
     if (a.num_tiles <= cooperative_capacity(coop, smem)) return launch_cooperative(coop, a.num_tiles, smem, s, a);
+    // more tiles than fit at once: the scan mode (three launches, no waits), unless
+    // the lookback is asked for (layout_mode 2, or the unpublished-tile test hook)
+    if (!L.lookback_only && L.unpublished_tile < 0 && tuning().layout_scan) {
+        const bool ov = tuning().overlap != 0;
+        if (launch_kernel(layout_count_kernel, dim3(a.num_tiles), dim3(kThreads), smem, s, ov, a) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (launch_kernel(layout_scan_kernel, dim3(R), dim3(kThreads), 0, s, ov, a) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        const int64_t n = (int64_t)T * k;
+        const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)device_sm_count() * 8);
+        return launch_kernel(layout_rows_scan_kernel, dim3(blocks), dim3(256), 0, s, ov, a) == cudaSuccess
+                   ? MOE_OK
+                   : MOE_ERR_CUDA;
+    }
 
     if (launch_kernel(layout_tiles_kernel<false>, dim3(a.num_tiles), dim3(kThreads), smem, s, tuning().overlap != 0, a) !=
         cudaSuccess)

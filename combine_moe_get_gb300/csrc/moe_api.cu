@@ -118,6 +118,7 @@ const Tuning &tuning() {
         x.dispatch_pool = MOE_TUNE_DISPATCH_POOL;
         x.combine_pool = MOE_TUNE_COMBINE_POOL;
         x.layout_cluster = MOE_TUNE_LAYOUT_CLUSTER;
+        x.layout_scan = MOE_TUNE_LAYOUT_SCAN;
         x.fp8_rows = MOE_TUNE_FP8_ROWS;
         x.fp8_in_slots = MOE_TUNE_FP8_IN_SLOTS;
         x.fp8_quant_warps = MOE_TUNE_FP8_QUANT_WARPS;
@@ -127,6 +128,7 @@ const Tuning &tuning() {
         x.l2_hints = MOE_TUNE_L2_HINTS & 3;
         x.spread_small = MOE_TUNE_SPREAD_SMALL;
         x.fused_small = MOE_TUNE_FUSED_SMALL;
+        x.fused_min_warps = MOE_TUNE_FUSED_MIN_WARPS;
         x.dispatch_prefetch = MOE_TUNE_DISPATCH_PREFETCH;
         x.dispatch_prefetch_keep = MOE_TUNE_DISPATCH_PREFETCH_KEEP;
         x.dispatch_prefetch_always = MOE_TUNE_DISPATCH_PREFETCH_ALWAYS;
@@ -225,12 +227,14 @@ MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, in
     return moe::layout_workspace_bytes(num_tokens, num_experts, num_ranks);
 }
 
+// mode: 0 by size, 1 never the cluster mode, 2 only the lookback modes
 static int layout_common(const int64_t *topk_idx, int T, int k, int E, int R, moe_layout_t o, void *workspace,
                          size_t workspace_bytes, int32_t *status, void *stream, int64_t timeout_ns,
-                         int unpublished_tile, bool no_cluster = false) {
+                         int unpublished_tile, int mode = 0) {
     moe::LayoutLaunch L;
     const int rc = moe::layout_prepare(topk_idx, T, k, E, R, o, workspace, workspace_bytes, status, stream,
-                                       timeout_ns, unpublished_tile, L, no_cluster);
+                                       timeout_ns, unpublished_tile, L, mode != 0);
+    L.lookback_only = mode == 2;
     return rc != MOE_OK ? rc : moe::launch_layout(L);
 }
 
@@ -246,15 +250,15 @@ MOE_API int moe_get_layout_ex(const int64_t *topk_idx, int num_tokens, int num_t
                               int32_t *status, void *stream, const moe_layout_options_t *options) {
     int64_t timeout = 0;
     int unpublished = -1;
-    bool no_cluster = false;
+    int mode = 0;
     if (options) {
         timeout = options->wait_timeout_ns;
         unpublished = options->test_unpublished_tile;
-        if (options->layout_mode != 0 && options->layout_mode != 1) return MOE_ERR_INVALID_ARG;
-        no_cluster = options->layout_mode == 1;
+        if (options->layout_mode < 0 || options->layout_mode > 2) return MOE_ERR_INVALID_ARG;
+        mode = options->layout_mode;
     }
     return layout_common(topk_idx, num_tokens, num_topk, num_experts, num_ranks, layout, workspace,
-                         workspace_bytes, status, stream, timeout, unpublished, no_cluster);
+                         workspace_bytes, status, stream, timeout, unpublished, mode);
 }
 
 MOE_API size_t moe_get_expand_layout_workspace_size(int num_tokens, int num_experts) {

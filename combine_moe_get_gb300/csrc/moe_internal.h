@@ -93,6 +93,12 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes);
 #ifndef MOE_TUNE_FUSED_SMALL
 #define MOE_TUNE_FUSED_SMALL 1
 #endif
+#ifndef MOE_TUNE_FUSED_MIN_WARPS
+#define MOE_TUNE_FUSED_MIN_WARPS 4
+#endif
+#ifndef MOE_TUNE_LAYOUT_SCAN
+#define MOE_TUNE_LAYOUT_SCAN 1
+#endif
 #ifndef MOE_TUNE_DISPATCH_PREFETCH
 #define MOE_TUNE_DISPATCH_PREFETCH (1 << 20)
 #endif
@@ -118,10 +124,12 @@ struct Tuning {
     int l2_hints;  // bit 0: evict-first on single-use loads; bit 1: evict-first on stores
     int spread_small;   // small batches: fewer dispatch warps per CTA, more CTAs
     int fused_small;    // moe_layout_dispatch: one fused launch for small batches
+    int fused_min_warps;  // ... only when each CTA gets at least this many warps
     int overlap;        // programmatic dependent launch of every non-cooperative kernel
     int dispatch_pool;  // % of dispatch units left to a shared pool when a cleared counter is at hand (>= 100: off)
     int combine_pool;   // % of combine tokens left to a shared pool when the caller gives a counter (>= 100: off)
     int layout_cluster; // CTAs of the cluster-mode layout (8 or 16; other values: off)
+    int layout_scan;    // the scan mode instead of the ticket lookback for more tiles than fit at once
     int dispatch_prefetch;       // input units per CTA prefetched into L2 (moe_layout_dispatch: during the layout)
     int dispatch_prefetch_keep;  // ... with an evict-last policy (else evict-normal)
     int dispatch_prefetch_always;  // ... in every chunked dispatch, not only behind the layout
@@ -141,7 +149,8 @@ struct LayoutLaunch {
     // let the next grid on the stream launch as soon as every CTA has passed its
     // dependency wait (the next launch is this library's dispatch)
     bool early_dependents = false;
-    bool no_cluster = false;   // never the cluster mode
+    bool no_cluster = false;      // never the cluster mode
+    bool lookback_only = false;   // only the lookback modes (not cluster, direct or scan)
 };
 
 size_t layout_workspace_bytes(int num_tokens, int num_experts, int num_ranks);

@@ -93,12 +93,14 @@ MOE_API size_t moe_get_layout_workspace_size(int num_tokens, int num_experts, in
  * [rank_prefix[r], rank_prefix[r+1]) in ascending source-token order, so
  *   token_dst_row[t, j] = rank_prefix[r] + #{t' < t : is_token_in_rank[t', r]}.
  * The in-rank position is a column-wise exclusive scan over tokens. For
- * 129..4096 tokens it is computed inside one 16-CTA thread-block cluster,
+ * 129..8192 tokens it is computed inside one 16-CTA thread-block cluster,
  * whose tiles exchange their counts through distributed shared memory (no
  * waits, no workspace use). Otherwise it is an all-tile sweep of published
- * counts (up to 128 tiles of 64 tokens) or a single-pass decoupled-lookback
- * scan over tiles of 128 tokens; both wait on other CTAs, bounded, with
- * MOE_ERR_TIMEOUT on expiry.
+ * counts (up to 128 tiles of 64 tokens), a single-pass decoupled-lookback
+ * scan over tiles of 128 tokens while every tile fits on the GPU at once
+ * (both wait on other CTAs, bounded, with MOE_ERR_TIMEOUT on expiry), and
+ * beyond that the scan mode: per-tile counts, a scan per rank, then the rows
+ * (three launches, no waits).
  *
  *   topk_idx   [T, k] int64, device. -1 = masked; other values outside [0, E)
  *              raise MOE_ERR_BAD_TOPK and are treated as masked.
@@ -125,13 +127,16 @@ typedef struct {
     /* Failure-injection hook for tests: the tile with this index (64 or 128
      * tokens, as the mode sizes it) never publishes its scan status, so that
      * the tiles after it (and the final count step) run out of their bounded
-     * waits and report MOE_ERR_TIMEOUT. Naming a tile also keeps the call off
-     * the cluster mode, which has no waits. -1 = off (the only value for
-     * production use). */
+     * waits and report MOE_ERR_TIMEOUT. Naming a tile also keeps the call on
+     * the lookback modes (off the cluster and scan modes, which have no
+     * waits). -1 = off (the only value for production use). */
     int32_t test_unpublished_tile;
-    /* 0: the mode is chosen by size (the cluster mode for 129..4096 tokens
-     * where the device can schedule it); 1: never the cluster mode (the
-     * direct or lookback mode by size). Both give the same outputs. */
+    /* 0: the mode is chosen by size (the cluster mode for 129..8192 tokens
+     * where the device can schedule it, the direct mode for few tiles, the
+     * cooperative lookback while every tile fits on the GPU at once, and
+     * beyond that the scan mode: three launches with no waits); 1: never the
+     * cluster mode; 2: only the lookback modes (cooperative, or with tickets
+     * beyond what fits at once). All give the same outputs. */
     int32_t layout_mode;
 } moe_layout_options_t;
 

@@ -225,7 +225,7 @@ def test_dispatch_ex_rejects_bad_arguments(lib, kw, code):
 
 
 def test_layout_ex_rejects_unknown_mode(lib):
-    opts = lib.MoeLayoutOptionsC(0, -1, 2)
+    opts = lib.MoeLayoutOptionsC(0, -1, 3)
     code = lib.LIB.moe_get_layout_ex(A, 128, 2, 16, 4, _layout_struct(lib), A + 0x100000, 1 << 30, A + 0x200000, None,
                                      ctypes.byref(opts))
     assert code == 1

@@ -53,7 +53,7 @@ def topk_for(w: wl.Workload, T=None):
 
 # ------------------------------------------------------------------ layout
 
-@pytest.mark.parametrize("layout_mode", [0, 1])   # 1: never the cluster mode
+@pytest.mark.parametrize("layout_mode", [0, 1, 2])   # 1: never the cluster mode; 2: only the lookback modes
 @pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "decode", "layout_2048", "layout_2048_1m"])
 def test_layout_parity_configs(moe, name, layout_mode):
     w = wl.CONFIGS[name]
@@ -97,6 +97,42 @@ def test_layout_many_distinct_shapes_in_one_process(moe):
         _, got, st = gpu_layout(moe, topk, E, R)
         assert st == 0, (E, R, k)
         assert_layout_equal(got, oracle.layout(topk.numpy(), E, R))
+
+
+@pytest.mark.parametrize("T,k,E,R,mask", [
+    (1 << 20, 8, 256, 8, 0.0),          # 8192 tiles of 128 tokens: more than fit on the GPU at once
+    (1 << 20, 8, 2048, 256, 0.1),
+    (400_000, 6, 48, 3, 0.3),            # a ragged last tile, ranks not a power of two
+    (300_001, 2, 16, 4, 0.0),
+    (250_000, 32, 8192, 1024, 0.2),      # the largest rank and expert counts
+])
+def test_layout_scan_mode_parity(moe, T, k, E, R, mask):
+    # the scan mode (per-tile counts, a scan per rank, then the rows; no waits) against the oracle, and
+    # against the lookback modes (layout_mode 2) on the same inputs; twice, reusing the workspace
+    g = torch.Generator().manual_seed(T % 1009 + R)
+    topk = wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), mask) if mask else wl.make_topk_uniform(g, T, E, k)
+    ref = oracle.layout(topk.numpy(), E, R)
+    assert ref["flags"] == 0
+    for _ in range(2):
+        _, got, st = gpu_layout(moe, topk, E, R)
+        assert st == 0
+        assert_layout_equal(got, ref)
+    _, got2, st2 = gpu_layout(moe, topk, E, R, layout_mode=2)
+    assert st2 == 0
+    assert_layout_equal(got2, ref)
+
+
+def test_layout_scan_mode_bad_entries_and_duplicates(moe):
+    g = torch.Generator().manual_seed(71)
+    T, k, E, R = 300_000, 8, 64, 8
+    topk = torch.randint(0, E, (T, k), generator=g)          # duplicates inside rows
+    topk[::13] = -1
+    topk[12345, 3] = E + 1
+    topk[299_999, 0] = -5
+    _, got, st = gpu_layout(moe, topk, E, R)
+    ref = oracle.layout(topk.numpy(), E, R)
+    assert ref["flags"] & oracle.ORACLE_BAD_TOPK and st == moe.MOE_ERR_BAD_TOPK
+    assert_layout_equal(got, ref)
 
 
 def test_layout_duplicates_all_masked_and_bad_entries(moe):

@@ -7,9 +7,9 @@ Checked through the C ABI against the CPU oracle's layout, on two calls in a
 row with different routings (the second call finds the first call's contents
 in the scratch), in every layout mode the scratch serves: the cluster mode
 (DeepSeek-V3 shape), the direct mode (skewed shape), a single tile (decode and
-tiny), the cooperative lookback (16,384 and 65,536 tokens) and the ticket
-lookback (2^20 tokens over 8 ranks, whose 0.5 MiB workspace still fits); and
-on its size limit. The file name sorts last so that a run stopping at the
+tiny), the cooperative lookback (16,384 and 65,536 tokens) and the scan
+mode (2^20 tokens over 8 ranks, whose 0.5 MiB workspace still fits); and on
+its size limit. The file name sorts last so that a run stopping at the
 first failure has already run every other test; it also passes alone in a
 fresh process (the first call performs the per-device set-up).
 """
@@ -77,8 +77,8 @@ def test_noalloc_layout_matches_oracle_twice(moe, name):
 
 @pytest.mark.parametrize("T,E,R", [(16384, 256, 8), (65536, 256, 64), (1 << 20, 256, 8)])
 def test_noalloc_layout_lookback_modes_match_oracle_twice(moe, T, E, R):
-    # beyond the cluster and direct modes: the lookback kernels, whose tile
-    # status words live in the scratch and are cleared by each call
+    # beyond the cluster and direct modes: the lookback kernels and the scan mode,
+    # whose tile words live in the scratch, cleared by each call
     assert moe.moe_get_layout_workspace_size(T, E, R) <= SCRATCH_BYTES
     routings = []
     for seed in (T + R, T + R + 1):
