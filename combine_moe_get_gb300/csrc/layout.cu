@@ -586,18 +586,19 @@ __global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
         __syncthreads();
     }
 
-    // ---- rank regions (warp 0) and, on tile 0, expert counts and prefix (warp 1)
+    // ---- rank regions (warp 0); on tile 0 the expert counts and prefix, by the
+    //      whole CTA (one warp walking 2048 experts took ~10 us)
     if (warp == 0) {
         if (tile == 0)
             for (int r = lane; r < R; r += 32) a.num_tokens_per_rank[r] = tot[r];
         __syncwarp();
         warp_exclusive_scan(tot, R, lane);
-    } else if (warp == 1 && tile == 0) {
-        for (int e = lane; e < E; e += 32) a.num_tokens_per_expert[e] = hist[e];
-        __syncwarp();
-        warp_exclusive_scan(hist, E, lane);
-        __syncwarp();
-        for (int e = lane; e <= E; e += 32) a.expert_prefix[e] = hist[e];
+    }
+    if (tile == 0) {
+        for (int e = threadIdx.x; e < E; e += kThreads) a.num_tokens_per_expert[e] = hist[e];
+        const int32_t n_entries = smem_exclusive_scan(hist, E);
+        for (int e = threadIdx.x; e < E; e += kThreads) a.expert_prefix[e] = hist[e];
+        if (threadIdx.x == 0) a.expert_prefix[E] = n_entries;
     }
     __syncthreads();
     for (int r = threadIdx.x; r < R; r += kThreads) {
