@@ -857,6 +857,68 @@ def run_profile(args):
     print(json.dumps({"profile_kernel": args.profile_kernel, "workload": w.name, "recv_rows": N}), flush=True)
 
 
+def run_trace(args):
+    """One step (moe_layout_dispatch, then moe_combine_ex with a balance counter,
+    replayed from a CUDA graph after an L2 flush) through the tracing build of
+    the library (compiled with MOE_PROFILE), printing per kernel: CTAs, warps
+    per CTA, SMs used, when its first warp started and its last warp ended (us
+    from the step's first warp), how long its warps lived, and how far apart its
+    CTAs finished (the tail). Every warp stamps the global timer twice and bumps
+    one counter, so these are a timeline, not a measurement."""
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from combine_moe_get_gb300 import binding as moe
+    from combine_moe_get_gb300 import build as moe_build
+    w = wl.CONFIGS[args.profile_workload]
+    tl = moe.load_library(moe_build.build_trace())
+    with moe.using(tl):
+        st = Step(moe, w, wl.make_inputs(w), device)
+        flush_l2 = Flush(device)
+        for _ in range(3):
+            flush_l2()
+            st.layout_dispatch()
+            st.combine()
+        cap = 1 << 20
+        buf = torch.zeros(cap * moe.TRACE_RECORD.itemsize, dtype=torch.uint8, device=device)
+        count = torch.zeros(1, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+        # captured in a CUDA graph as the benchmark times it (the launches keep the
+        # trace buffer they were captured with), then replayed once after a flush
+        moe.trace_enable(buf, count)
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                st.layout_dispatch()
+                st.combine()
+        finally:
+            moe.trace_enable(None, None)
+        count.zero_()
+        flush_l2()
+        graph.replay()
+        torch.cuda.synchronize()
+        moe.check_status(st.status, "traced step")
+        rec = moe.trace_read(buf, count)
+    t0 = int(rec["start_ns"].min())
+    us = lambda ns: round((int(ns) - t0) / 1e3, 2)
+    stamps = np.unique(np.concatenate([rec["start_ns"], rec["end_ns"]]))
+    kernels = []
+    for kid in sorted(np.unique(rec["kernel"]), key=lambda k: int(rec["start_ns"][rec["kernel"] == k].min())):
+        r = rec[rec["kernel"] == kid]
+        life = (r["end_ns"] - r["start_ns"]) / 1e3
+        cta_end = np.array([r["end_ns"][r["cta"] == c].max() for c in np.unique(r["cta"])])
+        kernels.append({
+            "kernel": moe.TRACE_KERNELS.get(int(kid), str(int(kid))), "ctas": int(len(cta_end)),
+            "warps_per_cta": int(r["warp"].max()) + 1, "sms": int(len(np.unique(r["sm"]))),
+            "first_start_us": us(r["start_ns"].min()), "last_end_us": us(r["end_ns"].max()),
+            "warp_life_us": {"median": round(float(np.median(life)), 2), "max": round(float(life.max()), 2)},
+            "cta_end_spread_us": {"p10_to_max": round(float(cta_end.max() - np.percentile(cta_end, 10)) / 1e3, 2)},
+        })
+    print(json.dumps({"trace": w.name, "records": int(count.item()),
+                      "step_us": us(rec["end_ns"].max()),
+                      "timer_step_ns": int(np.diff(stamps).min()) if len(stamps) > 1 else None,
+                      "kernels": kernels}), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 
 def run_reference(args, world, rank):
@@ -904,11 +966,16 @@ def main():
     ap.add_argument("--profile-kernel", choices=PROFILE_KERNELS, default=None,
                     help="run one call of this kernel for an ncu capture instead of the benchmark")
     ap.add_argument("--profile-workload", choices=["dsv3", "skewed", "decode"], default=WORKLOAD)
+    ap.add_argument("--trace", action="store_true",
+                    help="print one step's per-kernel timeline from the tracing build instead of the benchmark")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.profile_kernel:
         run_profile(args)
+        return
+    if args.trace:
+        run_trace(args)
         return
     world, rank, local = dist_env()
     if args.impl == "reference":

@@ -12,10 +12,13 @@ the library): call ``check_status`` after synchronising.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import dataclasses
 import os
 from typing import Optional
+
+import numpy as np
 
 import torch
 
@@ -57,8 +60,20 @@ def library_path() -> str:
 def _load():
     if not os.path.exists(_build.LIB) or not _build.up_to_date():
         _build.build()
-    lib = ctypes.CDLL(_build.LIB)
+    return _configure(ctypes.CDLL(_build.LIB))
+
+
+def load_library(path: str):
+    """A configured handle of another build of the library at `path` (e.g. the
+    tracing build, build.TRACE_LIB); route the functions below through it with
+    `using(handle)`."""
+    return _configure(ctypes.CDLL(path))
+
+
+def _configure(lib):
     lib.moe_get_version.restype = _I
+    lib.moe_trace_enable.argtypes = [_P, _I, _P]
+    lib.moe_trace_enable.restype = _I
     lib.moe_status_string.argtypes = [_I]
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_get_layout_workspace_size.argtypes = [_I, _I, _I]
@@ -92,6 +107,43 @@ def _load():
 
 
 LIB = _load()
+
+
+@contextlib.contextmanager
+def using(lib):
+    """Within the block, every function of this module calls `lib` (a handle from
+    load_library) instead of the default build."""
+    global LIB
+    old, LIB = LIB, lib
+    try:
+        yield lib
+    finally:
+        LIB = old
+
+
+# moe_trace_record_t, as written by a build with MOE_PROFILE
+TRACE_RECORD = np.dtype([("kernel", "<u4"), ("cta", "<u4"), ("warp", "<u4"), ("sm", "<u4"),
+                         ("start_ns", "<u8"), ("end_ns", "<u8")])
+TRACE_KERNELS = {1: "layout_tiles", 2: "layout_direct", 3: "layout_cluster", 4: "layout_count", 5: "layout_scan",
+                 6: "layout_rows_scan", 7: "expand_layout", 8: "expand_layout_cluster", 9: "dispatch",
+                 10: "dispatch_fp8_rows", 11: "combine", 12: "layout_rows"}
+
+
+def trace_enable(records: Optional[torch.Tensor], count: Optional[torch.Tensor]) -> None:
+    """Send the warps' records of later launches to `records` (a CUDA uint8 tensor
+    of n * TRACE_RECORD.itemsize bytes) and count them in `count` (a zeroed CUDA
+    int32 tensor of one element); None stops. Needs a build with MOE_PROFILE."""
+    if records is None:
+        _check(LIB.moe_trace_enable(None, 0, None), "moe_trace_enable")
+        return
+    cap = records.numel() // TRACE_RECORD.itemsize
+    _check(LIB.moe_trace_enable(_ptr(records), cap, _ptr(count)), "moe_trace_enable")
+
+
+def trace_read(records: torch.Tensor, count: torch.Tensor) -> np.ndarray:
+    """The records written so far (after the stream has synchronised)."""
+    n = min(int(count.item()), records.numel() // TRACE_RECORD.itemsize)
+    return records[: n * TRACE_RECORD.itemsize].cpu().numpy().view(TRACE_RECORD)
 
 
 def status_string(code: int) -> str:

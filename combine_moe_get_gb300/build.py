@@ -15,6 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_get.so")
+# the same library compiled with MOE_PROFILE: every kernel warp records its start and end (moe_trace_enable)
+TRACE_LIB = os.path.join(HERE, "libmoe_get_trace.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -40,25 +42,26 @@ def _inputs() -> list[str]:
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, defines: tuple = ()) -> str:
+def build(force: bool = False, verbose: bool = False, defines: tuple = (), lib: str = LIB,
+          build_dir: str = BUILD_DIR) -> str:
     """Compile and link the library in place. `defines` (e.g. ("MOE_TUNE_X=4",))
     builds a variant with other compile-time settings; the default build has none."""
-    if not force and up_to_date():
-        return LIB
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     common = [nvcc, *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
               "-I", INCLUDE, "--expt-relaxed-constexpr", *(f"-D{d}" for d in defines)]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = common + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,15 +73,20 @@ def build(force: bool = False, verbose: bool = False, defines: tuple = ()) -> st
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     for d in _cuda_lib_dirs(nvcc):
         link += ["-Xlinker", f"-rpath,{d}"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_trace(force: bool = False, verbose: bool = False) -> str:
+    """libmoe_get_trace.so: the library compiled with MOE_PROFILE (per-warp timer records)."""
+    return build(force, verbose, defines=("MOE_PROFILE=1",), lib=TRACE_LIB, build_dir=BUILD_DIR + "_trace")
 
 
 if __name__ == "__main__":

@@ -81,6 +81,7 @@ struct CombineArgs {
     // counts finished CTAs; the last one zeroes both). nullptr: all dealt.
     unsigned int *balance;
     int static_tokens;
+    TraceArgs trace;   // MOE_PROFILE builds: where the warps' records go
 };
 
 struct UnitEntry {
@@ -161,6 +162,7 @@ __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
 // runs more consumer warps.
 template <bool kWeighted, bool kFP8>
 __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(const CombineArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_COMBINE);
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kUnits;
@@ -482,6 +484,7 @@ int launch_combine(const CombineLaunch &L) {
 
     const bool fp8 = L.fp8;    // E4M3 rows with per-128 scales
     CombineArgs a;
+    a.trace = trace_args();
     a.partial = static_cast<const uint8_t *>(L.partial);
     a.row_bytes = fp8 ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
     a.scales = reinterpret_cast<const uint8_t *>(L.partial_scales);

@@ -82,6 +82,7 @@ struct DispatchArgs {
     // nullptr: every unit is dealt.
     unsigned int *pool;
     int64_t static_units;
+    TraceArgs trace;   // MOE_PROFILE builds: where the warps' records go
 };
 
 // Whether unit u's input rows were prefetched (evict-last) by the rule of
@@ -382,6 +383,7 @@ __device__ void fused_layout(const DispatchArgs &a, uint8_t *region) {
 
 template <bool kFP8, bool kFused>
 __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_DISPATCH);
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int warps = blockDim.x >> 5;
@@ -715,6 +717,7 @@ struct Fp8Args {
     // CTAs that claim no more; the last of them zeroes both). nullptr: all dealt.
     unsigned int *pool;
     int static_tokens;
+    TraceArgs trace;
 };
 
 __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
@@ -724,6 +727,7 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
 // 80 registers (no spills) allow 1 producer + 24 worker warps per SM
 template <bool kPool>
 __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
+    WarpTrace wt(a.trace, MOE_TRACE_DISPATCH_FP8_ROWS);
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *in_full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *in_empty = in_full + kFp8MaxSlots;
@@ -963,6 +967,7 @@ DispatchArgs base_args(const DispatchLaunch &L) {
     const bool fp8 = L.mode == MOE_DISPATCH_QUANTIZE_FP8;      // quantise in the kernel
     const bool fp8_in = L.mode == MOE_DISPATCH_FP8;             // relay E4M3 bytes and their scales
     DispatchArgs a = {};
+    a.trace = trace_args();
     a.x = static_cast<const uint8_t *>(L.x);
     a.row_bytes = fp8_in ? (int64_t)L.hidden : (int64_t)L.hidden * 2;
     a.k = L.num_topk;
@@ -1085,6 +1090,7 @@ int launch_dispatch(const DispatchLaunch &L) {
 
     if (fp8 && tu.fp8_rows) {
         Fp8Args f;
+        f.trace = a.trace;
         f.x = a.x;
         f.row_bytes = a.row_bytes;
         f.H = L.hidden;

@@ -74,9 +74,11 @@ struct ExpandArgs {
     int32_t *status;
     uint64_t timeout_ns;
     int unpublished_tile;  // test hook: this tile never publishes its status (-1 = none)
+    TraceArgs trace;       // MOE_PROFILE builds: where the warps' records go
 };
 
 __global__ void __launch_bounds__(kXThreads) layout_expand_kernel(const ExpandArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_EXPAND_LAYOUT);
     extern __shared__ __align__(16) uint8_t smem[];
     const int E = a.E, k = a.k;
     const XSmem sl = xsmem(E, k);
@@ -262,9 +264,11 @@ struct ExpandClusterArgs {
     const int32_t *expert_prefix;
     int32_t *token_expert_row;
     int32_t *status;
+    TraceArgs trace;
 };
 
 __global__ void __launch_bounds__(kXCThreads) layout_expand_cluster_kernel(const ExpandClusterArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_EXPAND_LAYOUT_CLUSTER);
     extern __shared__ __align__(16) uint8_t smem[];
     const int E = a.E, k = a.k, tile = a.tile;
     const XCSmem sl = xcsmem(tile, E, k);
@@ -424,6 +428,7 @@ int launch_expand_layout(const ExpandLaunch &L) {
     size_t csmem = 0;
     if (L.unpublished_tile < 0 && !L.no_cluster && expand_cluster_config(T, E, k, tile, csmem)) {
         ExpandClusterArgs c;
+        c.trace = trace_args();
         c.topk = L.topk_idx;
         c.T = T; c.k = k; c.E = E; c.tile = tile;
         c.expert_prefix = L.expert_prefix;
@@ -448,6 +453,7 @@ int launch_expand_layout(const ExpandLaunch &L) {
     const size_t ws = expand_workspace_bytes(T, E);
     if (cudaMemsetAsync(L.workspace, 0, ws, s) != cudaSuccess) return MOE_ERR_CUDA;
     ExpandArgs a;
+    a.trace = trace_args();
     a.topk = L.topk_idx;
     a.T = T; a.k = k; a.E = E;
     a.num_tiles = (T + kXTile - 1) / kXTile;

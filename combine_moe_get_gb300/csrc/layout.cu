@@ -204,10 +204,12 @@ struct TileArgs {
     int early_dependents;  // trigger the next grid's launch right after the dependency wait
     int cl_tile;           // cluster mode: tokens per CTA (a multiple of 32)
     unsigned int *spare;   // cluster mode: two workspace words to zero for the next launch (the others clear them)
+    TraceArgs trace;       // MOE_PROFILE builds: where the warps' records go
 };
 
 template <bool kCooperative>
 __global__ void __launch_bounds__(kThreads) layout_tiles_kernel(TileArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_LAYOUT_TILES);
     extern __shared__ __align__(16) uint8_t smem[];
     const int R = a.R, E = a.E, k = a.k;
     const SmemLayout sl = smem_layout(E, R, k);
@@ -484,6 +486,7 @@ __host__ __device__ inline DirectSmem direct_smem(int E, int R, int k) {
 // the expert counts and prefix. A batch of one tile exchanges nothing.
 template <int TILE>
 __global__ void __launch_bounds__(kThreads) layout_direct_kernel(TileArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_LAYOUT_DIRECT);
     constexpr int kTile = TILE;            // tokens per tile of this instance
     constexpr int kWords = TILE / 32;
     extern __shared__ __align__(16) uint8_t smem[];
@@ -710,6 +713,7 @@ __device__ __forceinline__ int32_t ld_cluster_i32(const void *local, uint32_t ra
 }
 
 __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_LAYOUT_CLUSTER);
     extern __shared__ __align__(16) uint8_t smem[];
     const int R = a.R, E = a.E, k = a.k, tile = a.cl_tile, W = tile / 32;
     const ClusterSmem sl = cluster_smem(tile, E, R, k);
@@ -901,7 +905,9 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
 }
 
 __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, int m,
-                                   const int32_t *__restrict__ rank_prefix, int32_t *__restrict__ token_dst_row) {
+                                   const int32_t *__restrict__ rank_prefix, int32_t *__restrict__ token_dst_row,
+                                   TraceArgs trace) {
+    WarpTrace wt(trace, MOE_TRACE_LAYOUT_ROWS);
     grid_dependency_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int32_t v = token_dst_row[i];
@@ -927,6 +933,7 @@ __global__ void layout_rows_kernel(const int64_t *__restrict__ topk, int64_t n, 
 //          its tile's prefix.
 
 __global__ void __launch_bounds__(kThreads) layout_count_kernel(TileArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_LAYOUT_COUNT);
     extern __shared__ __align__(16) uint8_t smem[];
     const int R = a.R, E = a.E, k = a.k;
     const SmemLayout sl = smem_layout(E, R, k);
@@ -1015,6 +1022,7 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(TileArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) layout_scan_kernel(TileArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_LAYOUT_SCAN);
     __shared__ int s_last;
     WsHeader *hdr = reinterpret_cast<WsHeader *>(a.ws);
     int32_t *ws_expert = reinterpret_cast<int32_t *>(a.ws + a.expert_off);
@@ -1037,6 +1045,7 @@ __global__ void __launch_bounds__(kThreads) layout_scan_kernel(TileArgs a) {
 }
 
 __global__ void layout_rows_scan_kernel(TileArgs a) {
+    WarpTrace wt(a.trace, MOE_TRACE_LAYOUT_ROWS_SCAN);
     grid_dependency_wait();
     const int64_t n = (int64_t)a.T * a.k;   // < 2^31 (checked on the host)
     const int32_t *counts = reinterpret_cast<const int32_t *>(a.ws + a.status_off);
@@ -1205,6 +1214,7 @@ int launch_layout(const LayoutLaunch &L) {
         return MOE_ERR_CUDA;
 
     TileArgs a;
+    a.trace = trace_args();
     a.topk = L.topk_idx;
     a.T = T; a.k = k; a.E = E; a.R = R; a.m = E / R;
     a.num_tiles = num_tiles;
@@ -1258,7 +1268,7 @@ int launch_layout(const LayoutLaunch &L) {
     const int threads = 256;
     const int blocks = (int)std::min<int64_t>((n + threads - 1) / threads, (int64_t)device_sm_count() * 8);
     if (launch_kernel(layout_rows_kernel, dim3(blocks), dim3(threads), 0, s, tuning().overlap != 0, L.topk_idx, n, a.m,
-                      (const int32_t *)o.rank_prefix, o.token_dst_row) != cudaSuccess)
+                      (const int32_t *)o.rank_prefix, o.token_dst_row, a.trace) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -99,6 +99,19 @@ int ensure_dynamic_smem(const void *kernel, size_t bytes) {
     return MOE_OK;
 }
 
+namespace {
+std::atomic<moe_trace_record_t *> g_trace_rec{nullptr};
+std::atomic<uint32_t *> g_trace_count{nullptr};
+std::atomic<int> g_trace_cap{0};
+}  // namespace
+
+TraceArgs trace_args() {
+    TraceArgs t{g_trace_rec.load(std::memory_order_acquire), g_trace_count.load(std::memory_order_acquire),
+                g_trace_cap.load(std::memory_order_acquire)};
+    if (t.rec == nullptr || t.count == nullptr) t = TraceArgs{nullptr, nullptr, 0};
+    return t;
+}
+
 const Tuning &tuning() {
     // Compile-time settings (moe_internal.h): nothing read from the environment,
     // so every call takes the configuration the parity tests ran.
@@ -207,6 +220,22 @@ int layout_prepare(const int64_t *topk_idx, int T, int k, int E, int R, moe_layo
 extern "C" {
 
 MOE_API int moe_get_version(void) { return 100; }
+
+MOE_API int moe_trace_enable(moe_trace_record_t *records, int capacity, uint32_t *count) {
+#ifdef MOE_PROFILE
+    if (records != nullptr && (capacity < 0 || count == nullptr || !aligned(records, 8) || !aligned(count, 4)))
+        return MOE_ERR_INVALID_ARG;
+    moe::g_trace_cap.store(records ? capacity : 0, std::memory_order_release);
+    moe::g_trace_count.store(records ? count : nullptr, std::memory_order_release);
+    moe::g_trace_rec.store(records, std::memory_order_release);
+    return MOE_OK;
+#else
+    (void)records;
+    (void)capacity;
+    (void)count;
+    return MOE_ERR_INVALID_ARG;   // a build without MOE_PROFILE records nothing
+#endif
+}
 
 MOE_API const char *moe_status_string(int status) {
     switch (status) {

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/moe_get.h"
+#include "moe_internal.h"
 
 namespace moe {
 
@@ -101,6 +102,40 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ------------------------------------------------------------------ shared-memory addresses
+
+// ------------------------------------------------------------------ tracing (MOE_PROFILE builds)
+
+// Declared first in a kernel: in a MOE_PROFILE build, lane 0 of each warp stamps
+// the global timer here and, when the warp returns (whichever return it takes),
+// appends one moe_trace_record_t to the buffer given to moe_trace_enable. In
+// the default build it is empty and compiles to nothing.
+struct WarpTrace {
+#ifdef MOE_PROFILE
+    TraceArgs t;
+    uint32_t kernel;
+    uint64_t t0 = 0;
+    __device__ __forceinline__ WarpTrace(const TraceArgs &ta, uint32_t k) : t(ta), kernel(k) {
+        if (t.rec != nullptr && (threadIdx.x & 31) == 0) t0 = globaltimer_ns();
+    }
+    __device__ __forceinline__ ~WarpTrace() {
+        if (t.rec == nullptr || (threadIdx.x & 31) != 0) return;
+        const uint32_t i = atomicAdd(t.count, 1u);
+        if (i >= (uint32_t)t.cap) return;
+        uint32_t sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        moe_trace_record_t r;
+        r.kernel = kernel;
+        r.cta = blockIdx.x;
+        r.warp = threadIdx.x >> 5;
+        r.sm = sm;
+        r.start_ns = t0;
+        r.end_ns = globaltimer_ns();
+        t.rec[i] = r;
+    }
+#else
+    __device__ __forceinline__ WarpTrace(const TraceArgs &, uint32_t) {}
+#endif
+};
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

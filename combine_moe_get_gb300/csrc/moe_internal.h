@@ -20,6 +20,15 @@ size_t device_l2_bytes();          // L2 cache size (bytes)
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` (cached).
 int ensure_dynamic_smem(const void *kernel, size_t bytes);
 
+// Where kernels built with MOE_PROFILE append their warps' records (all null /
+// zero: not tracing); every launcher copies it into its kernel's arguments.
+struct TraceArgs {
+    moe_trace_record_t *rec;
+    uint32_t *count;
+    int cap;
+};
+TraceArgs trace_args();
+
 // Tuning knobs. They are fixed when the library is compiled (the defaults
 // below are the measured best on this GPU and the configuration every parity
 // test runs); a variant build may override one with -DMOE_TUNE_<NAME>=<value>.

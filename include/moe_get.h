@@ -379,6 +379,56 @@ MOE_API int moe_combine_fp8_ex(const void *partial_codes, const float *partial_s
                                int num_tokens, int hidden, int num_topk, const int32_t *token_dst_row, void *out,
                                uint32_t *balance, int32_t *status, void *stream);
 
+/*
+ * Tracing -- a build option. The pages stamp their kernels' progress with the
+ * device's global timer (the GEMM + all-reduce page's command stamps) and count
+ * bytes in software counters (the Ascend send-ordering page); this is the
+ * equivalent for these kernels. In a library compiled with -DMOE_PROFILE
+ * (libmoe_get_trace.so, built beside libmoe_get.so), once moe_trace_enable has
+ * been given a buffer, every warp of every kernel launched afterwards appends
+ * one moe_trace_record_t when it returns: which kernel, CTA and warp, the SM it
+ * ran on, and %globaltimer (ns) when the warp began and when it returned. The
+ * default build compiles all of it out (no cost, no argument).
+ */
+enum {
+    MOE_TRACE_LAYOUT_TILES = 1,        /* lookback tiles (cooperative or ticket) */
+    MOE_TRACE_LAYOUT_DIRECT = 2,
+    MOE_TRACE_LAYOUT_CLUSTER = 3,
+    MOE_TRACE_LAYOUT_COUNT = 4,        /* scan mode: per-tile counts */
+    MOE_TRACE_LAYOUT_SCAN = 5,         /* scan mode: per-rank scans */
+    MOE_TRACE_LAYOUT_ROWS_SCAN = 6,    /* scan mode: rows */
+    MOE_TRACE_EXPAND_LAYOUT = 7,
+    MOE_TRACE_EXPAND_LAYOUT_CLUSTER = 8,
+    MOE_TRACE_DISPATCH = 9,            /* relay pipeline (bf16, E4M3 rows, chunked E4M3, fused small batches) */
+    MOE_TRACE_DISPATCH_FP8_ROWS = 10,  /* quantising row pipeline */
+    MOE_TRACE_COMBINE = 11,
+    MOE_TRACE_LAYOUT_ROWS = 12         /* lookback tiles launched one after another: rows */
+};
+
+typedef struct {
+    uint32_t kernel;     /* MOE_TRACE_* */
+    uint32_t cta;        /* blockIdx.x */
+    uint32_t warp;       /* warp index in the CTA */
+    uint32_t sm;         /* SM the CTA ran on */
+    uint64_t start_ns;   /* global timer when the warp began */
+    uint64_t end_ns;     /* global timer when it returned */
+} moe_trace_record_t;
+
+/*
+ * moe_trace_enable -- where the warps' records go, for the launches that follow.
+ *
+ *   records   device array of `capacity` records, or NULL to stop tracing.
+ *   count     device uint32, zeroed by the caller: each record claims the slot
+ *             *count (atomically incremented); records at or beyond `capacity`
+ *             are dropped, but still counted, so *count after the stream has
+ *             synchronised tells how many there were.
+ * Process-wide setting (all devices, all streams); not for concurrent use
+ * with launches on other host threads. MOE_OK in a -DMOE_PROFILE build;
+ * MOE_ERR_INVALID_ARG in the default build (nothing is recorded) or for a
+ * negative capacity, a null or misaligned count with non-null records.
+ */
+MOE_API int moe_trace_enable(moe_trace_record_t *records, int capacity, uint32_t *count);
+
 /* Size of the library's own layout scratch (bytes), used by moe_get_layout_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
 

@@ -229,3 +229,33 @@ def test_layout_ex_rejects_unknown_mode(lib):
     code = lib.LIB.moe_get_layout_ex(A, 128, 2, 16, 4, _layout_struct(lib), A + 0x100000, 1 << 30, A + 0x200000, None,
                                      ctypes.byref(opts))
     assert code == 1
+
+
+def test_default_build_records_no_trace(lib):
+    # only a build compiled with MOE_PROFILE records; the default one refuses, enabling or not
+    assert lib.LIB.moe_trace_enable(None, 0, None) == lib.MOE_ERR_INVALID_ARG
+
+
+def test_trace_build_exports_the_same_abi(lib):
+    from combine_moe_get_gb300 import build
+    path = build.build_trace()
+    raw = ctypes.CDLL(path)
+    for name in _declared_symbols():
+        assert hasattr(raw, name), f"{name} missing from the tracing build"
+    tl = lib.load_library(path)
+    assert tl.moe_get_version() == lib.LIB.moe_get_version()
+    assert tl.moe_trace_enable(None, 0, None) == lib.MOE_OK              # stop: accepted with no buffer
+    bad = ctypes.c_void_p(8)
+    assert tl.moe_trace_enable(bad, 4, None) == lib.MOE_ERR_INVALID_ARG  # a buffer needs a counter
+    assert tl.moe_trace_enable(bad, -1, bad) == lib.MOE_ERR_INVALID_ARG
+
+
+def test_trace_record_layout_matches_header(lib):
+    text = open(os.path.join(ROOT, "include", "moe_get.h")).read()
+    body = re.search(r"typedef struct\s*\{([^}]*)\}\s*moe_trace_record_t;", text, flags=re.S).group(1)
+    fields = re.findall(r"\b(uint32_t|uint64_t)\s+(\w+)\s*;", body)
+    np_code = {"uint32_t": "<u4", "uint64_t": "<u8"}
+    assert [(n, np_code[t]) for t, n in fields] == [(n, lib.TRACE_RECORD[n].str) for n in lib.TRACE_RECORD.names]
+    assert lib.TRACE_RECORD.itemsize == 32
+    kinds = dict((int(v), k) for k, v in re.findall(r"\b(MOE_TRACE_\w+)\s*=\s*(\d+)", text))
+    assert sorted(kinds) == sorted(lib.TRACE_KERNELS)
