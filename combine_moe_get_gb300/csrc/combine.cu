@@ -81,7 +81,8 @@ struct CombineArgs {
     // counts finished CTAs; the last one zeroes both). nullptr: all dealt.
     unsigned int *balance;
     int static_tokens;
-    TraceArgs trace;   // MOE_PROFILE builds: where the warps' records go
+    int prefetch_bytes;   // of the CTA's first rows, into L2 before the dependency wait (0: none)
+    TraceArgs trace;      // MOE_PROFILE builds: where the warps' records go
 };
 
 struct UnitEntry {
@@ -186,6 +187,26 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
         fence_barrier_init();
     }
     __syncthreads();
+    if (warp == 1 && a.prefetch_bytes > 0) {
+        // While the previous grid finishes, the first rows of this CTA's static range
+        // go into L2 (evict-normal), in the order the producer will load them. Only
+        // prefetch addresses come from these reads, so a row list still being written
+        // costs a useless prefetch, never a wrong result: rows out of range are
+        // skipped, and the lists are read past L1 (.cg), so no stale line of them is
+        // left for the loads after the wait.
+        const uint64_t pol = policy_evict_normal();
+        const int64_t first = (int64_t)s_begin * a.k, end = (int64_t)s_end * a.k;
+        int64_t done = 0;
+        for (int64_t i = first; i < end && done < a.prefetch_bytes; i += 32) {
+            const int row = i + lane < end ? __ldcg(a.dst_row + i + lane) : -1;
+            const bool ok = row >= 0 && row < a.num_rows;
+            const unsigned m = __ballot_sync(kFull, ok);
+            const int64_t before = done + (int64_t)__popc(m & ((1u << lane) - 1u)) * a.row_bytes;
+            if (ok && before < a.prefetch_bytes)
+                bulk_prefetch_l2(a.partial + (int64_t)row * a.row_bytes, (uint32_t)a.row_bytes, pol);
+            done += (int64_t)__popc(m) * a.row_bytes;
+        }
+    }
     grid_dependency_wait();
     grid_launch_dependents();
 
@@ -538,6 +559,7 @@ int launch_combine(const CombineLaunch &L) {
     const int pool_pct = fp8 ? tu.combine_fp8_pool : tu.combine_pool;
     if (pool_pct <= 0 || pool_pct >= 100) a.balance = nullptr;
     a.static_tokens = a.balance ? (int)((int64_t)a.T * (100 - pool_pct) / 100) : a.T;
+    a.prefetch_bytes = (tu.overlap != 0 && !fp8) ? std::max(0, tu.combine_prefetch) : 0;
     void (*kernel)(const CombineArgs) =
         fp8 ? combine_kernel<false, true> : (weighted ? combine_kernel<true, false> : combine_kernel<false, false>);
     return launch_kernel(kernel, dim3(grid), dim3((consumers + 1) * 32), smem, st, tu.overlap != 0, a) == cudaSuccess

@@ -130,6 +130,7 @@ const Tuning &tuning() {
         x.overlap = MOE_TUNE_OVERLAP;
         x.dispatch_pool = MOE_TUNE_DISPATCH_POOL;
         x.combine_pool = MOE_TUNE_COMBINE_POOL;
+        x.combine_prefetch = MOE_TUNE_COMBINE_PREFETCH;
         x.layout_cluster = MOE_TUNE_LAYOUT_CLUSTER;
         x.layout_scan = MOE_TUNE_LAYOUT_SCAN;
         x.fp8_rows = MOE_TUNE_FP8_ROWS;

@@ -24,7 +24,11 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s
 // grid_dependency_wait() before its first global memory access, read or
 // write: it returns once the previous grid has completed and its writes are
 // visible, so reads see the producer's results and writes cannot overtake
-// the previous grid's reads. grid_launch_dependents() then lets the next
+// the previous grid's reads. Two exceptions read before it, and neither can
+// change a result: L2 prefetches (the combine's first rows, and the address
+// lists they come from, read past L1), and the dispatch's first input-row
+// loads when it is launched right behind this library's own layout, which
+// does not write the input rows. grid_launch_dependents() then lets the next
 // grid's CTAs be placed as this grid's CTAs retire, so that its launch and
 // prologue (barrier set-up) overlap this grid's tail. Only the dispatch and
 // combine kernels call it: a layout kernel leaves the trigger to its exit,

@@ -69,6 +69,9 @@ TraceArgs trace_args();
 #ifndef MOE_TUNE_DISPATCH_POOL
 #define MOE_TUNE_DISPATCH_POOL 50
 #endif
+#ifndef MOE_TUNE_COMBINE_PREFETCH
+#define MOE_TUNE_COMBINE_PREFETCH (96 << 10)
+#endif
 #ifndef MOE_TUNE_COMBINE_POOL
 #define MOE_TUNE_COMBINE_POOL 30
 #endif
@@ -137,6 +140,7 @@ struct Tuning {
     int overlap;        // programmatic dependent launch of every non-cooperative kernel
     int dispatch_pool;  // % of dispatch units left to a shared pool when a cleared counter is at hand (>= 100: off)
     int combine_pool;   // % of combine tokens left to a shared pool when the caller gives a counter (>= 100: off)
+    int combine_prefetch;   // bytes of its first rows each combine CTA prefetches into L2 before the dependency wait
     int layout_cluster; // CTAs of the cluster-mode layout (8 or 16; other values: off)
     int layout_scan;    // the scan mode instead of the ticket lookback for more tiles than fit at once
     int dispatch_prefetch;       // input units per CTA prefetched into L2 (moe_layout_dispatch: during the layout)
