@@ -371,6 +371,22 @@ class Timer:
         return ms
 
 
+def algorithmic_bytes(T: int, H: int, N: int, NX: int) -> dict:
+    """Bytes each call must move at least (T tokens, hidden H, N receive rows,
+    NX expand rows)."""
+    row = H * 2
+    nb = H // 128
+    bf16 = T * row + N * row                            # x read once + one row per (token, rank)
+    return {
+        "dispatch": bf16, "combine": bf16,              # combine: the rows read, one bf16 row per token written
+        "dispatch_fp8": T * row + N * H + N * nb * 4,   # x read + e4m3 rows + scales
+        "dispatch_fp8_input": (T + N) * (H + nb * 4),   # e4m3 rows + scales read once, written per rank
+        "combine_weighted": bf16 + N * 4,               # + one weight per receive row
+        "dispatch_expand": T * row + NX * row,          # x read once + one row per valid entry
+        "combine_fp8": N * (H + nb * 4) + T * row,      # e4m3 rows + scales read, bf16 out written
+    }
+
+
 def gbs(nbytes: float, ms: float) -> float:
     return nbytes / (ms * 1e-3) / 1e9
 
@@ -539,15 +555,14 @@ def run_ours(args, world, rank, local):
     del sd
     skewed = measure_skewed(moe, device, rank, timer, reps)
     small = measure_small_configs(moe, device, rank, timer, reps)
+    # the fixed cost inside every event-timed figure: a one-kernel graph timed the same way
+    tiny = torch.zeros(16, device=device)
+    floor_ms = timer(lambda: tiny.add_(1), reps)
 
     peak, peak_kind = hbm_peak()
-    row = H * 2
-    bytes_bf16 = T * row + N * row                      # x read once + one row per (token, rank)
-    bytes_fp8 = T * row + N * H + N * (H // 128) * 4    # x read + e4m3 rows + scales
-    bytes_fp8in = (T + N) * (H + (H // 128) * 4)        # e4m3 rows + scales read once, written per rank
-    bytes_wcomb = bytes_bf16 + N * 4                    # + one weight per receive row
-    bytes_expand = T * row + NX * row                   # x read once + one row per valid entry
-    bytes_fcomb = N * (H + (H // 128) * 4) + T * row    # e4m3 rows + scales read, bf16 out written
+    ab = algorithmic_bytes(T, H, N, NX)
+    bytes_bf16, bytes_fp8, bytes_fp8in = ab["dispatch"], ab["dispatch_fp8"], ab["dispatch_fp8_input"]
+    bytes_wcomb, bytes_expand, bytes_fcomb = ab["combine_weighted"], ab["dispatch_expand"], ab["combine_fp8"]
     kern = {
         "layout_us": mean(lay_ms) * 1e3,
         "layout_median_us": med(lay_ms) * 1e3,
@@ -571,7 +586,10 @@ def run_ours(args, world, rank, local):
         "expand_step_tokens_per_s": T / (mean(xstep_ms) * 1e-3),
         "expand_rows": NX,
         **dec,
+        "timing_floor_us": mean(floor_ms) * 1e3,
         "notes": {
+            "timing_floor_us": "a graph holding one 16-element torch add, replayed after the same L2 flush and timed "
+                               "the same way: the fixed launch and cold-start cost inside every event-timed figure",
             "dispatch_us, combine_us": "inside the step (the per-kernel breakdown graph); the in-step combine also "
                                        "writes back the dispatch's receive rows still dirty in L2",
             "combine_alone_us": "the step's balanced combine timed alone after an L2 flush",
@@ -857,20 +875,66 @@ def run_profile(args):
     print(json.dumps({"profile_kernel": args.profile_kernel, "workload": w.name, "recv_rows": N}), flush=True)
 
 
+def _traced(moe, fn, flush_l2, buf, count):
+    """Records of one call of `fn`: captured in a CUDA graph with tracing on
+    (the launches keep the trace buffer they were captured with), then
+    replayed once after an L2 flush, as the benchmark times it."""
+    fn()
+    torch.cuda.synchronize()
+    moe.trace_enable(buf, count)
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+    finally:
+        moe.trace_enable(None, None)
+    count.zero_()
+    flush_l2()
+    graph.replay()
+    torch.cuda.synchronize()
+    return moe.trace_read(buf, count)
+
+
+def _timeline(moe, rec) -> list:
+    """Per kernel, in launch order: CTAs, warps per CTA, SMs, first warp start
+    and last warp end (us from the first warp of `rec`), warp lifetimes and CTA
+    end times."""
+    t0 = int(rec["start_ns"].min())
+    us = lambda ns: round((int(ns) - t0) / 1e3, 2)
+    out = []
+    for kid in sorted(np.unique(rec["kernel"]), key=lambda k: int(rec["start_ns"][rec["kernel"] == k].min())):
+        r = rec[rec["kernel"] == kid]
+        life = (r["end_ns"] - r["start_ns"]) / 1e3
+        cta_end = np.array([r["end_ns"][r["cta"] == c].max() for c in np.unique(r["cta"])])
+        out.append({
+            "kernel": moe.TRACE_KERNELS.get(int(kid), str(int(kid))), "ctas": int(len(cta_end)),
+            "warps_per_cta": int(r["warp"].max()) + 1, "sms": int(len(np.unique(r["sm"]))),
+            "first_start_us": us(r["start_ns"].min()), "last_end_us": us(r["end_ns"].max()),
+            "warp_life_us": {"median": round(float(np.median(life)), 2), "max": round(float(life.max()), 2)},
+            "cta_end_us": {q: us(np.percentile(cta_end, p)) for q, p in (("min", 0), ("p50", 50), ("max", 100))},
+        })
+    return out
+
+
 def run_trace(args):
-    """One step (moe_layout_dispatch, then moe_combine_ex with a balance counter,
-    replayed from a CUDA graph after an L2 flush) through the tracing build of
-    the library (compiled with MOE_PROFILE), printing per kernel: CTAs, warps
-    per CTA, SMs used, when its first warp started and its last warp ended (us
-    from the step's first warp), how long its warps lived, and how far apart its
-    CTAs finished (the tail). Every warp stamps the global timer twice and bumps
-    one counter, so these are a timeline, not a measurement."""
+    """Timelines from the tracing build of the library (compiled with
+    MOE_PROFILE): one step (moe_layout_dispatch, then moe_combine_ex with a
+    balance counter) and the dispatch, combine, quantising dispatch and FP8
+    combine called alone, each replayed from a CUDA graph after an L2 flush.
+    Per kernel: CTAs, warps per CTA, SMs used, when its first warp started and
+    its last warp ended, how long its warps lived and when its CTAs finished.
+    Per lone call also its span (first warp start to last warp end), and its
+    algorithmic bytes over the span as a fraction of the measured copy
+    bandwidth. Every warp stamps the global timer twice and claims a slot with
+    one atomic, so these are a timeline; the event-timed figures of the
+    benchmark are the measurement."""
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     from combine_moe_get_gb300 import binding as moe
     from combine_moe_get_gb300 import build as moe_build
     w = wl.CONFIGS[args.profile_workload]
     tl = moe.load_library(moe_build.build_trace())
+    peak, peak_kind = hbm_peak()
     with moe.using(tl):
         st = Step(moe, w, wl.make_inputs(w), device)
         flush_l2 = Flush(device)
@@ -878,45 +942,30 @@ def run_trace(args):
             flush_l2()
             st.layout_dispatch()
             st.combine()
-        cap = 1 << 20
-        buf = torch.zeros(cap * moe.TRACE_RECORD.itemsize, dtype=torch.uint8, device=device)
+        st.dispatch(fp8=True)       # E4M3 rows and scales for the FP8 combine's input
+        torch.cuda.synchronize()
+        N = int(st.lay.rank_prefix[-1].item())
+        ab = algorithmic_bytes(w.num_tokens, w.hidden, N, 0)
+        buf = torch.zeros((1 << 20) * moe.TRACE_RECORD.itemsize, dtype=torch.uint8, device=device)
         count = torch.zeros(1, dtype=torch.int32, device=device)
-        torch.cuda.synchronize()
-        # captured in a CUDA graph as the benchmark times it (the launches keep the
-        # trace buffer they were captured with), then replayed once after a flush
-        moe.trace_enable(buf, count)
-        try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                st.layout_dispatch()
-                st.combine()
-        finally:
-            moe.trace_enable(None, None)
-        count.zero_()
-        flush_l2()
-        graph.replay()
-        torch.cuda.synchronize()
-        moe.check_status(st.status, "traced step")
-        rec = moe.trace_read(buf, count)
-    t0 = int(rec["start_ns"].min())
-    us = lambda ns: round((int(ns) - t0) / 1e3, 2)
+        rec = _traced(moe, lambda: (st.layout_dispatch(), st.combine()), flush_l2, buf, count)
+        n_step = int(count.item())
+        calls = {}
+        for name, fn in (("dispatch", st.dispatch), ("combine", st.combine),
+                         ("dispatch_fp8", lambda: st.dispatch(fp8=True)), ("combine_fp8", st.combine_fp8)):
+            r = _traced(moe, fn, flush_l2, buf, count)
+            span_us = (int(r["end_ns"].max()) - int(r["start_ns"].min())) / 1e3
+            calls[name] = {"span_us": round(span_us, 2), "algorithmic_bytes": ab[name],
+                           "gbs_over_span": round(gbs(ab[name], span_us * 1e-3), 1),
+                           "frac_over_span": round(gbs(ab[name], span_us * 1e-3) / peak, 3),
+                           "kernels": _timeline(moe, r)}
+        moe.check_status(st.status, "traced calls")
     stamps = np.unique(np.concatenate([rec["start_ns"], rec["end_ns"]]))
-    kernels = []
-    for kid in sorted(np.unique(rec["kernel"]), key=lambda k: int(rec["start_ns"][rec["kernel"] == k].min())):
-        r = rec[rec["kernel"] == kid]
-        life = (r["end_ns"] - r["start_ns"]) / 1e3
-        cta_end = np.array([r["end_ns"][r["cta"] == c].max() for c in np.unique(r["cta"])])
-        kernels.append({
-            "kernel": moe.TRACE_KERNELS.get(int(kid), str(int(kid))), "ctas": int(len(cta_end)),
-            "warps_per_cta": int(r["warp"].max()) + 1, "sms": int(len(np.unique(r["sm"]))),
-            "first_start_us": us(r["start_ns"].min()), "last_end_us": us(r["end_ns"].max()),
-            "warp_life_us": {"median": round(float(np.median(life)), 2), "max": round(float(life.max()), 2)},
-            "cta_end_spread_us": {"p10_to_max": round(float(cta_end.max() - np.percentile(cta_end, 10)) / 1e3, 2)},
-        })
-    print(json.dumps({"trace": w.name, "records": int(count.item()),
-                      "step_us": us(rec["end_ns"].max()),
+    print(json.dumps({"trace": w.name, "records": n_step, "recv_rows": N,
+                      "step_us": round((int(rec["end_ns"].max()) - int(rec["start_ns"].min())) / 1e3, 2),
                       "timer_step_ns": int(np.diff(stamps).min()) if len(stamps) > 1 else None,
-                      "kernels": kernels}), flush=True)
+                      "kernels": _timeline(moe, rec), "calls": calls,
+                      "peak": {"gbs": peak, "kind": peak_kind}}), flush=True)
 
 
 # ------------------------------------------------------------------ reference arm (CPU oracle)

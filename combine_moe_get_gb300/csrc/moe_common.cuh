@@ -28,7 +28,8 @@ constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s
 // change a result: L2 prefetches (the combine's first rows, and the address
 // lists they come from, read past L1), and the dispatch's first input-row
 // loads when it is launched right behind this library's own layout, which
-// does not write the input rows. grid_launch_dependents() then lets the next
+// does not write the input rows (a MOE_PROFILE build's trace counter is
+// claimed there too). grid_launch_dependents() then lets the next
 // grid's CTAs be placed as this grid's CTAs retire, so that its launch and
 // prologue (barrier set-up) overlap this grid's tail. Only the dispatch and
 // combine kernels call it: a layout kernel leaves the trigger to its exit,
@@ -105,8 +106,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// ------------------------------------------------------------------ shared-memory addresses
-
 // ------------------------------------------------------------------ tracing (MOE_PROFILE builds)
 
 // Declared first in a kernel: in a MOE_PROFILE build, lane 0 of each warp stamps
@@ -117,13 +116,16 @@ struct WarpTrace {
 #ifdef MOE_PROFILE
     TraceArgs t;
     uint32_t kernel;
-    uint64_t t0 = 0;
+    uint32_t i = 0;      // the record's slot, claimed when the warp starts (the
+    uint64_t t0 = 0;     // atomic's round trip then overlaps the warp's work)
     __device__ __forceinline__ WarpTrace(const TraceArgs &ta, uint32_t k) : t(ta), kernel(k) {
-        if (t.rec != nullptr && (threadIdx.x & 31) == 0) t0 = globaltimer_ns();
+        if (t.rec != nullptr && (threadIdx.x & 31) == 0) {
+            t0 = globaltimer_ns();
+            i = atomicAdd(t.count, 1u);
+        }
     }
     __device__ __forceinline__ ~WarpTrace() {
         if (t.rec == nullptr || (threadIdx.x & 31) != 0) return;
-        const uint32_t i = atomicAdd(t.count, 1u);
         if (i >= (uint32_t)t.cap) return;
         uint32_t sm;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
@@ -140,6 +142,8 @@ struct WarpTrace {
     __device__ __forceinline__ WarpTrace(const TraceArgs &, uint32_t) {}
 #endif
 };
+
+// ------------------------------------------------------------------ shared-memory addresses
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
