@@ -837,7 +837,8 @@ def dataclass_replace_seed(w, seed):
 
 # ------------------------------------------------------------------ one kernel for an ncu capture
 
-PROFILE_KERNELS = ("layout", "dispatch", "combine", "dispatch_fp8", "combine_fp8", "layout_dispatch", "step")
+PROFILE_KERNELS = ("layout", "dispatch", "combine", "dispatch_fp8", "combine_fp8", "layout_dispatch", "expand_layout",
+                   "step")
 
 
 def run_profile(args):
@@ -858,7 +859,7 @@ def run_profile(args):
     st.dispatch(fp8=True)                       # E4M3 rows and scales for the FP8 combine's input
     fn = {"layout": st.layout, "dispatch": st.dispatch, "combine": st.combine,
           "dispatch_fp8": lambda: st.dispatch(fp8=True), "combine_fp8": st.combine_fp8,
-          "layout_dispatch": st.layout_dispatch,
+          "layout_dispatch": st.layout_dispatch, "expand_layout": st.expand_layout,
           "step": lambda: (st.layout_dispatch(), st.combine())}[args.profile_kernel]
     for _ in range(2):
         flush_l2()
