@@ -537,6 +537,41 @@ def test_combine_balanced_parity(moe, T, H, k, E, R):
         np.testing.assert_array_equal(bits16(out), ref)
 
 
+@pytest.mark.parametrize("name", ["dsv3", "skewed"])
+def test_combine_right_behind_a_new_layout(moe, name):
+    # The combine prefetches its first rows into L2 before its dependency wait, from row lists the
+    # previous grid may still be writing. Here that grid is a layout of a different routing writing
+    # the same buffers in place (launched back to back, each allowed to overlap the one before):
+    # every result must still be the oracle's for the routing of the moment.
+    w = wl.CONFIGS[name]
+    E, R, H = w.num_experts, w.num_ranks, w.hidden
+    T, k = w.num_tokens, w.num_topk
+    g = torch.Generator().manual_seed(99)
+    routings = [wl.make_inputs(w, with_partial=False).topk_idx, wl.make_topk_uniform(g, T, E, k),
+                wl.mask_random_lanes(g, wl.make_topk_uniform(g, T, E, k), 0.3)]
+    partial = wl.make_partial(g, wl.recv_capacity(T, k, R), H)
+    pd = partial.to(DEV)
+    lay = moe.Layout.empty(T, k, E, R, DEV)
+    ws = torch.empty(max(16, moe.moe_get_layout_workspace_size(T, E, R)), dtype=torch.uint8, device=DEV)
+    status = moe.new_status(DEV)
+    bal = moe.new_balance_counter(DEV)
+    seq = routings + routings[::-1]
+    topk_d = [t.to(DEV) for t in seq]
+    outs = [torch.empty(T, H, dtype=torch.bfloat16, device=DEV) for _ in seq]
+    torch.cuda.synchronize()
+    for topk, out in zip(topk_d, outs):     # nothing but these kernels on the stream
+        moe.moe_get_layout(topk, E, R, out=lay, workspace=ws, status=status)
+        moe.moe_combine_ex(pd, lay.token_dst_row, out=out, balance=bal, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert bal.tolist() == [0, 0]
+    pbits = bits16(partial)
+    for topk, out in zip(seq, outs):
+        ref, flags = oracle.combine(pbits, oracle.layout(topk.numpy(), E, R)["token_dst_row"])
+        assert flags == 0
+        np.testing.assert_array_equal(bits16(out), ref)
+
+
 def test_combine_weighted_balanced_parity(moe):
     # weighted rows and combined top-k weights with a balance counter: the oracle's results, counter left zero
     w = wl.CONFIGS["dsv3"]
