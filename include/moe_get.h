@@ -422,6 +422,9 @@ typedef struct {
  *             *count (atomically incremented); records at or beyond `capacity`
  *             are dropped, but still counted, so *count after the stream has
  *             synchronised tells how many there were.
+ * Each launch keeps the buffer it was given at launch: a CUDA graph captured
+ * while tracing is on writes to it on every replay, so the buffer and counter
+ * must outlive such a graph.
  * Process-wide setting (all devices, all streams); not for concurrent use
  * with launches on other host threads. MOE_OK in a -DMOE_PROFILE build;
  * MOE_ERR_INVALID_ARG in the default build (nothing is recorded) or for a
