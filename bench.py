@@ -876,13 +876,13 @@ def run_profile(args):
     print(json.dumps({"profile_kernel": args.profile_kernel, "workload": w.name, "recv_rows": N}), flush=True)
 
 
-def _traced(moe, fn, flush_l2, buf, count):
-    """Records of one call of `fn`: captured in a CUDA graph with tracing on
-    (the launches keep the trace buffer they were captured with), then
-    replayed once after an L2 flush, as the benchmark times it."""
+def _traced(moe, fn, flush_l2, buf, count, what):
+    """Records (`what`) of one call of `fn`: captured in a CUDA graph with
+    tracing on (the launches keep the trace buffer they were captured with),
+    then replayed once after an L2 flush, as the benchmark times it."""
     fn()
     torch.cuda.synchronize()
-    moe.trace_enable(buf, count)
+    moe.trace_enable(buf, count, what)
     try:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
@@ -896,24 +896,43 @@ def _traced(moe, fn, flush_l2, buf, count):
     return moe.trace_read(buf, count)
 
 
-def _timeline(moe, rec) -> list:
+def _timeline(moe, rec, rec_phases) -> list:
     """Per kernel, in launch order: CTAs, warps per CTA, SMs, first warp start
-    and last warp end (us from the first warp of `rec`), warp lifetimes and CTA
-    end times."""
-    t0 = int(rec["start_ns"].min())
+    and last warp end (us from the first warp of `rec`), warp lifetimes, CTA
+    end times and, where the kernel records them, its phases from `rec_phases`
+    (a replay recording phases only): median and longest duration over the
+    CTAs, and when the last CTA ended each (us from that replay's first
+    stamp)."""
+    warps, _ = moe.trace_split(rec)
+    _, phases = moe.trace_split(rec_phases)
+    t0 = int(warps["start_ns"].min())
     us = lambda ns: round((int(ns) - t0) / 1e3, 2)
+    p0 = int(phases["start_ns"].min()) if len(phases) else 0
+    pus = lambda ns: round((int(ns) - p0) / 1e3, 2)
     out = []
-    for kid in sorted(np.unique(rec["kernel"]), key=lambda k: int(rec["start_ns"][rec["kernel"] == k].min())):
-        r = rec[rec["kernel"] == kid]
+    for kid in sorted(np.unique(warps["kernel"]), key=lambda k: int(warps["start_ns"][warps["kernel"] == k].min())):
+        r = warps[warps["kernel"] == kid]
         life = (r["end_ns"] - r["start_ns"]) / 1e3
         cta_end = np.array([r["end_ns"][r["cta"] == c].max() for c in np.unique(r["cta"])])
-        out.append({
+        k = {
             "kernel": moe.TRACE_KERNELS.get(int(kid), str(int(kid))), "ctas": int(len(cta_end)),
             "warps_per_cta": int(r["warp"].max()) + 1, "sms": int(len(np.unique(r["sm"]))),
             "first_start_us": us(r["start_ns"].min()), "last_end_us": us(r["end_ns"].max()),
             "warp_life_us": {"median": round(float(np.median(life)), 2), "max": round(float(life.max()), 2)},
             "cta_end_us": {q: us(np.percentile(cta_end, p)) for q, p in (("min", 0), ("p50", 50), ("max", 100))},
-        })
+        }
+        ph = phases[phases["kernel"] == kid]
+        names = moe.TRACE_PHASE_NAMES.get(int(kid), ())
+        if len(ph) and names:
+            k["phases"] = []
+            for i, name in enumerate(names, start=1):
+                q = ph[ph["warp"] == moe.TRACE_PHASE + i]
+                if not len(q):
+                    continue
+                d = (q["end_ns"] - q["start_ns"]) / 1e3
+                k["phases"].append({"phase": name, "median_us": round(float(np.median(d)), 2),
+                                    "max_us": round(float(d.max()), 2), "last_end_us": pus(q["end_ns"].max())})
+        out.append(k)
     return out
 
 
@@ -923,12 +942,14 @@ def run_trace(args):
     balance counter) and the dispatch, combine, quantising dispatch and FP8
     combine called alone, each replayed from a CUDA graph after an L2 flush.
     Per kernel: CTAs, warps per CTA, SMs used, when its first warp started and
-    its last warp ended, how long its warps lived and when its CTAs finished.
+    its last warp ended, how long its warps lived, when its CTAs finished and,
+    for the cluster layout, dispatch and combine, the phases of its CTAs.
     Per lone call also its span (first warp start to last warp end), and its
     algorithmic bytes over the span as a fraction of the measured copy
-    bandwidth. Every warp stamps the global timer twice and claims a slot with
-    one atomic, so these are a timeline; the event-timed figures of the
-    benchmark are the measurement."""
+    bandwidth. The warps' records come from one replay and the phases from
+    another that records nothing else (a warp record costs its warp an
+    atomic, which slows the layout). These are a timeline; the event-timed
+    figures of the benchmark are the measurement."""
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     from combine_moe_get_gb300 import binding as moe
@@ -949,23 +970,26 @@ def run_trace(args):
         ab = algorithmic_bytes(w.num_tokens, w.hidden, N, 0)
         buf = torch.zeros((1 << 20) * moe.TRACE_RECORD.itemsize, dtype=torch.uint8, device=device)
         count = torch.zeros(1, dtype=torch.int32, device=device)
-        rec = _traced(moe, lambda: (st.layout_dispatch(), st.combine()), flush_l2, buf, count)
+        step = lambda: (st.layout_dispatch(), st.combine())
+        rec = _traced(moe, step, flush_l2, buf, count, moe.TRACE_WARPS)
         n_step = int(count.item())
+        rec_ph = _traced(moe, step, flush_l2, buf, count, moe.TRACE_PHASES)
         calls = {}
         for name, fn in (("dispatch", st.dispatch), ("combine", st.combine),
                          ("dispatch_fp8", lambda: st.dispatch(fp8=True)), ("combine_fp8", st.combine_fp8)):
-            r = _traced(moe, fn, flush_l2, buf, count)
+            r = _traced(moe, fn, flush_l2, buf, count, moe.TRACE_WARPS)
+            r_ph = _traced(moe, fn, flush_l2, buf, count, moe.TRACE_PHASES)
             span_us = (int(r["end_ns"].max()) - int(r["start_ns"].min())) / 1e3
             calls[name] = {"span_us": round(span_us, 2), "algorithmic_bytes": ab[name],
                            "gbs_over_span": round(gbs(ab[name], span_us * 1e-3), 1),
                            "frac_over_span": round(gbs(ab[name], span_us * 1e-3) / peak, 3),
-                           "kernels": _timeline(moe, r)}
+                           "kernels": _timeline(moe, r, r_ph)}
         moe.check_status(st.status, "traced calls")
     stamps = np.unique(np.concatenate([rec["start_ns"], rec["end_ns"]]))
     print(json.dumps({"trace": w.name, "records": n_step, "recv_rows": N,
                       "step_us": round((int(rec["end_ns"].max()) - int(rec["start_ns"].min())) / 1e3, 2),
                       "timer_step_ns": int(np.diff(stamps).min()) if len(stamps) > 1 else None,
-                      "kernels": _timeline(moe, rec), "calls": calls,
+                      "kernels": _timeline(moe, rec, rec_ph), "calls": calls,
                       "peak": {"gbs": peak, "kind": peak_kind}}), flush=True)
 
 

@@ -72,7 +72,7 @@ def load_library(path: str):
 
 def _configure(lib):
     lib.moe_get_version.restype = _I
-    lib.moe_trace_enable.argtypes = [_P, _I, _P]
+    lib.moe_trace_enable.argtypes = [_P, _I, _P, _I]
     lib.moe_trace_enable.restype = _I
     lib.moe_status_string.argtypes = [_I]
     lib.moe_status_string.restype = ctypes.c_char_p
@@ -127,23 +127,41 @@ TRACE_RECORD = np.dtype([("kernel", "<u4"), ("cta", "<u4"), ("warp", "<u4"), ("s
 TRACE_KERNELS = {1: "layout_tiles", 2: "layout_direct", 3: "layout_cluster", 4: "layout_count", 5: "layout_scan",
                  6: "layout_rows_scan", 7: "expand_layout", 8: "expand_layout_cluster", 9: "dispatch",
                  10: "dispatch_fp8_rows", 11: "combine", 12: "layout_rows"}
+TRACE_PHASE = 0x10000   # warp field of a per-CTA phase record: TRACE_PHASE + phase (1, 2, ...)
+TRACE_PHASE_NAMES = {3: ("dependency wait", "top-k tile loaded", "bitmap and expert histogram",
+                         "tile counts and first cluster barrier", "exchange and second barrier",
+                         "prefixes and count writes", "receive rows", "is_token_in_rank rows"),
+                     9: ("set-up (behind the layout: first loads, L2 prefetch)", "dependency wait", "the rest"),
+                     10: ("set-up", "dependency wait", "the rest"),
+                     11: ("set-up", "dependency wait", "the rest")}
 
 
-def trace_enable(records: Optional[torch.Tensor], count: Optional[torch.Tensor]) -> None:
-    """Send the warps' records of later launches to `records` (a CUDA uint8 tensor
-    of n * TRACE_RECORD.itemsize bytes) and count them in `count` (a zeroed CUDA
+TRACE_WARPS, TRACE_PHASES = 1, 2
+
+
+def trace_enable(records: Optional[torch.Tensor], count: Optional[torch.Tensor],
+                 what: int = TRACE_WARPS | TRACE_PHASES) -> None:
+    """Send the records of later launches (`what`: TRACE_WARPS, a record per
+    warp; TRACE_PHASES, per-CTA phases) to `records` (a CUDA uint8 tensor of
+    n * TRACE_RECORD.itemsize bytes) and count them in `count` (a zeroed CUDA
     int32 tensor of one element); None stops. Needs a build with MOE_PROFILE."""
     if records is None:
-        _check(LIB.moe_trace_enable(None, 0, None), "moe_trace_enable")
+        _check(LIB.moe_trace_enable(None, 0, None, 0), "moe_trace_enable")
         return
     cap = records.numel() // TRACE_RECORD.itemsize
-    _check(LIB.moe_trace_enable(_ptr(records), cap, _ptr(count)), "moe_trace_enable")
+    _check(LIB.moe_trace_enable(_ptr(records), cap, _ptr(count), int(what)), "moe_trace_enable")
 
 
 def trace_read(records: torch.Tensor, count: torch.Tensor) -> np.ndarray:
     """The records written so far (after the stream has synchronised)."""
     n = min(int(count.item()), records.numel() // TRACE_RECORD.itemsize)
     return records[: n * TRACE_RECORD.itemsize].cpu().numpy().view(TRACE_RECORD)
+
+
+def trace_split(rec: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """(per-warp records, per-CTA phase records) of trace_read's result."""
+    phase = rec["warp"] >= TRACE_PHASE
+    return rec[~phase], rec[phase]
 
 
 def status_string(code: int) -> str:

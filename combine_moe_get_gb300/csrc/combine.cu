@@ -164,6 +164,7 @@ __device__ __forceinline__ uint4 lds128(const uint8_t *p) {
 template <bool kWeighted, bool kFP8>
 __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(const CombineArgs a) {
     WarpTrace wt(a.trace, MOE_TRACE_COMBINE);
+    MOE_PHASES(MOE_TRACE_COMBINE, 3);
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kUnits;
@@ -207,7 +208,9 @@ __global__ void __launch_bounds__(kFP8 ? 32 * 13 : 32 * 9, 1) combine_kernel(con
             done += (int64_t)__popc(m) * a.row_bytes;
         }
     }
+    MOE_PHASE(1);
     grid_dependency_wait();
+    MOE_PHASE(2);
     grid_launch_dependents();
 
     if (warp == 0) {

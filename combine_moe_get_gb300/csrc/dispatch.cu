@@ -384,6 +384,7 @@ __device__ void fused_layout(const DispatchArgs &a, uint8_t *region) {
 template <bool kFP8, bool kFused>
 __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) {
     WarpTrace wt(a.trace, MOE_TRACE_DISPATCH);
+    MOE_PHASES(MOE_TRACE_DISPATCH, 3);
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int warps = blockDim.x >> 5;
@@ -400,12 +401,18 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
     // warp whose units had fewer destinations takes more of them.
     __shared__ int s_next_unit;
     __shared__ int s_retired;   // warps of this CTA that claim no more
+    __shared__ int s_pf_warps;  // warps whose share of the L2 prefetches is issued
     if (threadIdx.x == 0) {
         s_next_unit = 0;
         s_retired = 0;
+        s_pf_warps = 0;
     }
     __syncthreads();
-    if (!a.loads_before_wait) grid_dependency_wait();
+    if (!a.loads_before_wait) {
+        MOE_PHASE(1);
+        grid_dependency_wait();
+        MOE_PHASE(2);
+    }
     const int64_t G = gridDim.x;
     const int64_t dealt = a.pool ? a.static_units : a.num_units;
     const int64_t cta_units = dealt > (int64_t)blockIdx.x ? (dealt - 1 - blockIdx.x) / G + 1 : 0;
@@ -458,6 +465,7 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         }
     }
     __syncwarp();
+    bool pf_pending = false;   // the CTA's L2 prefetches may still be being issued
     // Bring the rows of this CTA's next units into L2 as well, all at once (the
     // input rows are complete here: after the dependency wait, or, launched
     // right behind this library's layout whose outputs are read only after the
@@ -478,10 +486,23 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
         }
         // every prefetch of the CTA is issued before any of its warps claims a unit
         // past its stages (a prefetch landing after the unit's own load would keep
-        // its lines evict-last)
+        // its lines evict-last): each warp counts itself in, and a warp waits for
+        // the count at its first claim instead of at a CTA barrier here, so the
+        // warps start on their stage loads while the prefetches are still being
+        // accepted by the copy engine (which takes them at the memory's pace)
+#if MOE_TUNE_DISPATCH_PREFETCH_NOSYNC
+        __syncwarp();
+        if (lane == 0) atomicAdd(&s_pf_warps, 1);
+        pf_pending = true;
+#else
         __syncthreads();
+#endif
     }
-    if (a.loads_before_wait) grid_dependency_wait();
+    if (a.loads_before_wait) {
+        MOE_PHASE(1);
+        grid_dependency_wait();
+        MOE_PHASE(2);
+    }
     grid_launch_dependents();
 
     // fused launch: the layout, computed while the first loads are in flight
@@ -650,6 +671,12 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
             // the stage stored one unit ago is free once its bulk stores have read it;
             // it takes the next unit claimed by this warp
             if (i >= 1) {
+                if (pf_pending) {   // bounded: the other warps only issue their prefetches
+                    const uint64_t until = globaltimer_ns() + a.timeout_ns;
+                    while (*reinterpret_cast<volatile int *>(&s_pf_warps) < warps && globaltimer_ns() < until)
+                        __nanosleep(64);
+                    pf_pending = false;
+                }
                 const int sp = s == 0 ? S - 1 : s - 1;
                 const int64_t un = claim();
                 ring[sp] = un;
@@ -728,6 +755,7 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t *bar) {
 template <bool kPool>
 __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     WarpTrace wt(a.trace, MOE_TRACE_DISPATCH_FP8_ROWS);
+    MOE_PHASES(MOE_TRACE_DISPATCH_FP8_ROWS, 3);
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *in_full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *in_empty = in_full + kFp8MaxSlots;
@@ -759,7 +787,9 @@ __global__ void __maxnreg__(80) dispatch_fp8_rows_kernel(const Fp8Args a) {
     // launched right behind this library's layout, the input rows were complete
     // before this grid could launch: the producer, which reads nothing else,
     // starts at once; the workers read the layout's outputs and wait
+    MOE_PHASE(1);
     if (!(a.loads_before_wait && warp == 0)) grid_dependency_wait();
+    MOE_PHASE(2);
     grid_launch_dependents();
     if (!kPool && n <= 0) return;
 

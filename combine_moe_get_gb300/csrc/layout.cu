@@ -714,6 +714,7 @@ __device__ __forceinline__ int32_t ld_cluster_i32(const void *local, uint32_t ra
 
 __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
     WarpTrace wt(a.trace, MOE_TRACE_LAYOUT_CLUSTER);
+    MOE_PHASES(MOE_TRACE_LAYOUT_CLUSTER, 8);
     extern __shared__ __align__(16) uint8_t smem[];
     const int R = a.R, E = a.E, k = a.k, tile = a.cl_tile, W = tile / 32;
     const ClusterSmem sl = cluster_smem(tile, E, R, k);
@@ -734,6 +735,7 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
     const int n_ent = tcount * k;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     grid_dependency_wait();
+    MOE_PHASE(1);
     if (a.early_dependents) grid_launch_dependents();
     if (c == 0 && threadIdx.x == 0 && a.spare != nullptr) {   // the workspace is not cleared in this mode
         a.spare[0] = 0u;
@@ -764,6 +766,7 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
         }
     }
     __syncthreads();
+    MOE_PHASE(2);
 
     // ---- pass 1: expert histogram, each rank of a token once (the lowest entry
     //      owns it), membership bits; ent[] becomes the owned rank (or -1)
@@ -808,6 +811,7 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
         }
     }
     __syncthreads();
+    MOE_PHASE(3);
 
     // ---- this tile's rank counts and word prefixes
     for (int r = threadIdx.x; r < R; r += kCThreads) {
@@ -822,6 +826,7 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
     // ---- exchange through distributed shared memory: every tile's counts are
     //      complete after the first barrier and read before the second
     cluster_sync_all();
+    MOE_PHASE(4);
     for (int idx = threadIdx.x; idx < C * R; idx += kCThreads) {
         const int cc = idx / R, r = idx - cc * R;
         const int32_t v = ld_cluster_i32(cnt + r, (uint32_t)cc);
@@ -840,6 +845,7 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
         }
     }
     cluster_sync_all();   // no tile reads another's shared memory after this
+    MOE_PHASE(5);
 
     // ---- rank regions (warp 0) and, on tile 0, expert counts and prefix (warp 1)
     if (warp == 0) {
@@ -862,6 +868,7 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
     if (c == 0 && threadIdx.x == 0) a.rank_prefix[R] = tot[R];
     __syncthreads();
 
+    MOE_PHASE(6);
     // ---- pass 2: global receive rows of the owning entries
     for (int i = threadIdx.x; i < n_ent; i += kCThreads) {
         const int r = ent[i];
@@ -874,6 +881,7 @@ __global__ void __launch_bounds__(kCThreads) layout_cluster_kernel(TileArgs a) {
         a.token_dst_row[(int64_t)t0 * k + i] = v;
     }
 
+    MOE_PHASE(7);
     // ---- is_token_in_rank rows: one warp per token row when rows are long, flat otherwise
     uint8_t *dst = a.is_token_in_rank + (int64_t)t0 * R;
     if ((R & 3) == 0 && R >= 128) {

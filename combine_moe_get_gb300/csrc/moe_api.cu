@@ -103,12 +103,13 @@ namespace {
 std::atomic<moe_trace_record_t *> g_trace_rec{nullptr};
 std::atomic<uint32_t *> g_trace_count{nullptr};
 std::atomic<int> g_trace_cap{0};
+std::atomic<int> g_trace_what{0};
 }  // namespace
 
 TraceArgs trace_args() {
     TraceArgs t{g_trace_rec.load(std::memory_order_acquire), g_trace_count.load(std::memory_order_acquire),
-                g_trace_cap.load(std::memory_order_acquire)};
-    if (t.rec == nullptr || t.count == nullptr) t = TraceArgs{nullptr, nullptr, 0};
+                g_trace_cap.load(std::memory_order_acquire), g_trace_what.load(std::memory_order_acquire)};
+    if (t.rec == nullptr || t.count == nullptr || t.what == 0) t = TraceArgs{nullptr, nullptr, 0, 0};
     return t;
 }
 
@@ -222,10 +223,12 @@ extern "C" {
 
 MOE_API int moe_get_version(void) { return 100; }
 
-MOE_API int moe_trace_enable(moe_trace_record_t *records, int capacity, uint32_t *count) {
+MOE_API int moe_trace_enable(moe_trace_record_t *records, int capacity, uint32_t *count, int what) {
 #ifdef MOE_PROFILE
-    if (records != nullptr && (capacity < 0 || count == nullptr || !aligned(records, 8) || !aligned(count, 4)))
+    if (records != nullptr && (capacity < 0 || count == nullptr || !aligned(records, 8) || !aligned(count, 4) ||
+                               what == 0 || (what & ~(MOE_TRACE_WARPS | MOE_TRACE_PHASES)) != 0))
         return MOE_ERR_INVALID_ARG;
+    moe::g_trace_what.store(records ? what : 0, std::memory_order_release);
     moe::g_trace_cap.store(records ? capacity : 0, std::memory_order_release);
     moe::g_trace_count.store(records ? count : nullptr, std::memory_order_release);
     moe::g_trace_rec.store(records, std::memory_order_release);
@@ -234,6 +237,7 @@ MOE_API int moe_trace_enable(moe_trace_record_t *records, int capacity, uint32_t
     (void)records;
     (void)capacity;
     (void)count;
+    (void)what;
     return MOE_ERR_INVALID_ARG;   // a build without MOE_PROFILE records nothing
 #endif
 }

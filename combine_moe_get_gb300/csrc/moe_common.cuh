@@ -119,6 +119,7 @@ struct WarpTrace {
     uint32_t i = 0;      // the record's slot, claimed when the warp starts (the
     uint64_t t0 = 0;     // atomic's round trip then overlaps the warp's work)
     __device__ __forceinline__ WarpTrace(const TraceArgs &ta, uint32_t k) : t(ta), kernel(k) {
+        if (!(t.what & MOE_TRACE_WARPS)) t.rec = nullptr;
         if (t.rec != nullptr && (threadIdx.x & 31) == 0) {
             t0 = globaltimer_ns();
             i = atomicAdd(t.count, 1u);
@@ -142,6 +143,62 @@ struct WarpTrace {
     __device__ __forceinline__ WarpTrace(const TraceArgs &, uint32_t) {}
 #endif
 };
+
+// Per-CTA phase records (MOE_PROFILE builds): MOE_PHASES(kernel, n), declared
+// after the WarpTrace of a kernel whose arguments are `a`, makes thread 0 stamp
+// the global timer at the kernel's start and claim n record slots at once;
+// MOE_PHASE(p) (1 <= p < n) ends phase p; thread 0's exit ends phase n. At
+// exit thread 0 writes the n phase intervals. In the default build both
+// macros are empty.
+#ifdef MOE_PROFILE
+constexpr int kMaxPhases = 8;
+struct CtaPhases {
+    TraceArgs t;
+    uint32_t kernel, n, base = 0;
+    uint64_t *v;   // v[0]: start; v[p]: end of phase p (0: not reached)
+    __device__ __forceinline__ CtaPhases(const TraceArgs &ta, uint32_t k, uint32_t np, uint64_t *sv)
+        : t(ta), kernel(k), n(np), v(sv) {
+        if (!(t.what & MOE_TRACE_PHASES)) t.rec = nullptr;
+        if (t.rec != nullptr && threadIdx.x == 0) {
+            v[0] = globaltimer_ns();
+            for (uint32_t i = 1; i <= n; ++i) v[i] = 0;
+            base = atomicAdd(t.count, n);
+        }
+    }
+    __device__ __forceinline__ void mark(uint32_t p) {
+        if (t.rec != nullptr && threadIdx.x == 0 && p < n) v[p] = globaltimer_ns();
+    }
+    __device__ __forceinline__ ~CtaPhases() {
+        if (t.rec == nullptr || threadIdx.x != 0) return;
+        v[n] = globaltimer_ns();
+        uint32_t sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        uint64_t prev = v[0];
+        for (uint32_t p = 1; p <= n; ++p) {
+            const uint64_t end = v[p] != 0 ? v[p] : prev;   // a phase not reached lasts 0 ns
+            if (base + p - 1 < (uint32_t)t.cap) {
+                moe_trace_record_t r;
+                r.kernel = kernel;
+                r.cta = blockIdx.x;
+                r.warp = MOE_TRACE_PHASE + p;
+                r.sm = sm;
+                r.start_ns = prev;
+                r.end_ns = end;
+                t.rec[base + p - 1] = r;
+            }
+            prev = end;
+        }
+    }
+};
+#define MOE_PHASES(kernel_id, nphases)                                                          \
+    static_assert((nphases) >= 1 && (nphases) <= kMaxPhases, "phase count");                   \
+    __shared__ uint64_t moe_phase_stamps_[kMaxPhases + 1];                                       \
+    CtaPhases moe_phases_(a.trace, (kernel_id), (nphases), moe_phase_stamps_)
+#define MOE_PHASE(p) moe_phases_.mark(p)
+#else
+#define MOE_PHASES(kernel_id, nphases) static_assert((nphases) >= 1, "phase count")
+#define MOE_PHASE(p) ((void)0)
+#endif
 
 // ------------------------------------------------------------------ shared-memory addresses
 

@@ -26,6 +26,7 @@ struct TraceArgs {
     moe_trace_record_t *rec;
     uint32_t *count;
     int cap;
+    int what;   // MOE_TRACE_WARPS | MOE_TRACE_PHASES
 };
 TraceArgs trace_args();
 
@@ -119,6 +120,9 @@ TraceArgs trace_args();
 #endif
 #ifndef MOE_TUNE_DISPATCH_PREFETCH_L2_PCT
 #define MOE_TUNE_DISPATCH_PREFETCH_L2_PCT 25
+#endif
+#ifndef MOE_TUNE_DISPATCH_PREFETCH_NOSYNC
+#define MOE_TUNE_DISPATCH_PREFETCH_NOSYNC 1
 #endif
 #ifndef MOE_TUNE_DISPATCH_PREFETCH_KEEP
 #define MOE_TUNE_DISPATCH_PREFETCH_KEEP 1

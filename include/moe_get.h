@@ -386,9 +386,26 @@ MOE_API int moe_combine_fp8_ex(const void *partial_codes, const float *partial_s
  * equivalent for these kernels. In a library compiled with -DMOE_PROFILE
  * (libmoe_get_trace.so, built beside libmoe_get.so), once moe_trace_enable has
  * been given a buffer, every warp of every kernel launched afterwards appends
- * one moe_trace_record_t when it returns: which kernel, CTA and warp, the SM it
- * ran on, and %globaltimer (ns) when the warp began and when it returned. The
- * default build compiles all of it out (no cost, no argument).
+ * one moe_trace_record_t when it returns (MOE_TRACE_WARPS): which kernel, CTA
+ * and warp, the SM it ran on, and %globaltimer (ns) when the warp began and
+ * when it returned. Thread 0 of each CTA of the cluster layout, dispatch and
+ * combine kernels appends one record per phase of its own path
+ * (MOE_TRACE_PHASES; warp field MOE_TRACE_PHASE + phase number, start and end
+ * of the phase), listed below.
+ * The default build compiles all of it out (no cost, no argument).
+ *
+ * Phases (thread 0's view; each ends where the next begins):
+ *   MOE_TRACE_LAYOUT_CLUSTER  1 dependency wait, 2 top-k tile loaded, 3 bitmap
+ *                             and expert histogram, 4 tile counts and first
+ *                             cluster barrier, 5 exchange and second barrier,
+ *                             6 prefixes and count writes, 7 receive rows,
+ *                             8 is_token_in_rank rows (to thread 0's exit)
+ *   MOE_TRACE_DISPATCH        1 set-up (launched behind this library's
+ *                             layout: with the first loads and the input
+ *                             rows' L2 prefetch), 2 dependency wait, 3 the
+ *                             rest (to thread 0's exit)
+ *   MOE_TRACE_DISPATCH_FP8_ROWS, MOE_TRACE_COMBINE
+ *                             1 set-up, 2 dependency wait, 3 the rest
  */
 enum {
     MOE_TRACE_LAYOUT_TILES = 1,        /* lookback tiles (cooperative or ticket) */
@@ -402,13 +419,17 @@ enum {
     MOE_TRACE_DISPATCH = 9,            /* relay pipeline (bf16, E4M3 rows, chunked E4M3, fused small batches) */
     MOE_TRACE_DISPATCH_FP8_ROWS = 10,  /* quantising row pipeline */
     MOE_TRACE_COMBINE = 11,
-    MOE_TRACE_LAYOUT_ROWS = 12         /* lookback tiles launched one after another: rows */
+    MOE_TRACE_LAYOUT_ROWS = 12,        /* lookback tiles launched one after another: rows */
+    MOE_TRACE_PHASE = 0x10000          /* warp field of a per-CTA phase record: MOE_TRACE_PHASE + phase */
 };
+
+/* what moe_trace_enable records (bits) */
+enum { MOE_TRACE_WARPS = 1, MOE_TRACE_PHASES = 2 };
 
 typedef struct {
     uint32_t kernel;     /* MOE_TRACE_* */
     uint32_t cta;        /* blockIdx.x */
-    uint32_t warp;       /* warp index in the CTA */
+    uint32_t warp;       /* warp index in the CTA, or MOE_TRACE_PHASE + phase */
     uint32_t sm;         /* SM the CTA ran on */
     uint64_t start_ns;   /* global timer when the warp began */
     uint64_t end_ns;     /* global timer when it returned */
@@ -418,8 +439,13 @@ typedef struct {
  * moe_trace_enable -- where the warps' records go, for the launches that follow.
  *
  *   records   device array of `capacity` records, or NULL to stop tracing.
+ *   what      MOE_TRACE_WARPS (a record per warp), MOE_TRACE_PHASES (the
+ *             per-CTA phase records) or both. Each warp record costs its warp
+ *             one atomic at its start, which slows the latency-bound layout
+ *             noticeably; phases alone cost one atomic per CTA.
  *   count     device uint32, zeroed by the caller: each record claims the slot
- *             *count (atomically incremented); records at or beyond `capacity`
+ *             *count (atomically incremented; a CTA's phase records claim
+ *             consecutive slots at once); records at or beyond `capacity`
  *             are dropped, but still counted, so *count after the stream has
  *             synchronised tells how many there were.
  * Each launch keeps the buffer it was given at launch: a CUDA graph captured
@@ -427,10 +453,11 @@ typedef struct {
  * must outlive such a graph.
  * Process-wide setting (all devices, all streams); not for concurrent use
  * with launches on other host threads. MOE_OK in a -DMOE_PROFILE build;
- * MOE_ERR_INVALID_ARG in the default build (nothing is recorded) or for a
- * negative capacity, a null or misaligned count with non-null records.
+ * MOE_ERR_INVALID_ARG in the default build (nothing is recorded) or, with
+ * non-null records, for a negative capacity, a null or misaligned count, or
+ * `what` empty or with other bits.
  */
-MOE_API int moe_trace_enable(moe_trace_record_t *records, int capacity, uint32_t *count);
+MOE_API int moe_trace_enable(moe_trace_record_t *records, int capacity, uint32_t *count, int what);
 
 /* Size of the library's own layout scratch (bytes), used by moe_get_layout_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)

@@ -233,7 +233,7 @@ def test_layout_ex_rejects_unknown_mode(lib):
 
 def test_default_build_records_no_trace(lib):
     # only a build compiled with MOE_PROFILE records; the default one refuses, enabling or not
-    assert lib.LIB.moe_trace_enable(None, 0, None) == lib.MOE_ERR_INVALID_ARG
+    assert lib.LIB.moe_trace_enable(None, 0, None, 0) == lib.MOE_ERR_INVALID_ARG
 
 
 def test_trace_build_exports_the_same_abi(lib):
@@ -244,10 +244,13 @@ def test_trace_build_exports_the_same_abi(lib):
         assert hasattr(raw, name), f"{name} missing from the tracing build"
     tl = lib.load_library(path)
     assert tl.moe_get_version() == lib.LIB.moe_get_version()
-    assert tl.moe_trace_enable(None, 0, None) == lib.MOE_OK              # stop: accepted with no buffer
+    assert tl.moe_trace_enable(None, 0, None, 0) == lib.MOE_OK           # stop: accepted with no buffer
     bad = ctypes.c_void_p(8)
-    assert tl.moe_trace_enable(bad, 4, None) == lib.MOE_ERR_INVALID_ARG  # a buffer needs a counter
-    assert tl.moe_trace_enable(bad, -1, bad) == lib.MOE_ERR_INVALID_ARG
+    assert tl.moe_trace_enable(bad, 4, None, 3) == lib.MOE_ERR_INVALID_ARG  # a buffer needs a counter
+    assert tl.moe_trace_enable(bad, -1, bad, 3) == lib.MOE_ERR_INVALID_ARG
+    assert tl.moe_trace_enable(bad, 4, bad, 0) == lib.MOE_ERR_INVALID_ARG   # nothing to record
+    assert tl.moe_trace_enable(bad, 4, bad, 4) == lib.MOE_ERR_INVALID_ARG   # unknown bit
+    assert tl.moe_trace_enable(None, 0, None, 0) == lib.MOE_OK
 
 
 def test_trace_record_layout_matches_header(lib):
@@ -257,5 +260,8 @@ def test_trace_record_layout_matches_header(lib):
     np_code = {"uint32_t": "<u4", "uint64_t": "<u8"}
     assert [(n, np_code[t]) for t, n in fields] == [(n, lib.TRACE_RECORD[n].str) for n in lib.TRACE_RECORD.names]
     assert lib.TRACE_RECORD.itemsize == 32
-    kinds = dict((int(v), k) for k, v in re.findall(r"\b(MOE_TRACE_\w+)\s*=\s*(\d+)", text))
-    assert sorted(kinds) == sorted(lib.TRACE_KERNELS)
+    named = {k: int(v, 0) for k, v in re.findall(r"\b(MOE_TRACE_\w+)\s*=\s*(0x[0-9a-fA-F]+|\d+)", text)}
+    assert named.pop("MOE_TRACE_PHASE") == lib.TRACE_PHASE
+    assert (named.pop("MOE_TRACE_WARPS"), named.pop("MOE_TRACE_PHASES")) == (lib.TRACE_WARPS, lib.TRACE_PHASES)
+    assert sorted(named.values()) == sorted(lib.TRACE_KERNELS)
+    assert set(lib.TRACE_PHASE_NAMES) <= set(lib.TRACE_KERNELS)

@@ -2,9 +2,11 @@
 
 Every warp of every launch leaves exactly one timer record (one per CTA index
 and warp index, the same warp count in every CTA, all warps of a CTA on one
-SM, start <= end); a dependent launch never starts before the launch it
-follows; records past the buffer are counted, not written; stopping stops
-them; and tracing changes no result: the outputs are the oracle's.
+SM, start <= end); the cluster layout, dispatch and combine kernels add one
+record per phase per CTA, contiguous and inside the lifetime of the CTA's
+warp 0; a dependent launch never starts before the launch it follows;
+records past the buffer are counted, not written; stopping stops them; and
+tracing changes no result: the outputs are the oracle's.
 """
 from __future__ import annotations
 
@@ -41,13 +43,14 @@ def bits16(t: torch.Tensor) -> np.ndarray:
 class Trace:
     """Records of the launches made inside the block."""
 
-    def __init__(self, moe, capacity=1 << 20):
+    def __init__(self, moe, capacity=1 << 20, what=None):
         self.moe = moe
+        self.what = moe.TRACE_WARPS | moe.TRACE_PHASES if what is None else what
         self.buf = torch.zeros(capacity * moe.TRACE_RECORD.itemsize, dtype=torch.uint8, device=DEV)
         self.count = torch.zeros(1, dtype=torch.int32, device=DEV)
 
     def __enter__(self):
-        self.moe.trace_enable(self.buf, self.count)
+        self.moe.trace_enable(self.buf, self.count, self.what)
         return self
 
     def __exit__(self, *exc):
@@ -75,7 +78,28 @@ def check_launch(r: np.ndarray) -> tuple[int, int]:
 
 
 def by_kernel(r: np.ndarray) -> dict:
+    """Per kernel id, its per-warp records (phase records left out)."""
+    r = r[r["warp"] < 0x10000]
     return {int(k): r[r["kernel"] == k] for k in np.unique(r["kernel"])}
+
+
+def check_phases(moe, rec: np.ndarray, kernel: int, ctas: int):
+    """The kernel's phase records: every phase of every CTA once, each CTA's
+    phases contiguous, on the SM of its warps and inside its warp 0's life."""
+    warps, phases = moe.trace_split(rec[rec["kernel"] == kernel])
+    n = len(moe.TRACE_PHASE_NAMES[kernel])
+    assert len(phases) == ctas * n
+    for c in range(ctas):
+        p = phases[phases["cta"] == c]
+        p = p[np.argsort(p["warp"])]
+        assert p["warp"].tolist() == [moe.TRACE_PHASE + i for i in range(1, n + 1)]
+        assert np.all(p["start_ns"] <= p["end_ns"])
+        assert np.array_equal(p["start_ns"][1:], p["end_ns"][:-1])
+        w0 = warps[(warps["cta"] == c) & (warps["warp"] == 0)]
+        assert len(w0) == 1
+        assert w0["start_ns"][0] <= p["start_ns"][0] and p["end_ns"][-1] <= w0["end_ns"][0]
+        assert np.all(p["sm"] == w0["sm"][0])
+    return phases
 
 
 def test_trace_dsv3_step(moe):
@@ -101,8 +125,12 @@ def test_trace_dsv3_step(moe):
         assert int(tr.count.item()) == len(rec)
         kinds = by_kernel(rec)
         assert set(kinds) <= expect and kinds, (name, set(kinds))
-        for r in kinds.values():
-            check_launch(r)
+        for kid, r in kinds.items():
+            ctas, _ = check_launch(r)
+            if kid in moe.TRACE_PHASE_NAMES:
+                check_phases(moe, rec, kid, ctas)
+            else:
+                assert not np.any((rec["kernel"] == kid) & (rec["warp"] >= moe.TRACE_PHASE))
         ids[name] = set(kinds)
     assert int(status.item()) == 0
 
@@ -143,10 +171,12 @@ def test_trace_quantising_dispatch(moe, name):
     with Trace(moe) as tr:
         out = moe.moe_dispatch(inp.x.to(DEV), topk, None, E, R, lay.token_dst_row, wl.recv_capacity(T, k, R),
                                quantize_fp8=True, status=status)
-    kinds = by_kernel(tr.records())
+    rec = tr.records()
+    kinds = by_kernel(rec)
     assert set(kinds) <= DISPATCH_IDS and kinds
-    for r in kinds.values():
-        check_launch(r)
+    for kid, r in kinds.items():
+        ctas, _ = check_launch(r)
+        check_phases(moe, rec, kid, ctas)
     assert int(status.item()) == 0
     ref_lay = oracle.layout(inp.topk_idx.numpy(), E, R)
     N = ref_lay["num_recv"]
@@ -212,10 +242,56 @@ def test_trace_overflow_and_stop(moe):
     assert n > 4
     assert np.all(buf[4 * size:].cpu().numpy() == 0xAB)
     rec = moe.trace_read(buf[: 4 * size], count)
-    assert len(rec) == 4 and set(np.unique(rec["kernel"]).tolist()) <= LAYOUT_IDS | COMBINE_IDS
+    assert len(rec) == 4 and set(np.unique(rec["kernel"]).tolist()) <= LAYOUT_IDS | COMBINE_IDS | {9}
     moe.moe_combine(inp.partial.to(DEV), lay.token_dst_row, out=out, status=status)
     torch.cuda.synchronize()
     assert int(count.item()) == n
     assert int(status.item()) == 0
     ref_c, _ = oracle.combine(bits16(inp.partial), oracle.layout(inp.topk_idx.numpy(), E, R)["token_dst_row"])
     np.testing.assert_array_equal(bits16(out), ref_c)
+
+
+def test_trace_warps_or_phases_alone(moe):
+    # what = warps only: no phase record; phases only: exactly the phase records, nothing else
+    w = wl.CONFIGS["dsv3"]
+    inp = wl.make_inputs(w)
+    E, R = w.num_experts, w.num_ranks
+    T, k = inp.topk_idx.shape
+    topk, x, pd = inp.topk_idx.to(DEV), inp.x.to(DEV), inp.partial.to(DEV)
+    status = moe.new_status(DEV)
+
+    def step():
+        lay = moe.moe_get_layout(topk, E, R, status=status)
+        out = moe.moe_dispatch(x, topk, None, E, R, lay.token_dst_row, wl.recv_capacity(T, k, R), status=status)
+        comb = moe.moe_combine(pd, lay.token_dst_row, status=status)
+        return lay, out, comb
+
+    step()
+    torch.cuda.synchronize()
+    with Trace(moe, what=moe.TRACE_WARPS) as tr:
+        step()
+    full = tr.records()
+    warps, phases = moe.trace_split(full)
+    assert len(phases) == 0 and len(warps) == len(full) > 0
+    shapes = {kid: check_launch(r) for kid, r in by_kernel(full).items()}
+    with Trace(moe, what=moe.TRACE_PHASES) as tr:
+        lay, out, comb = step()
+    rec = tr.records()
+    warps, phases = moe.trace_split(rec)
+    assert len(warps) == 0
+    expect = sum(ctas * len(moe.TRACE_PHASE_NAMES[kid]) for kid, (ctas, _) in shapes.items()
+                 if kid in moe.TRACE_PHASE_NAMES)
+    assert len(phases) == int(tr.count.item()) == expect
+    for kid in set(np.unique(phases["kernel"]).tolist()):
+        ph = phases[phases["kernel"] == kid]
+        n = len(moe.TRACE_PHASE_NAMES[kid])
+        for c in np.unique(ph["cta"]):
+            p = ph[ph["cta"] == c]
+            p = p[np.argsort(p["warp"])]
+            assert p["warp"].tolist() == [moe.TRACE_PHASE + i for i in range(1, n + 1)]
+            assert np.array_equal(p["start_ns"][1:], p["end_ns"][:-1]) and np.all(p["start_ns"] <= p["end_ns"])
+    assert int(status.item()) == 0
+    ref_lay = oracle.layout(inp.topk_idx.numpy(), E, R)
+    ref_c, _ = oracle.combine(bits16(inp.partial), ref_lay["token_dst_row"])
+    np.testing.assert_array_equal(bits16(comb), ref_c)
+
