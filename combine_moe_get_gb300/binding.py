@@ -131,7 +131,8 @@ TRACE_PHASE = 0x10000   # warp field of a per-CTA phase record: TRACE_PHASE + ph
 TRACE_PHASE_NAMES = {3: ("dependency wait", "top-k tile loaded", "bitmap and expert histogram",
                          "tile counts and first cluster barrier", "exchange and second barrier",
                          "prefixes and count writes", "receive rows", "is_token_in_rank rows"),
-                     9: ("set-up (behind the layout: first loads, L2 prefetch)", "dependency wait", "the rest"),
+                     9: ("set-up (behind the layout: first loads, L2 prefetch)", "dependency wait",
+                         "fused small-batch layout", "the rest"),
                      10: ("set-up", "dependency wait", "the rest"),
                      11: ("set-up", "dependency wait", "the rest")}
 

@@ -312,21 +312,19 @@ __device__ void fused_layout(const DispatchArgs &a, uint8_t *region) {
         }
     }
     __syncthreads();
-    // one thread per token: each rank of the token once (its lowest entry), membership bits
-    for (int t = threadIdx.x; t < a.T; t += blockDim.x) {
-        const int16_t *tr = rid + t * k;
-        for (int j = 0; j < k; ++j) {
-            const int r = tr[j];
-            if (r < 0) continue;
-            if (cta0) atomicAdd(&hist[eid[t * k + j]], 1);
-            bool first = true;
-            for (int jj = 0; jj < j; ++jj) first = first && tr[jj] != r;
-            if (first) atomicOr(&bitmap[(t >> 5) * R + r], 1u << (t & 31));
-        }
-    }
-    __syncthreads();
+    // a lane per (token, entry), 32 / k tokens per warp: each rank of a token once (its
+    // lowest entry, found among the token's lanes by one match), membership bits
     const int tpp = 32 / k, sub = lane / k, j = lane - sub * k;
     const bool lane_used = sub < tpp;
+    for (int base = warp * tpp; base < a.T; base += warps * tpp) {
+        const int t = base + sub;
+        const bool act = lane_used && t < a.T;
+        const int r = act ? (int)rid[t * k + j] : -1;
+        if (cta0 && r >= 0) atomicAdd(&hist[eid[t * k + j]], 1);
+        const unsigned peers = __match_any_sync(kFull, r >= 0 ? sub * R + r : -(lane + 1));
+        if (r >= 0 && __ffs(peers) - 1 == lane) atomicOr(&bitmap[(t >> 5) * R + r], 1u << (t & 31));
+    }
+    __syncthreads();
     for (int r = threadIdx.x; r < R; r += blockDim.x) {
         uint32_t run = 0;
         for (int w = 0; w < W; ++w) {
@@ -384,7 +382,7 @@ __device__ void fused_layout(const DispatchArgs &a, uint8_t *region) {
 template <bool kFP8, bool kFused>
 __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) {
     WarpTrace wt(a.trace, MOE_TRACE_DISPATCH);
-    MOE_PHASES(MOE_TRACE_DISPATCH, 3);
+    MOE_PHASES(MOE_TRACE_DISPATCH, 4);
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int warps = blockDim.x >> 5;
@@ -512,6 +510,7 @@ __global__ void __launch_bounds__(512, 1) dispatch_kernel(const DispatchArgs a) 
     const int16_t *fl_eid = nullptr, *fl_rid = nullptr;
     if constexpr (kFused) {
         fused_layout(a, smem + a.fl_off);
+        MOE_PHASE(3);
         const FusedSmem fs = fused_smem(a.T, a.R, a.E, a.k);
         fl_bitmap = reinterpret_cast<const uint32_t *>(smem + a.fl_off);
         fl_wprefix = reinterpret_cast<const uint16_t *>(smem + a.fl_off + fs.wprefix);

@@ -403,7 +403,8 @@ MOE_API int moe_combine_fp8_ex(const void *partial_codes, const float *partial_s
  *   MOE_TRACE_DISPATCH        1 set-up (launched behind this library's
  *                             layout: with the first loads and the input
  *                             rows' L2 prefetch), 2 dependency wait, 3 the
- *                             rest (to thread 0's exit)
+ *                             layout of a fused small batch (0 ns when not
+ *                             fused), 4 the rest (to thread 0's exit)
  *   MOE_TRACE_DISPATCH_FP8_ROWS, MOE_TRACE_COMBINE
  *                             1 set-up, 2 dependency wait, 3 the rest
  */
