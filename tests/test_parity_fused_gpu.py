@@ -149,6 +149,8 @@ def test_layout_dispatch_parity_full_configs(moe, name, mode):
     (1025, 1024, 8, 256, 8),        # two launches
     (200, 256, 32, 8192, 1024),     # largest rank and expert counts
     (130, 640, 3, 7, 7),            # R not a multiple of 4
+    (257, 7168, 1, 16, 16),         # one entry per token: 32 tokens per warp in the first pass
+    (96, 7168, 5, 40, 40),          # 6 tokens per warp, two lanes idle
 ])
 def test_layout_dispatch_parity_shapes(moe, T, H, k, E, R, mode):
     g = torch.Generator().manual_seed(T * 3 + H + R)
