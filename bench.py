@@ -558,6 +558,7 @@ def run_ours(args, world, rank, local):
     # the fixed cost inside every event-timed figure: a one-kernel graph timed the same way
     tiny = torch.zeros(16, device=device)
     floor_ms = timer(lambda: tiny.add_(1), reps)
+    pipelined = measure_pipelined(moe, st, w, device, rank)
 
     peak, peak_kind = hbm_peak()
     ab = algorithmic_bytes(T, H, N, NX)
@@ -616,6 +617,7 @@ def run_ours(args, world, rank, local):
         skewed[f"{key}_frac"] = skewed[f"{key}_gbs"] / peak
     kern["skewed"] = skewed
     kern.update(small)
+    kern["pipelined"] = pipelined
     if sus_ms:
         kern["sustained"] = {"steps": len(sus_ms), "ms_per_step_mean": mean(sus_ms),
                              "ms_per_step_median": med(sus_ms), "tokens_per_s": T / (mean(sus_ms) * 1e-3),
@@ -668,6 +670,51 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def measure_pipelined(moe, st, w, device, rank, rounds: int = 10, reps: int = 20):
+    """Steps back to back, as a stream of batches runs: 3 * `rounds` steps in one
+    CUDA graph, cycling over three full sets of buffers (the timed step's and two
+    more with other seeds; a step touches ~0.74 GB of its set, so no step finds
+    its inputs or its outputs' lines in the 129 MB L2 from the step before),
+    no flush in between, events only at the graph's two ends. Each step
+    is the timed one (moe_layout_dispatch + balanced moe_combine_ex); a step's
+    launches overlap the previous step's tail as consecutive launches do."""
+    sets = [st] + [Step(moe, w, wl.make_inputs(dataclass_replace_seed(w, w.seed + 1000 * (i + 1) + rank)), device)
+                   for i in range(2)]
+    for s_ in sets:
+        s_.layout_dispatch()
+        s_.combine()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True, external=True)
+    b = torch.cuda.Event(enable_timing=True, external=True)
+    M = 3 * rounds
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            a.record()
+            for i in range(M):
+                sets[i % 3].layout_dispatch()
+                sets[i % 3].combine()
+            b.record()
+    except Exception as exc:   # no graph: nothing to report
+        return {"unavailable": type(exc).__name__}
+    ms = []
+    for i in range(reps + 2):
+        g.replay()
+        torch.cuda.synchronize()
+        if i >= 2:
+            ms.append(a.elapsed_time(b) / M)
+    for s_ in sets:
+        moe.check_status(s_.status, "pipelined steps")
+    del g, sets
+    torch.cuda.empty_cache()
+    per = statistics.fmean(ms)
+    return {"steps_per_graph": M, "graphs": reps, "ms_per_step_mean": per,
+            "ms_per_step_median": statistics.median(ms), "tokens_per_s": w.num_tokens / (per * 1e-3),
+            "how": "3 x 10 steps back to back in one CUDA graph over three sets of buffers (inputs and outputs "
+                   "rotated; a step touches ~0.74 GB of its set, far above L2), no flush; events at the graph's "
+                   "ends only"}
 
 
 def measure_skewed(moe, device, rank, timer, reps):
