@@ -686,6 +686,7 @@ def measure_pipelined(moe, st, w, device, rank, rounds: int = 10, reps: int = 20
         s_.layout_dispatch()
         s_.combine()
     torch.cuda.synchronize()
+    refs = [s_.out.clone() for s_ in sets]   # each set's step output, which every later run must reproduce
     a = torch.cuda.Event(enable_timing=True, external=True)
     b = torch.cuda.Event(enable_timing=True, external=True)
     M = 3 * rounds
@@ -705,9 +706,11 @@ def measure_pipelined(moe, st, w, device, rank, rounds: int = 10, reps: int = 20
         torch.cuda.synchronize()
         if i >= 2:
             ms.append(a.elapsed_time(b) / M)
-    for s_ in sets:
+    for s_, ref in zip(sets, refs):
         moe.check_status(s_.status, "pipelined steps")
-    del g, sets
+        if not torch.equal(s_.out.view(torch.int16), ref.view(torch.int16)):
+            raise RuntimeError("pipelined steps: a step's output differs from its first run")
+    del g, sets, refs
     torch.cuda.empty_cache()
     per = statistics.fmean(ms)
     return {"steps_per_graph": M, "graphs": reps, "ms_per_step_mean": per,
