@@ -558,7 +558,7 @@ def run_ours(args, world, rank, local):
     # the fixed cost inside every event-timed figure: a one-kernel graph timed the same way
     tiny = torch.zeros(16, device=device)
     floor_ms = timer(lambda: tiny.add_(1), reps)
-    pipelined = measure_pipelined(moe, st, w, device, rank)
+    pipelined = measure_pipelined(moe, st, w, device, rank, reps=max(3, min(20, args.steps)))
 
     peak, peak_kind = hbm_peak()
     ab = algorithmic_bytes(T, H, N, NX)
