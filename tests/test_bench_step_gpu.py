@@ -220,3 +220,15 @@ def test_timed_variants_weighted_and_unbalanced_combine(case):
     torch.cuda.synchronize()
     case.moe.check_status(st.status, "static combine")
     case.check_combine(case.out)
+
+
+def test_pipelined_steps(case):
+    # bench.py's back-to-back measurement: three buffer sets cycled in one graph with no flush in
+    # between; it raises unless every set reproduces its first output bit for bit, and the timed
+    # set's output is the oracle's
+    if case.w.name != "dsv3":
+        pytest.skip("the benchmark runs the pipelined steps at the DeepSeek-V3 shape")
+    case.poison()
+    res = bench.measure_pipelined(case.moe, case.st, case.w, torch.device("cuda", 0), 0, rounds=2, reps=2)
+    assert res["steps_per_graph"] == 6 and res["ms_per_step_mean"] > 0
+    case.check_step()
