@@ -1043,7 +1043,11 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     a.num_units = (int64_t)num_tokens * a.num_chunks;
-    a.stages = std::min(kMaxStages, std::max(3, tu.dispatch_stages));   // the unit ring needs three
+    // behind this library's layout the stage loads are issued before the dependency wait,
+    // and fewer of them let the dispatch's first stores start sooner
+    const int want_warps = a.loads_before_wait ? tu.ld_dispatch_warps : tu.dispatch_warps;
+    const int want_stages = a.loads_before_wait ? tu.ld_dispatch_stages : tu.dispatch_stages;
+    a.stages = std::min(kMaxStages, std::max(3, want_stages));   // the unit ring needs three
     // stages take at most ~200 KB, so that some L1 cache is left (a full 227 KB of
     // stages measured slower)
     const int64_t room = std::min<int64_t>((int64_t)device_smem_optin(), (int64_t)tu.dispatch_smem) -
@@ -1054,13 +1058,13 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
         return round_up(b, 128);
     };
     // fewer stages (down to three) before fewer warps than requested
-    while (a.stages > 3 && room / warp_bytes(a.stages) < tu.dispatch_warps) --a.stages;
+    while (a.stages > 3 && room / warp_bytes(a.stages) < want_warps) --a.stages;
     const int64_t per_warp = warp_bytes(a.stages);
     a.warp_smem = (int)per_warp;
     // as many of the requested warps as fit in one CTA's shared memory
     const int fit = (int)std::min<int64_t>(16, room / per_warp);
     if (fit < 1) return MOE_ERR_INVALID_ARG;
-    warps = std::max(1, std::min(fit, tu.dispatch_warps));
+    warps = std::max(1, std::min(fit, want_warps));
     // a small batch: fewer warps per CTA, so that its units spread over every SM
     if (tu.spread_small) {
         const int64_t per_sm = (a.num_units + device_sm_count() - 1) / device_sm_count();

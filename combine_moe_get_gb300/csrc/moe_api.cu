@@ -120,6 +120,8 @@ const Tuning &tuning() {
         Tuning x;
         x.dispatch_warps = MOE_TUNE_DISPATCH_WARPS;
         x.dispatch_stages = MOE_TUNE_DISPATCH_STAGES;
+        x.ld_dispatch_warps = MOE_TUNE_LD_DISPATCH_WARPS;
+        x.ld_dispatch_stages = MOE_TUNE_LD_DISPATCH_STAGES;
         x.dispatch_chunk = MOE_TUNE_DISPATCH_CHUNK;
         x.dispatch_smem = MOE_TUNE_DISPATCH_SMEM;
         x.combine_warps = MOE_TUNE_COMBINE_WARPS;

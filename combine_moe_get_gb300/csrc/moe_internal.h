@@ -121,6 +121,14 @@ TraceArgs trace_args();
 #ifndef MOE_TUNE_DISPATCH_PREFETCH_L2_PCT
 #define MOE_TUNE_DISPATCH_PREFETCH_L2_PCT 25
 #endif
+// the dispatch launched behind this library's layout (moe_layout_dispatch, two
+// launches): fewer stage loads before its dependency wait measured faster
+#ifndef MOE_TUNE_LD_DISPATCH_WARPS
+#define MOE_TUNE_LD_DISPATCH_WARPS 2
+#endif
+#ifndef MOE_TUNE_LD_DISPATCH_STAGES
+#define MOE_TUNE_LD_DISPATCH_STAGES 4
+#endif
 #ifndef MOE_TUNE_DISPATCH_PREFETCH_NOSYNC
 #define MOE_TUNE_DISPATCH_PREFETCH_NOSYNC 1
 #endif
@@ -129,6 +137,7 @@ TraceArgs trace_args();
 #endif
 struct Tuning {
     int dispatch_warps, dispatch_stages, dispatch_chunk;
+    int ld_dispatch_warps, ld_dispatch_stages;              // ... launched behind this library's layout
     int dispatch_smem;                                       // shared-memory budget of a chunked dispatch CTA
     int combine_warps, combine_chunk, combine_ring_bytes;   // consumer warps, max chunk, ring budget
     int combine_fp8_warps;                                   // consumer warps for E4M3 partial rows
