@@ -1092,7 +1092,8 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     // the grid, and none at all when the first stage loads already take every
     // dealt unit and no pool unit would be prefetched (small batches)
     if (a.prefetch_units > 0) {
-        const int64_t budget = (int64_t)device_l2_bytes() * tu.dispatch_prefetch_l2_pct / 100;
+        const int pct = a.loads_before_wait ? tu.dispatch_prefetch_l2_pct : tu.dispatch_prefetch_l2_pct_alone;
+        const int64_t budget = (int64_t)device_l2_bytes() * pct / 100;
         a.prefetch_units = std::min<int64_t>(a.prefetch_units, budget / ((int64_t)grid * a.chunk_bytes));
         const int64_t first = (int64_t)warps * a.stages;
         const int64_t max_dealt = (a.static_units + grid - 1) / grid;

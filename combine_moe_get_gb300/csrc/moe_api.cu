@@ -150,6 +150,7 @@ const Tuning &tuning() {
         x.dispatch_prefetch_keep = MOE_TUNE_DISPATCH_PREFETCH_KEEP;
         x.dispatch_prefetch_always = MOE_TUNE_DISPATCH_PREFETCH_ALWAYS;
         x.dispatch_prefetch_l2_pct = MOE_TUNE_DISPATCH_PREFETCH_L2_PCT;
+        x.dispatch_prefetch_l2_pct_alone = MOE_TUNE_DISPATCH_PREFETCH_L2_PCT_ALONE;
         return x;
     }();
     return t;

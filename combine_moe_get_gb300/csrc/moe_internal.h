@@ -121,6 +121,9 @@ TraceArgs trace_args();
 #ifndef MOE_TUNE_DISPATCH_PREFETCH_L2_PCT
 #define MOE_TUNE_DISPATCH_PREFETCH_L2_PCT 25
 #endif
+#ifndef MOE_TUNE_DISPATCH_PREFETCH_L2_PCT_ALONE   // a dispatch not launched behind the layout
+#define MOE_TUNE_DISPATCH_PREFETCH_L2_PCT_ALONE 15
+#endif
 // the dispatch launched behind this library's layout (moe_layout_dispatch, two
 // launches): fewer stage loads before its dependency wait measured faster
 #ifndef MOE_TUNE_LD_DISPATCH_WARPS
@@ -160,6 +163,7 @@ struct Tuning {
     int dispatch_prefetch_keep;  // ... with an evict-last policy (else evict-normal)
     int dispatch_prefetch_always;  // ... in every chunked dispatch, not only behind the layout
     int dispatch_prefetch_l2_pct;  // ... holding at most this share of L2 evict-last
+    int dispatch_prefetch_l2_pct_alone;  // ... the same for a dispatch not launched behind the layout
 };
 const Tuning &tuning();
 
