@@ -1043,8 +1043,8 @@ int chunked_config(DispatchArgs &a, bool fp8, int num_tokens, size_t extra, int 
     a.chunk_bytes = (int)round_up((a.row_bytes + nch - 1) / nch, align);
     a.num_chunks = (int)((a.row_bytes + a.chunk_bytes - 1) / a.chunk_bytes);
     a.num_units = (int64_t)num_tokens * a.num_chunks;
-    // behind this library's layout the stage loads are issued before the dependency wait,
-    // and fewer of them let the dispatch's first stores start sooner
+    // behind this library's layout (stage loads issued before the dependency wait) a
+    // different shape measured faster: 2 warps x 4 stages, two CTAs per SM
     const int want_warps = a.loads_before_wait ? tu.ld_dispatch_warps : tu.dispatch_warps;
     const int want_stages = a.loads_before_wait ? tu.ld_dispatch_stages : tu.dispatch_stages;
     a.stages = std::min(kMaxStages, std::max(3, want_stages));   // the unit ring needs three
